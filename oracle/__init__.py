@@ -1,0 +1,277 @@
+"""float64 CPU oracle for the weight-only quantized GEMM -- TEST INFRASTRUCTURE ONLY.
+
+Only the test-suite, ``__graft_entry__.smoke()`` and the benchmark's CPU-baseline
+leg may import this package.  The product library never loads it and shares no
+code with it: the arithmetic lives in ``oracle.c`` (plain C, float64), written from
+the definitions on the source pages:
+
+* INT4 W4A16 -- "Low Bit Triton Kernels" (GPU MODE lecture 34), §03 core pattern:
+  unpack two nibbles per byte, subtract 8, multiply by the group scale
+  ``s[k // group_size, n]``, then the dot product.
+* FP8 W8A16 -- "FlashInfer W8A16 GEMM (mm_bf16_fp8) analysis" (PR #7495),
+  introduction: e4m3 weight, one fp32 per-tensor scale applied to the fp32
+  accumulator.
+* BF16 x FP4 -- "FlashInfer SM100 BF16 x FP4 GEMM" (PR #4466), §2: e2m1 weight
+  [N, K/2], e4m3 block scale per 16 along K, global alpha.
+
+This module only marshals numpy arrays into the C functions and builds the
+shared object with gcc on first use.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import subprocess
+import threading
+
+import numpy as np
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+_SRC = os.path.join(_HERE, "oracle.c")
+_LIB_PATH = os.path.join(_HERE, "liboracle.so")
+_lock = threading.Lock()
+_lib = None
+
+_c_i64p = ctypes.POINTER(ctypes.c_int64)
+
+
+def build(force: bool = False) -> str:
+    """Compile oracle.c into liboracle.so (gcc, -O2, no fast-math, no FMA contraction)."""
+    if not force and os.path.exists(_LIB_PATH) and os.path.getmtime(_LIB_PATH) >= os.path.getmtime(_SRC):
+        return _LIB_PATH
+    tmp = _LIB_PATH + f".tmp{os.getpid()}"
+    base = ["gcc", "-O2", "-fPIC", "-shared", "-ffp-contract=off", "-fno-fast-math", _SRC, "-o", tmp, "-lm"]
+    try:
+        subprocess.run(base[:1] + ["-fopenmp"] + base[1:], check=True, capture_output=True)
+    except subprocess.CalledProcessError:
+        # No OpenMP runtime on this host: build the serial oracle.
+        subprocess.run(base, check=True, capture_output=True)
+    os.replace(tmp, _LIB_PATH)
+    return _LIB_PATH
+
+
+def _load():
+    global _lib
+    with _lock:
+        if _lib is not None:
+            return _lib
+        # ORACLE_LIB points the tests at a deliberately altered build of oracle.c
+        # (tests/test_oracle_mutations.py); everything else uses the real one.
+        override = os.environ.get("ORACLE_LIB")
+        lib = ctypes.CDLL(override if override else build())
+        u8p = ctypes.c_void_p
+        lib.oracle_f16_to_double.restype = ctypes.c_double
+        lib.oracle_f16_to_double.argtypes = [ctypes.c_uint16]
+        lib.oracle_bf16_to_double.restype = ctypes.c_double
+        lib.oracle_bf16_to_double.argtypes = [ctypes.c_uint16]
+        lib.oracle_e4m3_to_double.restype = ctypes.c_double
+        lib.oracle_e4m3_to_double.argtypes = [ctypes.c_uint8]
+        lib.oracle_e2m1_to_double.restype = ctypes.c_double
+        lib.oracle_e2m1_to_double.argtypes = [ctypes.c_uint8]
+        lib.oracle_round_f16.restype = ctypes.c_uint16
+        lib.oracle_round_f16.argtypes = [ctypes.c_double]
+        lib.oracle_round_bf16.restype = ctypes.c_uint16
+        lib.oracle_round_bf16.argtypes = [ctypes.c_double]
+        lib.oracle_pack_int4.argtypes = [u8p, ctypes.c_int64, ctypes.c_int64, u8p]
+        lib.oracle_unpack_int4.argtypes = [u8p, ctypes.c_int64, ctypes.c_int64, u8p]
+        lib.oracle_dequant_int4.argtypes = [u8p, u8p, ctypes.c_int64, ctypes.c_int64, ctypes.c_int64, u8p]
+        lib.oracle_gemm_w4a16.argtypes = [u8p, ctypes.c_int, u8p, u8p, ctypes.c_int64, ctypes.c_int64,
+                                          ctypes.c_int64, ctypes.c_int64, u8p, ctypes.c_int64, u8p,
+                                          ctypes.c_int64, u8p]
+        lib.oracle_dequant_fp8.argtypes = [u8p, ctypes.c_int64, ctypes.c_int64, u8p]
+        lib.oracle_gemm_w8a16_fp8.argtypes = [u8p, ctypes.c_int, u8p, ctypes.c_double, u8p, ctypes.c_int64,
+                                              ctypes.c_int64, ctypes.c_int64, u8p, ctypes.c_int64, u8p,
+                                              ctypes.c_int64, u8p]
+        lib.oracle_dequant_fp4.argtypes = [u8p, u8p, ctypes.c_int64, ctypes.c_int64, u8p]
+        lib.oracle_gemm_bf16_fp4.argtypes = [u8p, u8p, u8p, ctypes.c_double, ctypes.c_int64, ctypes.c_int64,
+                                             ctypes.c_int64, u8p, ctypes.c_int64, u8p, ctypes.c_int64, u8p]
+        lib.oracle_num_threads.restype = ctypes.c_int
+        for fn in ("oracle_f16_array_to_double", "oracle_bf16_array_to_double",
+                   "oracle_round_f16_array", "oracle_round_bf16_array"):
+            getattr(lib, fn).argtypes = [u8p, ctypes.c_int64, u8p]
+        _lib = lib
+        return lib
+
+
+def _ptr(a):
+    return None if a is None else a.ctypes.data
+
+
+def _c(a, dtype):
+    a = np.ascontiguousarray(a)
+    if a.dtype != np.dtype(dtype):
+        raise TypeError(f"expected {np.dtype(dtype)}, got {a.dtype}")
+    return a
+
+
+def _index(idx, limit):
+    if idx is None:
+        return None, limit
+    idx = np.ascontiguousarray(np.asarray(idx, dtype=np.int64))
+    if idx.size and (idx.min() < 0 or idx.max() >= limit):
+        raise IndexError("row/column index out of range")
+    return idx, int(idx.size)
+
+
+# ------------------------------------------------------------------ formats
+
+def f16_to_double(bits: int) -> float:
+    return _load().oracle_f16_to_double(int(bits))
+
+
+def bf16_to_double(bits: int) -> float:
+    return _load().oracle_bf16_to_double(int(bits))
+
+
+def e4m3_to_double(code: int) -> float:
+    return _load().oracle_e4m3_to_double(int(code))
+
+
+def e2m1_to_double(code: int) -> float:
+    return _load().oracle_e2m1_to_double(int(code))
+
+
+def round_f16(x: float) -> int:
+    """RN16: round-to-nearest-even to fp16, as bits."""
+    return int(_load().oracle_round_f16(float(x)))
+
+
+def round_bf16(x: float) -> int:
+    """RN_bf: round-to-nearest-even to bf16, as bits."""
+    return int(_load().oracle_round_bf16(float(x)))
+
+
+def _array_call(fn, x, in_dtype, out_dtype):
+    x = np.ascontiguousarray(np.asarray(x, dtype=in_dtype))
+    out = np.empty(x.shape, dtype=out_dtype)
+    getattr(_load(), fn)(_ptr(x), x.size, _ptr(out))
+    return out
+
+
+def round_f16_array(x) -> np.ndarray:
+    """Element-wise RN16 of float64 values, as fp16 bits."""
+    return _array_call("oracle_round_f16_array", x, np.float64, np.uint16)
+
+
+def round_bf16_array(x) -> np.ndarray:
+    """Element-wise RN_bf of float64 values, as bf16 bits."""
+    return _array_call("oracle_round_bf16_array", x, np.float64, np.uint16)
+
+
+def f16_bits_to_double_array(bits) -> np.ndarray:
+    return _array_call("oracle_f16_array_to_double", bits, np.uint16, np.float64)
+
+
+def bf16_bits_to_double_array(bits) -> np.ndarray:
+    return _array_call("oracle_bf16_array_to_double", bits, np.uint16, np.float64)
+
+
+# ------------------------------------------------------------------ INT4
+
+def pack_int4(q: np.ndarray) -> np.ndarray:
+    """q uint8 [N, K] in 0..15 -> canonical packed uint8 [N, K/2]."""
+    q = _c(q, np.uint8)
+    N, K = q.shape
+    out = np.empty((N, K // 2), dtype=np.uint8)
+    _load().oracle_pack_int4(_ptr(q), N, K, _ptr(out))
+    return out
+
+
+def unpack_int4(w: np.ndarray, K: int) -> np.ndarray:
+    """canonical packed uint8 [N, K/2] -> codes uint8 [N, K]."""
+    w = _c(w, np.uint8)
+    N = w.shape[0]
+    out = np.empty((N, K), dtype=np.uint8)
+    _load().oracle_unpack_int4(_ptr(w), N, K, _ptr(out))
+    return out
+
+
+def dequant_int4(w: np.ndarray, s_bits: np.ndarray, K: int, G: int) -> np.ndarray:
+    """Exact fp32 weight [N, K] = (q - 8) * S[k // G, n]; s_bits fp16 bits [K/G, N]."""
+    w = _c(w, np.uint8)
+    s_bits = _c(s_bits, np.uint16)
+    N = w.shape[0]
+    out = np.empty((N, K), dtype=np.float32)
+    _load().oracle_dequant_int4(_ptr(w), _ptr(s_bits), N, K, G, _ptr(out))
+    return out
+
+
+def gemm_w4a16(a_bits, a_is_bf16, w, s_bits, M, N, K, G, rows=None, cols=None) -> np.ndarray:
+    """float64 out[rows, cols] = A[rows] . dequant(W)[cols]^T."""
+    a_bits = _c(a_bits, np.uint16)
+    w = _c(w, np.uint8)
+    s_bits = _c(s_bits, np.uint16)
+    r, nr = _index(rows, M)
+    c, nc = _index(cols, N)
+    out = np.empty((nr, nc), dtype=np.float64)
+    _load().oracle_gemm_w4a16(_ptr(a_bits), int(bool(a_is_bf16)), _ptr(w), _ptr(s_bits), M, N, K, G,
+                              _ptr(r), nr, _ptr(c), nc, _ptr(out))
+    return out
+
+
+# ------------------------------------------------------------------ FP8
+
+def dequant_fp8(w: np.ndarray) -> np.ndarray:
+    w = _c(w, np.uint8)
+    N, K = w.shape
+    out = np.empty((N, K), dtype=np.float32)
+    _load().oracle_dequant_fp8(_ptr(w), N, K, _ptr(out))
+    return out
+
+
+def gemm_w8a16_fp8(a_bits, a_is_bf16, w, alpha, M, N, K, bias_bits=None, rows=None, cols=None):
+    a_bits = _c(a_bits, np.uint16)
+    w = _c(w, np.uint8)
+    if bias_bits is not None:
+        bias_bits = _c(bias_bits, np.uint16)
+    r, nr = _index(rows, M)
+    c, nc = _index(cols, N)
+    out = np.empty((nr, nc), dtype=np.float64)
+    _load().oracle_gemm_w8a16_fp8(_ptr(a_bits), int(bool(a_is_bf16)), _ptr(w), float(alpha),
+                                  _ptr(bias_bits), M, N, K, _ptr(r), nr, _ptr(c), nc, _ptr(out))
+    return out
+
+
+# ------------------------------------------------------------------ FP4
+
+def dequant_fp4(w: np.ndarray, sf: np.ndarray, K: int) -> np.ndarray:
+    w = _c(w, np.uint8)
+    sf = _c(sf, np.uint8)
+    N = w.shape[0]
+    out = np.empty((N, K), dtype=np.float32)
+    _load().oracle_dequant_fp4(_ptr(w), _ptr(sf), N, K, _ptr(out))
+    return out
+
+
+def gemm_bf16_fp4(a_bits, w, sf, alpha, M, N, K, rows=None, cols=None) -> np.ndarray:
+    a_bits = _c(a_bits, np.uint16)
+    w = _c(w, np.uint8)
+    sf = _c(sf, np.uint8)
+    r, nr = _index(rows, M)
+    c, nc = _index(cols, N)
+    out = np.empty((nr, nc), dtype=np.float64)
+    _load().oracle_gemm_bf16_fp4(_ptr(a_bits), _ptr(w), _ptr(sf), float(alpha), M, N, K,
+                                 _ptr(r), nr, _ptr(c), nc, _ptr(out))
+    return out
+
+
+def num_threads() -> int:
+    return int(_load().oracle_num_threads())
+
+
+# ------------------------------------------------------------------ metrics
+
+def rel_errors(out, ref):
+    """(rel_max, rel_mean) of an output against the float64 reference.
+
+    rel_max  = max|out - ref| / max|ref|
+    rel_mean = mean|out - ref| / mean|ref|
+    The accuracy check of "Low Bit Triton Kernels" (lecture 34, exercise 4) asks for
+    mean / max relative error near 1e-3 / 5e-3 and to judge the error as a
+    distribution; normalising by the reference's own magnitude keeps near-zero
+    outputs from dominating.
+    """
+    out = np.asarray(out, dtype=np.float64)
+    ref = np.asarray(ref, dtype=np.float64)
+    err = np.abs(out - ref)
+    return float(err.max() / np.abs(ref).max()), float(err.mean() / np.abs(ref).mean())
