@@ -1,0 +1,207 @@
+/*
+ * wq.h -- C ABI of the weight-only quantized GEMM library for GB300 (sm_103a).
+ *
+ *   out[M, N] = A[M, K] . dequant(W)[N, K]^T      fp32 accumulation, 16-bit out
+ *
+ * Weight formats:
+ *   W4A16   INT4 codes, two per byte along K (even k in the low nibble), value
+ *           (q - 8) * S[k / G, n] with fp16 group scales S[K/G][N], G in {32, 64,
+ *           128, 256}.  Source: "Low Bit Triton Kernels" (GPU MODE lecture 34),
+ *           §03 core pattern (the gemlite-style BLOCK_K loop: unpack two nibbles,
+ *           subtract 8, multiply by s[k // GROUP_SIZE, n], dot product).
+ *   FP8     e4m3 codes W[N][K] and one fp32 per-tensor scale applied to the fp32
+ *           accumulator, optional bias.  Source: "FlashInfer W8A16 GEMM
+ *           (mm_bf16_fp8) analysis" (PR #7495), introduction and §2 (public API:
+ *           mm_bf16_fp8 / mm_fp16_fp8 take a, b, alpha, bias, out, workspace).
+ *   FP4     e2m1 codes W[N][K/2] (even k in the low nibble) with one e4m3 scale
+ *           per 16 values along K and a global fp32 alpha.  Source: "FlashInfer
+ *           SM100 BF16 x FP4 GEMM" (PR #4466), §2 (uint8 weight of shape [N, K/2],
+ *           block scale factors reordered by an offline preparation step) and §3
+ *           (the kernel takes weight, weight scale, activation, alpha, output).
+ *
+ * Conventions for every entry point:
+ *   - All arrays are row-major and live in device memory unless stated.  The
+ *     caller allocates and owns every buffer; the library never allocates,
+ *     frees or synchronises.
+ *   - Work is enqueued on `stream` (a cudaStream_t; NULL = legacy default stream)
+ *     and returns immediately.
+ *   - Arguments are validated on the host before anything is launched; a
+ *     non-WQ_OK status means nothing was enqueued.  WQ_ERR_CUDA reports a CUDA
+ *     runtime error from the launch itself (the CUDA error is left pending).
+ *   - Pointers named below as "16-byte aligned" are read by TMA / bulk copies;
+ *     scalars (alpha, bias) need only element alignment.
+ *   - Only compute capability 10.3 (GB300) is supported: other devices give
+ *     WQ_ERR_UNSUPPORTED_DEVICE.
+ *   - M == 0 is a valid empty problem and returns WQ_OK without launching.
+ */
+#ifndef WQ_H_
+#define WQ_H_
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef struct CUstream_st* wq_stream_t; /* same type as cudaStream_t */
+
+typedef enum { WQ_F16 = 0, WQ_BF16 = 1 } wq_dtype;
+
+typedef enum { WQ_OP_W4A16 = 0, WQ_OP_FP8 = 1, WQ_OP_FP4 = 2 } wq_op;
+
+typedef enum {
+    WQ_OK = 0,
+    WQ_ERR_NULL = 1,                /* a required pointer is NULL */
+    WQ_ERR_SHAPE = 2,               /* M < 0, N or K <= 0, or a size rule below */
+    WQ_ERR_GROUP = 3,               /* G not in {32, 64, 128, 256} or K % G != 0 */
+    WQ_ERR_MISALIGNED = 4,          /* a pointer misses its alignment */
+    WQ_ERR_DTYPE = 5,               /* activation dtype not supported by the op */
+    WQ_ERR_WORKSPACE = 6,           /* workspace missing or smaller than required */
+    WQ_ERR_UNSUPPORTED_DEVICE = 7,  /* current device is not compute capability 10.3 */
+    WQ_ERR_CUDA = 8,                /* a CUDA runtime call failed */
+    WQ_ERR_TIMEOUT = 9              /* a kernel gave up on a bounded wait (device status) */
+} wq_status;
+
+/* Human-readable name of a status. */
+const char* wq_status_string(wq_status s);
+
+/* ------------------------------------------------------------------ INT4 */
+
+/* Sizes of the kernel-order ("prepacked") INT4 weight and scale buffers for an
+ * N x K weight with group size G.  N is padded to a multiple of 128 and K to a
+ * multiple of 256 inside them.  Host only. */
+wq_status wq_int4_packed_bytes(int64_t N, int64_t K, int32_t G, size_t* w_bytes, size_t* s_bytes);
+
+/* Offline layout transform (a pure permutation; bit-exact and invertible).
+ * Reorders canonical packed codes w_canon uint8 [N][K/2] and fp16 scales s_canon
+ * [K/G][N] into the tile-major order the GEMM kernels stream with bulk copies:
+ * for each 128-row tile, 32-code chunks along K, and within a chunk each row's 16
+ * bytes with the even k of every 8 in the low half-word, so that the in-kernel
+ * unpack yields (k, k+1) operand pairs with shift/mask only.  Padding rows and
+ * columns get code 8 and scale 0 (weight 0).  Why: "Bitblas -- Mixed-Precision
+ * GEMM with the Ladder Compiler" (GPU MODE lecture 33), introduction -- when the
+ * weight layout does not match what the tensor-core operand wants, the layout
+ * conversion on the critical path costs more than half of the performance; the
+ * Ladder compiler moves it offline.
+ * Requirements: N > 0, K % 32 == 0, K % G == 0; w_kernel and s_kernel 16-byte
+ * aligned and of wq_int4_packed_bytes sizes; w_canon 1-byte, s_canon 2-byte
+ * aligned. */
+wq_status wq_pack_int4(const uint8_t* w_canon, const void* s_canon, int64_t N, int64_t K, int32_t G,
+                       uint8_t* w_kernel, void* s_kernel, wq_stream_t stream);
+
+/* Inverse of wq_pack_int4 (tests, export). */
+wq_status wq_unpack_int4(const uint8_t* w_kernel, const void* s_kernel, int64_t N, int64_t K, int32_t G,
+                         uint8_t* w_canon, void* s_canon, wq_stream_t stream);
+
+/* Debug export: the exact dequantized weight (q - 8) * s as fp32 [N][K], read
+ * from the prepacked buffers.  The fp32 value is exact (at most 15 significant
+ * bits). */
+wq_status wq_debug_dequant_int4(const uint8_t* w_kernel, const void* s_kernel, int64_t N, int64_t K, int32_t G,
+                                float* w_f32, wq_stream_t stream);
+
+/* W4A16 GEMM: out[M][N] (same 16-bit type as A) = A[M][K] . ((q - 8) * S)^T.
+ * A: a_dtype [M][K], 16-byte aligned.  w_kernel / s_kernel: output of
+ * wq_pack_int4 for this N, K, G.  out: 16-byte aligned, N % 8 == 0.
+ * ws: workspace of at least wq_workspace_bytes(WQ_OP_W4A16, ...) bytes,
+ * 16-byte aligned; may be NULL when that size is 0.  Its first 16 KiB hold
+ * split-K arrival counters: zero-fill them once after allocating the workspace;
+ * every call leaves them zero again (a call that ends with a timeout bit in the
+ * device status may not).  One workspace may serve calls of any shape, but calls
+ * that share it must not overlap on the GPU.  The dequantized operand is
+ * RN((q - 8) * s) in the type of A, accumulated in fp32; split-K partial sums
+ * are reduced in a fixed order, so results are identical run to run. */
+wq_status wq_gemm_w4a16(const void* A, wq_dtype a_dtype, const uint8_t* w_kernel, const void* s_kernel,
+                        int64_t M, int64_t N, int64_t K, int32_t G, void* out, void* ws, size_t ws_bytes,
+                        wq_stream_t stream);
+
+/* ------------------------------------------------------------------ FP8 */
+
+/* Debug export: e4m3 weight [N][K] decoded through the kernel's operand
+ * conversion to `operand` type and widened to fp32 (exact). */
+wq_status wq_debug_dequant_fp8(const uint8_t* w_e4m3, int64_t N, int64_t K, wq_dtype operand, float* w_f32,
+                               wq_stream_t stream);
+
+/* W8A16 FP8 GEMM: out[M][N] = alpha * (A . e4m3(W)^T) + bias, fp32 epilogue,
+ * rounded once to the type of A (bf16: mm_bf16_fp8, fp16: mm_fp16_fp8).
+ * A: a_dtype [M][K], 16-byte aligned, K % 16 == 0.  w_e4m3: uint8 [N][K],
+ * 16-byte aligned.  alpha: device pointer to one float (element aligned; read
+ * by the kernel, so a CUDA graph can capture the call).  bias: NULL or [N] of
+ * the type of A.  out, ws: as for wq_gemm_w4a16 (op WQ_OP_FP8). */
+wq_status wq_gemm_w8a16_fp8(const void* A, wq_dtype a_dtype, const uint8_t* w_e4m3, const float* alpha,
+                            const void* bias, int64_t M, int64_t N, int64_t K, void* out, void* ws,
+                            size_t ws_bytes, wq_stream_t stream);
+
+/* ------------------------------------------------------------------ FP4 */
+
+/* Size of the prepacked FP4 block-scale buffer (N padded to 128, K to 128). */
+wq_status wq_fp4_packed_sf_bytes(int64_t N, int64_t K, size_t* sf_bytes);
+
+/* Offline reorder of the e4m3 block scales sf_canon uint8 [N][K/16] into the
+ * tile-major order the kernel streams with one bulk copy per k-block (for each
+ * 128-row tile and each 64 values along K, 4 bytes per row).  Padding gets 0.
+ * Requirements: K % 32 == 0; sf_kernel 16-byte aligned. */
+wq_status wq_pack_fp4_sf(const uint8_t* sf_canon, int64_t N, int64_t K, uint8_t* sf_kernel, wq_stream_t stream);
+
+/* Debug export: e2m1(code) * e4m3(sf) as fp32 [N][K], through the kernel's
+ * operand conversion (exact). */
+wq_status wq_debug_dequant_fp4(const uint8_t* w_e2m1, const uint8_t* sf_kernel, int64_t N, int64_t K,
+                               float* w_f32, wq_stream_t stream);
+
+/* BF16 x FP4 GEMM: out[M][N] bf16 = alpha * (A . (e2m1(W) * e4m3(SF))^T).
+ * A: bf16 [M][K], 16-byte aligned, K % 32 == 0.  w_e2m1: uint8 [N][K/2], 16-byte
+ * aligned.  sf_kernel: output of wq_pack_fp4_sf.  alpha: device pointer to one
+ * float.  out, ws: as for wq_gemm_w4a16 (op WQ_OP_FP4). */
+wq_status wq_gemm_bf16_fp4(const void* A, const uint8_t* w_e2m1, const uint8_t* sf_kernel, const float* alpha,
+                           int64_t M, int64_t N, int64_t K, void* out, void* ws, size_t ws_bytes,
+                           wq_stream_t stream);
+
+/* ------------------------------------------------------------------ planning */
+
+/* The launch plan the library picks for a problem (deterministic in the
+ * arguments and the current device). */
+typedef struct {
+    int32_t bn;           /* tokens per tile (tcgen05 MMA N) */
+    int32_t bk;           /* k per pipeline stage */
+    int32_t stages;       /* shared-memory pipeline depth */
+    int32_t splits;       /* split-K slices per output tile */
+    int32_t grid;         /* CTAs launched */
+    int32_t threads;      /* threads per CTA */
+    int32_t smem_bytes;   /* dynamic shared memory per CTA */
+    int32_t n_items;      /* tiles x splits */
+    int32_t walk_n_fast;  /* 1: weight-row tiles are walked fastest */
+    int32_t tiles_n;
+    int32_t tiles_m;
+} wq_plan;
+
+/* Plan and workspace size for op (a_dtype is ignored for WQ_OP_FP4, G for FP8
+ * and FP4).  Either output pointer may be NULL.  Host only. */
+wq_status wq_get_plan(wq_op op, wq_dtype a_dtype, int64_t M, int64_t N, int64_t K, int32_t G, wq_plan* plan,
+                      size_t* ws_bytes);
+
+/* Workspace bytes an op needs (0 when no split-K is used).  Host only. */
+wq_status wq_workspace_bytes(wq_op op, wq_dtype a_dtype, int64_t M, int64_t N, int64_t K, int32_t G,
+                             size_t* bytes);
+
+/* ------------------------------------------------------------------ device status */
+
+/* Reads the current device's status word: bit 0..3 = a bounded wait timed out in
+ * the producer / MMA / transform / epilogue role, bit 4 = draining after a
+ * timeout timed out, bit 5 = the wait probe timed out.  Synchronous (copies one
+ * word); returns WQ_ERR_TIMEOUT when any bit is set. */
+wq_status wq_device_status(uint32_t* bits);
+
+/* Clears the current device's status word (synchronous). */
+wq_status wq_clear_device_status(void);
+
+/* Test hook: launches one CTA whose thread waits on an mbarrier that nothing
+ * arrives on, with the kernels' bounded wait of `timeout_ns` nanoseconds.  The
+ * wait runs out, the kernel sets bit 5 of the device status word and returns
+ * normally, leaving the context usable. */
+wq_status wq_debug_wait_probe(int64_t timeout_ns, wq_stream_t stream);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* WQ_H_ */

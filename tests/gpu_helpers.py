@@ -1,0 +1,59 @@
+"""Shared helpers for the GPU parity tests (not collected as tests)."""
+import numpy as np
+import torch
+
+import oracle
+from weight_only_quantized_tma_gb300 import synth
+
+# Accuracy bar for fp16 / bf16 outputs against the float64 oracle: max|out-ref|/max|ref|
+# and mean|out-ref|/mean|ref| ("Low Bit Triton Kernels", exercise 4: mean / max
+# relative error near 1e-3 / 5e-3).
+REL_MAX = 5e-3
+REL_MEAN = 1e-3
+
+DEV = torch.device("cuda:0")
+
+
+def to_dev_f16bits(bits: np.ndarray, dtype: str) -> torch.Tensor:
+    t = torch.from_numpy(np.ascontiguousarray(bits).view(np.int16))
+    t = t.view(torch.float16 if dtype == "f16" else torch.bfloat16)
+    return t.to(DEV)
+
+
+def out_to_f64(out: torch.Tensor) -> np.ndarray:
+    return out.float().cpu().numpy().astype(np.float64)
+
+
+def out_bits(out: torch.Tensor) -> np.ndarray:
+    return out.contiguous().view(torch.int16).cpu().numpy().view(np.uint16)
+
+
+class Int4Problem:
+    """Seeded INT4 problem on host and device, with the packed device buffers."""
+
+    def __init__(self, M, N, K, G, a_dtype="f16", seed=0, A_bits=None, wts=None):
+        self.M, self.N, self.K, self.G, self.a_dtype = M, N, K, G, a_dtype
+        self.A = A_bits if A_bits is not None else synth.activations(M, K, a_dtype, seed)
+        self.wts = wts if wts is not None else synth.int4_weights(N, K, G, seed + 1)
+        self.A_d = to_dev_f16bits(self.A, a_dtype)
+        self.w_d = torch.from_numpy(self.wts.w).to(DEV)
+        self.s_d = to_dev_f16bits(self.wts.s, "f16")
+
+    def pack(self):
+        import weight_only_quantized_tma_gb300 as wq
+        self.wk, self.sk = wq.wq_pack_int4(self.w_d, self.s_d, self.N, self.K, self.G)
+        return self
+
+    def run(self, out=None, ws=None):
+        import weight_only_quantized_tma_gb300 as wq
+        return wq.wq_gemm_w4a16(self.A_d, self.wk, self.sk, self.N, self.K, self.G, out=out, ws=ws)
+
+    def ref(self, rows=None):
+        return oracle.gemm_w4a16(self.A, self.a_dtype == "bf16", self.wts.w, self.wts.s, self.M, self.N, self.K,
+                                 self.G, rows=rows)
+
+
+def check_close(got, ref, rel_max=REL_MAX, rel_mean=REL_MEAN, what=""):
+    rmax, rmean = oracle.rel_errors(got, ref)
+    assert rmax <= rel_max and rmean <= rel_mean, f"{what} rel_max={rmax:.3e} rel_mean={rmean:.3e}"
+    return rmax, rmean

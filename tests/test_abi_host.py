@@ -1,0 +1,120 @@
+"""Host-side checks of the C ABI that need no GPU: the library loads, exports every
+entry point include/wq.h declares, and rejects bad arguments before touching the
+device (validation runs first; nothing is launched)."""
+import ctypes
+import os
+import re
+
+import pytest
+
+import weight_only_quantized_tma_gb300 as wq
+from weight_only_quantized_tma_gb300 import _lib
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+HEADER = os.path.join(ROOT, "include", "wq.h")
+
+OK, NULL, SHAPE, GROUP, MISALIGNED, DTYPE, WORKSPACE, UNSUPPORTED, CUDA, TIMEOUT = range(10)
+
+
+def _declared():
+    text = open(HEADER).read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    return sorted(set(re.findall(r"\b(wq_[a-z0-9_]+)\s*\(", text)))
+
+
+@pytest.fixture(scope="module")
+def L():
+    return wq.lib()
+
+
+def test_every_declared_symbol_is_exported(L):
+    names = _declared()
+    assert len(names) >= 15
+    for n in names:
+        assert hasattr(L, n), f"{n} declared in include/wq.h but not exported"
+    assert set(names) == set(_lib.exported_symbols())
+
+
+def test_status_strings(L):
+    for s in range(10):
+        assert L.wq_status_string(s).decode().startswith(_lib.STATUS_NAMES[s])
+
+
+def test_int4_packed_sizes(L):
+    wb, sb = ctypes.c_size_t(), ctypes.c_size_t()
+    assert L.wq_int4_packed_bytes(4096, 4096, 128, ctypes.byref(wb), ctypes.byref(sb)) == OK
+    assert wb.value == 4096 * 4096 // 2 and sb.value == 4096 * 32 * 2
+    # N padded to 128, K to 256
+    assert L.wq_int4_packed_bytes(200, 96, 32, ctypes.byref(wb), ctypes.byref(sb)) == OK
+    assert wb.value == 256 * 256 // 2 and sb.value == 256 * (256 // 32) * 2
+    assert L.wq_int4_packed_bytes(128, 100, 32, ctypes.byref(wb), ctypes.byref(sb)) == SHAPE
+    assert L.wq_int4_packed_bytes(128, 256, 48, ctypes.byref(wb), ctypes.byref(sb)) == GROUP
+    assert L.wq_int4_packed_bytes(128, 96, 64, ctypes.byref(wb), ctypes.byref(sb)) == GROUP
+
+
+def test_fp4_sf_sizes(L):
+    b = ctypes.c_size_t()
+    assert L.wq_fp4_packed_sf_bytes(12800, 5120, ctypes.byref(b)) == OK
+    assert b.value == 12800 * 5120 // 16
+    assert L.wq_fp4_packed_sf_bytes(100, 96, ctypes.byref(b)) == OK
+    assert b.value == 128 * 2 * 4          # N -> 128 rows, K -> 128 = two 64-wide quads, 4 bytes each
+    assert L.wq_fp4_packed_sf_bytes(128, 160, ctypes.byref(b)) == OK
+    assert b.value == 128 * 4 * 4          # K = 160 pads to 256: four quads
+
+
+P = 0x10000  # a 16-byte-aligned fake device address: validation never dereferences it
+
+
+def test_gemm_w4a16_validation(L):
+    f = L.wq_gemm_w4a16
+    assert f(None, 0, P, P, 4, 512, 1024, 128, P, None, 0, None) == NULL
+    assert f(P, 0, P, P, -1, 512, 1024, 128, P, None, 0, None) == SHAPE
+    assert f(P, 0, P, P, 4, 512, 1000, 128, P, None, 0, None) == SHAPE      # K % 32
+    assert f(P, 0, P, P, 4, 500, 1024, 128, P, None, 0, None) == SHAPE      # N % 8
+    assert f(P, 0, P, P, 4, 512, 1024, 96, P, None, 0, None) == GROUP
+    assert f(P, 0, P, P, 4, 512, 1056, 64, P, None, 0, None) == GROUP       # K % G
+    assert f(P, 7, P, P, 4, 512, 1024, 128, P, None, 0, None) == DTYPE
+    assert f(P + 8, 0, P, P, 4, 512, 1024, 128, P, None, 0, None) == MISALIGNED
+    assert f(P, 0, P, P + 4, 4, 512, 1024, 128, P, None, 0, None) == MISALIGNED
+    assert f(P, 0, P, P, 4, 512, 1024, 128, P + 2, None, 0, None) == MISALIGNED
+
+
+def test_gemm_fp8_validation(L):
+    f = L.wq_gemm_w8a16_fp8
+    assert f(P, 1, P, None, None, 4, 512, 1024, P, None, 0, None) == NULL    # alpha
+    assert f(P, 1, P, P, None, 4, 512, 1000, P, None, 0, None) == SHAPE      # K % 16
+    # a scalar alpha only needs 4-byte alignment (address % 16 == 4 is accepted by
+    # validation; it only fails later for want of a device here)
+    assert f(P, 1, P, P + 4, None, 4, 512, 1024, P, None, 0, None) != MISALIGNED
+    assert f(P, 1, P, P + 2, None, 4, 512, 1024, P, None, 0, None) == MISALIGNED
+    assert f(P, 1, P, P, P + 1, 4, 512, 1024, P, None, 0, None) == MISALIGNED   # bias
+
+
+def test_gemm_fp4_validation(L):
+    f = L.wq_gemm_bf16_fp4
+    assert f(P, P, None, P, 4, 512, 1024, P, None, 0, None) == NULL
+    assert f(P, P, P, P, 4, 512, 1040, P, None, 0, None) == SHAPE            # K % 32
+    assert f(P, P + 8, P, P, 4, 512, 1024, P, None, 0, None) == MISALIGNED
+
+
+def test_pack_validation(L):
+    assert L.wq_pack_int4(None, P, 128, 256, 128, P, P, None) == NULL
+    assert L.wq_pack_int4(P, P, 128, 250, 128, P, P, None) == SHAPE
+    assert L.wq_pack_int4(P, P, 128, 256, 100, P, P, None) == GROUP
+    assert L.wq_pack_int4(P, P, 128, 256, 128, P + 8, P, None) == MISALIGNED
+    assert L.wq_pack_fp4_sf(P, 128, 100, P, None) == SHAPE
+
+
+def test_no_device_is_an_error_not_a_crash(L):
+    import torch
+    if torch.cuda.is_available():
+        pytest.skip("a GPU is present")
+    st = L.wq_gemm_w4a16(P, 0, P, P, 4, 512, 1024, 128, P, None, 0, None)
+    assert st in (CUDA, UNSUPPORTED)
+
+
+def test_python_binding_rejects_bad_tensors():
+    import torch
+    with pytest.raises(ValueError):
+        wq.wq_gemm_w4a16(torch.zeros(4, 64, dtype=torch.float32), torch.zeros(1, dtype=torch.uint8),
+                         torch.zeros(1, dtype=torch.float16), 128, 64, 32)

@@ -1,0 +1,165 @@
+"""GPU parity of the W4A16 path (pack, debug export, GEMM) against the float64 oracle."""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+import weight_only_quantized_tma_gb300 as wq
+from weight_only_quantized_tma_gb300 import synth
+
+from gpu_helpers import DEV, Int4Problem, check_close, out_bits, out_to_f64, to_dev_f16bits
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.mark.parametrize("N,K,G", [(512, 1024, 128), (200, 96, 32), (256, 4096, 256), (384, 320, 64),
+                                   (4096, 11008, 128)])
+def test_pack_unpack_roundtrip_bit_exact(N, K, G):
+    p = Int4Problem(1, N, K, G, seed=101).pack()
+    w2, s2 = wq.wq_unpack_int4(p.wk, p.sk, N, K, G)
+    torch.cuda.synchronize()
+    assert torch.equal(w2.cpu(), p.w_d.cpu())
+    assert torch.equal(s2.view(torch.int16).cpu(), p.s_d.view(torch.int16).cpu())
+
+
+@pytest.mark.parametrize("N,K,G", [(512, 1024, 128), (200, 96, 32), (136, 512, 64), (256, 768, 256)])
+def test_debug_dequant_bit_exact(N, K, G):
+    p = Int4Problem(1, N, K, G, seed=102).pack()
+    got = wq.wq_debug_dequant_int4(p.wk, p.sk, N, K, G).cpu().numpy()
+    want = oracle.dequant_int4(p.wts.w, p.wts.s, K, G)
+    assert np.array_equal(got.view(np.uint32), want.view(np.uint32))
+
+
+def test_smoke_config():
+    case = synth.SMOKE[0]
+    p = Int4Problem(case.M, case.N, case.K, case.G, seed=synth.seed_for(0, 0)).pack()
+    out = p.run()
+    torch.cuda.synchronize()
+    check_close(out_to_f64(out), p.ref(), what="smoke")
+
+
+@pytest.mark.parametrize("a_dtype", ["f16", "bf16"])
+@pytest.mark.parametrize("G", [32, 64, 128, 256])
+def test_identity_A_returns_rounded_weight_bit_exact(G, a_dtype):
+    # one non-zero product per output: out[m, n] = RN(w[n, m]) exactly
+    K = 256
+    N = 384
+    eye = np.eye(K, dtype=np.float32)
+    A = eye.astype(np.float16).view(np.uint16) if a_dtype == "f16" else \
+        torch.from_numpy(eye).to(torch.bfloat16).view(torch.int16).numpy().view(np.uint16)
+    p = Int4Problem(K, N, K, G, a_dtype=a_dtype, seed=103, A_bits=A).pack()
+    out = p.run()
+    torch.cuda.synchronize()
+    w = oracle.dequant_int4(p.wts.w, p.wts.s, K, G).astype(np.float64)   # [N, K]
+    rn = oracle.round_f16_array(w.T) if a_dtype == "f16" else oracle.round_bf16_array(w.T)
+    assert np.array_equal(out_bits(out), rn)
+
+
+def test_small_integer_problem_is_exact():
+    # scales 0.5 and A in {-1, 0, 1}: every product and partial sum is exact in fp32
+    # and every output (|out| <= 1024, multiples of 0.5) is exact in fp16.
+    M, N, K, G = 16, 256, 256, 64
+    rng = np.random.Generator(np.random.PCG64(104))
+    Af = rng.integers(-1, 2, size=(M, K)).astype(np.float32)
+    wts = synth.int4_weights(N, K, G, seed=105)
+    wts.s[:] = np.float16(0.5).view(np.uint16)
+    p = Int4Problem(M, N, K, G, A_bits=Af.astype(np.float16).view(np.uint16), wts=wts).pack()
+    out = p.run()
+    torch.cuda.synchronize()
+    ref = p.ref()
+    assert np.array_equal(out_to_f64(out), ref)
+
+
+@pytest.mark.parametrize("case", synth.DECODE, ids=lambda c: f"M{c.M}_N{c.N}_K{c.K}")
+def test_decode_configs(case):
+    p = Int4Problem(case.M, case.N, case.K, case.G, seed=synth.seed_for(1, synth.DECODE.index(case))).pack()
+    out = p.run()
+    torch.cuda.synchronize()
+    check_close(out_to_f64(out), p.ref(), what=f"decode {case}")
+    plan = wq.get_plan(wq.WQ_OP_W4A16, wq.WQ_F16, case.M, case.N, case.K, case.G)
+    assert plan["splits"] > 1          # decode grids are too small to fill the GPU without split-K
+
+
+@pytest.mark.parametrize("M", [1, 3, 4, 15, 16, 17, 64, 100, 128, 129, 300])
+def test_odd_M(M):
+    p = Int4Problem(M, 256, 512, 128, seed=106 + M).pack()
+    out = p.run()
+    torch.cuda.synchronize()
+    check_close(out_to_f64(out), p.ref(), what=f"M={M}")
+
+
+@pytest.mark.parametrize("N,K,G", [(8, 32, 32), (136, 96, 32), (520, 1056, 32), (264, 2304, 256)])
+def test_ragged_shapes(N, K, G):
+    p = Int4Problem(5, N, K, G, seed=107).pack()
+    out = p.run()
+    torch.cuda.synchronize()
+    check_close(out_to_f64(out), p.ref(), what=f"N={N} K={K} G={G}")
+
+
+@pytest.mark.parametrize("case", synth.PREFILL, ids=lambda c: f"G{c.G}")
+def test_prefill_configs_sampled_rows(case):
+    p = Int4Problem(case.M, case.N, case.K, case.G, seed=synth.seed_for(2, synth.PREFILL.index(case))).pack()
+    out = p.run()
+    torch.cuda.synchronize()
+    rows = synth.sample_rows(case.M, 128, seed=108)
+    got = out_to_f64(out)[rows]
+    check_close(got, p.ref(rows=rows), what=f"prefill {case}")
+
+
+def test_prefill_bf16_activations():
+    p = Int4Problem(1024, 1024, 2048, 128, a_dtype="bf16", seed=109).pack()
+    out = p.run()
+    torch.cuda.synchronize()
+    rows = synth.sample_rows(1024, 96, seed=110)
+    check_close(out_to_f64(out)[rows], p.ref(rows=rows), what="prefill bf16")
+
+
+def test_decode_bf16_activations():
+    p = Int4Problem(7, 4096, 4096, 128, a_dtype="bf16", seed=111).pack()
+    out = p.run()
+    torch.cuda.synchronize()
+    check_close(out_to_f64(out), p.ref(), what="decode bf16")
+
+
+def test_split_k_is_deterministic():
+    p = Int4Problem(16, 4096, 11008, 128, seed=112).pack()
+    first = out_bits(p.run())
+    for _ in range(20):
+        assert np.array_equal(out_bits(p.run()), first)
+
+
+def test_output_guard_bands_untouched():
+    M, N, K, G = 9, 512, 1024, 128
+    p = Int4Problem(M, N, K, G, seed=113).pack()
+    pad = 4096
+    buf = torch.full((pad + M * N + pad,), 12345, dtype=torch.int16, device=DEV)
+    out = buf[pad:pad + M * N].view(torch.float16).view(M, N)
+    p.run(out=out)
+    torch.cuda.synchronize()
+    host = buf.cpu()
+    assert bool((host[:pad] == 12345).all()) and bool((host[pad + M * N:] == 12345).all())
+    check_close(out_to_f64(out), p.ref(), what="guarded")
+
+
+def test_empty_M_is_a_noop():
+    p = Int4Problem(1, 256, 256, 128, seed=114).pack()
+    A0 = torch.empty((0, 256), dtype=torch.float16, device=DEV)
+    out = wq.wq_gemm_w4a16(A0, p.wk, p.sk, 256, 256, 128)
+    assert out.shape == (0, 256)
+
+
+def test_workspace_shared_across_shapes():
+    # one workspace serves different decode shapes back to back
+    ws = torch.zeros(64 << 20, dtype=torch.uint8, device=DEV)
+    probs = [Int4Problem(1, 4096, 4096, 128, seed=115).pack(), Int4Problem(16, 11008, 4096, 128, seed=116).pack(),
+             Int4Problem(3, 4096, 11008, 128, seed=117).pack()]
+    for _ in range(2):
+        for p in probs:
+            out = p.run(ws=ws)
+            torch.cuda.synchronize()
+            check_close(out_to_f64(out), p.ref(), what="shared ws")
+    assert int(ws[:16384].count_nonzero()) == 0     # counters left zero
+
+
+def test_device_status_clean_after_gemms():
+    assert wq.wq_device_status() == 0

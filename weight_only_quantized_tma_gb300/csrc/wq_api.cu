@@ -1,0 +1,483 @@
+// wq_api.cu -- the C ABI (include/wq.h): argument validation, launch planning,
+// tensor-map encoding and kernel launches.  Host code only, apart from the
+// per-device status word.
+#include <cuda.h>
+#include <cudaTypedefs.h>
+#include <cuda_runtime.h>
+
+#include <atomic>
+#include <cstdint>
+#include <cstring>
+#include <mutex>
+
+#include "../../include/wq.h"
+#include "wq_internal.h"
+
+namespace wq {
+
+// One status word per device (bounded-wait timeouts, see include/wq.h).
+__device__ uint32_t g_device_status;
+
+namespace {
+
+constexpr int kMaxDevices = 64;
+constexpr long long kTimeoutNs = 2000000000LL;  // 2 s bound on every barrier wait
+
+struct DeviceInfo {
+    std::once_flag once;
+    bool supported = false;
+    int sms = 0;
+    uint32_t* status = nullptr;
+    cudaError_t err = cudaSuccess;
+};
+DeviceInfo g_dev[kMaxDevices];
+
+wq_status device_info(DeviceInfo** out) {
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess) return WQ_ERR_CUDA;
+    if (dev < 0 || dev >= kMaxDevices) return WQ_ERR_UNSUPPORTED_DEVICE;
+    DeviceInfo& d = g_dev[dev];
+    std::call_once(d.once, [&]() {
+        int major = 0, minor = 0;
+        d.err = cudaDeviceGetAttribute(&major, cudaDevAttrComputeCapabilityMajor, dev);
+        if (d.err == cudaSuccess) d.err = cudaDeviceGetAttribute(&minor, cudaDevAttrComputeCapabilityMinor, dev);
+        if (d.err == cudaSuccess) d.err = cudaDeviceGetAttribute(&d.sms, cudaDevAttrMultiProcessorCount, dev);
+        d.supported = (d.err == cudaSuccess) && major == 10 && minor == 3;
+        if (d.supported) {
+            void* p = nullptr;
+            d.err = cudaGetSymbolAddress(&p, g_device_status);
+            d.status = static_cast<uint32_t*>(p);
+            if (d.err != cudaSuccess) d.supported = false;
+        }
+    });
+    if (d.err != cudaSuccess) return WQ_ERR_CUDA;
+    if (!d.supported) return WQ_ERR_UNSUPPORTED_DEVICE;
+    *out = &d;
+    return WQ_OK;
+}
+
+bool aligned(const void* p, uintptr_t a) { return (reinterpret_cast<uintptr_t>(p) % a) == 0; }
+
+bool valid_group(int32_t G) { return G == 32 || G == 64 || G == 128 || G == 256; }
+
+// ------------------------------------------------------------------ tensor maps
+
+PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
+    static std::once_flag once;
+    static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+    std::call_once(once, []() {
+        cudaDriverEntryPointQueryResult q;
+        void* f = nullptr;
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &f, 12000, cudaEnableDefault, &q) ==
+                cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(f);
+    });
+    return fn;
+}
+
+bool encode_2d(CUtensorMap* m, CUtensorMapDataType dt, const void* base, uint64_t inner, uint64_t outer,
+               uint64_t row_bytes, uint32_t box_inner, uint32_t box_outer, CUtensorMapSwizzle swz) {
+    auto fn = encode_fn();
+    if (!fn) return false;
+    cuuint64_t dims[2] = {inner, outer};
+    cuuint64_t strides[1] = {row_bytes};
+    cuuint32_t box[2] = {box_inner, box_outer};
+    cuuint32_t es[2] = {1, 1};
+    CUresult r = fn(m, dt, 2, const_cast<void*>(base), dims, strides, box, es, CU_TENSOR_MAP_INTERLEAVE_NONE, swz,
+                    CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    return r == CUDA_SUCCESS;
+}
+
+CUtensorMapSwizzle swizzle_for_pitch(int pitch_bytes) {
+    switch (pitch_bytes) {
+        case 128: return CU_TENSOR_MAP_SWIZZLE_128B;
+        case 64: return CU_TENSOR_MAP_SWIZZLE_64B;
+        default: return CU_TENSOR_MAP_SWIZZLE_32B;
+    }
+}
+
+// ------------------------------------------------------------------ planning
+
+struct Plan {
+    KernelConfig cfg;
+    int tiles_n, tiles_m, nkb, splits, n_items, grid, walk_n_fast;
+    size_t ws_bytes;
+};
+
+bool get_config(int fmt, bool bf16, int bn, bool query, KernelConfig* cfg) {
+    switch (fmt) {
+        case FMT_INT4: return config_int4(bf16, bn, query, cfg);
+        case FMT_FP8: return config_fp8(bf16, bn, query, cfg);
+        case FMT_FP4: return config_fp4(bf16, bn, query, cfg);
+    }
+    return false;
+}
+
+// Split-K workspace: a fixed region of arrival counters (8 per output tile, room
+// for kMaxSplitTiles tiles) followed by the fp32 partials.  Keeping the counters
+// at a fixed place lets calls of different shapes share one workspace: every
+// call leaves the counters zero again.
+constexpr int kMaxSplitTiles = 512;
+constexpr size_t kCounterBytes = (size_t)kMaxSplitTiles * 8 * sizeof(uint32_t);
+
+size_t split_ws_bytes(int tiles, int splits, int bn) {
+    if (splits <= 1) return 0;
+    return kCounterBytes + (size_t)tiles * splits * bn * TILE_N * sizeof(float);
+}
+
+// Deterministic in (fmt, dtype, M, N, K) and the device's SM count.
+//  * token tile BN: the smallest compiled tile that covers M (16, 64, 128), 256
+//    for larger M;
+//  * split-K when the output tiles cannot occupy every CTA slot of the GPU
+//    (decode): slices = slots / tiles, each slice at least two k-blocks, at most
+//    16 -- the motivation is the "fused split-K fix-up for grids that do not fill
+//    the SMs" of "FlashInfer W8A16 GEMM (mm_bf16_fp8) analysis", §1;
+//  * tile walk order ("FlashInfer W8A16 GEMM (mm_bf16_fp8) analysis", §4): when
+//    the weight is the smaller operand, walk weight-row tiles fastest so the
+//    activation panel being reused stays in L2, else walk token tiles fastest.
+wq_status make_plan(int fmt, bool bf16, int64_t M, int64_t N, int64_t K, int sms, int w_bits, Plan* plan) {
+    static const int kTiles[4] = {16, 64, 128, 256};
+    KernelConfig cfg{};
+    bool found = false;
+    for (int i = 0; i < 4 && !found; ++i) {
+        if (M <= kTiles[i] || i == 3) found = get_config(fmt, bf16, kTiles[i], sms > 0, &cfg);
+    }
+    for (int i = 3; i >= 0 && !found; --i) found = get_config(fmt, bf16, kTiles[i], sms > 0, &cfg);
+    if (!found) return WQ_ERR_DTYPE;
+    Plan p{};
+    p.cfg = cfg;
+    p.tiles_n = (int)((N + TILE_N - 1) / TILE_N);
+    p.tiles_m = (int)((M + cfg.bn - 1) / cfg.bn);
+    p.nkb = (int)((K + cfg.bk - 1) / cfg.bk);
+    const long long tiles = (long long)p.tiles_n * p.tiles_m;
+    const int slots = (sms > 0 ? sms : 148) * (cfg.ctas_per_sm > 0 ? cfg.ctas_per_sm : 1);
+    int splits = 1;
+    if (tiles < slots && tiles <= kMaxSplitTiles) {
+        splits = (int)(slots / tiles);
+        const int max_by_k = p.nkb / 2 > 1 ? p.nkb / 2 : 1;
+        if (splits > max_by_k) splits = max_by_k;
+        if (splits > 16) splits = 16;
+        if (splits < 1) splits = 1;
+    }
+    p.splits = splits;
+    const long long items = tiles * splits;
+    if (items >= (1LL << 31)) return WQ_ERR_SHAPE;
+    p.n_items = (int)items;
+    p.grid = (int)(items < slots ? items : slots);
+    const double w_bytes = (double)N * (double)K * w_bits / 8.0;
+    const double a_bytes = (double)M * (double)K * 2.0;
+    p.walk_n_fast = w_bytes < a_bytes ? 1 : 0;
+    p.ws_bytes = split_ws_bytes((int)tiles, splits, cfg.bn);
+    *plan = p;
+    return WQ_OK;
+}
+
+int w_bits_of(int fmt) { return fmt == FMT_INT4 ? 4 : fmt == FMT_FP8 ? 8 : 4; }
+
+wq_status plan_for(int fmt, bool bf16, int64_t M, int64_t N, int64_t K, Plan* plan) {
+    DeviceInfo* d = nullptr;
+    wq_status st = device_info(&d);
+    if (st != WQ_OK) return st;
+    return make_plan(fmt, bf16, M, N, K, d->sms, w_bits_of(fmt), plan);
+}
+
+void fill_common(GemmParams& gp, const Plan& pl, int64_t M, int64_t N, int64_t K, void* out, void* ws,
+                 uint32_t* status) {
+    gp.out = out;
+    gp.M = (int)M;
+    gp.N = (int)N;
+    gp.K = (int)K;
+    gp.tiles_n = pl.tiles_n;
+    gp.tiles_m = pl.tiles_m;
+    gp.splits = pl.splits;
+    gp.nkb = pl.nkb;
+    gp.n_items = pl.n_items;
+    gp.walk_n_fast = pl.walk_n_fast;
+    gp.w_evict_first = pl.tiles_m == 1 ? 1 : 0;
+    gp.div_walk = make_fastdiv(pl.walk_n_fast ? pl.tiles_n : pl.tiles_m, (uint32_t)(pl.n_items / pl.splits));
+    gp.div_splits = make_fastdiv(pl.splits, (uint32_t)pl.n_items);
+    gp.status = status;
+    gp.timeout_ns = kTimeoutNs;
+    if (pl.splits > 1) {
+        gp.ws_count = static_cast<uint32_t*>(ws);
+        gp.ws_part = reinterpret_cast<float*>(static_cast<uint8_t*>(ws) + kCounterBytes);
+    }
+}
+
+wq_status check_ws(const Plan& pl, const void* ws, size_t ws_bytes) {
+    if (pl.ws_bytes == 0) return WQ_OK;
+    if (ws == nullptr || ws_bytes < pl.ws_bytes) return WQ_ERR_WORKSPACE;
+    if (!aligned(ws, 16)) return WQ_ERR_MISALIGNED;
+    return WQ_OK;
+}
+
+bool encode_a(GemmParams& gp, const void* A, bool bf16, int64_t M, int64_t K, int bn) {
+    return encode_2d(&gp.tmap_a, bf16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT16, A,
+                     (uint64_t)K, (uint64_t)M, (uint64_t)K * 2, 64, (uint32_t)bn, CU_TENSOR_MAP_SWIZZLE_128B);
+}
+
+wq_status finish_launch(cudaError_t e) { return e == cudaSuccess ? WQ_OK : WQ_ERR_CUDA; }
+
+const int64_t kMaxDim = (1LL << 31) - 1;
+
+}  // namespace
+}  // namespace wq
+
+using namespace wq;
+
+extern "C" {
+
+const char* wq_status_string(wq_status s) {
+    switch (s) {
+        case WQ_OK: return "WQ_OK";
+        case WQ_ERR_NULL: return "WQ_ERR_NULL: a required pointer is NULL";
+        case WQ_ERR_SHAPE: return "WQ_ERR_SHAPE: unsupported problem shape";
+        case WQ_ERR_GROUP: return "WQ_ERR_GROUP: group size must be 32, 64, 128 or 256 and divide K";
+        case WQ_ERR_MISALIGNED: return "WQ_ERR_MISALIGNED: pointer misses its required alignment";
+        case WQ_ERR_DTYPE: return "WQ_ERR_DTYPE: activation dtype not supported by this op";
+        case WQ_ERR_WORKSPACE: return "WQ_ERR_WORKSPACE: workspace missing or too small";
+        case WQ_ERR_UNSUPPORTED_DEVICE: return "WQ_ERR_UNSUPPORTED_DEVICE: requires compute capability 10.3";
+        case WQ_ERR_CUDA: return "WQ_ERR_CUDA: CUDA runtime error";
+        case WQ_ERR_TIMEOUT: return "WQ_ERR_TIMEOUT: a kernel gave up on a bounded wait";
+    }
+    return "unknown wq_status";
+}
+
+wq_status wq_int4_packed_bytes(int64_t N, int64_t K, int32_t G, size_t* w_bytes, size_t* s_bytes) {
+    if (N <= 0 || K <= 0 || N > kMaxDim || K > kMaxDim || K % 32 != 0) return WQ_ERR_SHAPE;
+    if (!valid_group(G) || K % G != 0) return WQ_ERR_GROUP;
+    const int64_t Np = round_up(N, TILE_N), Kp = round_up(K, KPAD_INT4);
+    if (w_bytes) *w_bytes = (size_t)(Np * Kp / 2);
+    if (s_bytes) *s_bytes = (size_t)(Np * (Kp / G) * 2);
+    return WQ_OK;
+}
+
+static wq_status check_pack_args(const void* a, const void* b, const void* c, const void* d, int64_t N, int64_t K,
+                                 int32_t G) {
+    if (!a || !b || !c || !d) return WQ_ERR_NULL;
+    return wq_int4_packed_bytes(N, K, G, nullptr, nullptr);
+}
+
+wq_status wq_pack_int4(const uint8_t* w_canon, const void* s_canon, int64_t N, int64_t K, int32_t G,
+                       uint8_t* w_kernel, void* s_kernel, wq_stream_t stream) {
+    wq_status st = check_pack_args(w_canon, s_canon, w_kernel, s_kernel, N, K, G);
+    if (st != WQ_OK) return st;
+    if (!aligned(w_kernel, 16) || !aligned(s_kernel, 16) || !aligned(s_canon, 2)) return WQ_ERR_MISALIGNED;
+    DeviceInfo* d = nullptr;
+    if ((st = device_info(&d)) != WQ_OK) return st;
+    return finish_launch(launch_pack_int4(w_canon, static_cast<const uint16_t*>(s_canon), N, K, G, w_kernel,
+                                          static_cast<uint16_t*>(s_kernel), (cudaStream_t)stream));
+}
+
+wq_status wq_unpack_int4(const uint8_t* w_kernel, const void* s_kernel, int64_t N, int64_t K, int32_t G,
+                         uint8_t* w_canon, void* s_canon, wq_stream_t stream) {
+    wq_status st = check_pack_args(w_kernel, s_kernel, w_canon, s_canon, N, K, G);
+    if (st != WQ_OK) return st;
+    if (!aligned(w_kernel, 16) || !aligned(s_kernel, 16) || !aligned(s_canon, 2)) return WQ_ERR_MISALIGNED;
+    DeviceInfo* d = nullptr;
+    if ((st = device_info(&d)) != WQ_OK) return st;
+    return finish_launch(launch_unpack_int4(w_kernel, static_cast<const uint16_t*>(s_kernel), N, K, G, w_canon,
+                                            static_cast<uint16_t*>(s_canon), (cudaStream_t)stream));
+}
+
+wq_status wq_debug_dequant_int4(const uint8_t* w_kernel, const void* s_kernel, int64_t N, int64_t K, int32_t G,
+                                float* w_f32, wq_stream_t stream) {
+    wq_status st = check_pack_args(w_kernel, s_kernel, w_f32, w_f32, N, K, G);
+    if (st != WQ_OK) return st;
+    if (!aligned(w_kernel, 16) || !aligned(s_kernel, 16) || !aligned(w_f32, 4)) return WQ_ERR_MISALIGNED;
+    DeviceInfo* d = nullptr;
+    if ((st = device_info(&d)) != WQ_OK) return st;
+    return finish_launch(launch_dequant_int4(w_kernel, static_cast<const uint16_t*>(s_kernel), N, K, G, w_f32,
+                                             (cudaStream_t)stream));
+}
+
+wq_status wq_fp4_packed_sf_bytes(int64_t N, int64_t K, size_t* sf_bytes) {
+    if (N <= 0 || K <= 0 || N > kMaxDim || K > kMaxDim || K % 32 != 0) return WQ_ERR_SHAPE;
+    if (sf_bytes) *sf_bytes = (size_t)(round_up(N, TILE_N) * (round_up(K, KPAD_FP4SF) / 64) * 4);
+    return WQ_OK;
+}
+
+wq_status wq_pack_fp4_sf(const uint8_t* sf_canon, int64_t N, int64_t K, uint8_t* sf_kernel, wq_stream_t stream) {
+    if (!sf_canon || !sf_kernel) return WQ_ERR_NULL;
+    wq_status st = wq_fp4_packed_sf_bytes(N, K, nullptr);
+    if (st != WQ_OK) return st;
+    if (!aligned(sf_kernel, 16)) return WQ_ERR_MISALIGNED;
+    DeviceInfo* d = nullptr;
+    if ((st = device_info(&d)) != WQ_OK) return st;
+    return finish_launch(launch_pack_fp4_sf(sf_canon, N, K, sf_kernel, (cudaStream_t)stream));
+}
+
+wq_status wq_debug_dequant_fp4(const uint8_t* w_e2m1, const uint8_t* sf_kernel, int64_t N, int64_t K, float* w_f32,
+                               wq_stream_t stream) {
+    if (!w_e2m1 || !sf_kernel || !w_f32) return WQ_ERR_NULL;
+    wq_status st = wq_fp4_packed_sf_bytes(N, K, nullptr);
+    if (st != WQ_OK) return st;
+    if (!aligned(sf_kernel, 16) || !aligned(w_f32, 4)) return WQ_ERR_MISALIGNED;
+    DeviceInfo* d = nullptr;
+    if ((st = device_info(&d)) != WQ_OK) return st;
+    return finish_launch(launch_dequant_fp4(w_e2m1, sf_kernel, N, K, w_f32, (cudaStream_t)stream));
+}
+
+wq_status wq_debug_dequant_fp8(const uint8_t* w_e4m3, int64_t N, int64_t K, wq_dtype operand, float* w_f32,
+                               wq_stream_t stream) {
+    if (!w_e4m3 || !w_f32) return WQ_ERR_NULL;
+    if (N <= 0 || K <= 0 || N > kMaxDim || K > kMaxDim || K % 16 != 0) return WQ_ERR_SHAPE;
+    if (operand != WQ_F16 && operand != WQ_BF16) return WQ_ERR_DTYPE;
+    if (!aligned(w_f32, 4)) return WQ_ERR_MISALIGNED;
+    DeviceInfo* d = nullptr;
+    wq_status st = device_info(&d);
+    if (st != WQ_OK) return st;
+    return finish_launch(launch_dequant_fp8(w_e4m3, N, K, operand == WQ_BF16, w_f32, (cudaStream_t)stream));
+}
+
+wq_status wq_get_plan(wq_op op, wq_dtype a_dtype, int64_t M, int64_t N, int64_t K, int32_t G, wq_plan* plan,
+                      size_t* ws_bytes) {
+    if (M < 0 || N <= 0 || K <= 0 || M > kMaxDim || N > kMaxDim || K > kMaxDim) return WQ_ERR_SHAPE;
+    if (op != WQ_OP_W4A16 && op != WQ_OP_FP8 && op != WQ_OP_FP4) return WQ_ERR_SHAPE;
+    if (op == WQ_OP_W4A16 && (!valid_group(G) || K % G != 0)) return WQ_ERR_GROUP;
+    if (a_dtype != WQ_F16 && a_dtype != WQ_BF16) return WQ_ERR_DTYPE;
+    const bool bf16 = (op == WQ_OP_FP4) ? true : (a_dtype == WQ_BF16);
+    Plan pl{};
+    wq_status st = plan_for((int)op, bf16, M > 0 ? M : 1, N, K, &pl);
+    if (st != WQ_OK) return st;
+    if (plan) {
+        plan->bn = pl.cfg.bn;
+        plan->bk = pl.cfg.bk;
+        plan->stages = pl.cfg.stages;
+        plan->splits = pl.splits;
+        plan->grid = pl.grid;
+        plan->threads = pl.cfg.threads;
+        plan->smem_bytes = pl.cfg.smem_bytes;
+        plan->n_items = pl.n_items;
+        plan->walk_n_fast = pl.walk_n_fast;
+        plan->tiles_n = pl.tiles_n;
+        plan->tiles_m = pl.tiles_m;
+    }
+    if (ws_bytes) *ws_bytes = (M == 0) ? 0 : pl.ws_bytes;
+    return WQ_OK;
+}
+
+wq_status wq_workspace_bytes(wq_op op, wq_dtype a_dtype, int64_t M, int64_t N, int64_t K, int32_t G, size_t* bytes) {
+    if (!bytes) return WQ_ERR_NULL;
+    return wq_get_plan(op, a_dtype, M, N, K, G, nullptr, bytes);
+}
+
+wq_status wq_gemm_w4a16(const void* A, wq_dtype a_dtype, const uint8_t* w_kernel, const void* s_kernel, int64_t M,
+                        int64_t N, int64_t K, int32_t G, void* out, void* ws, size_t ws_bytes, wq_stream_t stream) {
+    if (!A || !w_kernel || !s_kernel || !out) return WQ_ERR_NULL;
+    if (M < 0 || N <= 0 || K <= 0 || M > kMaxDim || N > kMaxDim || K > kMaxDim) return WQ_ERR_SHAPE;
+    if (K % 32 != 0 || N % 8 != 0) return WQ_ERR_SHAPE;
+    if (!valid_group(G) || K % G != 0) return WQ_ERR_GROUP;
+    if (a_dtype != WQ_F16 && a_dtype != WQ_BF16) return WQ_ERR_DTYPE;
+    if (!aligned(A, 16) || !aligned(w_kernel, 16) || !aligned(s_kernel, 16) || !aligned(out, 16))
+        return WQ_ERR_MISALIGNED;
+    DeviceInfo* d = nullptr;
+    wq_status st = device_info(&d);
+    if (st != WQ_OK) return st;
+    if (M == 0) return WQ_OK;
+    const bool bf16 = a_dtype == WQ_BF16;
+    Plan pl{};
+    if ((st = make_plan(FMT_INT4, bf16, M, N, K, d->sms, 4, &pl)) != WQ_OK) return st;
+    if ((st = check_ws(pl, ws, ws_bytes)) != WQ_OK) return st;
+    GemmParams gp;
+    std::memset(&gp, 0, sizeof(gp));
+    if (!encode_a(gp, A, bf16, M, K, pl.cfg.bn)) return WQ_ERR_CUDA;
+    gp.w = w_kernel;
+    gp.sc = static_cast<const uint8_t*>(s_kernel);
+    gp.G = G;
+    const int64_t Kp = round_up(K, KPAD_INT4);
+    gp.ngroups_pad = (int)(Kp / G);
+    gp.nchunks_pad = (int)(Kp / 32);
+    fill_common(gp, pl, M, N, K, out, ws, d->status);
+    return finish_launch(launch_gemm_int4(gp, bf16, pl.cfg.bn, pl.grid, (cudaStream_t)stream));
+}
+
+wq_status wq_gemm_w8a16_fp8(const void* A, wq_dtype a_dtype, const uint8_t* w_e4m3, const float* alpha,
+                            const void* bias, int64_t M, int64_t N, int64_t K, void* out, void* ws, size_t ws_bytes,
+                            wq_stream_t stream) {
+    if (!A || !w_e4m3 || !alpha || !out) return WQ_ERR_NULL;
+    if (M < 0 || N <= 0 || K <= 0 || M > kMaxDim || N > kMaxDim || K > kMaxDim) return WQ_ERR_SHAPE;
+    if (K % 16 != 0 || N % 8 != 0) return WQ_ERR_SHAPE;
+    if (a_dtype != WQ_F16 && a_dtype != WQ_BF16) return WQ_ERR_DTYPE;
+    if (!aligned(A, 16) || !aligned(w_e4m3, 16) || !aligned(out, 16) || !aligned(alpha, 4) ||
+        (bias && !aligned(bias, 2)))
+        return WQ_ERR_MISALIGNED;
+    DeviceInfo* d = nullptr;
+    wq_status st = device_info(&d);
+    if (st != WQ_OK) return st;
+    if (M == 0) return WQ_OK;
+    const bool bf16 = a_dtype == WQ_BF16;
+    Plan pl{};
+    if ((st = make_plan(FMT_FP8, bf16, M, N, K, d->sms, 8, &pl)) != WQ_OK) return st;
+    if ((st = check_ws(pl, ws, ws_bytes)) != WQ_OK) return st;
+    GemmParams gp;
+    std::memset(&gp, 0, sizeof(gp));
+    if (!encode_a(gp, A, bf16, M, K, pl.cfg.bn)) return WQ_ERR_CUDA;
+    const int bk = pl.cfg.bk;
+    if (!encode_2d(&gp.tmap_w, CU_TENSOR_MAP_DATA_TYPE_UINT8, w_e4m3, (uint64_t)K, (uint64_t)N, (uint64_t)K,
+                   (uint32_t)bk, TILE_N, swizzle_for_pitch(bk)))
+        return WQ_ERR_CUDA;
+    gp.alpha = alpha;
+    gp.bias = bias;
+    fill_common(gp, pl, M, N, K, out, ws, d->status);
+    return finish_launch(launch_gemm_fp8(gp, bf16, pl.cfg.bn, pl.grid, (cudaStream_t)stream));
+}
+
+wq_status wq_gemm_bf16_fp4(const void* A, const uint8_t* w_e2m1, const uint8_t* sf_kernel, const float* alpha,
+                           int64_t M, int64_t N, int64_t K, void* out, void* ws, size_t ws_bytes,
+                           wq_stream_t stream) {
+    if (!A || !w_e2m1 || !sf_kernel || !alpha || !out) return WQ_ERR_NULL;
+    if (M < 0 || N <= 0 || K <= 0 || M > kMaxDim || N > kMaxDim || K > kMaxDim) return WQ_ERR_SHAPE;
+    if (K % 32 != 0 || N % 8 != 0) return WQ_ERR_SHAPE;
+    if (!aligned(A, 16) || !aligned(w_e2m1, 16) || !aligned(sf_kernel, 16) || !aligned(out, 16) ||
+        !aligned(alpha, 4))
+        return WQ_ERR_MISALIGNED;
+    DeviceInfo* d = nullptr;
+    wq_status st = device_info(&d);
+    if (st != WQ_OK) return st;
+    if (M == 0) return WQ_OK;
+    Plan pl{};
+    if ((st = make_plan(FMT_FP4, true, M, N, K, d->sms, 4, &pl)) != WQ_OK) return st;
+    if ((st = check_ws(pl, ws, ws_bytes)) != WQ_OK) return st;
+    GemmParams gp;
+    std::memset(&gp, 0, sizeof(gp));
+    if (!encode_a(gp, A, true, M, K, pl.cfg.bn)) return WQ_ERR_CUDA;
+    const int pitch = pl.cfg.bk / 2;
+    if (!encode_2d(&gp.tmap_w, CU_TENSOR_MAP_DATA_TYPE_UINT8, w_e2m1, (uint64_t)(K / 2), (uint64_t)N,
+                   (uint64_t)(K / 2), (uint32_t)pitch, TILE_N, swizzle_for_pitch(pitch)))
+        return WQ_ERR_CUDA;
+    gp.sc = sf_kernel;
+    gp.alpha = alpha;
+    gp.nchunks_pad = (int)(round_up(K, KPAD_FP4SF) / 64);
+    fill_common(gp, pl, M, N, K, out, ws, d->status);
+    return finish_launch(launch_gemm_fp4(gp, true, pl.cfg.bn, pl.grid, (cudaStream_t)stream));
+}
+
+wq_status wq_device_status(uint32_t* bits) {
+    if (!bits) return WQ_ERR_NULL;
+    DeviceInfo* d = nullptr;
+    wq_status st = device_info(&d);
+    if (st != WQ_OK) return st;
+    if (cudaMemcpy(bits, d->status, sizeof(uint32_t), cudaMemcpyDeviceToHost) != cudaSuccess) return WQ_ERR_CUDA;
+    return *bits ? WQ_ERR_TIMEOUT : WQ_OK;
+}
+
+wq_status wq_clear_device_status(void) {
+    DeviceInfo* d = nullptr;
+    wq_status st = device_info(&d);
+    if (st != WQ_OK) return st;
+    return cudaMemset(d->status, 0, sizeof(uint32_t)) == cudaSuccess && cudaDeviceSynchronize() == cudaSuccess
+               ? WQ_OK
+               : WQ_ERR_CUDA;
+}
+
+wq_status wq_debug_wait_probe(int64_t timeout_ns, wq_stream_t stream) {
+    if (timeout_ns <= 0 || timeout_ns > 10000000000LL) return WQ_ERR_SHAPE;
+    DeviceInfo* d = nullptr;
+    wq_status st = device_info(&d);
+    if (st != WQ_OK) return st;
+    return finish_launch(launch_wait_probe(d->status, (long long)timeout_ns, (cudaStream_t)stream));
+}
+
+}  // extern "C"

@@ -1,0 +1,607 @@
+// wq_gemm.cuh -- the weight-only quantized GEMM kernel for sm_103a.
+//
+//   out[m, n] = alpha * sum_k A[m, k] * dequant(W)[n, k]   (+ bias[n] for FP8)
+//
+// Orientation: dequantized weight rows are the tcgen05 A operand (MMA M = 128
+// weight rows per CTA tile), activation rows (tokens) are the B operand (MMA N =
+// BN tokens).  A lives in tensor memory: the transform warpgroup writes it there
+// with tcgen05.st, so the 16-bit weight copy never touches shared memory or HBM.
+// ("FlashInfer W8A16 GEMM (mm_bf16_fp8) analysis", §1: on sm_100a/sm_103a a
+// dedicated transform warpgroup converts the weights into TMEM.)
+//
+// Warp roles (128 * (1 + NWG) threads):
+//   warp 0      TMA producer: packed weight tile, its scales, activation tile per
+//               k-block, through a STAGES-deep mbarrier ring;
+//   warp 1      MMA issuer: tcgen05.mma kind::f16, accumulator in TMEM, commits
+//               free the shared-memory stage and the TMEM operand stage;
+//   warp 2      TMEM allocator;
+//   warps 4..   transform: unpack / decode + scale into 16-bit operands, then the
+//               epilogue (TMEM -> registers -> alpha/bias -> 16-bit -> global),
+//               including the deterministic split-K reduction.
+//
+// Dequantization per format (all exact until the final rounding to the operand
+// type, see the conversion helpers below):
+//   INT4  w = RN((q - 8) * s[k / G, n])           ("Low Bit Triton Kernels", §03)
+//   FP8   w = e4m3(code)       (scale on the fp32 accumulator, PR #7495 intro)
+//   FP4   w = e2m1(code) * e4m3(sf[n, k / 16])    (alpha on the accumulator, PR #4466 §2)
+//
+// Every barrier wait is bounded; on a timeout the kernel records a status bit,
+// stops issuing work, waits (bounded) for its own copies and MMAs in flight,
+// releases its tensor memory and returns.
+#pragma once
+
+#include <cstdint>
+#include <cuda_bf16.h>
+#include <cuda_fp16.h>
+
+#include "sm103_ptx.cuh"
+#include "wq_internal.h"
+
+namespace wq {
+
+template <int FMT, bool BF16, int BN, int BK, int STAGES, int NWG>
+struct GemmCfg {
+    static constexpr int NT = 128 * (1 + NWG);
+    static constexpr int B_STAGE = BN * BK * 2;                       // activation tile bytes
+    static constexpr int W_STAGE = (FMT == FMT_FP8) ? TILE_N * BK : TILE_N * BK / 2;
+    static constexpr int SC_STAGE = (FMT == FMT_INT4) ? (BK / 32) * TILE_N * 2
+                                  : (FMT == FMT_FP4)  ? TILE_N * BK / 16 : 0;
+    static constexpr int TMEM_COLS = (BN <= 128) ? 256 : 512;
+    static constexpr int A_BASE = (BN < 64) ? 64 : BN;                // first TMEM column of operand stages
+    static constexpr int A_COLS = BK / 2;                             // 16-bit operand: 2 per column
+    static constexpr int A_ST_RAW = (TMEM_COLS - A_BASE) / A_COLS;
+    static constexpr int A_ST = A_ST_RAW > 4 ? 4 : A_ST_RAW;          // TMEM operand stages
+    // shared memory carve-up (offsets from a 1024-aligned base)
+    static constexpr int OFF_B = 0;
+    static constexpr int OFF_W = OFF_B + STAGES * B_STAGE;
+    static constexpr int OFF_SC = OFF_W + STAGES * W_STAGE;
+    static constexpr int OFF_BAR = (OFF_SC + STAGES * SC_STAGE + 127) / 128 * 128;
+    static constexpr int NBARS = 2 * STAGES + 2 * A_ST + 3;
+    static constexpr int OFF_MISC = OFF_BAR + NBARS * 8;
+    static constexpr int SMEM_USED = OFF_MISC + 16;
+    static constexpr int SMEM_BYTES = SMEM_USED + 1024;               // alignment slack
+    // FP8 / FP4 weight tiles arrive through TMA with a row pitch of W_PITCH bytes
+    // and the matching swizzle; the XOR mask applies to 16-byte chunk indices.
+    static constexpr int W_PITCH = W_STAGE / TILE_N;
+    static constexpr uint32_t W_SWZ = (W_PITCH == 128) ? 7u : (W_PITCH == 64) ? 3u : 1u;
+    // two CTAs per SM when shared and tensor memory allow it (decode, split-K)
+    static constexpr int MIN_BLOCKS = (2 * (SMEM_BYTES + 1024) <= 228 * 1024 && TMEM_COLS <= 256) ? 2 : 1;
+    static_assert(BK == 64 || BK == 128, "BK");
+    static_assert(BN % 16 == 0 && BN >= 16 && BN <= 256, "BN");
+    static_assert(A_ST >= 2, "need at least two TMEM operand stages");
+    static_assert(SMEM_BYTES <= 227 * 1024, "shared memory");
+    static_assert(B_STAGE % 1024 == 0 && W_STAGE % 1024 == 0, "1024-byte stage alignment");
+};
+
+// Physical byte offset of a logical offset inside a TMA-swizzled tile whose base
+// is 1024-byte aligned (16-byte chunk index XOR the 128-byte row index bits).
+__device__ __forceinline__ uint32_t swz(uint32_t a, uint32_t mask) { return a ^ (((a >> 7) & mask) << 4); }
+
+// Bounded wait on an mbarrier phase, executed by every lane that calls it.
+// Returns false if the CTA is aborting or the wait timed out (which starts the abort).
+__device__ __forceinline__ bool bounded_wait(uint32_t bar, uint32_t parity, volatile uint32_t* abort_flag,
+                                             uint32_t* status, uint32_t code, long long timeout_ns) {
+    if (ptx::mbar_try_wait(bar, parity)) return true;
+    const uint64_t t0 = ptx::globaltimer();
+    while (true) {
+        if (ptx::mbar_try_wait(bar, parity)) return true;
+        if (*abort_flag) return false;
+        if ((long long)(ptx::globaltimer() - t0) > timeout_ns) {
+            *abort_flag = 1u;
+            atomicOr(status, code);
+            return false;
+        }
+    }
+}
+
+// Wait used while draining after an abort: ignores the abort flag.
+__device__ __forceinline__ bool drain_wait(uint32_t bar, uint32_t parity, long long timeout_ns) {
+    const uint64_t t0 = ptx::globaltimer();
+    while (!ptx::mbar_try_wait(bar, parity)) {
+        if ((long long)(ptx::globaltimer() - t0) > timeout_ns) return false;
+    }
+    return true;
+}
+
+// ---------------------------------------------------------------- conversions
+
+// INT4 -> f16 operands for one 16-byte chunk of the prepacked layout (32 codes of
+// one weight row).  Word j holds k = 8j..8j+7 of the chunk: the even k in its low
+// half-word (nibble i at bits 4i), the odd k in its high half-word.  The fp16
+// "magic number" trick turns a nibble into 1024 + q (nibble at bits 0-3, exponent
+// 2^10) or 64 + q (nibble at bits 4-7, exponent 2^6, where the mantissa unit is
+// 1/16); subtracting 1032 or 72 gives q - 8 exactly, and one multiply by the
+// group scale rounds once: RN16((q - 8) * s).  Output o[4j + i] holds the pair
+// (k = 8j + 2i, 8j + 2i + 1), low half first.
+__device__ __forceinline__ void int4_to_f16(const uint4& q, uint32_t s2, uint32_t (&o)[16]) {
+    const uint32_t wv[4] = {q.x, q.y, q.z, q.w};
+#pragma unroll
+    for (int j = 0; j < 4; ++j) {
+        const uint32_t x = wv[j];
+        const uint32_t x8 = x >> 8;
+        o[4 * j + 0] = ptx::hmul2_u32(ptx::hsub2_u32(ptx::lop3_and_or(x, 0x000F000Fu, 0x64006400u), 0x64086408u), s2);
+        o[4 * j + 1] = ptx::hmul2_u32(ptx::hsub2_u32(ptx::lop3_and_or(x, 0x00F000F0u, 0x54005400u), 0x54805480u), s2);
+        o[4 * j + 2] = ptx::hmul2_u32(ptx::hsub2_u32(ptx::lop3_and_or(x8, 0x000F000Fu, 0x64006400u), 0x64086408u), s2);
+        o[4 * j + 3] = ptx::hmul2_u32(ptx::hsub2_u32(ptx::lop3_and_or(x8, 0x00F000F0u, 0x54005400u), 0x54805480u), s2);
+    }
+}
+
+// INT4 -> bf16 operands: (q - 8) is exact in fp32 (2^23 magic), (q - 8) * s is
+// exact in fp32 (4 + 11 significant bits), one rounding to bf16.
+__device__ __forceinline__ void int4_to_bf16(const uint4& q, float s, uint32_t (&o)[16]) {
+    const uint32_t wv[4] = {q.x, q.y, q.z, q.w};
+#pragma unroll
+    for (int j = 0; j < 4; ++j) {
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+            const uint32_t t = (wv[j] >> (4 * i)) & 0x000F000Fu;
+            const float lo = __uint_as_float(0x4B000000u | (t & 0xFu)) - 8388616.0f;
+            const float hi = __uint_as_float(0x4B000000u | (t >> 16)) - 8388616.0f;
+            o[4 * j + i] = ptx::f32x2_to_bf16x2(lo * s, hi * s);
+        }
+    }
+}
+
+// FP8: 16 e4m3 codes (one 16-byte chunk, k ascending) -> 8 operand words.
+template <bool BF16>
+__device__ __forceinline__ void fp8_to_operand(const uint4& q, uint32_t (&o)[8]) {
+    const uint32_t wv[4] = {q.x, q.y, q.z, q.w};
+#pragma unroll
+    for (int j = 0; j < 4; ++j) {
+        uint32_t lo = ptx::e4m3x2_to_f16x2((uint16_t)(wv[j] & 0xFFFFu));
+        uint32_t hi = ptx::e4m3x2_to_f16x2((uint16_t)(wv[j] >> 16));
+        if (BF16) {
+            lo = ptx::f16x2_to_bf16x2_exact(lo);
+            hi = ptx::f16x2_to_bf16x2_exact(hi);
+        }
+        o[2 * j] = lo;
+        o[2 * j + 1] = hi;
+    }
+}
+
+// FP4: 32 e2m1 codes (one 16-byte chunk, byte b holds k = 2b (low nibble) and
+// 2b + 1) times the two e4m3 block scales of the chunk -> 16 bf16x2 words.
+// e2m1 * e4m3 has at most 5 significant bits and stays inside the normal fp16
+// range, so the f16 product and its bf16 copy are exact.
+__device__ __forceinline__ void fp4_to_bf16(const uint4& q, uint16_t sf_pair, uint32_t (&o)[16]) {
+    const uint32_t sf2 = ptx::e4m3x2_to_f16x2(sf_pair);
+    const uint32_t s_lo = __byte_perm(sf2, 0, 0x1010);   // {sf0, sf0}
+    const uint32_t s_hi = __byte_perm(sf2, 0, 0x3232);   // {sf1, sf1}
+    const uint32_t wv[4] = {q.x, q.y, q.z, q.w};
+#pragma unroll
+    for (int j = 0; j < 4; ++j) {
+        uint32_t h[4];
+        ptx::e2m1x8_to_f16x2x4(wv[j], h);
+        const uint32_t s2 = (j < 2) ? s_lo : s_hi;
+#pragma unroll
+        for (int i = 0; i < 4; ++i) o[4 * j + i] = ptx::f16x2_to_bf16x2_exact(ptx::hmul2_u32(h[i], s2));
+    }
+}
+
+template <bool BF16>
+__device__ __forceinline__ void store_out(void* out, size_t idx, float v) {
+    if (BF16)
+        reinterpret_cast<__nv_bfloat16*>(out)[idx] = __float2bfloat16_rn(v);
+    else
+        reinterpret_cast<__half*>(out)[idx] = __float2half_rn(v);
+}
+
+template <bool BF16>
+__device__ __forceinline__ float load_16bit(const void* p, size_t idx) {
+    if (BF16) return __bfloat162float(reinterpret_cast<const __nv_bfloat16*>(p)[idx]);
+    return __half2float(reinterpret_cast<const __half*>(p)[idx]);
+}
+
+struct Item {
+    int n_tile, m_tile, slice, kb_begin, kb_end;
+};
+
+__device__ __forceinline__ Item decode_item(const GemmParams& p, int item) {
+    Item it;
+    const uint32_t t = fastdiv((uint32_t)item, p.div_splits);
+    it.slice = item - (int)t * p.splits;
+    if (p.walk_n_fast) {
+        const uint32_t mt = fastdiv(t, p.div_walk);
+        it.m_tile = (int)mt;
+        it.n_tile = (int)t - (int)mt * p.tiles_n;
+    } else {
+        const uint32_t nt = fastdiv(t, p.div_walk);
+        it.n_tile = (int)nt;
+        it.m_tile = (int)t - (int)nt * p.tiles_m;
+    }
+    it.kb_begin = (int)(((long long)it.slice * p.nkb) / p.splits);
+    it.kb_end = (int)(((long long)(it.slice + 1) * p.nkb) / p.splits);
+    return it;
+}
+
+template <int FMT, bool BF16, int BN, int BK, int STAGES, int NWG>
+__global__ void __launch_bounds__(128 * (1 + NWG), (GemmCfg<FMT, BF16, BN, BK, STAGES, NWG>::MIN_BLOCKS))
+    wq_gemm_kernel(const __grid_constant__ GemmParams p) {
+    using C = GemmCfg<FMT, BF16, BN, BK, STAGES, NWG>;
+    extern __shared__ uint8_t smem_raw[];
+    uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+    const uint32_t sbase = ptx::smem_u32(smem);
+    const uint32_t bar0 = sbase + C::OFF_BAR;
+    auto full_bar = [&](int s) { return bar0 + 8u * s; };
+    auto empty_bar = [&](int s) { return bar0 + 8u * (STAGES + s); };
+    auto afull_bar = [&](int a) { return bar0 + 8u * (2 * STAGES + a); };
+    auto aempty_bar = [&](int a) { return bar0 + 8u * (2 * STAGES + C::A_ST + a); };
+    const uint32_t accfull_bar = bar0 + 8u * (2 * STAGES + 2 * C::A_ST);
+    const uint32_t accempty_bar = accfull_bar + 8u;
+    const uint32_t final_bar = accfull_bar + 16u;
+    uint32_t* misc = reinterpret_cast<uint32_t*>(smem + C::OFF_MISC);
+    volatile uint32_t* tmem_slot = misc + 0;
+    volatile uint32_t* abort_flag = misc + 1;
+
+    const int warp = threadIdx.x >> 5;
+    const int lane = threadIdx.x & 31;
+    const int n_epi = 128 * NWG;
+
+    if (threadIdx.x == 0) {
+        for (int s = 0; s < STAGES; ++s) {
+            ptx::mbar_init(full_bar(s), 1);
+            ptx::mbar_init(empty_bar(s), 1);
+        }
+        for (int a = 0; a < C::A_ST; ++a) {
+            ptx::mbar_init(afull_bar(a), n_epi);
+            ptx::mbar_init(aempty_bar(a), 1);
+        }
+        ptx::mbar_init(accfull_bar, 1);
+        ptx::mbar_init(accempty_bar, n_epi);
+        ptx::mbar_init(final_bar, 1);
+        *abort_flag = 0u;
+        ptx::fence_barrier_init();
+        ptx::fence_proxy_async_smem();
+    }
+    if (warp == 0 && lane == 0) {
+        ptx::prefetch_tmap(&p.tmap_a);
+        if (FMT != FMT_INT4) ptx::prefetch_tmap(&p.tmap_w);
+    }
+    if (warp == 2) {
+        ptx::tmem_alloc(sbase + C::OFF_MISC, C::TMEM_COLS);
+        ptx::tmem_relinquish();
+    }
+    ptx::tc_fence_before();
+    __syncthreads();
+    ptx::tc_fence_after();
+    const uint32_t tmem = *tmem_slot;
+
+    if (warp == 0) {
+        // ------------------------------------------------------------ producer
+        if (lane == 0) {
+            const uint64_t pol_w = p.w_evict_first ? ptx::policy_evict_first() : ptx::policy_evict_last();
+            const uint64_t pol_a = ptx::policy_evict_last();
+            int s = 0;
+            uint32_t ph = 0;
+            long long issued = 0;
+            bool ok = true;
+            for (int item = blockIdx.x; item < p.n_items && ok; item += gridDim.x) {
+                const Item it = decode_item(p, item);
+                for (int kb = it.kb_begin; kb < it.kb_end; ++kb) {
+                    if (!bounded_wait(empty_bar(s), ph ^ 1u, abort_flag, p.status, DEVICE_TIMEOUT_PRODUCER,
+                                      p.timeout_ns)) {
+                        ok = false;
+                        break;
+                    }
+                    const uint32_t fb = full_bar(s);
+                    uint32_t bytes = (uint32_t)C::B_STAGE;
+                    const uint32_t w_dst = sbase + C::OFF_W + s * C::W_STAGE;
+                    const uint32_t sc_dst = sbase + C::OFF_SC + s * C::SC_STAGE;
+                    uint32_t sc_bytes = 0;
+                    if (FMT == FMT_INT4) {
+                        const int gcnt = (p.G >= BK) ? 1 : BK / p.G;
+                        sc_bytes = (uint32_t)gcnt * TILE_N * 2;
+                        bytes += C::W_STAGE + sc_bytes;
+                    } else if (FMT == FMT_FP4) {
+                        sc_bytes = (uint32_t)C::SC_STAGE;
+                        bytes += C::W_STAGE + sc_bytes;
+                    } else {
+                        bytes += C::W_STAGE;
+                    }
+                    ptx::mbar_arrive_expect_tx(fb, bytes);
+                    if (FMT == FMT_INT4) {
+                        const uint8_t* wsrc =
+                            p.w + ((size_t)it.n_tile * p.nchunks_pad + (size_t)kb * (BK / 32)) * (TILE_N * 16);
+                        ptx::bulk_load(w_dst, wsrc, C::W_STAGE, fb, pol_w);
+                        const int g0 = (kb * BK) / p.G;
+                        const uint8_t* ssrc = p.sc + ((size_t)it.n_tile * p.ngroups_pad + g0) * (TILE_N * 2);
+                        ptx::bulk_load(sc_dst, ssrc, sc_bytes, fb, pol_w);
+                    } else if (FMT == FMT_FP4) {
+                        ptx::tma_load_2d(w_dst, &p.tmap_w, kb * (BK / 2), it.n_tile * TILE_N, fb, pol_w);
+                        const uint8_t* ssrc =
+                            p.sc + ((size_t)it.n_tile * p.nchunks_pad + (size_t)kb * (BK / 64)) * (TILE_N * 4);
+                        ptx::bulk_load(sc_dst, ssrc, sc_bytes, fb, pol_w);
+                    } else {
+                        ptx::tma_load_2d(w_dst, &p.tmap_w, kb * BK, it.n_tile * TILE_N, fb, pol_w);
+                    }
+                    const uint32_t b_dst = sbase + C::OFF_B + s * C::B_STAGE;
+#pragma unroll
+                    for (int j = 0; j < BK / 64; ++j)
+                        ptx::tma_load_2d(b_dst + j * (BN * 128), &p.tmap_a, kb * BK + j * 64, it.m_tile * BN, fb,
+                                         pol_a);
+                    ++issued;
+                    if (++s == STAGES) {
+                        s = 0;
+                        ph ^= 1u;
+                    }
+                }
+            }
+            if (*abort_flag) {
+                // wait for this CTA's own copies in flight before the CTA can exit
+                const long long first = issued > STAGES ? issued - STAGES : 0;
+                for (long long j = first; j < issued; ++j) {
+                    if (!drain_wait(full_bar((int)(j % STAGES)), (uint32_t)((j / STAGES) & 1), p.timeout_ns))
+                        atomicOr(p.status, DEVICE_TIMEOUT_DRAIN);
+                }
+            }
+        }
+        __syncwarp();
+    } else if (warp == 1) {
+        // ------------------------------------------------------------ MMA issuer
+        if (lane == 0) {
+            constexpr uint32_t idesc = ptx::make_idesc_f16(BF16, 128, BN);
+            int s = 0, a = 0;
+            uint32_t ph = 0, aph = 0, accph = 0;
+            bool ok = true;
+            for (int item = blockIdx.x; item < p.n_items && ok; item += gridDim.x) {
+                const Item it = decode_item(p, item);
+                if (!bounded_wait(accempty_bar, accph ^ 1u, abort_flag, p.status, DEVICE_TIMEOUT_MMA, p.timeout_ns)) {
+                    ok = false;
+                    break;
+                }
+                ptx::tc_fence_after();
+                for (int kb = it.kb_begin; kb < it.kb_end; ++kb) {
+                    if (!bounded_wait(afull_bar(a), aph, abort_flag, p.status, DEVICE_TIMEOUT_MMA, p.timeout_ns) ||
+                        !bounded_wait(full_bar(s), ph, abort_flag, p.status, DEVICE_TIMEOUT_MMA, p.timeout_ns)) {
+                        ok = false;
+                        break;
+                    }
+                    ptx::tc_fence_after();
+                    const uint32_t b_base = sbase + C::OFF_B + s * C::B_STAGE;
+                    const uint32_t a_tmem = tmem + C::A_BASE + a * C::A_COLS;
+#pragma unroll
+                    for (int kk = 0; kk < BK / 16; ++kk) {
+                        const uint32_t b_addr = b_base + (kk / 4) * (BN * 128) + (kk % 4) * 32;
+                        ptx::mma_f16_ts(tmem, a_tmem + kk * 8, ptx::make_sdesc_sw128(b_addr), idesc,
+                                        (kb > it.kb_begin || kk > 0) ? 1u : 0u);
+                    }
+                    ptx::mma_commit(empty_bar(s));
+                    ptx::mma_commit(aempty_bar(a));
+                    if (++s == STAGES) {
+                        s = 0;
+                        ph ^= 1u;
+                    }
+                    if (++a == C::A_ST) {
+                        a = 0;
+                        aph ^= 1u;
+                    }
+                }
+                if (!ok) break;
+                ptx::mma_commit(accfull_bar);
+                accph ^= 1u;
+            }
+            if (*abort_flag) {
+                ptx::mma_commit(final_bar);
+                if (!drain_wait(final_bar, 0, p.timeout_ns)) atomicOr(p.status, DEVICE_TIMEOUT_DRAIN);
+            }
+        }
+        __syncwarp();
+    } else if (warp >= 4) {
+        // ------------------------------------------------------------ transform + epilogue
+        const int ew = warp - 4;            // 0 .. 4*NWG-1
+        const int wg = ew >> 2;             // transform warpgroup
+        const int quarter = warp & 3;       // TMEM lane quarter this warp may access
+        const int r = quarter * 32 + lane;  // weight row inside the tile == TMEM lane
+        const uint32_t lane_addr = (uint32_t)(quarter * 32) << 16;
+        int s = 0, a = 0;
+        uint32_t ph = 0, aph = 0, accph = 0;
+        bool ok = true;
+        const float alpha = (FMT == FMT_INT4) ? 1.0f : __ldg(p.alpha);
+        for (int item = blockIdx.x; item < p.n_items && ok; item += gridDim.x) {
+            const Item it = decode_item(p, item);
+            for (int kb = it.kb_begin; kb < it.kb_end; ++kb) {
+                bool w1 = bounded_wait(full_bar(s), ph, abort_flag, p.status, DEVICE_TIMEOUT_TRANSFORM, p.timeout_ns);
+                bool w2 = w1 && bounded_wait(aempty_bar(a), aph ^ 1u, abort_flag, p.status, DEVICE_TIMEOUT_TRANSFORM,
+                                             p.timeout_ns);
+                if (!__all_sync(0xffffffffu, w2)) {
+                    ok = false;
+                    break;
+                }
+                ptx::tc_fence_after();
+                const uint8_t* wt = smem + C::OFF_W + s * C::W_STAGE;
+                const uint8_t* sct = smem + C::OFF_SC + s * C::SC_STAGE;
+                const uint32_t a_col = tmem + lane_addr + C::A_BASE + a * C::A_COLS;
+                if (FMT == FMT_FP8) {
+                    constexpr int CH = BK / 16;  // 16-byte chunks (16 codes, 8 columns) per row
+#pragma unroll
+                    for (int c = wg * (CH / NWG); c < (wg + 1) * (CH / NWG); ++c) {
+                        const uint4 q = *reinterpret_cast<const uint4*>(wt + swz(r * C::W_PITCH + c * 16, C::W_SWZ));
+                        uint32_t o[8];
+                        fp8_to_operand<BF16>(q, o);
+                        ptx::tmem_st8(a_col + c * 8, o);
+                    }
+                } else {
+                    constexpr int CH = BK / 32;  // 16-byte chunks (32 codes, 16 columns) per row
+#pragma unroll
+                    for (int c = wg * (CH / NWG); c < (wg + 1) * (CH / NWG); ++c) {
+                        uint32_t o[16];
+                        if (FMT == FMT_INT4) {
+                            const uint4 q = *reinterpret_cast<const uint4*>(wt + (c * TILE_N + r) * 16);
+                            const uint16_t sbits =
+                                *reinterpret_cast<const uint16_t*>(sct + (((c * 32) / p.G) * TILE_N + r) * 2);
+                            if (BF16) {
+                                int4_to_bf16(q, __half2float(__ushort_as_half(sbits)), o);
+                            } else {
+                                const uint32_t s2 = (uint32_t)sbits | ((uint32_t)sbits << 16);
+                                int4_to_f16(q, s2, o);
+                            }
+                        } else {
+                            const uint4 q = *reinterpret_cast<const uint4*>(wt + swz(r * C::W_PITCH + c * 16, C::W_SWZ));
+                            const uint16_t sfp =
+                                *reinterpret_cast<const uint16_t*>(sct + (c >> 1) * (TILE_N * 4) + r * 4 + (c & 1) * 2);
+                            fp4_to_bf16(q, sfp, o);
+                        }
+                        ptx::tmem_st16(a_col + c * 16, o);
+                    }
+                }
+                ptx::tmem_wait_st();
+                ptx::tc_fence_before();
+                ptx::mbar_arrive(afull_bar(a));
+                if (++s == STAGES) {
+                    s = 0;
+                    ph ^= 1u;
+                }
+                if (++a == C::A_ST) {
+                    a = 0;
+                    aph ^= 1u;
+                }
+            }
+            if (!ok) break;
+
+            // ------------------------------------------------ epilogue
+            const bool wacc = bounded_wait(accfull_bar, accph, abort_flag, p.status, DEVICE_TIMEOUT_EPILOGUE,
+                                           p.timeout_ns);
+            if (!__all_sync(0xffffffffu, wacc)) {
+                ok = false;
+                break;
+            }
+            accph ^= 1u;
+            ptx::tc_fence_after();
+            const int n = it.n_tile * TILE_N + r;
+            const int m0 = it.m_tile * BN;
+            constexpr int COLS = BN / NWG;         // accumulator columns per warpgroup
+            constexpr int STEP = COLS >= 16 ? 16 : 8;
+            const int c_begin = wg * COLS;
+            const uint32_t acc_addr = tmem + lane_addr;
+            const int tile = it.n_tile + p.tiles_n * it.m_tile;
+            const bool nvalid = n < p.N;
+            float bias_v = 0.0f;
+            if (FMT == FMT_FP8 && p.bias != nullptr && nvalid) bias_v = load_16bit<BF16>(p.bias, (size_t)n);
+
+            if (p.splits == 1) {
+#pragma unroll 1
+                for (int cc = c_begin; cc < c_begin + COLS; cc += STEP) {
+                    uint32_t v[16];
+                    if (STEP == 16) {
+                        ptx::tmem_ld16(acc_addr + cc, v);
+                    } else {
+                        uint32_t v8[8];
+                        ptx::tmem_ld8(acc_addr + cc, v8);
+#pragma unroll
+                        for (int j = 0; j < 8; ++j) v[j] = v8[j];
+                    }
+                    ptx::tmem_wait_ld();
+#pragma unroll
+                    for (int j = 0; j < STEP; ++j) {
+                        const int m = m0 + cc + j;
+                        if (nvalid && m < p.M)
+                            store_out<BF16>(p.out, (size_t)m * p.N + n, alpha * __uint_as_float(v[j]) + bias_v);
+                    }
+                }
+            } else {
+                // deterministic split-K: every slice writes its fp32 partial, the last
+                // slice to arrive sums all slices in slice order 0..S-1 and stores.
+                float* part = p.ws_part + (size_t)(tile * p.splits + it.slice) * BN * TILE_N;
+#pragma unroll 1
+                for (int cc = c_begin; cc < c_begin + COLS; cc += STEP) {
+                    uint32_t v[16];
+                    if (STEP == 16) {
+                        ptx::tmem_ld16(acc_addr + cc, v);
+                    } else {
+                        uint32_t v8[8];
+                        ptx::tmem_ld8(acc_addr + cc, v8);
+#pragma unroll
+                        for (int j = 0; j < 8; ++j) v[j] = v8[j];
+                    }
+                    ptx::tmem_wait_ld();
+#pragma unroll
+                    for (int j = 0; j < STEP; ++j) {
+                        if (m0 + cc + j < p.M) __stcg(part + (size_t)(cc + j) * TILE_N + r, __uint_as_float(v[j]));
+                    }
+                }
+                // Each epilogue warp owns 32 rows x COLS columns of the tile and takes
+                // its own ticket, so no warp ever waits for another one.
+                __threadfence();
+                __syncwarp();
+                uint32_t last = 0;
+                if (lane == 0) {
+                    uint32_t* cnt = p.ws_count + (size_t)tile * 8 + ew;
+                    const uint32_t old = atomicAdd(cnt, 1u);
+                    last = (old == (uint32_t)(p.splits - 1)) ? 1u : 0u;
+                    if (last) atomicExch(cnt, 0u);
+                }
+                last = __shfl_sync(0xffffffffu, last, 0);
+                if (last) {
+                    __threadfence();
+                    const float* base = p.ws_part + (size_t)(tile * p.splits) * BN * TILE_N;
+#pragma unroll 1
+                    for (int cc = c_begin; cc < c_begin + COLS; ++cc) {
+                        const int m = m0 + cc;
+                        if (m >= p.M) break;
+                        float acc = 0.0f;
+                        for (int sl = 0; sl < p.splits; ++sl)
+                            acc += __ldcg(base + ((size_t)sl * BN + cc) * TILE_N + r);
+                        if (nvalid) store_out<BF16>(p.out, (size_t)m * p.N + n, alpha * acc + bias_v);
+                    }
+                }
+            }
+            ptx::tc_fence_before();
+            ptx::mbar_arrive(accempty_bar);
+        }
+        (void)ok;
+    }
+
+    ptx::tc_fence_before();
+    __syncthreads();
+    if (warp == 2) {
+        ptx::tc_fence_after();
+        ptx::tmem_dealloc(tmem, C::TMEM_COLS);
+    }
+}
+
+// Host-side launcher for one instantiation.
+template <int FMT, bool BF16, int BN, int BK, int STAGES, int NWG>
+struct GemmLauncher {
+    using C = GemmCfg<FMT, BF16, BN, BK, STAGES, NWG>;
+    static cudaError_t prepare() {
+        // per device: allow the dynamic shared memory this configuration needs
+        static int attr_set[64] = {0};
+        int dev = 0;
+        cudaError_t e = cudaGetDevice(&dev);
+        if (e != cudaSuccess) return e;
+        if (dev < 64 && attr_set[dev]) return cudaSuccess;
+        e = cudaFuncSetAttribute(wq_gemm_kernel<FMT, BF16, BN, BK, STAGES, NWG>,
+                                 cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM_BYTES);
+        if (e == cudaSuccess && dev < 64) attr_set[dev] = 1;
+        return e;
+    }
+    // Static configuration; with query_device, also the resident CTAs per SM on
+    // the current device (otherwise the value implied by shared/tensor memory).
+    static KernelConfig config(bool query_device = false) {
+        KernelConfig k{FMT, BF16 ? 1 : 0, BN, BK, STAGES, NWG, C::NT, C::SMEM_BYTES, C::TMEM_COLS, C::MIN_BLOCKS};
+        if (query_device && prepare() == cudaSuccess) {
+            int n = 0;
+            if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, wq_gemm_kernel<FMT, BF16, BN, BK, STAGES, NWG>, C::NT,
+                                                              C::SMEM_BYTES) == cudaSuccess && n > 0) {
+                const int tmem_limit = 512 / C::TMEM_COLS;
+                k.ctas_per_sm = n < tmem_limit ? n : tmem_limit;
+            }
+        }
+        return k;
+    }
+    static cudaError_t launch(const GemmParams& p, int grid, cudaStream_t st) {
+        auto kern = wq_gemm_kernel<FMT, BF16, BN, BK, STAGES, NWG>;
+        cudaError_t e = prepare();
+        if (e != cudaSuccess) return e;
+        cudaLaunchConfig_t cfg = {};
+        cfg.gridDim = dim3((unsigned)grid, 1, 1);
+        cfg.blockDim = dim3(C::NT, 1, 1);
+        cfg.dynamicSmemBytes = C::SMEM_BYTES;
+        cfg.stream = st;
+        cfg.attrs = nullptr;
+        cfg.numAttrs = 0;
+        return cudaLaunchKernelEx(&cfg, kern, p);
+    }
+};
+
+}  // namespace wq

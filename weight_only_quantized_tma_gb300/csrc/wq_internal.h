@@ -1,0 +1,128 @@
+// wq_internal.h -- declarations shared by the host API (wq_api.cu) and the kernel
+// translation units.  Not part of the public C ABI (include/wq.h).
+#pragma once
+
+#include <cstddef>
+#include <cstdint>
+#include <cuda.h>
+#include <cuda_runtime.h>
+
+namespace wq {
+
+enum WFmt : int { FMT_INT4 = 0, FMT_FP8 = 1, FMT_FP4 = 2 };
+
+// Weight rows per CTA tile (the MMA M dimension: dequantized weight rows are the
+// tcgen05 A operand, tokens are the N dimension).
+constexpr int TILE_N = 128;
+// Padding granularity of the prepacked INT4 / FP4-scale layouts along K.
+constexpr int KPAD_INT4 = 256;
+constexpr int KPAD_FP4SF = 128;  // covers a whole k-block of the largest BK
+
+// Division by a runtime constant with a multiply-shift.  For x < 2^31 and
+// 1 <= d < 2^31, magic = ceil(2^(31+l) / d) with l = ceil(log2 d) gives
+// floor(x * magic / 2^(31+l)) == x / d.  The product is only used when the
+// largest dividend times magic fits in 63 bits; otherwise magic = 0 and the
+// plain division is used.  (The overflow guard is the lesson of the
+// magic-number division bug in "FlashInfer W8A16 GEMM (mm_bf16_fp8) analysis",
+// §3(b): a divisor of 1 produced a 2^40 magic that overflowed int64.)
+struct FastDiv {
+    uint32_t d;
+    uint32_t shift;
+    uint64_t magic;
+};
+
+inline FastDiv make_fastdiv(uint32_t d, uint32_t x_max) {
+    FastDiv f{d, 0, 0};
+    if (d == 0 || d >= (1u << 31) || x_max >= (1u << 31)) return f;
+    uint32_t l = 0;
+    while ((1ull << l) < d) ++l;
+    uint32_t shift = 31 + l;
+    unsigned __int128 num = ((unsigned __int128)1) << shift;
+    uint64_t magic = (uint64_t)((num + d - 1) / d);
+    // overflow guard: x_max * magic must stay below 2^63
+    if (x_max != 0 && magic > (uint64_t)INT64_MAX / x_max) return f;
+    f.shift = shift;
+    f.magic = magic;
+    return f;
+}
+
+__host__ __device__ __forceinline__ uint32_t fastdiv(uint32_t x, const FastDiv& f) {
+    return f.magic ? (uint32_t)((x * f.magic) >> f.shift) : x / f.d;
+}
+
+// Everything a GEMM launch needs.  Passed by value as a __grid_constant__ so the
+// tensor maps live in parameter space.
+struct GemmParams {
+    CUtensorMap tmap_a;      // activations [M][K], 16-bit, box {64, BN}, 128-byte swizzle
+    CUtensorMap tmap_w;      // FP8 [N][K] / FP4 [N][K/2] weights (unused for INT4)
+    const uint8_t* w;        // INT4 prepacked weight tiles
+    const uint8_t* sc;       // INT4 prepacked group scales / FP4 prepacked block scales
+    const float* alpha;      // FP8 / FP4 global scale (device), unused for INT4
+    const void* bias;        // FP8 optional bias [N], same 16-bit type as A
+    void* out;               // [M][N], 16-bit
+    float* ws_part;          // split-K partials
+    uint32_t* ws_count;      // split-K arrival tickets, one per output tile
+    uint32_t* status;        // device status word (WQ_DEVICE_* bits)
+    int M, N, K;
+    int G;                   // INT4 group size
+    int tiles_n, tiles_m;
+    int splits;              // split-K slices per output tile
+    int nkb;                 // k-blocks
+    int n_items;             // tiles_n * tiles_m * splits
+    int walk_n_fast;         // tile walk order: weight rows fastest
+    int w_evict_first;       // weights are streamed once (decode)
+    int ngroups_pad;         // INT4: padded K / G
+    int nchunks_pad;         // INT4: padded K / 32 ; FP4: padded K / 64
+    FastDiv div_walk;        // divides a tile index by tiles_n (or tiles_m)
+    FastDiv div_splits;      // divides an item index by splits
+    long long timeout_ns;    // bound on every barrier wait
+};
+
+// Device status bits (OR-ed into *status by the kernels).
+constexpr uint32_t DEVICE_TIMEOUT_PRODUCER = 1u << 0;
+constexpr uint32_t DEVICE_TIMEOUT_MMA = 1u << 1;
+constexpr uint32_t DEVICE_TIMEOUT_TRANSFORM = 1u << 2;
+constexpr uint32_t DEVICE_TIMEOUT_EPILOGUE = 1u << 3;
+constexpr uint32_t DEVICE_TIMEOUT_DRAIN = 1u << 4;
+
+// Static description of one compiled kernel configuration.
+struct KernelConfig {
+    int fmt;
+    int bf16;
+    int bn;          // token tile (MMA N)
+    int bk;          // k per pipeline stage
+    int stages;
+    int nwg;         // transform warpgroups
+    int threads;
+    int smem_bytes;  // dynamic shared memory
+    int tmem_cols;
+    int ctas_per_sm;  // resident CTAs per SM (registers, shared and tensor memory)
+};
+
+// Per-format launch entry points, defined in wq_gemm_{int4,fp8,fp4}.cu.
+// `bn` selects the instantiation; returns cudaErrorInvalidValue if none matches.
+cudaError_t launch_gemm_int4(const GemmParams& p, bool bf16, int bn, int grid, cudaStream_t st);
+cudaError_t launch_gemm_fp8(const GemmParams& p, bool bf16, int bn, int grid, cudaStream_t st);
+cudaError_t launch_gemm_fp4(const GemmParams& p, bool bf16, int bn, int grid, cudaStream_t st);
+// Configuration of the instantiation for (bf16, bn); `query` asks the current
+// device for the resident CTAs per SM.  False if no such instantiation exists.
+bool config_int4(bool bf16, int bn, bool query, KernelConfig* cfg);
+bool config_fp8(bool bf16, int bn, bool query, KernelConfig* cfg);
+bool config_fp4(bool bf16, int bn, bool query, KernelConfig* cfg);
+
+// Layout transforms, defined in wq_pack.cu.
+cudaError_t launch_pack_int4(const uint8_t* w, const uint16_t* s, int64_t N, int64_t K, int G, uint8_t* wk,
+                             uint16_t* sk, cudaStream_t st);
+cudaError_t launch_unpack_int4(const uint8_t* wk, const uint16_t* sk, int64_t N, int64_t K, int G, uint8_t* w,
+                               uint16_t* s, cudaStream_t st);
+cudaError_t launch_dequant_int4(const uint8_t* wk, const uint16_t* sk, int64_t N, int64_t K, int G, float* out,
+                                cudaStream_t st);
+cudaError_t launch_pack_fp4_sf(const uint8_t* sf, int64_t N, int64_t K, uint8_t* sfk, cudaStream_t st);
+cudaError_t launch_dequant_fp4(const uint8_t* w, const uint8_t* sfk, int64_t N, int64_t K, float* out,
+                               cudaStream_t st);
+cudaError_t launch_dequant_fp8(const uint8_t* w, int64_t N, int64_t K, bool bf16, float* out, cudaStream_t st);
+cudaError_t launch_wait_probe(uint32_t* status, long long timeout_ns, cudaStream_t st);
+
+inline int64_t round_up(int64_t x, int64_t m) { return (x + m - 1) / m * m; }
+
+}  // namespace wq
