@@ -32,7 +32,8 @@
  *     scalars (alpha, bias) need only element alignment.
  *   - Only compute capability 10.3 (GB300) is supported: other devices give
  *     WQ_ERR_UNSUPPORTED_DEVICE.
- *   - M == 0 is a valid empty problem and returns WQ_OK without launching.
+ *   - M == 0 (with N, K > 0) is a valid empty problem: it returns WQ_OK without
+ *     launching or looking at any pointer.
  */
 #ifndef WQ_H_
 #define WQ_H_
@@ -172,6 +173,7 @@ typedef struct {
     int32_t walk_n_fast;  /* 1: weight-row tiles are walked fastest */
     int32_t tiles_n;
     int32_t tiles_m;
+    int32_t ctas_per_sm;  /* resident CTAs per SM assumed by the plan */
 } wq_plan;
 
 /* Plan and workspace size for op (a_dtype is ignored for WQ_OP_FP4, G for FP8

@@ -48,12 +48,29 @@ class Int4Problem:
         import weight_only_quantized_tma_gb300 as wq
         return wq.wq_gemm_w4a16(self.A_d, self.wk, self.sk, self.N, self.K, self.G, out=out, ws=ws)
 
+    @property
+    def out_dtype(self):
+        return self.a_dtype
+
     def ref(self, rows=None):
         return oracle.gemm_w4a16(self.A, self.a_dtype == "bf16", self.wts.w, self.wts.s, self.M, self.N, self.K,
                                  self.G, rows=rows)
 
 
-def check_close(got, ref, rel_max=REL_MAX, rel_mean=REL_MEAN, what=""):
+def rounded_ref(ref, out_dtype):
+    """The float64 reference correctly rounded (RNE) to the output type."""
+    if out_dtype == "bf16":
+        return oracle.bf16_bits_to_double_array(oracle.round_bf16_array(ref))
+    return oracle.f16_bits_to_double_array(oracle.round_f16_array(ref))
+
+
+def check_close(got, ref, out_dtype="f16", rel_max=REL_MAX, rel_mean=REL_MEAN, what=""):
+    """rel_max against the float64 reference; rel_mean against it for fp16 outputs and
+    against the correctly rounded reference for bf16 outputs, whose own rounding
+    (8 significant bits) already costs ~1.4e-3 in mean relative error."""
     rmax, rmean = oracle.rel_errors(got, ref)
-    assert rmax <= rel_max and rmean <= rel_mean, f"{what} rel_max={rmax:.3e} rel_mean={rmean:.3e}"
+    mean_ref = ref if out_dtype == "f16" else rounded_ref(ref, out_dtype)
+    _, rmean_vs = oracle.rel_errors(got, mean_ref)
+    assert rmax <= rel_max and rmean_vs <= rel_mean, \
+        f"{what} rel_max={rmax:.3e} rel_mean={rmean:.3e} rel_mean_vs_rounded={rmean_vs:.3e}"
     return rmax, rmean

@@ -77,7 +77,8 @@ def test_decode_configs(case):
     torch.cuda.synchronize()
     check_close(out_to_f64(out), p.ref(), what=f"decode {case}")
     plan = wq.get_plan(wq.WQ_OP_W4A16, wq.WQ_F16, case.M, case.N, case.K, case.G)
-    assert plan["splits"] > 1          # decode grids are too small to fill the GPU without split-K
+    # decode grids (< 100 output tiles) are too small to fill the GPU without split-K
+    assert plan["splits"] > 1 and plan["grid"] >= 2 * plan["tiles_n"]
 
 
 @pytest.mark.parametrize("M", [1, 3, 4, 15, 16, 17, 64, 100, 128, 129, 300])
@@ -106,19 +107,28 @@ def test_prefill_configs_sampled_rows(case):
     check_close(got, p.ref(rows=rows), what=f"prefill {case}")
 
 
-def test_prefill_bf16_activations():
-    p = Int4Problem(1024, 1024, 2048, 128, a_dtype="bf16", seed=109).pack()
-    out = p.run()
-    torch.cuda.synchronize()
-    rows = synth.sample_rows(1024, 96, seed=110)
-    check_close(out_to_f64(out)[rows], p.ref(rows=rows), what="prefill bf16")
+def _bf16_cast_copy(p):
+    # materialise RN_bf of the exact weight, then a dense bf16 GEMM with fp32 accumulation
+    w = oracle.dequant_int4(p.wts.w, p.wts.s, p.K, p.G)
+    w16 = torch.from_numpy(w).to(DEV).to(torch.bfloat16)
+    return torch.nn.functional.linear(p.A_d, w16)
 
 
-def test_decode_bf16_activations():
-    p = Int4Problem(7, 4096, 4096, 128, a_dtype="bf16", seed=111).pack()
+@pytest.mark.parametrize("M,N,K", [(7, 4096, 4096), (1024, 1024, 2048)])
+def test_bf16_activations_match_cast_copy(M, N, K):
+    # with bf16 activations the MMA operand is RN_bf((q - 8) * s): bf16's 8-bit
+    # significand costs ~1e-3 relative per weight, so the bar is the same rounding
+    # done by materialising the bf16 weight and calling a dense GEMM
+    p = Int4Problem(M, N, K, 128, a_dtype="bf16", seed=109 + M).pack()
     out = p.run()
+    cast = _bf16_cast_copy(p)
     torch.cuda.synchronize()
-    check_close(out_to_f64(out), p.ref(), what="decode bf16")
+    rows = synth.sample_rows(M, 96, seed=110)
+    ref = p.ref(rows=rows)
+    k_max, k_mean = oracle.rel_errors(out_to_f64(out)[rows], ref)
+    c_max, c_mean = oracle.rel_errors(out_to_f64(cast)[rows], ref)
+    assert k_max <= 5e-3
+    assert k_mean <= 1.02 * c_mean, f"kernel {k_mean:.3e} vs cast-copy {c_mean:.3e}"
 
 
 def test_split_k_is_deterministic():

@@ -353,6 +353,7 @@ wq_status wq_get_plan(wq_op op, wq_dtype a_dtype, int64_t M, int64_t N, int64_t 
         plan->walk_n_fast = pl.walk_n_fast;
         plan->tiles_n = pl.tiles_n;
         plan->tiles_m = pl.tiles_m;
+        plan->ctas_per_sm = pl.cfg.ctas_per_sm;
     }
     if (ws_bytes) *ws_bytes = (M == 0) ? 0 : pl.ws_bytes;
     return WQ_OK;
@@ -365,6 +366,7 @@ wq_status wq_workspace_bytes(wq_op op, wq_dtype a_dtype, int64_t M, int64_t N, i
 
 wq_status wq_gemm_w4a16(const void* A, wq_dtype a_dtype, const uint8_t* w_kernel, const void* s_kernel, int64_t M,
                         int64_t N, int64_t K, int32_t G, void* out, void* ws, size_t ws_bytes, wq_stream_t stream) {
+    if (M == 0 && N > 0 && K > 0) return WQ_OK;   // empty problem: A and out may be NULL
     if (!A || !w_kernel || !s_kernel || !out) return WQ_ERR_NULL;
     if (M < 0 || N <= 0 || K <= 0 || M > kMaxDim || N > kMaxDim || K > kMaxDim) return WQ_ERR_SHAPE;
     if (K % 32 != 0 || N % 8 != 0) return WQ_ERR_SHAPE;
@@ -396,6 +398,7 @@ wq_status wq_gemm_w4a16(const void* A, wq_dtype a_dtype, const uint8_t* w_kernel
 wq_status wq_gemm_w8a16_fp8(const void* A, wq_dtype a_dtype, const uint8_t* w_e4m3, const float* alpha,
                             const void* bias, int64_t M, int64_t N, int64_t K, void* out, void* ws, size_t ws_bytes,
                             wq_stream_t stream) {
+    if (M == 0 && N > 0 && K > 0) return WQ_OK;   // empty problem: A and out may be NULL
     if (!A || !w_e4m3 || !alpha || !out) return WQ_ERR_NULL;
     if (M < 0 || N <= 0 || K <= 0 || M > kMaxDim || N > kMaxDim || K > kMaxDim) return WQ_ERR_SHAPE;
     if (K % 16 != 0 || N % 8 != 0) return WQ_ERR_SHAPE;
@@ -427,6 +430,7 @@ wq_status wq_gemm_w8a16_fp8(const void* A, wq_dtype a_dtype, const uint8_t* w_e4
 wq_status wq_gemm_bf16_fp4(const void* A, const uint8_t* w_e2m1, const uint8_t* sf_kernel, const float* alpha,
                            int64_t M, int64_t N, int64_t K, void* out, void* ws, size_t ws_bytes,
                            wq_stream_t stream) {
+    if (M == 0 && N > 0 && K > 0) return WQ_OK;   // empty problem: A and out may be NULL
     if (!A || !w_e2m1 || !sf_kernel || !alpha || !out) return WQ_ERR_NULL;
     if (M < 0 || N <= 0 || K <= 0 || M > kMaxDim || N > kMaxDim || K > kMaxDim) return WQ_ERR_SHAPE;
     if (K % 32 != 0 || N % 8 != 0) return WQ_ERR_SHAPE;

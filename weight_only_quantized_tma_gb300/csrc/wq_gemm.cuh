@@ -78,18 +78,25 @@ struct GemmCfg {
 __device__ __forceinline__ uint32_t swz(uint32_t a, uint32_t mask) { return a ^ (((a >> 7) & mask) << 4); }
 
 // Bounded wait on an mbarrier phase, executed by every lane that calls it.
-// Returns false if the CTA is aborting or the wait timed out (which starts the abort).
+// Returns false if the CTA is aborting or the wait timed out (which starts the
+// abort).  The global timer is slow to read, so it is only consulted every 256
+// failed probes; the abort flag (shared memory) is checked on every probe.
 __device__ __forceinline__ bool bounded_wait(uint32_t bar, uint32_t parity, volatile uint32_t* abort_flag,
                                              uint32_t* status, uint32_t code, long long timeout_ns) {
     if (ptx::mbar_try_wait(bar, parity)) return true;
-    const uint64_t t0 = ptx::globaltimer();
-    while (true) {
+    uint64_t t0 = 0;
+    for (uint32_t i = 1;; ++i) {
         if (ptx::mbar_try_wait(bar, parity)) return true;
         if (*abort_flag) return false;
-        if ((long long)(ptx::globaltimer() - t0) > timeout_ns) {
-            *abort_flag = 1u;
-            atomicOr(status, code);
-            return false;
+        if ((i & 255u) == 0u) {
+            const uint64_t now = ptx::globaltimer();
+            if (t0 == 0) {
+                t0 = now;
+            } else if ((long long)(now - t0) > timeout_ns) {
+                *abort_flag = 1u;
+                atomicOr(status, code);
+                return false;
+            }
         }
     }
 }
@@ -97,8 +104,8 @@ __device__ __forceinline__ bool bounded_wait(uint32_t bar, uint32_t parity, vola
 // Wait used while draining after an abort: ignores the abort flag.
 __device__ __forceinline__ bool drain_wait(uint32_t bar, uint32_t parity, long long timeout_ns) {
     const uint64_t t0 = ptx::globaltimer();
-    while (!ptx::mbar_try_wait(bar, parity)) {
-        if ((long long)(ptx::globaltimer() - t0) > timeout_ns) return false;
+    for (uint32_t i = 1; !ptx::mbar_try_wait(bar, parity); ++i) {
+        if ((i & 255u) == 0u && (long long)(ptx::globaltimer() - t0) > timeout_ns) return false;
     }
     return true;
 }
@@ -242,12 +249,13 @@ __global__ void __launch_bounds__(128 * (1 + NWG), (GemmCfg<FMT, BF16, BN, BK, S
             ptx::mbar_init(full_bar(s), 1);
             ptx::mbar_init(empty_bar(s), 1);
         }
+        // operand-full and accumulator-empty take one arrival per transform warp
         for (int a = 0; a < C::A_ST; ++a) {
-            ptx::mbar_init(afull_bar(a), n_epi);
+            ptx::mbar_init(afull_bar(a), n_epi / 32);
             ptx::mbar_init(aempty_bar(a), 1);
         }
         ptx::mbar_init(accfull_bar, 1);
-        ptx::mbar_init(accempty_bar, n_epi);
+        ptx::mbar_init(accempty_bar, n_epi / 32);
         ptx::mbar_init(final_bar, 1);
         *abort_flag = 0u;
         ptx::fence_barrier_init();
@@ -444,9 +452,11 @@ __global__ void __launch_bounds__(128 * (1 + NWG), (GemmCfg<FMT, BF16, BN, BK, S
                         ptx::tmem_st16(a_col + c * 16, o);
                     }
                 }
+                // every lane's TMEM stores are complete before the warp's one arrival
                 ptx::tmem_wait_st();
                 ptx::tc_fence_before();
-                ptx::mbar_arrive(afull_bar(a));
+                __syncwarp();
+                if (lane == 0) ptx::mbar_arrive(afull_bar(a));
                 if (++s == STAGES) {
                     s = 0;
                     ph ^= 1u;
@@ -546,7 +556,8 @@ __global__ void __launch_bounds__(128 * (1 + NWG), (GemmCfg<FMT, BF16, BN, BK, S
                 }
             }
             ptx::tc_fence_before();
-            ptx::mbar_arrive(accempty_bar);
+            __syncwarp();
+            if (lane == 0) ptx::mbar_arrive(accempty_bar);
         }
         (void)ok;
     }
@@ -572,21 +583,37 @@ struct GemmLauncher {
         if (dev < 64 && attr_set[dev]) return cudaSuccess;
         e = cudaFuncSetAttribute(wq_gemm_kernel<FMT, BF16, BN, BK, STAGES, NWG>,
                                  cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM_BYTES);
+        // all of L1 as shared memory, so that two CTAs fit where the sizes allow it
+        if (e == cudaSuccess)
+            e = cudaFuncSetAttribute(wq_gemm_kernel<FMT, BF16, BN, BK, STAGES, NWG>,
+                                     cudaFuncAttributePreferredSharedMemoryCarveout, 100);
         if (e == cudaSuccess && dev < 64) attr_set[dev] = 1;
         return e;
     }
     // Static configuration; with query_device, also the resident CTAs per SM on
-    // the current device (otherwise the value implied by shared/tensor memory).
+    // the current device, from the kernel's registers, its shared memory (plus the
+    // per-block reservation), threads per SM and tensor memory (512 columns).
     static KernelConfig config(bool query_device = false) {
         KernelConfig k{FMT, BF16 ? 1 : 0, BN, BK, STAGES, NWG, C::NT, C::SMEM_BYTES, C::TMEM_COLS, C::MIN_BLOCKS};
-        if (query_device && prepare() == cudaSuccess) {
-            int n = 0;
-            if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, wq_gemm_kernel<FMT, BF16, BN, BK, STAGES, NWG>, C::NT,
-                                                              C::SMEM_BYTES) == cudaSuccess && n > 0) {
-                const int tmem_limit = 512 / C::TMEM_COLS;
-                k.ctas_per_sm = n < tmem_limit ? n : tmem_limit;
-            }
-        }
+        if (!query_device || prepare() != cudaSuccess) return k;
+        int dev = 0, smem_sm = 0, smem_rsv = 0, regs_sm = 0, thr_sm = 0;
+        cudaFuncAttributes fa;
+        if (cudaGetDevice(&dev) != cudaSuccess ||
+            cudaFuncGetAttributes(&fa, wq_gemm_kernel<FMT, BF16, BN, BK, STAGES, NWG>) != cudaSuccess ||
+            cudaDeviceGetAttribute(&smem_sm, cudaDevAttrMaxSharedMemoryPerMultiprocessor, dev) != cudaSuccess ||
+            cudaDeviceGetAttribute(&smem_rsv, cudaDevAttrReservedSharedMemoryPerBlock, dev) != cudaSuccess ||
+            cudaDeviceGetAttribute(&regs_sm, cudaDevAttrMaxRegistersPerMultiprocessor, dev) != cudaSuccess ||
+            cudaDeviceGetAttribute(&thr_sm, cudaDevAttrMaxThreadsPerMultiProcessor, dev) != cudaSuccess)
+            return k;
+        const int regs_warp = ((fa.numRegs * 32 + 255) / 256) * 256;
+        int n = regs_sm / (regs_warp * (C::NT / 32));
+        const int by_smem = smem_sm / (C::SMEM_BYTES + fa.sharedSizeBytes + smem_rsv);
+        const int by_thr = thr_sm / C::NT;
+        const int by_tmem = 512 / C::TMEM_COLS;
+        if (by_smem < n) n = by_smem;
+        if (by_thr < n) n = by_thr;
+        if (by_tmem < n) n = by_tmem;
+        if (n >= 1) k.ctas_per_sm = n;
         return k;
     }
     static cudaError_t launch(const GemmParams& p, int grid, cudaStream_t st) {

@@ -3,11 +3,11 @@
 
 namespace wq {
 
-using F8BF16_16 = GemmLauncher<FMT_FP8, true, 16, 128, 5, 1>;
-using F8BF16_64 = GemmLauncher<FMT_FP8, true, 64, 128, 3, 1>;
-using F8BF16_128 = GemmLauncher<FMT_FP8, true, 128, 128, 2, 1>;
+using F8BF16_16 = GemmLauncher<FMT_FP8, true, 16, 128, 5, 2>;
+using F8BF16_64 = GemmLauncher<FMT_FP8, true, 64, 128, 3, 2>;
+using F8BF16_128 = GemmLauncher<FMT_FP8, true, 128, 128, 2, 2>;
 using F8BF16_256 = GemmLauncher<FMT_FP8, true, 256, 64, 5, 2>;
-using F8F16_16 = GemmLauncher<FMT_FP8, false, 16, 128, 5, 1>;
+using F8F16_16 = GemmLauncher<FMT_FP8, false, 16, 128, 5, 2>;
 using F8F16_256 = GemmLauncher<FMT_FP8, false, 256, 64, 5, 2>;
 
 bool config_fp8(bool bf16, int bn, bool query, KernelConfig* cfg) {

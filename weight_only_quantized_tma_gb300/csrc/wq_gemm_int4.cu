@@ -5,11 +5,11 @@ namespace wq {
 
 // (BN, BK, STAGES, NWG) per activation type.  BN <= 128 configurations fit two
 // CTAs per SM (decode / split-K); BN = 256 runs one persistent CTA per SM.
-using I4F16_16 = GemmLauncher<FMT_INT4, false, 16, 128, 8, 1>;
-using I4F16_64 = GemmLauncher<FMT_INT4, false, 64, 128, 4, 1>;
-using I4F16_128 = GemmLauncher<FMT_INT4, false, 128, 128, 2, 1>;
+using I4F16_16 = GemmLauncher<FMT_INT4, false, 16, 128, 8, 2>;
+using I4F16_64 = GemmLauncher<FMT_INT4, false, 64, 128, 4, 2>;
+using I4F16_128 = GemmLauncher<FMT_INT4, false, 128, 128, 2, 2>;
 using I4F16_256 = GemmLauncher<FMT_INT4, false, 256, 64, 5, 2>;
-using I4BF16_16 = GemmLauncher<FMT_INT4, true, 16, 128, 8, 1>;
+using I4BF16_16 = GemmLauncher<FMT_INT4, true, 16, 128, 8, 2>;
 using I4BF16_256 = GemmLauncher<FMT_INT4, true, 256, 64, 5, 2>;
 
 bool config_int4(bool bf16, int bn, bool query, KernelConfig* cfg) {
