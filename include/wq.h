@@ -185,6 +185,27 @@ wq_status wq_get_plan(wq_op op, wq_dtype a_dtype, int64_t M, int64_t N, int64_t 
 wq_status wq_workspace_bytes(wq_op op, wq_dtype a_dtype, int64_t M, int64_t N, int64_t K, int32_t G,
                              size_t* bytes);
 
+/* ------------------------------------------------------------------ no caller workspace */
+
+/* Bytes of split-K scratch built into the library for wq_gemm_w4a16_noalloc. */
+#define WQ_NOALLOC_SCRATCH_BYTES (4u << 20)
+
+/* W4A16 GEMM that takes no workspace.  The paper has no counterpart: this entry
+ * point is for callers that cannot allocate device memory themselves -- a framework
+ * that owns all device memory through its own pool, or a decode loop where a
+ * cudaMalloc (which may synchronise the device) is not allowed.  Arguments and
+ * results are those of wq_gemm_w4a16 without ws / ws_bytes, and it allocates
+ * nothing.  Its split-K scratch is one array of WQ_NOALLOC_SCRATCH_BYTES inside the
+ * library, held on every GPU that loads the library until the process exits; a
+ * problem whose scratch would not fit returns WQ_ERR_WORKSPACE and launches nothing.
+ * The first call on a device looks up the array's device address (once per device,
+ * with that device current): make that first call before any stream capture.  Each
+ * call clears the array's 16 KiB of arrival counters on `stream`, then runs the GEMM.
+ * All calls share the array and it keeps the last call's contents, so calls that
+ * overlap on the GPU (unordered streams) race; order them on one stream. */
+wq_status wq_gemm_w4a16_noalloc(const void* A, wq_dtype a_dtype, const uint8_t* w_kernel, const void* s_kernel,
+                                int64_t M, int64_t N, int64_t K, int32_t G, void* out, wq_stream_t stream);
+
 /* ------------------------------------------------------------------ device status */
 
 /* Reads the current device's status word: bit 0..3 = a bounded wait timed out in

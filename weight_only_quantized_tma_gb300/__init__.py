@@ -18,6 +18,7 @@ from ._lib import (  # noqa: F401
     wq_fp4_packed_sf_bytes,
     wq_gemm_bf16_fp4,
     wq_gemm_w4a16,
+    wq_gemm_w4a16_noalloc,
     wq_gemm_w8a16_fp8,
     wq_int4_packed_bytes,
     wq_pack_fp4_sf,

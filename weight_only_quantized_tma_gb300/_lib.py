@@ -70,7 +70,10 @@ _SIGNATURES = {
     "wq_device_status": (ctypes.c_int, [ctypes.POINTER(ctypes.c_uint32)]),
     "wq_clear_device_status": (ctypes.c_int, []),
     "wq_debug_wait_probe": (ctypes.c_int, [_i64, _vp]),
+    "wq_gemm_w4a16_noalloc": (ctypes.c_int, [_vp, ctypes.c_int, _vp, _vp, _i64, _i64, _i64, _i32, _vp, _vp]),
 }
+
+WQ_NOALLOC_SCRATCH_BYTES = 4 << 20
 
 
 def lib():
@@ -212,6 +215,21 @@ def wq_gemm_w4a16(A: torch.Tensor, w_kernel: torch.Tensor, s_kernel: torch.Tenso
         ws_bytes = ws.numel() * ws.element_size()
     _check(lib().wq_gemm_w4a16(_ptr(A), a_dtype, _ptr(w_kernel), _ptr(s_kernel), M, N, K, G, _ptr(out), _ptr(ws),
                                ws_bytes, _stream(A)), "wq_gemm_w4a16")
+    return out
+
+
+def wq_gemm_w4a16_noalloc(A: torch.Tensor, w_kernel: torch.Tensor, s_kernel: torch.Tensor, N: int, K: int, G: int,
+                          out: torch.Tensor = None) -> torch.Tensor:
+    """wq_gemm_w4a16 without a workspace argument, for callers that cannot allocate
+    device memory (the split-K scratch is a fixed array inside the library)."""
+    a_dtype = _adtype(A)
+    _need(A, "A", A.dtype)
+    M = A.shape[0]
+    if out is None:
+        out = torch.empty((M, N), dtype=A.dtype, device=A.device)
+    _need(out, "out", A.dtype, (M, N))
+    _check(lib().wq_gemm_w4a16_noalloc(_ptr(A), a_dtype, _ptr(w_kernel), _ptr(s_kernel), M, N, K, G, _ptr(out),
+                                       _stream(A)), "wq_gemm_w4a16_noalloc")
     return out
 
 
