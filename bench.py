@@ -405,6 +405,47 @@ def run_ours(args, rank, world, local_rank):
     print(json.dumps(line), flush=True)
 
 
+def run_case(args):
+    """Runs one GEMM `--reps` times (a small, self-contained target for ncu)."""
+    import torch
+    import weight_only_quantized_tma_gb300 as wq
+    from weight_only_quantized_tma_gb300 import build as wq_build
+    from weight_only_quantized_tma_gb300 import synth
+    wq_build.build()
+    op, *dims = args.case.split(":")
+    M, N, K = (int(x) for x in dims[:3])
+    dev = torch.device("cuda", 0)
+    seed = 7
+    if op == "w4a16":
+        Gc = int(dims[3]) if len(dims) > 3 else 128
+        A = torch.from_numpy(synth.activations(M, K, "f16", seed).view(np.float16)).to(dev)
+        w = synth.int4_weights(N, K, Gc, seed + 1)
+        wk, sk = wq.wq_pack_int4(torch.from_numpy(w.w).to(dev), torch.from_numpy(w.s.view(np.float16)).to(dev),
+                                 N, K, Gc)
+        fn = lambda: wq.wq_gemm_w4a16(A, wk, sk, N, K, Gc)
+    elif op == "fp8":
+        A = torch.from_numpy(synth.activations(M, K, "bf16", seed).view(np.int16)).view(torch.bfloat16).to(dev)
+        w = synth.fp8_weights(N, K, seed + 1)
+        wd = torch.from_numpy(w.w).to(dev)
+        alpha = torch.tensor([w.scale], dtype=torch.float32, device=dev)
+        fn = lambda: wq.wq_gemm_w8a16_fp8(A, wd, alpha)
+    elif op == "fp4":
+        A = torch.from_numpy(synth.activations(M, K, "bf16", seed).view(np.int16)).view(torch.bfloat16).to(dev)
+        w = synth.fp4_weights(N, K, seed + 1)
+        wd = torch.from_numpy(w.w).to(dev)
+        sfk = wq.wq_pack_fp4_sf(torch.from_numpy(w.sf).to(dev), N, K)
+        alpha = torch.tensor([w.alpha], dtype=torch.float32, device=dev)
+        fn = lambda: wq.wq_gemm_bf16_fp4(A, wd, sfk, alpha)
+    else:
+        raise SystemExit(f"unknown case {args.case}")
+    for _ in range(args.reps):
+        fn()
+    torch.cuda.synchronize(dev)
+    print(json.dumps({"case": args.case, "reps": args.reps, "plan": wq.get_plan(
+        {"w4a16": wq.WQ_OP_W4A16, "fp8": wq.WQ_OP_FP8, "fp4": wq.WQ_OP_FP4}[op],
+        wq.WQ_F16 if op == "w4a16" else wq.WQ_BF16, M, N, K, int(dims[3]) if len(dims) > 3 else 128)}))
+
+
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
@@ -414,7 +455,13 @@ def main():
     ap.add_argument("--skip-prefill", action="store_true")
     ap.add_argument("--skip-cpu", action="store_true")
     ap.add_argument("--cpu-seconds", type=float, default=10.0)
+    ap.add_argument("--case", default=None,
+                    help="profiling target: run one GEMM, e.g. w4a16:16:4096:4096:128, fp8:M:N:K, fp4:M:N:K")
+    ap.add_argument("--reps", type=int, default=5)
     args = ap.parse_args()
+    if args.case:
+        run_case(args)
+        return
     if args.warmup < 3:
         ap.error("--warmup must be at least 3")
     world = int(os.environ.get("WORLD_SIZE", "1"))
