@@ -109,6 +109,16 @@ class ClockSampler:
                                          stdout=self.f, stderr=subprocess.DEVNULL)
         except OSError:
             self.proc = None
+        # nvidia-smi takes a moment to print its first line: wait for it (bounded) so
+        # the sampler is live when the timed region starts
+        t0 = time.time()
+        while self.proc is not None and time.time() - t0 < 5.0:
+            try:
+                if os.path.getsize(self.path) > 0:
+                    break
+            except OSError:
+                break
+            time.sleep(0.05)
         return self
 
     def __exit__(self, *exc):
@@ -390,7 +400,7 @@ def run_ours(args, rank, world, local_rank):
                      "frac": round(achieved / peaks["hbm_gbs"], 4), "traffic": traffic,
                      "peak_source": f"{peaks_src} (MEASURED_PEAKS.json hbm_gbs)" if peaks_src == "measured"
                      else "fallback 6.8 TB/s",
-                     "kernel": "wq_gemm_kernel<INT4, f16, BN=16> (decode, split-K)",
+                     "kernel": "wq_decode_mma_kernel<f16, NT=1|2, BK=128> (register-resident mma.sync, split-K)",
                      "achieved_from": "CUDA events around each launch, per-launch pass after the timed region"},
         "per_gemm": sorted(per_gemm, key=lambda d: (d["M"], d["N"], d["K"])),
         "prefill": prefill,

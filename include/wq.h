@@ -77,9 +77,11 @@ wq_status wq_int4_packed_bytes(int64_t N, int64_t K, int32_t G, size_t* w_bytes,
 /* Offline layout transform (a pure permutation; bit-exact and invertible).
  * Reorders canonical packed codes w_canon uint8 [N][K/2] and fp16 scales s_canon
  * [K/G][N] into the tile-major order the GEMM kernels stream with bulk copies:
- * for each 128-row tile, 32-code chunks along K, and within a chunk each row's 16
- * bytes with the even k of every 8 in the low half-word, so that the in-kernel
- * unpack yields (k, k+1) operand pairs with shift/mask only.  Padding rows and
+ * for each 128-row tile and 128-value k-block, the codes of every 16-row group in
+ * the register order of a 16x16 tensor-core operand fragment (each 32-bit word is
+ * one lane's fragment for one 16-wide k step), so the in-kernel unpack is one
+ * mask-and-or per operand register and needs no shared-memory shuffle; scales as
+ * [tile][K/G][128 rows].  Padding rows and
  * columns get code 8 and scale 0 (weight 0).  Why: "Bitblas -- Mixed-Precision
  * GEMM with the Ladder Compiler" (GPU MODE lecture 33), introduction -- when the
  * weight layout does not match what the tensor-core operand wants, the layout
@@ -111,7 +113,14 @@ wq_status wq_debug_dequant_int4(const uint8_t* w_kernel, const void* s_kernel, i
  * device status may not).  One workspace may serve calls of any shape, but calls
  * that share it must not overlap on the GPU.  The dequantized operand is
  * RN((q - 8) * s) in the type of A, accumulated in fp32; split-K partial sums
- * are reduced in a fixed order, so results are identical run to run. */
+ * are reduced in a fixed order, so results are identical run to run.  For
+ * M <= 16 with K % 64 == 0 the sum is formed as s * sum_k A (q - 8) per group in
+ * fp32 (exact products, no rounding of the operand).
+ * The kernel may start while the kernel before it on the stream is finishing
+ * (programmatic dependent launch); it reads w_kernel and s_kernel before it waits
+ * for that kernel, and A, out and ws only after.  So the kernel immediately before
+ * the call on the stream must not write w_kernel or s_kernel (wq_pack_int4 ends
+ * with an ordinary launch for this reason). */
 wq_status wq_gemm_w4a16(const void* A, wq_dtype a_dtype, const uint8_t* w_kernel, const void* s_kernel,
                         int64_t M, int64_t N, int64_t K, int32_t G, void* out, void* ws, size_t ws_bytes,
                         wq_stream_t stream);
@@ -165,7 +174,7 @@ typedef struct {
     int32_t bn;           /* tokens per tile (tcgen05 MMA N) */
     int32_t bk;           /* k per pipeline stage */
     int32_t stages;       /* shared-memory pipeline depth */
-    int32_t splits;       /* split-K slices per output tile */
+    int32_t splits;       /* CTAs sharing one output tile's K range (decode: rounded up) */
     int32_t grid;         /* CTAs launched */
     int32_t threads;      /* threads per CTA */
     int32_t smem_bytes;   /* dynamic shared memory per CTA */
@@ -174,7 +183,14 @@ typedef struct {
     int32_t tiles_n;
     int32_t tiles_m;
     int32_t ctas_per_sm;  /* resident CTAs per SM assumed by the plan */
+    int32_t kernel;       /* WQ_KERNEL_TILE or WQ_KERNEL_DECODE */
 } wq_plan;
+
+/* Kernels a plan can pick.  TILE: the tcgen05 kernel (weights dequantized into
+ * tensor memory, any M).  DECODE: W4A16 with M <= 16 and K % 64 == 0, operands
+ * built in registers from the fragment-order layout, group scale applied in fp32. */
+#define WQ_KERNEL_TILE 0
+#define WQ_KERNEL_DECODE 1
 
 /* Plan and workspace size for op (a_dtype is ignored for WQ_OP_FP4, G for FP8
  * and FP4).  Either output pointer may be NULL.  Host only. */
@@ -188,7 +204,7 @@ wq_status wq_workspace_bytes(wq_op op, wq_dtype a_dtype, int64_t M, int64_t N, i
 /* ------------------------------------------------------------------ no caller workspace */
 
 /* Bytes of split-K scratch built into the library for wq_gemm_w4a16_noalloc. */
-#define WQ_NOALLOC_SCRATCH_BYTES (4u << 20)
+#define WQ_NOALLOC_SCRATCH_BYTES (8u << 20)
 
 /* W4A16 GEMM that takes no workspace.  The paper has no counterpart: this entry
  * point is for callers that cannot allocate device memory themselves -- a framework

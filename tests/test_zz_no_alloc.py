@@ -30,12 +30,17 @@ def _call(L, p, out):
                                    ctypes.c_void_p(out.data_ptr()), stream)
 
 
-@pytest.mark.parametrize("M,N,K", [(16, 4096, 4096), (1, 11008, 4096)])
-def test_noalloc_matches_workspace_entry_on_two_calls(M, N, K):
+@pytest.mark.parametrize("M,N,K,scratch", [(32, 4096, 1024, True), (20, 1024, 2048, True), (1, 11008, 4096, False),
+                                           (16, 4096, 4096, False)])
+def test_noalloc_matches_workspace_entry_on_two_calls(M, N, K, scratch):
     G = 128
     plan = wq.get_plan(wq.WQ_OP_W4A16, wq.WQ_F16, M, N, K, G)
-    # the problem uses split-K, so the built-in scratch is really exercised
-    assert plan["splits"] > 1 and 0 < plan["ws_bytes"] <= _lib.WQ_NOALLOC_SCRATCH_BYTES
+    if scratch:
+        # tile-kernel split-K: the built-in scratch is really exercised
+        assert plan["splits"] > 1 and 0 < plan["ws_bytes"] <= _lib.WQ_NOALLOC_SCRATCH_BYTES
+    else:
+        # the decode kernel reduces split-K inside a cluster and needs no scratch
+        assert plan["kernel"] == wq.WQ_KERNEL_DECODE and plan["ws_bytes"] == 0
     p = Int4Problem(M, N, K, G, seed=901 + M).pack()
     expected = p.run()                       # the entry point with a caller workspace
     torch.cuda.synchronize()
@@ -49,7 +54,7 @@ def test_noalloc_matches_workspace_entry_on_two_calls(M, N, K):
 
 
 def test_noalloc_rejects_problems_beyond_its_scratch():
-    M, N, K, G = 64, 4096, 4096, 128
+    M, N, K, G = 256, 2048, 4096, 128
     plan = wq.get_plan(wq.WQ_OP_W4A16, wq.WQ_F16, M, N, K, G)
     assert plan["ws_bytes"] > _lib.WQ_NOALLOC_SCRATCH_BYTES
     p = Int4Problem(M, N, K, G, seed=950).pack()

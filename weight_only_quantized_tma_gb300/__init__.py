@@ -26,6 +26,8 @@ from ._lib import (  # noqa: F401
     wq_unpack_int4,
     WQ_BF16,
     WQ_F16,
+    WQ_KERNEL_DECODE,
+    WQ_KERNEL_TILE,
     WQ_OP_FP4,
     WQ_OP_FP8,
     WQ_OP_W4A16,

@@ -20,6 +20,7 @@ LIB_PATH = os.path.join(_HERE, "libwq.so")
 
 WQ_F16, WQ_BF16 = 0, 1
 WQ_OP_W4A16, WQ_OP_FP8, WQ_OP_FP4 = 0, 1, 2
+WQ_KERNEL_TILE, WQ_KERNEL_DECODE = 0, 1
 STATUS_NAMES = {
     0: "WQ_OK", 1: "WQ_ERR_NULL", 2: "WQ_ERR_SHAPE", 3: "WQ_ERR_GROUP", 4: "WQ_ERR_MISALIGNED",
     5: "WQ_ERR_DTYPE", 6: "WQ_ERR_WORKSPACE", 7: "WQ_ERR_UNSUPPORTED_DEVICE", 8: "WQ_ERR_CUDA",
@@ -44,7 +45,7 @@ class WQError(RuntimeError):
 class WqPlan(ctypes.Structure):
     _fields_ = [(n, ctypes.c_int32) for n in (
         "bn", "bk", "stages", "splits", "grid", "threads", "smem_bytes", "n_items", "walk_n_fast",
-        "tiles_n", "tiles_m", "ctas_per_sm")]
+        "tiles_n", "tiles_m", "ctas_per_sm", "kernel")]
 
     def as_dict(self):
         return {n: getattr(self, n) for n, _ in self._fields_}
@@ -73,7 +74,7 @@ _SIGNATURES = {
     "wq_gemm_w4a16_noalloc": (ctypes.c_int, [_vp, ctypes.c_int, _vp, _vp, _i64, _i64, _i64, _i32, _vp, _vp]),
 }
 
-WQ_NOALLOC_SCRATCH_BYTES = 4 << 20
+WQ_NOALLOC_SCRATCH_BYTES = 8 << 20
 
 
 def lib():

@@ -103,15 +103,43 @@ struct Plan {
     KernelConfig cfg;
     int tiles_n, tiles_m, nkb, splits, n_items, grid, walk_n_fast;
     size_t ws_bytes;
+    bool decode;   // W4A16 decode kernel (register-resident mma.sync, M <= 16)
 };
 
-bool get_config(int fmt, bool bf16, int bn, bool query, KernelConfig* cfg) {
+bool get_config_uncached(int fmt, bool bf16, int bn, bool query, KernelConfig* cfg) {
+    if (fmt == FMT_INT4 + 16) return config_int4_decode(bf16, query, cfg);
     switch (fmt) {
         case FMT_INT4: return config_int4(bf16, bn, query, cfg);
         case FMT_FP8: return config_fp8(bf16, bn, query, cfg);
         case FMT_FP4: return config_fp4(bf16, bn, query, cfg);
     }
     return false;
+}
+
+// The device query behind a configuration (attributes, residency) is done once per
+// device and instantiation; later calls read the cached answer.
+struct ConfigCache {
+    std::mutex mu;
+    bool have[kMaxDevices][4][2][4] = {};
+    bool found[kMaxDevices][4][2][4] = {};
+    KernelConfig cfg[kMaxDevices][4][2][4];
+};
+ConfigCache g_cfg_cache;
+
+bool get_config(int fmt, bool bf16, int bn, bool query, KernelConfig* cfg) {
+    const int bi = bn == 16 ? 0 : bn == 64 ? 1 : bn == 128 ? 2 : bn == 256 ? 3 : -1;
+    const int fi = fmt == FMT_INT4 + 16 ? 3 : fmt;     // slot 3: the W4A16 decode kernel
+    int dev = 0;
+    if (!query || bi < 0 || fi < 0 || fi > 3 || cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices)
+        return get_config_uncached(fmt, bf16, bn, query, cfg);
+    std::lock_guard<std::mutex> lock(g_cfg_cache.mu);
+    const int b = bf16 ? 1 : 0;
+    if (!g_cfg_cache.have[dev][fi][b][bi]) {
+        g_cfg_cache.found[dev][fi][b][bi] = get_config_uncached(fmt, bf16, bn, true, &g_cfg_cache.cfg[dev][fi][b][bi]);
+        g_cfg_cache.have[dev][fi][b][bi] = true;
+    }
+    if (g_cfg_cache.found[dev][fi][b][bi]) *cfg = g_cfg_cache.cfg[dev][fi][b][bi];
+    return g_cfg_cache.found[dev][fi][b][bi];
 }
 
 // Split-K workspace: a fixed region of arrival counters (8 per output tile, room
@@ -132,14 +160,20 @@ size_t split_ws_bytes(int tiles, int splits, int bn) {
 //  * split-K when the output tiles cannot occupy every CTA slot of the GPU
 //    (decode): slices = slots / tiles, each slice at least two k-blocks, at most
 //    16 -- the motivation is the "fused split-K fix-up for grids that do not fill
-//    the SMs" of "FlashInfer W8A16 GEMM (mm_bf16_fp8) analysis", §1;
+//    the SMs" of "FlashInfer W8A16 GEMM (mm_bf16_fp8) analysis", §1.  The decode
+//    kernel reduces its slices inside a thread-block cluster instead (no workspace);
 //  * tile walk order ("FlashInfer W8A16 GEMM (mm_bf16_fp8) analysis", §4): when
 //    the weight is the smaller operand, walk weight-row tiles fastest so the
 //    activation panel being reused stays in L2, else walk token tiles fastest.
-wq_status make_plan(int fmt, bool bf16, int64_t M, int64_t N, int64_t K, int sms, int w_bits, Plan* plan) {
+wq_status make_plan(int fmt, bool bf16, int64_t M, int64_t N, int64_t K, int sms, int w_bits, Plan* plan,
+                    int G = 0) {
     static const int kTiles[4] = {16, 64, 128, 256};
     KernelConfig cfg{};
     bool found = false;
+    // decode (M <= 16): the register-resident kernel; its activation copy views A
+    // as 64-wide boxes, so it needs K % 64 == 0
+    const bool decode = fmt == FMT_INT4 && M <= 16 && K % 64 == 0;
+    if (decode) found = get_config(FMT_INT4 + 16, bf16, 16, sms > 0, &cfg);
     for (int i = 0; i < 4 && !found; ++i) {
         if (M <= kTiles[i] || i == 3) found = get_config(fmt, bf16, kTiles[i], sms > 0, &cfg);
     }
@@ -147,6 +181,7 @@ wq_status make_plan(int fmt, bool bf16, int64_t M, int64_t N, int64_t K, int sms
     if (!found) return WQ_ERR_DTYPE;
     Plan p{};
     p.cfg = cfg;
+    p.decode = decode;
     p.tiles_n = (int)((N + TILE_N - 1) / TILE_N);
     p.tiles_m = (int)((M + cfg.bn - 1) / cfg.bn);
     p.nkb = (int)((K + cfg.bk - 1) / cfg.bk);
@@ -161,25 +196,38 @@ wq_status make_plan(int fmt, bool bf16, int64_t M, int64_t N, int64_t K, int sms
         if (splits < 1) splits = 1;
     }
     p.splits = splits;
-    const long long items = tiles * splits;
+    long long items = tiles * splits;
+    if (decode) {
+        // split-K across a cluster of S CTAs (one slice each): S <= 16, at least two
+        // k-blocks per slice, tiles x S within the CTAs the GPU holds at once (the
+        // kernel's shared memory is sized so that this is two per SM: the decode
+        // consumer is compute-bound, and a third CTA on some SMs would make them the
+        // tail), and all clusters in one wave; the largest such S
+        const long long budget = (long long)(sms > 0 ? sms : 148) * (cfg.ctas_per_sm > 0 ? cfg.ctas_per_sm : 1);
+        int best = 1;
+        for (int S = 2; S <= kMaxDecodeCluster; ++S)
+            if (p.nkb >= 2 * S && tiles * S <= budget && tiles <= cfg.max_clusters[S]) best = S;
+        p.splits = best;
+        items = tiles * best;
+    }
     if (items >= (1LL << 31)) return WQ_ERR_SHAPE;
     p.n_items = (int)items;
-    p.grid = (int)(items < slots ? items : slots);
+    p.grid = (int)(items < slots || decode ? items : slots);
     const double w_bytes = (double)N * (double)K * w_bits / 8.0;
     const double a_bytes = (double)M * (double)K * 2.0;
     p.walk_n_fast = w_bytes < a_bytes ? 1 : 0;
-    p.ws_bytes = split_ws_bytes((int)tiles, splits, cfg.bn);
+    p.ws_bytes = decode ? 0 : split_ws_bytes((int)tiles, splits, cfg.bn);
     *plan = p;
     return WQ_OK;
 }
 
 int w_bits_of(int fmt) { return fmt == FMT_INT4 ? 4 : fmt == FMT_FP8 ? 8 : 4; }
 
-wq_status plan_for(int fmt, bool bf16, int64_t M, int64_t N, int64_t K, Plan* plan) {
+wq_status plan_for(int fmt, bool bf16, int64_t M, int64_t N, int64_t K, Plan* plan, int G) {
     DeviceInfo* d = nullptr;
     wq_status st = device_info(&d);
     if (st != WQ_OK) return st;
-    return make_plan(fmt, bf16, M, N, K, d->sms, w_bits_of(fmt), plan);
+    return make_plan(fmt, bf16, M, N, K, d->sms, w_bits_of(fmt), plan, G);
 }
 
 void fill_common(GemmParams& gp, const Plan& pl, int64_t M, int64_t N, int64_t K, void* out, void* ws,
@@ -192,6 +240,8 @@ void fill_common(GemmParams& gp, const Plan& pl, int64_t M, int64_t N, int64_t K
     gp.tiles_m = pl.tiles_m;
     gp.splits = pl.splits;
     gp.nkb = pl.nkb;
+    gp.kb_base = pl.nkb / pl.splits;
+    gp.kb_rem = pl.nkb % pl.splits;
     gp.n_items = pl.n_items;
     gp.walk_n_fast = pl.walk_n_fast;
     gp.w_evict_first = pl.tiles_m == 1 ? 1 : 0;
@@ -199,7 +249,7 @@ void fill_common(GemmParams& gp, const Plan& pl, int64_t M, int64_t N, int64_t K
     gp.div_splits = make_fastdiv(pl.splits, (uint32_t)pl.n_items);
     gp.status = status;
     gp.timeout_ns = kTimeoutNs;
-    if (pl.splits > 1) {
+    if (pl.ws_bytes > 0) {
         gp.ws_count = static_cast<uint32_t*>(ws);
         gp.ws_part = reinterpret_cast<float*>(static_cast<uint8_t*>(ws) + kCounterBytes);
     }
@@ -212,9 +262,32 @@ wq_status check_ws(const Plan& pl, const void* ws, size_t ws_bytes) {
     return WQ_OK;
 }
 
+// Activation tensor map.  When one token tile covers all M rows, the box holds only
+// those rows: the tile's remaining rows stay unwritten (they only reach accumulator
+// columns that are never stored) and the copy engine does no out-of-range fill.
 bool encode_a(GemmParams& gp, const void* A, bool bf16, int64_t M, int64_t K, int bn) {
+    const int rows = M < bn ? (int)M : bn;
+    gp.a_box_rows = rows;
     return encode_2d(&gp.tmap_a, bf16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT16, A,
-                     (uint64_t)K, (uint64_t)M, (uint64_t)K * 2, 64, (uint32_t)bn, CU_TENSOR_MAP_SWIZZLE_128B);
+                     (uint64_t)K, (uint64_t)M, (uint64_t)K * 2, 64, (uint32_t)rows, CU_TENSOR_MAP_SWIZZLE_128B);
+}
+
+// Activation tensor map of the decode kernel: A [M][K] viewed as {64 k, M rows,
+// K / 64 boxes} (strides 2K and 128 bytes), so one copy brings a whole k-block of
+// every token row, 64-wide boxes one after the other in shared memory (row
+// z * M + m), each row 128 bytes with the 128-byte swizzle.  Needs K % 64 == 0.
+bool encode_a_boxes(GemmParams& gp, const void* A, bool bf16, int64_t M, int64_t K, int bk) {
+    auto fn = encode_fn();
+    if (!fn || K % 64 != 0 || M > 16) return false;
+    gp.a_box_rows = (int)M;
+    cuuint64_t dims[3] = {64, (cuuint64_t)M, (cuuint64_t)(K / 64)};
+    cuuint64_t strides[2] = {(cuuint64_t)K * 2, 128};
+    cuuint32_t box[3] = {64, (cuuint32_t)M, (cuuint32_t)(bk / 64)};
+    cuuint32_t es[3] = {1, 1, 1};
+    CUresult r = fn(&gp.tmap_a, bf16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 3,
+                    const_cast<void*>(A), dims, strides, box, es, CU_TENSOR_MAP_INTERLEAVE_NONE,
+                    CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    return r == CUDA_SUCCESS;
 }
 
 wq_status finish_launch(cudaError_t e) { return e == cudaSuccess ? WQ_OK : WQ_ERR_CUDA; }
@@ -339,7 +412,7 @@ wq_status wq_get_plan(wq_op op, wq_dtype a_dtype, int64_t M, int64_t N, int64_t 
     if (a_dtype != WQ_F16 && a_dtype != WQ_BF16) return WQ_ERR_DTYPE;
     const bool bf16 = (op == WQ_OP_FP4) ? true : (a_dtype == WQ_BF16);
     Plan pl{};
-    wq_status st = plan_for((int)op, bf16, M > 0 ? M : 1, N, K, &pl);
+    wq_status st = plan_for((int)op, bf16, M > 0 ? M : 1, N, K, &pl, op == WQ_OP_W4A16 ? G : 0);
     if (st != WQ_OK) return st;
     if (plan) {
         plan->bn = pl.cfg.bn;
@@ -354,6 +427,7 @@ wq_status wq_get_plan(wq_op op, wq_dtype a_dtype, int64_t M, int64_t N, int64_t 
         plan->tiles_n = pl.tiles_n;
         plan->tiles_m = pl.tiles_m;
         plan->ctas_per_sm = pl.cfg.ctas_per_sm;
+        plan->kernel = pl.decode ? WQ_KERNEL_DECODE : WQ_KERNEL_TILE;
     }
     if (ws_bytes) *ws_bytes = (M == 0) ? 0 : pl.ws_bytes;
     return WQ_OK;
@@ -380,18 +454,21 @@ wq_status wq_gemm_w4a16(const void* A, wq_dtype a_dtype, const uint8_t* w_kernel
     if (M == 0) return WQ_OK;
     const bool bf16 = a_dtype == WQ_BF16;
     Plan pl{};
-    if ((st = make_plan(FMT_INT4, bf16, M, N, K, d->sms, 4, &pl)) != WQ_OK) return st;
+    if ((st = make_plan(FMT_INT4, bf16, M, N, K, d->sms, 4, &pl, G)) != WQ_OK) return st;
     if ((st = check_ws(pl, ws, ws_bytes)) != WQ_OK) return st;
     GemmParams gp;
     std::memset(&gp, 0, sizeof(gp));
-    if (!encode_a(gp, A, bf16, M, K, pl.cfg.bn)) return WQ_ERR_CUDA;
+    if (pl.decode ? !encode_a_boxes(gp, A, bf16, M, K, pl.cfg.bk) : !encode_a(gp, A, bf16, M, K, pl.cfg.bn))
+        return WQ_ERR_CUDA;
     gp.w = w_kernel;
     gp.sc = static_cast<const uint8_t*>(s_kernel);
     gp.G = G;
+    gp.g_shift = G == 32 ? 5 : G == 64 ? 6 : G == 128 ? 7 : 8;
     const int64_t Kp = round_up(K, KPAD_INT4);
     gp.ngroups_pad = (int)(Kp / G);
     gp.nchunks_pad = (int)(Kp / 32);
     fill_common(gp, pl, M, N, K, out, ws, d->status);
+    if (pl.decode) return finish_launch(launch_gemm_int4_decode(gp, bf16, pl.grid, (cudaStream_t)stream));
     return finish_launch(launch_gemm_int4(gp, bf16, pl.cfg.bn, pl.grid, (cudaStream_t)stream));
 }
 

@@ -112,39 +112,54 @@ __device__ __forceinline__ bool drain_wait(uint32_t bar, uint32_t parity, long l
 
 // ---------------------------------------------------------------- conversions
 
-// INT4 -> f16 operands for one 16-byte chunk of the prepacked layout (32 codes of
-// one weight row).  Word j holds k = 8j..8j+7 of the chunk: the even k in its low
-// half-word (nibble i at bits 4i), the odd k in its high half-word.  The fp16
-// "magic number" trick turns a nibble into 1024 + q (nibble at bits 0-3, exponent
-// 2^10) or 64 + q (nibble at bits 4-7, exponent 2^6, where the mantissa unit is
-// 1/16); subtracting 1032 or 72 gives q - 8 exactly, and one multiply by the
-// group scale rounds once: RN16((q - 8) * s).  Output o[4j + i] holds the pair
-// (k = 8j + 2i, 8j + 2i + 1), low half first.
-__device__ __forceinline__ void int4_to_f16(const uint4& q, uint32_t s2, uint32_t (&o)[16]) {
-    const uint32_t wv[4] = {q.x, q.y, q.z, q.w};
+// INT4 operands of one weight row for 32 values of K, gathered from the
+// fragment-order layout (wq_internal.h): four lanes' 8-byte halves (c = 0..3), two
+// words each (k steps t = 0, 1 of the unit).  The row is the lower (h = 0) or the
+// upper (h = 1) half of its 16-row group, so its codes sit at bits 0-3/16-19 and
+// 8-11/24-27 of each word (h = 0) or at bits 4-7/20-23 and 12-15/28-31 (h = 1).
+// The fp16 "magic number" trick turns a nibble into 1024 + q (bits 0-3, exponent
+// 2^10) or 64 + q (bits 4-7, exponent 2^6 where the mantissa unit is 1/16);
+// subtracting 1032 or 72 gives q - 8 exactly, and one multiply by the group scale
+// rounds once: RN16((q - 8) * s).  Output o[8t + c] holds the pair
+// (k = 16t + 2c, +1), o[8t + 4 + c] the pair (k = 16t + 8 + 2c, +1).
+struct Int4RowConsts {
+    uint32_t mask, magic, bias;   // per row half
+};
+__device__ __forceinline__ Int4RowConsts int4_row_consts(int h) {
+    return h ? Int4RowConsts{0x00F000F0u, 0x54005400u, 0x54805480u}   // 64 + q, minus 72
+             : Int4RowConsts{0x000F000Fu, 0x64006400u, 0x64086408u};  // 1024 + q, minus 1032
+}
+
+__device__ __forceinline__ void int4_row_to_f16(const uint2 (&w)[4], const Int4RowConsts& k, uint32_t s2,
+                                                uint32_t (&o)[16]) {
 #pragma unroll
-    for (int j = 0; j < 4; ++j) {
-        const uint32_t x = wv[j];
-        const uint32_t x8 = x >> 8;
-        o[4 * j + 0] = ptx::hmul2_u32(ptx::hsub2_u32(ptx::lop3_and_or(x, 0x000F000Fu, 0x64006400u), 0x64086408u), s2);
-        o[4 * j + 1] = ptx::hmul2_u32(ptx::hsub2_u32(ptx::lop3_and_or(x, 0x00F000F0u, 0x54005400u), 0x54805480u), s2);
-        o[4 * j + 2] = ptx::hmul2_u32(ptx::hsub2_u32(ptx::lop3_and_or(x8, 0x000F000Fu, 0x64006400u), 0x64086408u), s2);
-        o[4 * j + 3] = ptx::hmul2_u32(ptx::hsub2_u32(ptx::lop3_and_or(x8, 0x00F000F0u, 0x54005400u), 0x54805480u), s2);
+    for (int c = 0; c < 4; ++c) {
+        const uint32_t wt[2] = {w[c].x, w[c].y};
+#pragma unroll
+        for (int t = 0; t < 2; ++t) {
+            const uint32_t lo = ptx::lop3_and_or(wt[t], k.mask, k.magic);
+            const uint32_t hi = ptx::lop3_and_or(wt[t] >> 8, k.mask, k.magic);
+            o[8 * t + c] = ptx::hmul2_u32(ptx::hsub2_u32(lo, k.bias), s2);
+            o[8 * t + 4 + c] = ptx::hmul2_u32(ptx::hsub2_u32(hi, k.bias), s2);
+        }
     }
 }
 
-// INT4 -> bf16 operands: (q - 8) is exact in fp32 (2^23 magic), (q - 8) * s is
-// exact in fp32 (4 + 11 significant bits), one rounding to bf16.
-__device__ __forceinline__ void int4_to_bf16(const uint4& q, float s, uint32_t (&o)[16]) {
-    const uint32_t wv[4] = {q.x, q.y, q.z, q.w};
+// Same gather for bf16 operands: q - 8 is exact in fp16, (q - 8) * s is exact in
+// fp32 (4 + 11 significant bits), one rounding to bf16.
+__device__ __forceinline__ void int4_row_to_bf16(const uint2 (&w)[4], const Int4RowConsts& k, float s,
+                                                 uint32_t (&o)[16]) {
 #pragma unroll
-    for (int j = 0; j < 4; ++j) {
+    for (int c = 0; c < 4; ++c) {
+        const uint32_t wt[2] = {w[c].x, w[c].y};
 #pragma unroll
-        for (int i = 0; i < 4; ++i) {
-            const uint32_t t = (wv[j] >> (4 * i)) & 0x000F000Fu;
-            const float lo = __uint_as_float(0x4B000000u | (t & 0xFu)) - 8388616.0f;
-            const float hi = __uint_as_float(0x4B000000u | (t >> 16)) - 8388616.0f;
-            o[4 * j + i] = ptx::f32x2_to_bf16x2(lo * s, hi * s);
+        for (int t = 0; t < 2; ++t) {
+            const uint32_t lo = ptx::hsub2_u32(ptx::lop3_and_or(wt[t], k.mask, k.magic), k.bias);
+            const uint32_t hi = ptx::hsub2_u32(ptx::lop3_and_or(wt[t] >> 8, k.mask, k.magic), k.bias);
+            const float2 fl = __half22float2(*reinterpret_cast<const __half2*>(&lo));
+            const float2 fh = __half22float2(*reinterpret_cast<const __half2*>(&hi));
+            o[8 * t + c] = ptx::f32x2_to_bf16x2(fl.x * s, fl.y * s);
+            o[8 * t + 4 + c] = ptx::f32x2_to_bf16x2(fh.x * s, fh.y * s);
         }
     }
 }
@@ -216,8 +231,10 @@ __device__ __forceinline__ Item decode_item(const GemmParams& p, int item) {
         it.n_tile = (int)nt;
         it.m_tile = (int)t - (int)nt * p.tiles_m;
     }
-    it.kb_begin = (int)(((long long)it.slice * p.nkb) / p.splits);
-    it.kb_end = (int)(((long long)(it.slice + 1) * p.nkb) / p.splits);
+    // no division on the device: nkb = kb_base * splits + kb_rem, the first kb_rem
+    // slices take one extra k-block
+    it.kb_begin = it.slice * p.kb_base + min(it.slice, p.kb_rem);
+    it.kb_end = it.kb_begin + p.kb_base + (it.slice < p.kb_rem ? 1 : 0);
     return it;
 }
 
@@ -273,6 +290,9 @@ __global__ void __launch_bounds__(128 * (1 + NWG), (GemmCfg<FMT, BF16, BN, BK, S
     __syncthreads();
     ptx::tc_fence_after();
     const uint32_t tmem = *tmem_slot;
+    // The next kernel on the stream may start its own set-up now (programmatic
+    // dependent launch); it waits for this grid before touching shared data.
+    if (threadIdx.x == 0) ptx::grid_launch_dependents();
 
     if (warp == 0) {
         // ------------------------------------------------------------ producer
@@ -283,6 +303,9 @@ __global__ void __launch_bounds__(128 * (1 + NWG), (GemmCfg<FMT, BF16, BN, BK, S
             uint32_t ph = 0;
             long long issued = 0;
             bool ok = true;
+            // every global input may have been written by the previous kernel on the
+            // stream: wait for it (programmatic dependent launch) before the first copy
+            ptx::grid_dependency_wait();
             for (int item = blockIdx.x; item < p.n_items && ok; item += gridDim.x) {
                 const Item it = decode_item(p, item);
                 for (int kb = it.kb_begin; kb < it.kb_end; ++kb) {
@@ -292,12 +315,15 @@ __global__ void __launch_bounds__(128 * (1 + NWG), (GemmCfg<FMT, BF16, BN, BK, S
                         break;
                     }
                     const uint32_t fb = full_bar(s);
-                    uint32_t bytes = (uint32_t)C::B_STAGE;
+                    // activation rows >= M are not loaded: they only feed accumulator
+                    // columns that are never stored, and out-of-range rows would cost
+                    // the copy engine a zero fill
+                    uint32_t bytes = (uint32_t)((BK / 64) * p.a_box_rows * 128);
                     const uint32_t w_dst = sbase + C::OFF_W + s * C::W_STAGE;
                     const uint32_t sc_dst = sbase + C::OFF_SC + s * C::SC_STAGE;
                     uint32_t sc_bytes = 0;
                     if (FMT == FMT_INT4) {
-                        const int gcnt = (p.G >= BK) ? 1 : BK / p.G;
+                        const int gcnt = (p.G >= BK) ? 1 : (BK >> p.g_shift);
                         sc_bytes = (uint32_t)gcnt * TILE_N * 2;
                         bytes += C::W_STAGE + sc_bytes;
                     } else if (FMT == FMT_FP4) {
@@ -311,7 +337,7 @@ __global__ void __launch_bounds__(128 * (1 + NWG), (GemmCfg<FMT, BF16, BN, BK, S
                         const uint8_t* wsrc =
                             p.w + ((size_t)it.n_tile * p.nchunks_pad + (size_t)kb * (BK / 32)) * (TILE_N * 16);
                         ptx::bulk_load(w_dst, wsrc, C::W_STAGE, fb, pol_w);
-                        const int g0 = (kb * BK) / p.G;
+                        const int g0 = (kb * BK) >> p.g_shift;
                         const uint8_t* ssrc = p.sc + ((size_t)it.n_tile * p.ngroups_pad + g0) * (TILE_N * 2);
                         ptx::bulk_load(sc_dst, ssrc, sc_bytes, fb, pol_w);
                     } else if (FMT == FMT_FP4) {
@@ -404,6 +430,7 @@ __global__ void __launch_bounds__(128 * (1 + NWG), (GemmCfg<FMT, BF16, BN, BK, S
         int s = 0, a = 0;
         uint32_t ph = 0, aph = 0, accph = 0;
         bool ok = true;
+        ptx::grid_dependency_wait();   // alpha / bias are global inputs too
         const float alpha = (FMT == FMT_INT4) ? 1.0f : __ldg(p.alpha);
         for (int item = blockIdx.x; item < p.n_items && ok; item += gridDim.x) {
             const Item it = decode_item(p, item);
@@ -430,29 +457,45 @@ __global__ void __launch_bounds__(128 * (1 + NWG), (GemmCfg<FMT, BF16, BN, BK, S
                     }
                 } else {
                     constexpr int CH = BK / 32;  // 16-byte chunks (32 codes, 16 columns) per row
+                    constexpr int CPW = CH / NWG;  // chunks per transform warpgroup
+                    const int c0 = wg * CPW;
+                    // all shared-memory loads first, then the conversions, then the TMEM
+                    // stores, so the units overlap instead of running back to back
+                    uint2 qi[CPW][4];     // INT4: four lanes' halves per 32-k unit
+                    uint4 q[CPW];         // FP4: one 16-byte chunk per 32-k unit
+                    uint16_t sv[CPW];
+                    const int gr = r >> 4, g8 = r & 7;
 #pragma unroll
-                    for (int c = wg * (CH / NWG); c < (wg + 1) * (CH / NWG); ++c) {
-                        uint32_t o[16];
+                    for (int i = 0; i < CPW; ++i) {
+                        const int c = c0 + i;
                         if (FMT == FMT_INT4) {
-                            const uint4 q = *reinterpret_cast<const uint4*>(wt + (c * TILE_N + r) * 16);
-                            const uint16_t sbits =
-                                *reinterpret_cast<const uint16_t*>(sct + (((c * 32) / p.G) * TILE_N + r) * 2);
-                            if (BF16) {
-                                int4_to_bf16(q, __half2float(__ushort_as_half(sbits)), o);
-                            } else {
-                                const uint32_t s2 = (uint32_t)sbits | ((uint32_t)sbits << 16);
-                                int4_to_f16(q, s2, o);
-                            }
+                            // unit c: quad c / 2 of the stage, k steps 2 (c % 2) and 2 (c % 2) + 1
+                            const uint8_t* ub = wt + (c >> 1) * 4096 + gr * 512 + (c & 1) * 8;
+#pragma unroll
+                            for (int l = 0; l < 4; ++l)
+                                qi[i][l] = *reinterpret_cast<const uint2*>(ub + int4_slot(4 * g8 + l) * 16);
+                            sv[i] = *reinterpret_cast<const uint16_t*>(sct + (((c * 32) >> p.g_shift) * TILE_N + r) * 2);
                         } else {
-                            const uint4 q = *reinterpret_cast<const uint4*>(wt + swz(r * C::W_PITCH + c * 16, C::W_SWZ));
-                            const uint16_t sfp =
-                                *reinterpret_cast<const uint16_t*>(sct + (c >> 1) * (TILE_N * 4) + r * 4 + (c & 1) * 2);
-                            fp4_to_bf16(q, sfp, o);
+                            q[i] = *reinterpret_cast<const uint4*>(wt + swz(r * C::W_PITCH + c * 16, C::W_SWZ));
+                            sv[i] = *reinterpret_cast<const uint16_t*>(sct + (c >> 1) * (TILE_N * 4) + r * 4 + (c & 1) * 2);
                         }
-                        ptx::tmem_st16(a_col + c * 16, o);
                     }
+                    uint32_t o[CPW][16];
+#pragma unroll
+                    for (int i = 0; i < CPW; ++i) {
+                        if (FMT == FMT_INT4) {
+                            const Int4RowConsts kc = int4_row_consts((r >> 3) & 1);
+                            if (BF16)
+                                int4_row_to_bf16(qi[i], kc, __half2float(__ushort_as_half(sv[i])), o[i]);
+                            else
+                                int4_row_to_f16(qi[i], kc, (uint32_t)sv[i] | ((uint32_t)sv[i] << 16), o[i]);
+                        } else {
+                            fp4_to_bf16(q[i], sv[i], o[i]);
+                        }
+                    }
+#pragma unroll
+                    for (int i = 0; i < CPW; ++i) ptx::tmem_st16(a_col + (c0 + i) * 16, o[i]);
                 }
-                // every lane's TMEM stores are complete before the warp's one arrival
                 ptx::tmem_wait_st();
                 ptx::tc_fence_before();
                 __syncwarp();
@@ -477,6 +520,7 @@ __global__ void __launch_bounds__(128 * (1 + NWG), (GemmCfg<FMT, BF16, BN, BK, S
             }
             accph ^= 1u;
             ptx::tc_fence_after();
+            ptx::grid_dependency_wait();   // outputs and workspace may still be in use by the previous kernel
             const int n = it.n_tile * TILE_N + r;
             const int m0 = it.m_tile * BN;
             constexpr int COLS = BN / NWG;         // accumulator columns per warpgroup
@@ -544,13 +588,21 @@ __global__ void __launch_bounds__(128 * (1 + NWG), (GemmCfg<FMT, BF16, BN, BK, S
                 if (last) {
                     __threadfence();
                     const float* base = p.ws_part + (size_t)(tile * p.splits) * BN * TILE_N;
+                    // all slices of a column are loaded before any is added (one L2 round
+                    // trip instead of one per slice), then summed in slice order 0..S-1
+                    constexpr int MAX_SPLITS = 16;
 #pragma unroll 1
                     for (int cc = c_begin; cc < c_begin + COLS; ++cc) {
                         const int m = m0 + cc;
                         if (m >= p.M) break;
+                        float v[MAX_SPLITS];
+#pragma unroll
+                        for (int sl = 0; sl < MAX_SPLITS; ++sl)
+                            v[sl] = sl < p.splits ? __ldcg(base + ((size_t)sl * BN + cc) * TILE_N + r) : 0.0f;
                         float acc = 0.0f;
-                        for (int sl = 0; sl < p.splits; ++sl)
-                            acc += __ldcg(base + ((size_t)sl * BN + cc) * TILE_N + r);
+#pragma unroll
+                        for (int sl = 0; sl < MAX_SPLITS; ++sl)
+                            if (sl < p.splits) acc += v[sl];
                         if (nvalid) store_out<BF16>(p.out, (size_t)m * p.N + n, alpha * acc + bias_v);
                     }
                 }
@@ -625,8 +677,12 @@ struct GemmLauncher {
         cfg.blockDim = dim3(C::NT, 1, 1);
         cfg.dynamicSmemBytes = C::SMEM_BYTES;
         cfg.stream = st;
-        cfg.attrs = nullptr;
-        cfg.numAttrs = 0;
+        // programmatic dependent launch: set-up overlaps the previous kernel's tail
+        cudaLaunchAttribute attr[1];
+        attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+        attr[0].val.programmaticStreamSerializationAllowed = 1;
+        cfg.attrs = attr;
+        cfg.numAttrs = 1;
         return cudaLaunchKernelEx(&cfg, kern, p);
     }
 };

@@ -1,5 +1,6 @@
 // wq_gemm_int4.cu -- W4A16 instantiations of the GEMM kernel.
 #include "wq_gemm.cuh"
+#include "wq_gemm_mma.cuh"
 
 namespace wq {
 
@@ -11,6 +12,34 @@ using I4F16_128 = GemmLauncher<FMT_INT4, false, 128, 128, 2, 2>;
 using I4F16_256 = GemmLauncher<FMT_INT4, false, 256, 64, 5, 2>;
 using I4BF16_16 = GemmLauncher<FMT_INT4, true, 16, 128, 8, 2>;
 using I4BF16_256 = GemmLauncher<FMT_INT4, true, 256, 64, 5, 2>;
+
+// Decode (M <= 16): register-resident mma.sync kernel, one 8-token column tile for
+// M <= 8, two for M <= 16, and the fold position (k steps per group) fixed at compile
+// time.  All instantiations share shared memory, threads and the cluster limits.
+template <bool BF16, int NT, int GSTEPS>
+using I4Dec = MmaDecodeLauncher<BF16, NT, GSTEPS, 128, 6>;
+
+bool config_int4_decode(bool bf16, bool query, KernelConfig* cfg) {
+    *cfg = bf16 ? I4Dec<true, 2, 8>::config(query) : I4Dec<false, 2, 8>::config(query);
+    return true;
+}
+
+template <bool BF16, int NT>
+static cudaError_t launch_dec_g(const GemmParams& p, int grid, cudaStream_t st) {
+    switch (p.G) {
+        case 32: return I4Dec<BF16, NT, 2>::launch(p, grid, st);
+        case 64: return I4Dec<BF16, NT, 4>::launch(p, grid, st);
+        case 128:
+        case 256: return I4Dec<BF16, NT, 8>::launch(p, grid, st);
+    }
+    return cudaErrorInvalidValue;
+}
+
+cudaError_t launch_gemm_int4_decode(const GemmParams& p, bool bf16, int grid, cudaStream_t st) {
+    if (p.M <= 8) return bf16 ? launch_dec_g<true, 1>(p, grid, st) : launch_dec_g<false, 1>(p, grid, st);
+    if (p.M <= 16) return bf16 ? launch_dec_g<true, 2>(p, grid, st) : launch_dec_g<false, 2>(p, grid, st);
+    return cudaErrorInvalidValue;
+}
 
 bool config_int4(bool bf16, int bn, bool query, KernelConfig* cfg) {
     if (!bf16) {

@@ -1,0 +1,526 @@
+// wq_gemm_mma.cuh -- W4A16 decode kernel (M <= 16 tokens).
+//
+// Decode is bound by HBM: each weight is used by at most 16 tokens.  The tcgen05
+// path pays a fixed cost per MMA instruction that, at 16 tokens, is larger than the
+// time HBM takes to deliver the instruction's weights (measured on GB300: ~38 ns per
+// M=128 N=16 K=16 MMA, ~50 ns per commit, ~170 ns per TMEM operand hand-off).  This
+// kernel keeps the contraction in registers instead: packed weights stream through a
+// bulk-copy ring into shared memory, each lane turns its 32-bit word straight into an
+// m16n8k16 A fragment, and mma.sync accumulates in fp32.  At full HBM rate an SM has
+// ~360 cycles per 8 KB of weights, so the instruction count per word decides the
+// speed: one shift and four AND-ORs per word (8 weights), no per-weight arithmetic.
+//
+// Operand: the fragment-order layout puts the codes of a fragment register at bits
+// 0-3/16-19 (rows g) or 4-7/20-23 (rows g + 8) of a word.  One AND-OR with an fp16
+// "magic number" gives b + q with b = 1024 (exponent 2^10) or b = 64 (exponent 2^6,
+// whose mantissa unit is 1/16); bf16 operands give 128 + q.  The MMA sums A (b + q)
+// exactly in fp32, and the group scale and the offset are applied once per group:
+//
+//   sum_{k in g} A[m,k] (q - 8) s  =  s * ( D[n,m] - (b_n + 8) * S_g[m] )
+//   D[n,m] = sum_{k in g} A[m,k] (b_n + q[n,k]),   S_g[m] = sum_{k in g} A[m,k]
+//
+// ("Low Bit Triton Kernels", §03: the dequantized value is (q - 8) * s).  S_g is the
+// same for every weight row: one warp of the CTA computes it per stage (an MMA with
+// an all-ones operand) and shares it through shared memory.
+//
+// Work split: one CTA per (128-row tile, K slice).  Warps: 0-3 compute (warp w owns
+// rows 32w .. 32w + 31 of the tile, so each row's sum lives in one warp), 4 computes
+// S, 5 is the producer.  When K is split, the S slices of a tile are the CTAs of one
+// thread-block cluster: each parks its fp32 partial tile in its own shared memory and
+// rank r adds rows [r R, r R + R) over the ranks in rank order through distributed
+// shared memory (R = ceil(128 / S)) -- deterministic, no workspace, and the
+// reduction is spread over all S CTAs.  The producer streams the weights and scales
+// of its first stages before waiting for the preceding kernel on the stream
+// (programmatic dependent launch): they are constant inputs; activations and outputs
+// are touched only after that wait.
+#pragma once
+
+#include "wq_gemm.cuh"
+
+namespace wq {
+
+template <int BK, int STAGES>
+struct MmaDecodeCfg {
+    static constexpr int NCW = 4;                             // compute warps
+    static constexpr int RGW = TILE_N / 16 / NCW;             // 16-row groups per compute warp
+    static constexpr int S_WARP = NCW;                        // activation-sum warp
+    static constexpr int P_WARP = NCW + 1;                    // producer warp
+    static constexpr int NTHREADS = 32 * (NCW + 2);
+    static constexpr int NZ = BK / 64;                        // 64-wide activation boxes per stage
+    // per stage: packed weights, scales (up to BK / 32 groups, G = 32) and the offset
+    // terms -(b + 8) S_g[m] for both row halves in one region; the 128-byte-swizzled
+    // activation boxes in a second, 1024-byte aligned region
+    static constexpr int W_STAGE = TILE_N * BK / 2;
+    static constexpr int SC_OFF = W_STAGE;
+    static constexpr int S_OFF = SC_OFF + (BK / 32) * TILE_N * 2;
+    static constexpr int WS_STAGE = S_OFF + (BK / 32) * 2 * 16 * 4;   // -(b + 8) S_g[m], fp32 [BK / 32][2][16]
+    static constexpr int A_STAGE = 16 * 128 * NZ;             // up to 16 token rows of 128 bytes per box
+    static constexpr int A_BASE = (STAGES * WS_STAGE + 1023) / 1024 * 1024;
+    static constexpr int OFF_BAR = A_BASE + STAGES * A_STAGE;
+    static constexpr int SMEM_USED = OFF_BAR + 3 * STAGES * 8 + 16;
+    static constexpr int SMEM_BYTES = SMEM_USED + 1024;
+    static_assert(BK == 128, "BK");
+    static_assert(WS_STAGE % 16 == 0 && A_STAGE % 1024 == 0, "bulk-copy and swizzle alignment");
+};
+
+// Pure register operations: not volatile, so the compiler may interleave them.
+__device__ __forceinline__ void mma_16816(float (&d)[4], const uint32_t (&a)[4], uint32_t b0, uint32_t b1,
+                                          bool bf16) {
+    if (bf16)
+        asm("mma.sync.aligned.m16n8k16.row.col.f32.bf16.bf16.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, {%8,%9}, "
+            "{%0,%1,%2,%3};"
+            : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
+            : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b0), "r"(b1));
+    else
+        asm("mma.sync.aligned.m16n8k16.row.col.f32.f16.f16.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, {%8,%9}, "
+            "{%0,%1,%2,%3};"
+            : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
+            : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b0), "r"(b1));
+}
+
+// Shared-memory reads: volatile with a memory clobber, so they stay after the
+// barrier wait that makes the data valid.
+__device__ __forceinline__ void ldmatrix_x2(uint32_t addr, uint32_t& r0, uint32_t& r1) {
+    asm volatile("ldmatrix.sync.aligned.m8n8.x2.shared.b16 {%0, %1}, [%2];" : "=r"(r0), "=r"(r1) : "r"(addr)
+                 : "memory");
+}
+__device__ __forceinline__ void ldmatrix_x4(uint32_t addr, uint32_t& r0, uint32_t& r1, uint32_t& r2,
+                                            uint32_t& r3) {
+    asm volatile("ldmatrix.sync.aligned.m8n8.x4.shared.b16 {%0, %1, %2, %3}, [%4];"
+                 : "=r"(r0), "=r"(r1), "=r"(r2), "=r"(r3)
+                 : "r"(addr)
+                 : "memory");
+}
+
+// One 32-bit word of the fragment-order layout -> the four A-fragment registers of
+// one k step, each holding two values b + q, exact.
+template <bool BF16>
+__device__ __forceinline__ void int4_word_to_frag(uint32_t w, uint32_t (&a)[4]) {
+    if (BF16) {
+        a[0] = (w & 0x000F000Fu) | 0x43004300u;           // rows g,     k       (128 + q)
+        a[1] = ((w >> 4) & 0x000F000Fu) | 0x43004300u;    // rows g + 8, k
+        a[2] = ((w >> 8) & 0x000F000Fu) | 0x43004300u;    // rows g,     k + 8
+        a[3] = ((w >> 12) & 0x000F000Fu) | 0x43004300u;   // rows g + 8, k + 8
+    } else {
+        const uint32_t w8 = w >> 8;
+        a[0] = (w & 0x000F000Fu) | 0x64006400u;           // 1024 + q
+        a[1] = (w & 0x00F000F0u) | 0x54005400u;           // 64 + q
+        a[2] = (w8 & 0x000F000Fu) | 0x64006400u;
+        a[3] = (w8 & 0x00F000F0u) | 0x54005400u;
+    }
+}
+
+// NT: 8-token MMA column tiles (1 for M <= 8, 2 for M <= 16).  GSTEPS: 16-wide k
+// steps per scale group inside a 128-value stage (2, 4 or 8; G >= 128 folds once per
+// stage).  One CTA per item (tile, K slice): gridDim.x == n_items, and the slices of
+// a tile form one cluster of p.splits CTAs.
+template <bool BF16, int NT, int GSTEPS, int BK, int STAGES>
+__global__ void __launch_bounds__(192) wq_decode_mma_kernel(const __grid_constant__ GemmParams p) {
+    using C = MmaDecodeCfg<BK, STAGES>;
+    constexpr int NZ = C::NZ;
+    constexpr int NCW = C::NCW;
+    constexpr int RGW = C::RGW;
+    constexpr int KSTEPS = BK / 16;
+    constexpr int SETS = NT == 1 ? 2 : 1;               // accumulator sets per chain (even / odd k steps)
+    constexpr float CORR_LO = BF16 ? 136.0f : 1032.0f;  // b + 8, rows g
+    constexpr float CORR_HI = BF16 ? 136.0f : 72.0f;    // b + 8, rows g + 8
+    constexpr uint32_t ONES = BF16 ? 0x3F803F80u : 0x3C003C00u;
+    static_assert(GSTEPS == 2 || GSTEPS == 4 || GSTEPS == 8, "GSTEPS");
+    extern __shared__ uint8_t smem_raw[];
+    uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+    const uint32_t sbase = ptx::smem_u32(smem);
+    const uint32_t bar0 = sbase + C::OFF_BAR;
+    auto full_bar = [&](int s) { return bar0 + 8u * s; };
+    auto sready_bar = [&](int s) { return bar0 + 8u * (STAGES + s); };
+    auto empty_bar = [&](int s) { return bar0 + 8u * (2 * STAGES + s); };
+    volatile uint32_t* abort_flag = reinterpret_cast<volatile uint32_t*>(smem + C::OFF_BAR + 3 * STAGES * 8);
+
+    const int warp = threadIdx.x >> 5;
+    const int lane = threadIdx.x & 31;
+    if (threadIdx.x == 0) {
+        for (int s = 0; s < STAGES; ++s) {
+            ptx::mbar_init(full_bar(s), 1);
+            ptx::mbar_init(sready_bar(s), 1);
+            ptx::mbar_init(empty_bar(s), NCW + 1);   // compute warps and the S warp
+        }
+        *abort_flag = 0u;
+        ptx::fence_barrier_init();
+        ptx::fence_proxy_async_smem();
+    }
+    if (warp == C::P_WARP && lane == 0) ptx::prefetch_tmap(&p.tmap_a);
+    __syncthreads();
+    if (threadIdx.x == 0) ptx::grid_launch_dependents();
+
+    const Item it = decode_item(p, (int)blockIdx.x);
+    const int nunits = it.kb_end - it.kb_begin;
+    const int tile = it.n_tile;
+
+    // activation fragment addresses inside a stage's boxes (box z = t / 4 holds k
+    // 64z .. 64z + 63 as 128-byte token rows, row z * M + m, 128-byte swizzle);
+    // ldmatrix lane l addresses row l % 8 of matrix l / 8: (tokens 0-7, k 0-7),
+    // (0-7, k 8-15), (8-15, k 0-7), (8-15, k 8-15) of a k step
+    uint32_t a_off[KSTEPS];
+    {
+        const int mi = lane >> 3;
+        const int a_row = (NT == 2 ? (mi >> 1) * 8 : 0) + (lane & 7);
+#pragma unroll
+        for (int t = 0; t < KSTEPS; ++t) {
+            const int row = (t >> 2) * p.a_box_rows + a_row;
+            const int chunk = (t & 3) * 2 + (mi & 1);
+            a_off[t] = row * 128 + ((chunk ^ (row & 7)) << 4);
+        }
+    }
+
+    // compute warps: rows 32w + 16j + g (e = 0, 1) and + 8 (e = 2, 3) of the tile
+    float acc[RGW][NT][4];
+#pragma unroll
+    for (int j = 0; j < RGW; ++j)
+#pragma unroll
+        for (int nt = 0; nt < NT; ++nt)
+#pragma unroll
+            for (int e = 0; e < 4; ++e) acc[j][nt][e] = 0.0f;
+
+    if (warp == C::P_WARP) {
+        // ------------------------------------------------------------ producer
+        if (lane == 0) {
+            const uint64_t pol_w = ptx::policy_evict_first();
+            const uint64_t pol_a = ptx::policy_evict_last();
+            const uint32_t a_bytes = (uint32_t)NZ * (uint32_t)p.a_box_rows * 128u;
+            const int gcnt = (p.G >= BK) ? 1 : (BK >> p.g_shift);
+            const uint32_t sc_bytes = (uint32_t)gcnt * TILE_N * 2;
+            auto load_w = [&](int s, int kb) {
+                const uint32_t fb = full_bar(s);
+                const uint32_t st = sbase + s * C::WS_STAGE;
+                ptx::mbar_arrive_expect_tx(fb, (uint32_t)C::W_STAGE + sc_bytes + a_bytes);
+                const uint8_t* wsrc =
+                    p.w + ((size_t)tile * p.nchunks_pad + (size_t)kb * (BK / 32)) * (TILE_N * 16);
+                ptx::bulk_load(st, wsrc, C::W_STAGE, fb, pol_w);
+                const int g0 = (kb * BK) >> p.g_shift;
+                const uint8_t* ssrc = p.sc + ((size_t)tile * p.ngroups_pad + g0) * (TILE_N * 2);
+                ptx::bulk_load(st + C::SC_OFF, ssrc, sc_bytes, fb, pol_w);
+            };
+            // Weights and scales of the first STAGES units go out before the grid
+            // dependency wait; the loop below then issues only their activation
+            // copies.  It can stop early only at a wait, and it waits only after
+            // passing them, so every barrier armed here gets all of its bytes.
+            const int pre = nunits < STAGES ? nunits : STAGES;
+            for (int i = 0; i < pre; ++i) load_w(i, it.kb_begin + i);
+            ptx::grid_dependency_wait();
+            int s = 0;
+            uint32_t ph = 0;
+            int issued = 0;
+            for (int i = 0; i < nunits; ++i) {
+                const int kb = it.kb_begin + i;
+                if (i >= pre) {
+                    if (!bounded_wait(empty_bar(s), ph ^ 1u, abort_flag, p.status, DEVICE_TIMEOUT_PRODUCER,
+                                      p.timeout_ns))
+                        break;
+                    load_w(s, kb);
+                }
+                // activation box {64 k, M tokens, NZ}: k-block kb starts at z = kb * NZ
+                ptx::tma_load_3d(sbase + C::A_BASE + s * C::A_STAGE, &p.tmap_a, 0, 0, kb * NZ, full_bar(s), pol_a);
+                ++issued;
+                if (++s == STAGES) {
+                    s = 0;
+                    ph ^= 1u;
+                }
+            }
+            if (*abort_flag) {
+                const int first = issued > STAGES ? issued - STAGES : 0;
+                for (int j = first; j < issued; ++j)
+                    if (!drain_wait(full_bar(j % STAGES), (uint32_t)((j / STAGES) & 1), p.timeout_ns))
+                        atomicOr(p.status, DEVICE_TIMEOUT_DRAIN);
+            }
+        }
+        __syncwarp();
+    } else if (warp == C::S_WARP) {
+        // ------------------------------------------------------------ activation sums
+        // S_g[m] per scale group of the stage, from an MMA with an all-ones operand;
+        // row g = 0 of the accumulator (lanes 0-3) holds tokens 2c, 2c + 1 (+ 8 nt).
+        // Stored as the starting values of the compute warps' group sums:
+        // -(b + 8) S_g[m] for rows g (b = 1024, bf16 128) and rows g + 8 (b = 64).
+        // This warp runs up to STAGES stages ahead of the compute warps.
+        const uint32_t ones[4] = {ONES, ONES, ONES, ONES};
+        int s = 0;
+        uint32_t ph = 0;
+        for (int i = 0; i < nunits; ++i) {
+            const bool w1 = bounded_wait(full_bar(s), ph, abort_flag, p.status, DEVICE_TIMEOUT_TRANSFORM,
+                                         p.timeout_ns);
+            if (!__all_sync(0xffffffffu, w1)) break;
+            const uint32_t st = sbase + C::A_BASE + s * C::A_STAGE;   // this stage's activation boxes
+            float* sg = reinterpret_cast<float*>(smem + s * C::WS_STAGE + C::S_OFF);
+            float sacc[NT][4];
+#pragma unroll
+            for (int t = 0; t < KSTEPS; ++t) {
+                if (t % GSTEPS == 0) {
+#pragma unroll
+                    for (int nt = 0; nt < NT; ++nt)
+#pragma unroll
+                        for (int e = 0; e < 4; ++e) sacc[nt][e] = 0.0f;
+                }
+                uint32_t b[NT][2];
+                if constexpr (NT == 2)
+                    ldmatrix_x4(st + a_off[t], b[0][0], b[0][1], b[NT - 1][0], b[NT - 1][1]);
+                else
+                    ldmatrix_x2(st + a_off[t], b[0][0], b[0][1]);
+#pragma unroll
+                for (int nt = 0; nt < NT; ++nt) mma_16816(sacc[nt], ones, b[nt][0], b[nt][1], BF16);
+                if ((t + 1) % GSTEPS == 0 && lane < 4) {
+                    float* dst = sg + (t / GSTEPS) * 32;
+#pragma unroll
+                    for (int nt = 0; nt < NT; ++nt) {
+                        const int m = nt * 8 + 2 * lane;
+                        *reinterpret_cast<float2*>(dst + m) = make_float2(-CORR_LO * sacc[nt][0], -CORR_LO * sacc[nt][1]);
+                        *reinterpret_cast<float2*>(dst + 16 + m) =
+                            make_float2(-CORR_HI * sacc[nt][0], -CORR_HI * sacc[nt][1]);
+                    }
+                }
+            }
+            __syncwarp();
+            if (lane == 0) {
+                ptx::mbar_arrive(sready_bar(s));
+                ptx::mbar_arrive(empty_bar(s));
+            }
+            if (++s == STAGES) {
+                s = 0;
+                ph ^= 1u;
+            }
+        }
+    } else {
+        // ------------------------------------------------------------ compute warps
+        const int g = lane >> 2, c = lane & 3;
+        const int slot = int4_slot(lane);
+        const int w_off = warp * RGW * 512 + slot * 16;   // this warp's first 16-row group, this lane's slot
+        int s = 0;
+        uint32_t ph = 0;
+        for (int i = 0; i < nunits; ++i) {
+            const bool w1 = bounded_wait(full_bar(s), ph, abort_flag, p.status, DEVICE_TIMEOUT_TRANSFORM,
+                                         p.timeout_ns);
+            if (!__all_sync(0xffffffffu, w1)) break;
+            const uint8_t* stp = smem + s * C::WS_STAGE;
+            const uint32_t st = sbase + C::A_BASE + s * C::A_STAGE;   // this stage's activation boxes
+            const uint16_t* sc = reinterpret_cast<const uint16_t*>(stp + C::SC_OFF);
+            const float* sg = reinterpret_cast<const float*>(stp + C::S_OFF);
+            uint4 wv[KSTEPS / 4][RGW];
+#pragma unroll
+            for (int tq = 0; tq < KSTEPS / 4; ++tq)
+#pragma unroll
+                for (int j = 0; j < RGW; ++j)
+                    wv[tq][j] = *reinterpret_cast<const uint4*>(stp + tq * 4096 + w_off + j * 512);
+            // the offset terms of this stage's groups (written by the S warp)
+            const bool w2 = bounded_wait(sready_bar(s), ph, abort_flag, p.status, DEVICE_TIMEOUT_TRANSFORM,
+                                         p.timeout_ns);
+            if (!__all_sync(0xffffffffu, w2)) break;
+            float tmp[RGW][SETS][NT][4];
+#pragma unroll
+            for (int t = 0; t < KSTEPS; ++t) {
+                if (t % GSTEPS == 0) {
+                    // group start: D begins at -(b + 8) S_g, so that it ends as D - (b + 8) S_g
+                    const float* so = sg + (t / GSTEPS) * 32;
+#pragma unroll
+                    for (int nt = 0; nt < NT; ++nt) {
+                        const float2 lo = *reinterpret_cast<const float2*>(so + nt * 8 + 2 * c);
+                        const float2 hi = *reinterpret_cast<const float2*>(so + 16 + nt * 8 + 2 * c);
+#pragma unroll
+                        for (int j = 0; j < RGW; ++j) {
+                            tmp[j][0][nt][0] = lo.x;
+                            tmp[j][0][nt][1] = lo.y;
+                            tmp[j][0][nt][2] = hi.x;
+                            tmp[j][0][nt][3] = hi.y;
+#pragma unroll
+                            for (int h = 1; h < SETS; ++h)
+#pragma unroll
+                                for (int e = 0; e < 4; ++e) tmp[j][h][nt][e] = 0.0f;
+                        }
+                    }
+                }
+                uint32_t b[NT][2];
+                if constexpr (NT == 2)
+                    ldmatrix_x4(st + a_off[t], b[0][0], b[0][1], b[NT - 1][0], b[NT - 1][1]);
+                else
+                    ldmatrix_x2(st + a_off[t], b[0][0], b[0][1]);
+#pragma unroll
+                for (int j = 0; j < RGW; ++j) {
+                    const uint4& q4 = wv[t >> 2][j];
+                    const uint32_t word = (t & 3) == 0 ? q4.x : (t & 3) == 1 ? q4.y : (t & 3) == 2 ? q4.z : q4.w;
+                    uint32_t a[4];
+                    int4_word_to_frag<BF16>(word, a);
+#pragma unroll
+                    for (int nt = 0; nt < NT; ++nt) mma_16816(tmp[j][t % SETS][nt], a, b[nt][0], b[nt][1], BF16);
+                }
+                if ((t + 1) % GSTEPS == 0) {
+                    // acc += s * (D - (b + 8) S_g)
+                    const int gi = t / GSTEPS;
+#pragma unroll
+                    for (int j = 0; j < RGW; ++j) {
+                        const uint16_t* sp = sc + gi * TILE_N + (warp * RGW + j) * 16 + g;
+                        const float s_lo = __half2float(__ushort_as_half(sp[0]));
+                        const float s_hi = __half2float(__ushort_as_half(sp[8]));
+#pragma unroll
+                        for (int nt = 0; nt < NT; ++nt)
+#pragma unroll
+                            for (int e = 0; e < 4; ++e) {
+                                float d = tmp[j][0][nt][e];
+                                if constexpr (SETS == 2) d += tmp[j][1][nt][e];
+                                acc[j][nt][e] = fmaf((e < 2) ? s_lo : s_hi, d, acc[j][nt][e]);
+                            }
+                    }
+                }
+            }
+            __syncwarp();
+            if (lane == 0) ptx::mbar_arrive(empty_bar(s));
+            if (++s == STAGES) {
+                s = 0;
+                ph ^= 1u;
+            }
+
+        }
+    }
+    // Every stage was consumed, or drained after an abort: the stage memory is free.
+    // From here on every thread of the CTA runs the same sequence (no early exit), so
+    // the cluster barriers below are always reached.
+    __syncthreads();
+    ptx::grid_dependency_wait();   // out may still be read upstream
+    const int g = lane >> 2, c = lane & 3;
+    if (p.splits == 1) {
+        if (warp < NCW) {
+#pragma unroll
+            for (int j = 0; j < RGW; ++j)
+#pragma unroll
+                for (int nt = 0; nt < NT; ++nt)
+#pragma unroll
+                    for (int e = 0; e < 4; ++e) {
+                        const int n = tile * TILE_N + (warp * RGW + j) * 16 + g + 8 * (e >> 1);
+                        const int m = nt * 8 + 2 * c + (e & 1);
+                        if (n < p.N && m < p.M) store_out<BF16>(p.out, (size_t)m * p.N + n, acc[j][nt][e]);
+                    }
+        }
+    } else {
+        float* part = reinterpret_cast<float*>(smem);   // [16 tokens][128 rows]
+        if (warp < NCW) {
+#pragma unroll
+            for (int j = 0; j < RGW; ++j)
+#pragma unroll
+                for (int nt = 0; nt < NT; ++nt)
+#pragma unroll
+                    for (int e = 0; e < 4; ++e) {
+                        const int r = (warp * RGW + j) * 16 + g + 8 * (e >> 1);
+                        const int m = nt * 8 + 2 * c + (e & 1);
+                        if (m < p.M) part[m * TILE_N + r] = acc[j][nt][e];
+                    }
+        }
+        ptx::cluster_sync();
+        const int S = p.splits;
+        const int rank = (int)ptx::cluster_ctarank();
+        const int rows_per = (TILE_N + S - 1) / S;
+        const int row0 = rank * rows_per;
+        const int rows = min(TILE_N, row0 + rows_per) - row0;
+        const uint32_t part_addr = ptx::smem_u32(part);
+        const int cnt = p.M * rows;
+        for (int e = threadIdx.x; e < cnt; e += blockDim.x) {
+            const int m = e / rows;
+            const int row = row0 + (e - m * rows);
+            const uint32_t off = part_addr + (uint32_t)(m * TILE_N + row) * 4u;
+            float tot = 0.0f;
+#pragma unroll
+            for (int q0 = 0; q0 < kMaxDecodeCluster; q0 += 8) {
+                if (q0 >= S) break;
+                float v[8];
+#pragma unroll
+                for (int q = 0; q < 8; ++q)
+                    v[q] = q0 + q < S ? ptx::ld_shared_cluster_f32(ptx::mapa_shared(off, (uint32_t)(q0 + q))) : 0.0f;
+#pragma unroll
+                for (int q = 0; q < 8; ++q)
+                    if (q0 + q < S) tot += v[q];
+            }
+            const int n = tile * TILE_N + row;
+            if (n < p.N) store_out<BF16>(p.out, (size_t)m * p.N + n, tot);
+        }
+        ptx::cluster_sync();
+    }
+}
+
+template <bool BF16, int NT, int GSTEPS, int BK, int STAGES>
+struct MmaDecodeLauncher {
+    using C = MmaDecodeCfg<BK, STAGES>;
+    static constexpr auto kernel = wq_decode_mma_kernel<BF16, NT, GSTEPS, BK, STAGES>;
+    static cudaError_t prepare() {
+        static int attr_set[64] = {0};
+        int dev = 0;
+        cudaError_t e = cudaGetDevice(&dev);
+        if (e != cudaSuccess) return e;
+        if (dev < 64 && attr_set[dev]) return cudaSuccess;
+        e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM_BYTES);
+        if (e == cudaSuccess) e = cudaFuncSetAttribute(kernel, cudaFuncAttributePreferredSharedMemoryCarveout, 100);
+        // clusters of up to 16 CTAs (the split-K slices of one tile)
+        if (e == cudaSuccess) e = cudaFuncSetAttribute(kernel, cudaFuncAttributeNonPortableClusterSizeAllowed, 1);
+        if (e == cudaSuccess && dev < 64) attr_set[dev] = 1;
+        return e;
+    }
+    // Resident CTAs per SM from registers, shared memory, threads and the block
+    // limit; and, per cluster size S = 2..16, how many S-CTA clusters the device can
+    // hold at once (the plan keeps a split-K grid within one such wave).
+    static KernelConfig config(bool query_device) {
+        KernelConfig k{FMT_INT4, BF16 ? 1 : 0, 16, BK, STAGES, 0, C::NTHREADS, C::SMEM_BYTES, 0, 1};
+        if (!query_device || prepare() != cudaSuccess) return k;
+        int dev = 0, smem_sm = 0, smem_rsv = 0, regs_sm = 0, thr_sm = 0, blk_sm = 0;
+        cudaFuncAttributes fa;
+        if (cudaGetDevice(&dev) != cudaSuccess || cudaFuncGetAttributes(&fa, kernel) != cudaSuccess ||
+            cudaDeviceGetAttribute(&smem_sm, cudaDevAttrMaxSharedMemoryPerMultiprocessor, dev) != cudaSuccess ||
+            cudaDeviceGetAttribute(&smem_rsv, cudaDevAttrReservedSharedMemoryPerBlock, dev) != cudaSuccess ||
+            cudaDeviceGetAttribute(&regs_sm, cudaDevAttrMaxRegistersPerMultiprocessor, dev) != cudaSuccess ||
+            cudaDeviceGetAttribute(&thr_sm, cudaDevAttrMaxThreadsPerMultiProcessor, dev) != cudaSuccess ||
+            cudaDeviceGetAttribute(&blk_sm, cudaDevAttrMaxBlocksPerMultiprocessor, dev) != cudaSuccess)
+            return k;
+        const int regs_warp = ((fa.numRegs * 32 + 255) / 256) * 256;
+        int n = regs_sm / (regs_warp * (C::NTHREADS / 32));
+        const int by_smem = smem_sm / (C::SMEM_BYTES + (int)fa.sharedSizeBytes + smem_rsv);
+        if (by_smem < n) n = by_smem;
+        if (thr_sm / C::NTHREADS < n) n = thr_sm / C::NTHREADS;
+        if (blk_sm < n) n = blk_sm;
+        if (n >= 1) k.ctas_per_sm = n;
+        for (int S = 2; S <= kMaxDecodeCluster; ++S) {
+            cudaLaunchConfig_t cfg = {};
+            cfg.gridDim = dim3((unsigned)S, 1, 1);
+            cfg.blockDim = dim3(C::NTHREADS, 1, 1);
+            cfg.dynamicSmemBytes = C::SMEM_BYTES;
+            cudaLaunchAttribute attr[1];
+            attr[0].id = cudaLaunchAttributeClusterDimension;
+            attr[0].val.clusterDim.x = (unsigned)S;
+            attr[0].val.clusterDim.y = 1;
+            attr[0].val.clusterDim.z = 1;
+            cfg.attrs = attr;
+            cfg.numAttrs = 1;
+            int nc = 0;
+            if (cudaOccupancyMaxActiveClusters(&nc, kernel, &cfg) != cudaSuccess) {
+                (void)cudaGetLastError();
+                nc = 0;
+            }
+            k.max_clusters[S] = nc;
+        }
+        return k;
+    }
+    // One CTA per (tile, slice); the slices of a tile form one cluster.
+    static cudaError_t launch(const GemmParams& p, int grid, cudaStream_t st) {
+        cudaError_t e = prepare();
+        if (e != cudaSuccess) return e;
+        if (p.splits > kMaxDecodeCluster || grid != p.n_items || p.M > 16 || p.M < 1) return cudaErrorInvalidValue;
+        cudaLaunchConfig_t cfg = {};
+        cfg.gridDim = dim3((unsigned)grid, 1, 1);
+        cfg.blockDim = dim3(C::NTHREADS, 1, 1);
+        cfg.dynamicSmemBytes = C::SMEM_BYTES;
+        cfg.stream = st;
+        cudaLaunchAttribute attr[2];
+        attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+        attr[0].val.programmaticStreamSerializationAllowed = 1;
+        attr[1].id = cudaLaunchAttributeClusterDimension;
+        attr[1].val.clusterDim.x = (unsigned)(p.splits > 1 ? p.splits : 1);
+        attr[1].val.clusterDim.y = 1;
+        attr[1].val.clusterDim.z = 1;
+        cfg.attrs = attr;
+        cfg.numAttrs = p.splits > 1 ? 2 : 1;
+        return cudaLaunchKernelEx(&cfg, kernel, p);
+    }
+};
+
+}  // namespace wq

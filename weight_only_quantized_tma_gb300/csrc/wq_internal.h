@@ -14,6 +14,24 @@ enum WFmt : int { FMT_INT4 = 0, FMT_FP8 = 1, FMT_FP4 = 2 };
 // Weight rows per CTA tile (the MMA M dimension: dequantized weight rows are the
 // tcgen05 A operand, tokens are the N dimension).
 constexpr int TILE_N = 128;
+
+// INT4 kernel order (output of wq_pack_int4), N padded to 128 and K to 256:
+//   [N/128][K/128][2 quads of 64 k][8 groups of 16 rows][32 slots][16 bytes]
+// The 16 bytes of lane l = 4g + c (g = l / 4, c = l % 4) of a 16-row group hold,
+// for the four 16-wide k steps t of the quad, one 32-bit word each: exactly the
+// codes of the m16n8k16 A fragment of that lane --
+//   bits  0- 3 / 16-19: row g,     k = 16t + 2c / 16t + 2c + 1
+//   bits  4- 7 / 20-23: row g + 8, k = 16t + 2c / 16t + 2c + 1
+//   bits  8-11 / 24-27: row g,     k = 16t + 8 + 2c / +1
+//   bits 12-15 / 28-31: row g + 8, k = 16t + 8 + 2c / +1
+// so one LOP3 with an fp16 "magic number" turns a nibble pair into a fragment
+// register.  Lane l's 16 bytes sit at slot int4_slot(l): an XOR swizzle that keeps
+// both a warp reading its lanes' slots (fragment order) and 8 threads gathering one
+// row each (row order, the tcgen05 operand path) free of shared-memory bank conflicts.
+__host__ __device__ __forceinline__ int int4_slot(int lane) {
+    const int g = lane >> 2, c = lane & 3;
+    return 4 * g + (c ^ ((g >> 1) & 3));
+}
 // Padding granularity of the prepacked INT4 / FP4-scale layouts along K.
 constexpr int KPAD_INT4 = 256;
 constexpr int KPAD_FP4SF = 128;  // covers a whole k-block of the largest BK
@@ -65,9 +83,12 @@ struct GemmParams {
     uint32_t* status;        // device status word (WQ_DEVICE_* bits)
     int M, N, K;
     int G;                   // INT4 group size
+    int g_shift;             // log2(G)
     int tiles_n, tiles_m;
     int splits;              // split-K slices per output tile
     int nkb;                 // k-blocks
+    int a_box_rows;          // activation rows per TMA box (M when one token tile covers M, else BN)
+    int kb_base, kb_rem;     // slice s covers kb_base * s + min(s, kb_rem) .. (nkb split as evenly as possible)
     int n_items;             // tiles_n * tiles_m * splits
     int walk_n_fast;         // tile walk order: weight rows fastest
     int w_evict_first;       // weights are streamed once (decode)
@@ -85,6 +106,9 @@ constexpr uint32_t DEVICE_TIMEOUT_TRANSFORM = 1u << 2;
 constexpr uint32_t DEVICE_TIMEOUT_EPILOGUE = 1u << 3;
 constexpr uint32_t DEVICE_TIMEOUT_DRAIN = 1u << 4;
 
+// Largest split-K cluster of the decode kernel (non-portable cluster size).
+constexpr int kMaxDecodeCluster = 16;
+
 // Static description of one compiled kernel configuration.
 struct KernelConfig {
     int fmt;
@@ -97,6 +121,7 @@ struct KernelConfig {
     int smem_bytes;  // dynamic shared memory
     int tmem_cols;
     int ctas_per_sm;  // resident CTAs per SM (registers, shared and tensor memory)
+    int max_clusters[kMaxDecodeCluster + 1];  // decode kernel: S-CTA clusters held at once (S = 2..16)
 };
 
 // Per-format launch entry points, defined in wq_gemm_{int4,fp8,fp4}.cu.
@@ -107,6 +132,12 @@ cudaError_t launch_gemm_fp4(const GemmParams& p, bool bf16, int bn, int grid, cu
 // Configuration of the instantiation for (bf16, bn); `query` asks the current
 // device for the resident CTAs per SM.  False if no such instantiation exists.
 bool config_int4(bool bf16, int bn, bool query, KernelConfig* cfg);
+// W4A16 decode kernel (M <= 16, K % 64 == 0): register-resident mma.sync with the
+// group scale applied on fp32, split-K reduced inside a thread-block cluster
+// (wq_gemm_mma.cuh).  The configuration is that of the
+// two-column-tile instantiation; both use the same shared memory and threads.
+bool config_int4_decode(bool bf16, bool query, KernelConfig* cfg);
+cudaError_t launch_gemm_int4_decode(const GemmParams& p, bool bf16, int grid, cudaStream_t st);
 bool config_fp8(bool bf16, int bn, bool query, KernelConfig* cfg);
 bool config_fp4(bool bf16, int bn, bool query, KernelConfig* cfg);
 

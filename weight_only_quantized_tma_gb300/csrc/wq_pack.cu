@@ -1,17 +1,11 @@
 // wq_pack.cu -- offline layout transforms, debug exports and the wait probe.
 //
-// INT4 kernel order (output of wq_pack_int4), for N padded to a multiple of 128
-// and K padded to a multiple of 256:
-//   weights: [N/128][K/32][128 rows][16 bytes]
-//     the 16 bytes of (tile, chunk, row) hold that row's codes for k in
-//     [32*chunk, 32*chunk + 32) as four 32-bit words; word j covers k = 8j..8j+7
-//     of the chunk with q(8j + 2i) at bits 4i and q(8j + 2i + 1) at bits 16 + 4i.
+// INT4 kernel order (output of wq_pack_int4): see wq_internal.h.  The
+// permutation is the offline layout transform of "Bitblas -- Mixed-Precision GEMM
+// with the Ladder Compiler" (GPU MODE lecture 33), introduction: the packed codes
+// are stored in the order the tensor-core operand fragments want, so no layout
+// conversion sits on the GEMM's critical path.
 //   scales:  [N/128][K/G][128 rows] fp16
-// A k-block of any multiple of 32 codes is one contiguous run per tile, so one
-// bulk copy moves it, and rows of a 32-thread warp read consecutive 16-byte units
-// (no shared-memory bank conflicts).  The permutation is the offline layout
-// transform of "Bitblas -- Mixed-Precision GEMM with the Ladder Compiler"
-// (GPU MODE lecture 33), introduction.
 //
 // FP4 block-scale kernel order (output of wq_pack_fp4_sf), N padded to 128 and K
 // to 128:  [N/128][K/64][128 rows][4 bytes], byte b of (tile, quad, row) is the
@@ -41,29 +35,32 @@ __device__ __forceinline__ uint32_t canon_code(const uint8_t* w, int64_t N, int6
     return (k & 1) ? (uint32_t)(b >> 4) : (uint32_t)(b & 0xF);
 }
 
-__global__ void pack_int4_w_kernel(const uint8_t* __restrict__ w, int64_t N, int64_t K, int64_t nchunks,
+// One thread per 16-byte unit: (tile, k-block, quad, group, lane).
+__global__ void pack_int4_w_kernel(const uint8_t* __restrict__ w, int64_t N, int64_t K, int64_t nkb,
                                    int64_t units, uint8_t* __restrict__ wk) {
     for (int64_t u = blockIdx.x * (int64_t)blockDim.x + threadIdx.x; u < units;
          u += (int64_t)gridDim.x * blockDim.x) {
-        const int64_t r = u % TILE_N;
-        const int64_t t = u / TILE_N;
-        const int64_t ck = t % nchunks;
-        const int64_t nt = t / nchunks;
-        const int64_t n = nt * TILE_N + r;
-        const int64_t k0 = ck * 32;
+        const int lane = (int)(u % 32);
+        const int64_t t1 = u / 32;
+        const int gr = (int)(t1 % 8);
+        const int64_t t2 = t1 / 8;
+        const int tq = (int)(t2 % 2);
+        const int64_t t3 = t2 / 2;
+        const int64_t kb = t3 % nkb;
+        const int64_t tile = t3 / nkb;
+        const int g = lane >> 2, c = lane & 3;
+        const int64_t n_lo = tile * TILE_N + gr * 16 + g, n_hi = n_lo + 8;
         uint32_t words[4];
 #pragma unroll
-        for (int j = 0; j < 4; ++j) {
-            uint32_t x = 0;
-#pragma unroll
-            for (int i = 0; i < 4; ++i) {
-                const int64_t k = k0 + 8 * j + 2 * i;
-                x |= canon_code(w, N, K, n, k) << (4 * i);
-                x |= canon_code(w, N, K, n, k + 1) << (16 + 4 * i);
-            }
-            words[j] = x;
+        for (int t = 0; t < 4; ++t) {
+            const int64_t k0 = kb * 128 + 16 * (4 * tq + t) + 2 * c, k2 = k0 + 8;
+            words[t] = canon_code(w, N, K, n_lo, k0) | (canon_code(w, N, K, n_lo, k0 + 1) << 16) |
+                       (canon_code(w, N, K, n_hi, k0) << 4) | (canon_code(w, N, K, n_hi, k0 + 1) << 20) |
+                       (canon_code(w, N, K, n_lo, k2) << 8) | (canon_code(w, N, K, n_lo, k2 + 1) << 24) |
+                       (canon_code(w, N, K, n_hi, k2) << 12) | (canon_code(w, N, K, n_hi, k2 + 1) << 28);
         }
-        reinterpret_cast<uint4*>(wk)[u] = make_uint4(words[0], words[1], words[2], words[3]);
+        const int64_t dst = (u - lane) + int4_slot(lane);
+        reinterpret_cast<uint4*>(wk)[dst] = make_uint4(words[0], words[1], words[2], words[3]);
     }
 }
 
@@ -80,24 +77,30 @@ __global__ void pack_int4_s_kernel(const uint16_t* __restrict__ s, int64_t N, in
     }
 }
 
-__device__ __forceinline__ uint32_t packed_code(const uint8_t* wk, int64_t nchunks, int64_t n, int64_t k) {
-    const int64_t nt = n / TILE_N, r = n % TILE_N, ck = k / 32;
-    const int kin = (int)(k % 32);
-    const uint32_t* unit = reinterpret_cast<const uint32_t*>(wk + ((nt * nchunks + ck) * TILE_N + r) * 16);
-    const uint32_t word = unit[kin / 8];
-    const int i = (kin % 8) / 2;
-    const int shift = (kin & 1) ? 16 + 4 * i : 4 * i;
-    return (word >> shift) & 0xFu;
+// Code of weight (n, k) read back from the kernel-order layout.
+__device__ __forceinline__ uint32_t packed_code(const uint8_t* wk, int64_t nkb, int64_t n, int64_t k) {
+    const int64_t tile = n / TILE_N;
+    const int r = (int)(n % TILE_N);
+    const int gr = r / 16, h = (r % 16) / 8, g = r % 8;
+    const int64_t kb = k / 128;
+    const int kl = (int)(k % 128);
+    const int tabs = kl / 16, kk = kl % 16;
+    const int hi8 = kk / 8, c = (kk % 8) / 2, odd = kk & 1;
+    const int tq = tabs / 4, t = tabs % 4;
+    const int lane = 4 * g + c;
+    const int64_t unit = (((tile * nkb + kb) * 2 + tq) * 8 + gr) * 32 + int4_slot(lane);
+    const uint32_t word = reinterpret_cast<const uint32_t*>(wk + unit * 16)[t];
+    return (word >> (4 * (h + 2 * hi8) + 16 * odd)) & 0xFu;
 }
 
-__global__ void unpack_int4_w_kernel(const uint8_t* __restrict__ wk, int64_t N, int64_t K, int64_t nchunks,
+__global__ void unpack_int4_w_kernel(const uint8_t* __restrict__ wk, int64_t N, int64_t K, int64_t nkb,
                                      uint8_t* __restrict__ w) {
     const int64_t total = N * (K / 2);
     for (int64_t u = blockIdx.x * (int64_t)blockDim.x + threadIdx.x; u < total;
          u += (int64_t)gridDim.x * blockDim.x) {
         const int64_t n = u / (K / 2), j = u % (K / 2);
-        const uint32_t lo = packed_code(wk, nchunks, n, 2 * j);
-        const uint32_t hi = packed_code(wk, nchunks, n, 2 * j + 1);
+        const uint32_t lo = packed_code(wk, nkb, n, 2 * j);
+        const uint32_t hi = packed_code(wk, nkb, n, 2 * j + 1);
         w[u] = (uint8_t)(lo | (hi << 4));
     }
 }
@@ -113,12 +116,12 @@ __global__ void unpack_int4_s_kernel(const uint16_t* __restrict__ sk, int64_t N,
 }
 
 __global__ void dequant_int4_kernel(const uint8_t* __restrict__ wk, const uint16_t* __restrict__ sk, int64_t N,
-                                    int64_t K, int G, int64_t nchunks, int64_t groups_pad, float* __restrict__ out) {
+                                    int64_t K, int G, int64_t nkb, int64_t groups_pad, float* __restrict__ out) {
     const int64_t total = N * K;
     for (int64_t u = blockIdx.x * (int64_t)blockDim.x + threadIdx.x; u < total;
          u += (int64_t)gridDim.x * blockDim.x) {
         const int64_t n = u / K, k = u % K;
-        const int q = (int)packed_code(wk, nchunks, n, k);
+        const int q = (int)packed_code(wk, nkb, n, k);
         const uint16_t sb = sk[((n / TILE_N) * groups_pad + k / G) * TILE_N + (n % TILE_N)];
         out[u] = (float)(q - 8) * __half2float(__ushort_as_half(sb));
     }
@@ -217,22 +220,31 @@ __global__ void wait_probe_kernel(uint32_t* status, long long timeout_ns) {
 
 }  // namespace
 
+__global__ void stream_fence_kernel() {}
+
 cudaError_t launch_pack_int4(const uint8_t* w, const uint16_t* s, int64_t N, int64_t K, int G, uint8_t* wk,
                              uint16_t* sk, cudaStream_t st) {
     const int64_t Np = round_up(N, TILE_N), Kp = round_up(K, KPAD_INT4);
-    const int64_t nchunks = Kp / 32, units = (Np / TILE_N) * nchunks * TILE_N;
-    pack_int4_w_kernel<<<grid_for(units), kThreads, 0, st>>>(w, N, K, nchunks, units, wk);
+    const int64_t nkb = Kp / 128, units = (Np / TILE_N) * nkb * 2 * 8 * 32;
+    pack_int4_w_kernel<<<grid_for(units), kThreads, 0, st>>>(w, N, K, nkb, units, wk);
     cudaError_t e = cudaGetLastError();
     if (e != cudaSuccess) return e;
     const int64_t groups_pad = Kp / G, total = (Np / TILE_N) * groups_pad * TILE_N;
     pack_int4_s_kernel<<<grid_for(total), kThreads, 0, st>>>(s, N, K / G, groups_pad, total, sk);
+    e = cudaGetLastError();
+    if (e != cudaSuccess) return e;
+    // The decode GEMM may start while the kernel before it on the stream is still
+    // finishing and reads the packed weights before it waits for that kernel.  An
+    // ordinary (non-overlapping) launch after the pack kernels makes sure that kernel
+    // is never one that wrote them.
+    stream_fence_kernel<<<1, 32, 0, st>>>();
     return cudaGetLastError();
 }
 
 cudaError_t launch_unpack_int4(const uint8_t* wk, const uint16_t* sk, int64_t N, int64_t K, int G, uint8_t* w,
                                uint16_t* s, cudaStream_t st) {
     const int64_t Kp = round_up(K, KPAD_INT4);
-    unpack_int4_w_kernel<<<grid_for(N * (K / 2)), kThreads, 0, st>>>(wk, N, K, Kp / 32, w);
+    unpack_int4_w_kernel<<<grid_for(N * (K / 2)), kThreads, 0, st>>>(wk, N, K, Kp / 128, w);
     cudaError_t e = cudaGetLastError();
     if (e != cudaSuccess) return e;
     unpack_int4_s_kernel<<<grid_for((K / G) * N), kThreads, 0, st>>>(sk, N, K / G, Kp / G, s);
@@ -242,7 +254,7 @@ cudaError_t launch_unpack_int4(const uint8_t* wk, const uint16_t* sk, int64_t N,
 cudaError_t launch_dequant_int4(const uint8_t* wk, const uint16_t* sk, int64_t N, int64_t K, int G, float* out,
                                 cudaStream_t st) {
     const int64_t Kp = round_up(K, KPAD_INT4);
-    dequant_int4_kernel<<<grid_for(N * K), kThreads, 0, st>>>(wk, sk, N, K, G, Kp / 32, Kp / G, out);
+    dequant_int4_kernel<<<grid_for(N * K), kThreads, 0, st>>>(wk, sk, N, K, G, Kp / 128, Kp / G, out);
     return cudaGetLastError();
 }
 
