@@ -26,10 +26,12 @@
 // Work split: one CTA per (128-row tile, K slice).  Warps: 0-3 compute (warp w owns
 // rows 32w .. 32w + 31 of the tile, so each row's sum lives in one warp), 4 computes
 // S, 5 is the producer.  When K is split, the S slices of a tile are the CTAs of one
-// thread-block cluster: each parks its fp32 partial tile in its own shared memory and
-// rank r adds rows [r R, r R + R) over the ranks in rank order through distributed
-// shared memory (R = ceil(128 / S)) -- deterministic, no workspace, and the
-// reduction is spread over all S CTAs.  The producer streams the weights and scales
+// thread-block cluster: each sends the fp32 partial sums of the rows it does not own
+// to the owning CTA's shared memory (CTA r owns rows [r R, r R + R), R = ceil(128 /
+// S)), and after one cluster barrier each adds its own rows over the ranks in rank
+// order, reading only its own
+// shared memory -- deterministic, no workspace, and the reduction is spread over all
+// S CTAs.  The producer streams the weights and scales
 // of its first stages before waiting for the preceding kernel on the stream
 // (programmatic dependent launch): they are constant inputs; activations and outputs
 // are touched only after that wait.
@@ -56,7 +58,15 @@ struct MmaDecodeCfg {
     static constexpr int WS_STAGE = S_OFF + (BK / 32) * 2 * 16 * 4;   // -(b + 8) S_g[m], fp32 [BK / 32][2][16]
     static constexpr int A_STAGE = 16 * 128 * NZ;             // up to 16 token rows of 128 bytes per box
     static constexpr int A_BASE = (STAGES * WS_STAGE + 1023) / 1024 * 1024;
-    static constexpr int OFF_BAR = A_BASE + STAGES * A_STAGE;
+    // split-K inbox: the partial sums the S CTAs of a cluster send to the CTA that
+    // owns R = ceil(128 / S) of the tile's rows, fp32 [S][R][16 token slots] -- at
+    // most 16 * (128 + 15) values; never used by the main loop, so a peer may write
+    // into it while this CTA is still streaming.  Token slot 4c + i holds token
+    // 2c + (i & 1) + 8 (i >> 1): the order of a lane's accumulator values, so each
+    // lane sends a row's values with one vector store.
+    static constexpr int INBOX = A_BASE + STAGES * A_STAGE;
+    static constexpr int INBOX_BYTES = 16 * (TILE_N + 16) * 4;
+    static constexpr int OFF_BAR = INBOX + INBOX_BYTES;
     static constexpr int SMEM_USED = OFF_BAR + 3 * STAGES * 8 + 16;
     static constexpr int SMEM_BYTES = SMEM_USED + 1024;
     static_assert(BK == 128, "BK");
@@ -182,10 +192,19 @@ __global__ void __launch_bounds__(192) wq_decode_mma_kernel(const __grid_constan
 
     if (warp == C::P_WARP) {
         // ------------------------------------------------------------ producer
+        // Lane 0 streams weights and scales; the first STAGES k-blocks' go out at once,
+        // before the grid dependency wait (constant inputs).  Their activation copies
+        // are issued by the S warp (below) as soon as the preceding kernel is done, so
+        // the first stage is not held behind the other stages' weight copies.  The
+        // order in which a stage's bytes land does not matter: its phase cannot
+        // complete before this lane's arrive-expect-tx.  The loop after that can stop
+        // early only at a wait, and it waits only after passing those stages, so every
+        // barrier armed here gets all of its bytes.
+        const int pre = nunits < STAGES ? nunits : STAGES;
+        const uint32_t a_bytes = (uint32_t)NZ * (uint32_t)p.a_box_rows * 128u;
         if (lane == 0) {
             const uint64_t pol_w = ptx::policy_evict_first();
             const uint64_t pol_a = ptx::policy_evict_last();
-            const uint32_t a_bytes = (uint32_t)NZ * (uint32_t)p.a_box_rows * 128u;
             const int gcnt = (p.G >= BK) ? 1 : (BK >> p.g_shift);
             const uint32_t sc_bytes = (uint32_t)gcnt * TILE_N * 2;
             auto load_w = [&](int s, int kb) {
@@ -199,24 +218,17 @@ __global__ void __launch_bounds__(192) wq_decode_mma_kernel(const __grid_constan
                 const uint8_t* ssrc = p.sc + ((size_t)tile * p.ngroups_pad + g0) * (TILE_N * 2);
                 ptx::bulk_load(st + C::SC_OFF, ssrc, sc_bytes, fb, pol_w);
             };
-            // Weights and scales of the first STAGES units go out before the grid
-            // dependency wait; the loop below then issues only their activation
-            // copies.  It can stop early only at a wait, and it waits only after
-            // passing them, so every barrier armed here gets all of its bytes.
-            const int pre = nunits < STAGES ? nunits : STAGES;
             for (int i = 0; i < pre; ++i) load_w(i, it.kb_begin + i);
             ptx::grid_dependency_wait();
-            int s = 0;
-            uint32_t ph = 0;
-            int issued = 0;
-            for (int i = 0; i < nunits; ++i) {
+            int s = pre % STAGES;
+            uint32_t ph = pre == STAGES ? 1u : 0u;
+            int issued = pre;
+            for (int i = pre; i < nunits; ++i) {
                 const int kb = it.kb_begin + i;
-                if (i >= pre) {
-                    if (!bounded_wait(empty_bar(s), ph ^ 1u, abort_flag, p.status, DEVICE_TIMEOUT_PRODUCER,
-                                      p.timeout_ns))
-                        break;
-                    load_w(s, kb);
-                }
+                if (!bounded_wait(empty_bar(s), ph ^ 1u, abort_flag, p.status, DEVICE_TIMEOUT_PRODUCER,
+                                  p.timeout_ns))
+                    break;
+                load_w(s, kb);
                 // activation box {64 k, M tokens, NZ}: k-block kb starts at z = kb * NZ
                 ptx::tma_load_3d(sbase + C::A_BASE + s * C::A_STAGE, &p.tmap_a, 0, 0, kb * NZ, full_bar(s), pol_a);
                 ++issued;
@@ -239,7 +251,17 @@ __global__ void __launch_bounds__(192) wq_decode_mma_kernel(const __grid_constan
         // row g = 0 of the accumulator (lanes 0-3) holds tokens 2c, 2c + 1 (+ 8 nt).
         // Stored as the starting values of the compute warps' group sums:
         // -(b + 8) S_g[m] for rows g (b = 1024, bf16 128) and rows g + 8 (b = 64).
-        // This warp runs up to STAGES stages ahead of the compute warps.
+        // This warp runs up to STAGES stages ahead of the compute warps.  First, its
+        // lane 0 issues the activation copies of the producer's first STAGES stages.
+        if (lane == 0) {
+            const uint64_t pol_a = ptx::policy_evict_last();
+            const int pre = nunits < STAGES ? nunits : STAGES;
+            ptx::grid_dependency_wait();
+            for (int i = 0; i < pre; ++i)
+                ptx::tma_load_3d(sbase + C::A_BASE + i * C::A_STAGE, &p.tmap_a, 0, 0, (it.kb_begin + i) * NZ,
+                                 full_bar(i), pol_a);
+        }
+        __syncwarp();
         const uint32_t ones[4] = {ONES, ONES, ONES, ONES};
         int s = 0;
         uint32_t ph = 0;
@@ -396,47 +418,49 @@ __global__ void __launch_bounds__(192) wq_decode_mma_kernel(const __grid_constan
                     }
         }
     } else {
-        float* part = reinterpret_cast<float*>(smem);   // [16 tokens][128 rows]
+        // Each CTA sends the rows it does not own to their owners' inboxes (remote
+        // shared-memory stores), one cluster barrier makes them visible, and each CTA
+        // adds its own rows over the ranks in rank order: deterministic, and no CTA
+        // reads another's shared memory, so none waits for its peers after the barrier.
+        const int S = p.splits;
+        const int rank = (int)ptx::cluster_ctarank();
+        const int R = (TILE_N + S - 1) / S;
+        const uint32_t inbox = sbase + C::INBOX;
         if (warp < NCW) {
 #pragma unroll
             for (int j = 0; j < RGW; ++j)
 #pragma unroll
-                for (int nt = 0; nt < NT; ++nt)
-#pragma unroll
-                    for (int e = 0; e < 4; ++e) {
-                        const int r = (warp * RGW + j) * 16 + g + 8 * (e >> 1);
-                        const int m = nt * 8 + 2 * c + (e & 1);
-                        if (m < p.M) part[m * TILE_N + r] = acc[j][nt][e];
-                    }
+                for (int h = 0; h < 2; ++h) {
+                    const int r = (warp * RGW + j) * 16 + g + 8 * h;   // e = 2h, 2h + 1
+                    const int owner = r / R;
+                    const uint32_t off = inbox + (uint32_t)((rank * R + (r - owner * R)) * 16 + 4 * c) * 4u;
+                    const uint32_t dst = ptx::mapa_shared(off, (uint32_t)owner);
+                    if constexpr (NT == 2)
+                        ptx::st_shared_cluster_v4f32(dst, acc[j][0][2 * h], acc[j][0][2 * h + 1], acc[j][1][2 * h],
+                                                     acc[j][1][2 * h + 1]);
+                    else
+                        ptx::st_shared_cluster_v2f32(dst, acc[j][0][2 * h], acc[j][0][2 * h + 1]);
+                }
         }
         ptx::cluster_sync();
-        const int S = p.splits;
-        const int rank = (int)ptx::cluster_ctarank();
-        const int rows_per = (TILE_N + S - 1) / S;
-        const int row0 = rank * rows_per;
-        const int rows = min(TILE_N, row0 + rows_per) - row0;
-        const uint32_t part_addr = ptx::smem_u32(part);
-        const int cnt = p.M * rows;
-        for (int e = threadIdx.x; e < cnt; e += blockDim.x) {
-            const int m = e / rows;
-            const int row = row0 + (e - m * rows);
-            const uint32_t off = part_addr + (uint32_t)(m * TILE_N + row) * 4u;
+        const int row0 = rank * R;
+        const int rows = min(TILE_N, row0 + R) - row0;
+        const float* box = reinterpret_cast<const float*>(smem + C::INBOX);
+        // token fastest: a warp reads whole 16-slot rows of the inbox (no bank conflicts)
+        for (int e = threadIdx.x; e < p.M * rows; e += blockDim.x) {
+            const int r = e / p.M;
+            const int m = e - r * p.M;
+            const int slot = 4 * ((m & 7) >> 1) + (m & 1) + 2 * (m >> 3);
+            float v[kMaxDecodeCluster];
+#pragma unroll
+            for (int q = 0; q < kMaxDecodeCluster; ++q) v[q] = q < S ? box[(q * R + r) * 16 + slot] : 0.0f;
             float tot = 0.0f;
 #pragma unroll
-            for (int q0 = 0; q0 < kMaxDecodeCluster; q0 += 8) {
-                if (q0 >= S) break;
-                float v[8];
-#pragma unroll
-                for (int q = 0; q < 8; ++q)
-                    v[q] = q0 + q < S ? ptx::ld_shared_cluster_f32(ptx::mapa_shared(off, (uint32_t)(q0 + q))) : 0.0f;
-#pragma unroll
-                for (int q = 0; q < 8; ++q)
-                    if (q0 + q < S) tot += v[q];
-            }
-            const int n = tile * TILE_N + row;
+            for (int q = 0; q < kMaxDecodeCluster; ++q)
+                if (q < S) tot += v[q];
+            const int n = tile * TILE_N + row0 + r;
             if (n < p.N) store_out<BF16>(p.out, (size_t)m * p.N + n, tot);
         }
-        ptx::cluster_sync();
     }
 }
 
