@@ -183,18 +183,14 @@ typedef struct {
     int32_t tiles_n;
     int32_t tiles_m;
     int32_t ctas_per_sm;  /* resident CTAs per SM assumed by the plan */
-    int32_t kernel;       /* WQ_KERNEL_TILE, WQ_KERNEL_DECODE or WQ_KERNEL_TILE_PAIR */
+    int32_t kernel;       /* WQ_KERNEL_TILE or WQ_KERNEL_DECODE */
 } wq_plan;
 
 /* Kernels a plan can pick.  TILE: the tcgen05 kernel (weights dequantized into
  * tensor memory, any M).  DECODE: W4A16 with M <= 16 and K % 64 == 0, operands
- * built in registers from the fragment-order layout, group scale applied in fp32.
- * TILE_PAIR: the tcgen05 kernel in clusters of two CTAs on adjacent weight tiles
- * that share each 256-token activation tile (W4A16, M > 128, no split-K, an even
- * number of 128-row weight tiles). */
+ * built in registers from the fragment-order layout, group scale applied in fp32. */
 #define WQ_KERNEL_TILE 0
 #define WQ_KERNEL_DECODE 1
-#define WQ_KERNEL_TILE_PAIR 2
 
 /* Plan and workspace size for op (a_dtype is ignored for WQ_OP_FP4, G for FP8
  * and FP4).  Either output pointer may be NULL.  Host only. */

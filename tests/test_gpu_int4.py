@@ -178,18 +178,18 @@ def test_device_status_clean_after_gemms():
     assert wq.wq_device_status() == 0
 
 
+
 @pytest.mark.parametrize("a_dtype", ["f16", "bf16"])
-def test_pair_kernel_identity_rows_bit_exact(a_dtype):
-    # M = K = 256 tokens, 80 weight tiles (enough that no split-K is planned): the
-    # clustered tile kernel (two CTAs share each activation tile through multicast);
-    # out[m, n] = RN(w[n, m]) exactly
+def test_unsplit_wide_tiles_identity_rows_bit_exact(a_dtype):
+    # M = K = 256 tokens over 80 weight tiles: the 256-token, 128-value k-block tile
+    # kernel without split-K; out[m, n] = RN(w[n, m]) exactly
     M = K = 256
     N, G = 10240, 64
     eye = np.eye(K, dtype=np.float32)
     A = eye.astype(np.float16).view(np.uint16) if a_dtype == "f16" else \
         torch.from_numpy(eye).to(torch.bfloat16).view(torch.int16).numpy().view(np.uint16)
     plan = wq.get_plan(wq.WQ_OP_W4A16, wq.WQ_F16 if a_dtype == "f16" else wq.WQ_BF16, M, N, K, G)
-    assert plan["kernel"] == wq.WQ_KERNEL_TILE_PAIR and plan["grid"] % 2 == 0
+    assert plan["kernel"] == wq.WQ_KERNEL_TILE and plan["bn"] == 256 and plan["splits"] == 1
     p = Int4Problem(M, N, K, G, a_dtype=a_dtype, seed=130, A_bits=A).pack()
     out = p.run()
     torch.cuda.synchronize()
@@ -198,19 +198,14 @@ def test_pair_kernel_identity_rows_bit_exact(a_dtype):
     assert np.array_equal(out_bits(out), rn)
 
 
-@pytest.mark.parametrize("M,N,K,G", [(1040, 2048, 512, 128), (1300, 2048, 256, 32), (4100, 2304, 768, 256)])
-def test_pair_kernel_ragged(M, N, K, G):
-    # ragged M: the second half of the last token tile is partly or wholly past M
-    # (more than 76 output tiles, so no split-K is planned)
+@pytest.mark.parametrize("M,N,K,G", [(1040, 2048, 512, 128), (1300, 2048, 320, 32), (4100, 2304, 768, 256)])
+def test_unsplit_wide_tiles_ragged(M, N, K, G):
+    # ragged M (the last 256-token tile partly past M), more than 76 output tiles so
+    # no split-K is planned; K = 320 ends on half of a 128-value k-block
     plan = wq.get_plan(wq.WQ_OP_W4A16, wq.WQ_F16, M, N, K, G)
-    assert plan["kernel"] == wq.WQ_KERNEL_TILE_PAIR
+    assert plan["bn"] == 256 and plan["bk"] == 128 and plan["splits"] == 1
     p = Int4Problem(M, N, K, G, seed=131 + M).pack()
     out = p.run()
     torch.cuda.synchronize()
     rows = synth.sample_rows(M, 96, seed=132)
-    check_close(out_to_f64(out)[rows], p.ref(rows=rows), what=f"pair M={M} N={N} K={K} G={G}")
-
-
-def test_pair_kernel_not_used_for_odd_tile_counts():
-    plan = wq.get_plan(wq.WQ_OP_W4A16, wq.WQ_F16, 512, 384, 512, 128)   # 3 weight tiles
-    assert plan["kernel"] == wq.WQ_KERNEL_TILE
+    check_close(out_to_f64(out)[rows], p.ref(rows=rows), what=f"M={M} N={N} K={K} G={G}")

@@ -6,8 +6,7 @@
 //   * tcgen05: TMEM alloc/dealloc, MMA (kind::f16, A operand in TMEM), commit,
 //     32x32b loads/stores, and the thread-sync fences,
 //   * narrow-float converts (e4m3x2 / e2m1x2 -> f16x2).
-// One multicast copy form exists (tma_load_2d_multicast): its source is always this
-// GPU's own global memory, its destinations the CTAs of one cluster on this GPU.
+// No multicast form of any copy is defined here.
 #pragma once
 
 #include <cstdint>
@@ -92,18 +91,6 @@ __device__ __forceinline__ void tma_load_2d(uint32_t dst, const void* tmap, int3
         : "memory");
 }
 
-// Tiled 2D tensor load delivered to the same shared-memory offset (and completing
-// on the same barrier offset) in every CTA of the cluster named in cta_mask.  The
-// source is this GPU's own memory.
-__device__ __forceinline__ void tma_load_2d_multicast(uint32_t dst, const void* tmap, int32_t x, int32_t y,
-                                                      uint32_t bar, uint16_t cta_mask, uint64_t policy) {
-    asm volatile(
-        "cp.async.bulk.tensor.2d.shared::cluster.global.mbarrier::complete_tx::bytes.multicast::cluster"
-        ".L2::cache_hint [%0], [%1, {%2, %3}], [%4], %5, %6;" ::"r"(dst),
-        "l"(tmap), "r"(x), "r"(y), "r"(bar), "h"(cta_mask), "l"(policy)
-        : "memory");
-}
-
 // Tiled 3D tensor load; x innermost, then y, then z.
 __device__ __forceinline__ void tma_load_3d(uint32_t dst, const void* tmap, int32_t x, int32_t y, int32_t z,
                                             uint32_t bar, uint64_t policy) {
@@ -169,16 +156,6 @@ __device__ __forceinline__ void mma_f16_ts(uint32_t d_tmem, uint32_t a_tmem, uin
 __device__ __forceinline__ void mma_commit(uint32_t bar) {
     asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(bar)
                  : "memory");
-}
-
-// Arrives once on the barrier at the same offset in every CTA of cta_mask when all
-// prior tcgen05 async ops of this thread complete.
-__device__ __forceinline__ void mma_commit_multicast(uint32_t bar, uint16_t cta_mask) {
-    asm volatile(
-        "tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.multicast::cluster.b64 [%0], %1;" ::"r"(
-            bar),
-        "h"(cta_mask)
-        : "memory");
 }
 
 __device__ __forceinline__ void tmem_wait_st() { asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory"); }

@@ -104,12 +104,10 @@ struct Plan {
     int tiles_n, tiles_m, nkb, splits, n_items, grid, walk_n_fast;
     size_t ws_bytes;
     bool decode;   // W4A16 decode kernel (register-resident mma.sync, M <= 16)
-    bool pair;     // W4A16 tile kernel in clusters of two sharing the activation tile
 };
 
 bool get_config_uncached(int fmt, bool bf16, int bn, bool query, KernelConfig* cfg) {
     if (fmt == FMT_INT4 + 16) return config_int4_decode(bf16, query, cfg);
-    if (fmt == FMT_INT4 + 32) return config_int4_pair(bf16, query, cfg);
     switch (fmt) {
         case FMT_INT4: return config_int4(bf16, bn, query, cfg);
         case FMT_FP8: return config_fp8(bf16, bn, query, cfg);
@@ -122,18 +120,17 @@ bool get_config_uncached(int fmt, bool bf16, int bn, bool query, KernelConfig* c
 // device and instantiation; later calls read the cached answer.
 struct ConfigCache {
     std::mutex mu;
-    bool have[kMaxDevices][5][2][4] = {};
-    bool found[kMaxDevices][5][2][4] = {};
-    KernelConfig cfg[kMaxDevices][5][2][4];
+    bool have[kMaxDevices][4][2][4] = {};
+    bool found[kMaxDevices][4][2][4] = {};
+    KernelConfig cfg[kMaxDevices][4][2][4];
 };
 ConfigCache g_cfg_cache;
 
 bool get_config(int fmt, bool bf16, int bn, bool query, KernelConfig* cfg) {
     const int bi = bn == 16 ? 0 : bn == 64 ? 1 : bn == 128 ? 2 : bn == 256 ? 3 : -1;
-    // slot 3: the W4A16 decode kernel, slot 4: the paired W4A16 tile kernel
-    const int fi = fmt == FMT_INT4 + 16 ? 3 : fmt == FMT_INT4 + 32 ? 4 : fmt;
+    const int fi = fmt == FMT_INT4 + 16 ? 3 : fmt;     // slot 3: the W4A16 decode kernel
     int dev = 0;
-    if (!query || bi < 0 || fi < 0 || fi > 4 || cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices)
+    if (!query || bi < 0 || fi < 0 || fi > 3 || cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices)
         return get_config_uncached(fmt, bf16, bn, query, cfg);
     std::lock_guard<std::mutex> lock(g_cfg_cache.mu);
     const int b = bf16 ? 1 : 0;
@@ -213,23 +210,9 @@ wq_status make_plan(int fmt, bool bf16, int64_t M, int64_t N, int64_t K, int sms
         p.splits = best;
         items = tiles * best;
     }
-    // W4A16 at BN = 256 without split-K: clusters of two CTAs on adjacent weight tiles
-    // share each activation tile (multicast), halving the activation reloads from L2
-    // that bound this regime; the grid is as many pairs as the device holds at once
-    KernelConfig pcfg{};
-    if (!decode && fmt == FMT_INT4 && cfg.bn == 256 && p.splits == 1 && p.tiles_n % 2 == 0 && sms > 0 &&
-        get_config(FMT_INT4 + 32, bf16, 256, true, &pcfg) && pcfg.max_clusters[2] > 0) {
-        p.pair = true;
-        items = tiles / 2;
-        if (items >= (1LL << 31)) return WQ_ERR_SHAPE;
-        const long long pairs = items < pcfg.max_clusters[2] ? items : pcfg.max_clusters[2];
-        p.n_items = (int)items;
-        p.grid = (int)(2 * pairs);
-    } else {
-        if (items >= (1LL << 31)) return WQ_ERR_SHAPE;
-        p.n_items = (int)items;
-        p.grid = (int)(items < slots || decode ? items : slots);   // decode: one CTA per item
-    }
+    if (items >= (1LL << 31)) return WQ_ERR_SHAPE;
+    p.n_items = (int)items;
+    p.grid = (int)(items < slots || decode ? items : slots);   // decode: one CTA per item
     const double w_bytes = (double)N * (double)K * w_bits / 8.0;
     const double a_bytes = (double)M * (double)K * 2.0;
     p.walk_n_fast = w_bytes < a_bytes ? 1 : 0;
@@ -444,7 +427,7 @@ wq_status wq_get_plan(wq_op op, wq_dtype a_dtype, int64_t M, int64_t N, int64_t 
         plan->tiles_n = pl.tiles_n;
         plan->tiles_m = pl.tiles_m;
         plan->ctas_per_sm = pl.cfg.ctas_per_sm;
-        plan->kernel = pl.decode ? WQ_KERNEL_DECODE : pl.pair ? WQ_KERNEL_TILE_PAIR : WQ_KERNEL_TILE;
+        plan->kernel = pl.decode ? WQ_KERNEL_DECODE : WQ_KERNEL_TILE;
     }
     if (ws_bytes) *ws_bytes = (M == 0) ? 0 : pl.ws_bytes;
     return WQ_OK;
@@ -475,9 +458,7 @@ wq_status wq_gemm_w4a16(const void* A, wq_dtype a_dtype, const uint8_t* w_kernel
     if ((st = check_ws(pl, ws, ws_bytes)) != WQ_OK) return st;
     GemmParams gp;
     std::memset(&gp, 0, sizeof(gp));
-    // (pair: each CTA of a cluster loads half of a 256-token activation tile)
-    if (pl.decode ? !encode_a_boxes(gp, A, bf16, M, K, pl.cfg.bk)
-                  : !encode_a(gp, A, bf16, M, K, pl.pair ? pl.cfg.bn / 2 : pl.cfg.bn))
+    if (pl.decode ? !encode_a_boxes(gp, A, bf16, M, K, pl.cfg.bk) : !encode_a(gp, A, bf16, M, K, pl.cfg.bn))
         return WQ_ERR_CUDA;
     gp.w = w_kernel;
     gp.sc = static_cast<const uint8_t*>(s_kernel);
@@ -488,12 +469,6 @@ wq_status wq_gemm_w4a16(const void* A, wq_dtype a_dtype, const uint8_t* w_kernel
     gp.nchunks_pad = (int)(Kp / 32);
     fill_common(gp, pl, M, N, K, out, ws, d->status);
     if (pl.decode) return finish_launch(launch_gemm_int4_decode(gp, bf16, pl.grid, (cudaStream_t)stream));
-    if (pl.pair) {
-        // items are weight-tile pairs: the kernel walks tiles_n / 2 pairs per token tile
-        gp.tiles_n = pl.tiles_n / 2;
-        gp.div_walk = make_fastdiv(pl.walk_n_fast ? gp.tiles_n : pl.tiles_m, (uint32_t)pl.n_items);
-        return finish_launch(launch_gemm_int4_pair(gp, bf16, pl.grid, (cudaStream_t)stream));
-    }
     return finish_launch(launch_gemm_int4(gp, bf16, pl.cfg.bn, pl.grid, (cudaStream_t)stream));
 }
 

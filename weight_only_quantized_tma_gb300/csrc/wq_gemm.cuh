@@ -238,11 +238,7 @@ __device__ __forceinline__ Item decode_item(const GemmParams& p, int item) {
     return it;
 }
 
-// PAIR: the CTAs run as clusters of two on adjacent 128-row weight tiles with the same
-// token tile.  Each loads half of the activation tile and multicasts it to both, so the
-// activation tile is read from L2 once per two weight tiles (at BN = 256 the activation
-// reloads, not the MMAs, bound the kernel); each MMA warp releases a stage in both CTAs.
-template <int FMT, bool BF16, int BN, int BK, int STAGES, int NWG, bool PAIR = false>
+template <int FMT, bool BF16, int BN, int BK, int STAGES, int NWG>
 __global__ void __launch_bounds__(128 * (1 + NWG), (GemmCfg<FMT, BF16, BN, BK, STAGES, NWG>::MIN_BLOCKS))
     wq_gemm_kernel(const __grid_constant__ GemmParams p) {
     using C = GemmCfg<FMT, BF16, BN, BK, STAGES, NWG>;
@@ -264,20 +260,11 @@ __global__ void __launch_bounds__(128 * (1 + NWG), (GemmCfg<FMT, BF16, BN, BK, S
     const int warp = threadIdx.x >> 5;
     const int lane = threadIdx.x & 31;
     const int n_epi = 128 * NWG;
-    // PAIR: items are per cluster; this CTA takes weight tile 2 n + rank of item n
-    const int rank = PAIR ? (int)ptx::cluster_ctarank() : 0;
-    const int item0 = PAIR ? (int)(blockIdx.x >> 1) : (int)blockIdx.x;
-    const int istep = PAIR ? (int)(gridDim.x >> 1) : (int)gridDim.x;
-    auto item_at = [&](int item) {
-        Item it = decode_item(p, item);
-        if (PAIR) it.n_tile = 2 * it.n_tile + rank;
-        return it;
-    };
 
     if (threadIdx.x == 0) {
         for (int s = 0; s < STAGES; ++s) {
             ptx::mbar_init(full_bar(s), 1);
-            ptx::mbar_init(empty_bar(s), PAIR ? 2 : 1);   // PAIR: both CTAs' MMA warps release a stage
+            ptx::mbar_init(empty_bar(s), 1);
         }
         // operand-full and accumulator-empty take one arrival per transform warp
         for (int a = 0; a < C::A_ST; ++a) {
@@ -302,9 +289,6 @@ __global__ void __launch_bounds__(128 * (1 + NWG), (GemmCfg<FMT, BF16, BN, BK, S
     ptx::tc_fence_before();
     __syncthreads();
     ptx::tc_fence_after();
-    // PAIR: the peer's copies and commits target this CTA's barriers, so both CTAs'
-    // barriers must be initialised before either issues anything
-    if (PAIR) ptx::cluster_sync();
     const uint32_t tmem = *tmem_slot;
     // The next kernel on the stream may start its own set-up now (programmatic
     // dependent launch); it waits for this grid before touching shared data.
@@ -322,8 +306,8 @@ __global__ void __launch_bounds__(128 * (1 + NWG), (GemmCfg<FMT, BF16, BN, BK, S
             // every global input may have been written by the previous kernel on the
             // stream: wait for it (programmatic dependent launch) before the first copy
             ptx::grid_dependency_wait();
-            for (int item = item0; item < p.n_items && ok; item += istep) {
-                const Item it = item_at(item);
+            for (int item = blockIdx.x; item < p.n_items && ok; item += gridDim.x) {
+                const Item it = decode_item(p, item);
                 for (int kb = it.kb_begin; kb < it.kb_end; ++kb) {
                     if (!bounded_wait(empty_bar(s), ph ^ 1u, abort_flag, p.status, DEVICE_TIMEOUT_PRODUCER,
                                       p.timeout_ns)) {
@@ -334,8 +318,7 @@ __global__ void __launch_bounds__(128 * (1 + NWG), (GemmCfg<FMT, BF16, BN, BK, S
                     // activation rows >= M are not loaded: they only feed accumulator
                     // columns that are never stored, and out-of-range rows would cost
                     // the copy engine a zero fill
-                    // (PAIR: both halves of the activation tile land here, one from each CTA)
-                    uint32_t bytes = (uint32_t)((BK / 64) * (PAIR ? 2 : 1) * p.a_box_rows * 128);
+                    uint32_t bytes = (uint32_t)((BK / 64) * p.a_box_rows * 128);
                     const uint32_t w_dst = sbase + C::OFF_W + s * C::W_STAGE;
                     const uint32_t sc_dst = sbase + C::OFF_SC + s * C::SC_STAGE;
                     uint32_t sc_bytes = 0;
@@ -367,15 +350,9 @@ __global__ void __launch_bounds__(128 * (1 + NWG), (GemmCfg<FMT, BF16, BN, BK, S
                     }
                     const uint32_t b_dst = sbase + C::OFF_B + s * C::B_STAGE;
 #pragma unroll
-                    for (int j = 0; j < BK / 64; ++j) {
-                        if (PAIR)   // this CTA's half of the token rows, into both CTAs
-                            ptx::tma_load_2d_multicast(b_dst + j * (BN * 128) + rank * (BN / 2) * 128, &p.tmap_a,
-                                                       kb * BK + j * 64, it.m_tile * BN + rank * (BN / 2), fb, 0x3,
-                                                       pol_a);
-                        else
-                            ptx::tma_load_2d(b_dst + j * (BN * 128), &p.tmap_a, kb * BK + j * 64, it.m_tile * BN, fb,
-                                             pol_a);
-                    }
+                    for (int j = 0; j < BK / 64; ++j)
+                        ptx::tma_load_2d(b_dst + j * (BN * 128), &p.tmap_a, kb * BK + j * 64, it.m_tile * BN, fb,
+                                         pol_a);
                     ++issued;
                     if (++s == STAGES) {
                         s = 0;
@@ -400,8 +377,8 @@ __global__ void __launch_bounds__(128 * (1 + NWG), (GemmCfg<FMT, BF16, BN, BK, S
             int s = 0, a = 0;
             uint32_t ph = 0, aph = 0, accph = 0;
             bool ok = true;
-            for (int item = item0; item < p.n_items && ok; item += istep) {
-                const Item it = item_at(item);
+            for (int item = blockIdx.x; item < p.n_items && ok; item += gridDim.x) {
+                const Item it = decode_item(p, item);
                 if (!bounded_wait(accempty_bar, accph ^ 1u, abort_flag, p.status, DEVICE_TIMEOUT_MMA, p.timeout_ns)) {
                     ok = false;
                     break;
@@ -422,10 +399,7 @@ __global__ void __launch_bounds__(128 * (1 + NWG), (GemmCfg<FMT, BF16, BN, BK, S
                         ptx::mma_f16_ts(tmem, a_tmem + kk * 8, ptx::make_sdesc_sw128(b_addr), idesc,
                                         (kb > it.kb_begin || kk > 0) ? 1u : 0u);
                     }
-                    if (PAIR)
-                        ptx::mma_commit_multicast(empty_bar(s), 0x3);   // the stage is free in both CTAs
-                    else
-                        ptx::mma_commit(empty_bar(s));
+                    ptx::mma_commit(empty_bar(s));
                     ptx::mma_commit(aempty_bar(a));
                     if (++s == STAGES) {
                         s = 0;
@@ -458,8 +432,8 @@ __global__ void __launch_bounds__(128 * (1 + NWG), (GemmCfg<FMT, BF16, BN, BK, S
         bool ok = true;
         ptx::grid_dependency_wait();   // alpha / bias are global inputs too
         const float alpha = (FMT == FMT_INT4) ? 1.0f : __ldg(p.alpha);
-        for (int item = item0; item < p.n_items && ok; item += istep) {
-            const Item it = item_at(item);
+        for (int item = blockIdx.x; item < p.n_items && ok; item += gridDim.x) {
+            const Item it = decode_item(p, item);
             for (int kb = it.kb_begin; kb < it.kb_end; ++kb) {
                 bool w1 = bounded_wait(full_bar(s), ph, abort_flag, p.status, DEVICE_TIMEOUT_TRANSFORM, p.timeout_ns);
                 bool w2 = w1 && bounded_wait(aempty_bar(a), aph ^ 1u, abort_flag, p.status, DEVICE_TIMEOUT_TRANSFORM,
@@ -646,16 +620,13 @@ __global__ void __launch_bounds__(128 * (1 + NWG), (GemmCfg<FMT, BF16, BN, BK, S
         ptx::tc_fence_after();
         ptx::tmem_dealloc(tmem, C::TMEM_COLS);
     }
-    // PAIR: neither CTA leaves while the other may still write into its shared memory
-    // or arrive on its barriers (every thread of both CTAs gets here, also after an abort)
-    if (PAIR) ptx::cluster_sync();
 }
 
 // Host-side launcher for one instantiation.
-template <int FMT, bool BF16, int BN, int BK, int STAGES, int NWG, bool PAIR = false>
+template <int FMT, bool BF16, int BN, int BK, int STAGES, int NWG>
 struct GemmLauncher {
     using C = GemmCfg<FMT, BF16, BN, BK, STAGES, NWG>;
-    static constexpr auto kernel = wq_gemm_kernel<FMT, BF16, BN, BK, STAGES, NWG, PAIR>;
+    static constexpr auto kernel = wq_gemm_kernel<FMT, BF16, BN, BK, STAGES, NWG>;
     static cudaError_t prepare() {
         // per device: allow the dynamic shared memory this configuration needs
         static int attr_set[64] = {0};
@@ -696,48 +667,22 @@ struct GemmLauncher {
         if (by_thr < n) n = by_thr;
         if (by_tmem < n) n = by_tmem;
         if (n >= 1) k.ctas_per_sm = n;
-        if (PAIR) {
-            // clusters of two the device holds at once (the plan sizes the grid to it)
-            cudaLaunchConfig_t cfg = {};
-            cfg.gridDim = dim3(2, 1, 1);
-            cfg.blockDim = dim3(C::NT, 1, 1);
-            cfg.dynamicSmemBytes = C::SMEM_BYTES;
-            cudaLaunchAttribute attr[1];
-            attr[0].id = cudaLaunchAttributeClusterDimension;
-            attr[0].val.clusterDim.x = 2;
-            attr[0].val.clusterDim.y = 1;
-            attr[0].val.clusterDim.z = 1;
-            cfg.attrs = attr;
-            cfg.numAttrs = 1;
-            int nc = 0;
-            if (cudaOccupancyMaxActiveClusters(&nc, kernel, &cfg) != cudaSuccess) {
-                (void)cudaGetLastError();
-                nc = 0;
-            }
-            k.max_clusters[2] = nc;
-        }
         return k;
     }
     static cudaError_t launch(const GemmParams& p, int grid, cudaStream_t st) {
         cudaError_t e = prepare();
-        if (PAIR && (grid % 2 != 0 || p.splits != 1)) return cudaErrorInvalidValue;
         if (e != cudaSuccess) return e;
         cudaLaunchConfig_t cfg = {};
         cfg.gridDim = dim3((unsigned)grid, 1, 1);
         cfg.blockDim = dim3(C::NT, 1, 1);
         cfg.dynamicSmemBytes = C::SMEM_BYTES;
         cfg.stream = st;
-        // programmatic dependent launch: set-up overlaps the previous kernel's tail;
-        // PAIR: clusters of two CTAs
-        cudaLaunchAttribute attr[2];
+        // programmatic dependent launch: set-up overlaps the previous kernel's tail
+        cudaLaunchAttribute attr[1];
         attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
         attr[0].val.programmaticStreamSerializationAllowed = 1;
-        attr[1].id = cudaLaunchAttributeClusterDimension;
-        attr[1].val.clusterDim.x = 2;
-        attr[1].val.clusterDim.y = 1;
-        attr[1].val.clusterDim.z = 1;
         cfg.attrs = attr;
-        cfg.numAttrs = PAIR ? 2 : 1;
+        cfg.numAttrs = 1;
         return cudaLaunchKernelEx(&cfg, kernel, p);
     }
 };

@@ -138,10 +138,6 @@ bool config_int4(bool bf16, int bn, bool query, KernelConfig* cfg);
 // two-column-tile instantiation; both use the same shared memory and threads.
 bool config_int4_decode(bool bf16, bool query, KernelConfig* cfg);
 cudaError_t launch_gemm_int4_decode(const GemmParams& p, bool bf16, int grid, cudaStream_t st);
-// W4A16 at BN = 256 in clusters of two CTAs that share the activation tile
-// (multicast); unsplit problems with an even number of weight tiles.
-bool config_int4_pair(bool bf16, bool query, KernelConfig* cfg);
-cudaError_t launch_gemm_int4_pair(const GemmParams& p, bool bf16, int grid, cudaStream_t st);
 bool config_fp8(bool bf16, int bn, bool query, KernelConfig* cfg);
 bool config_fp4(bool bf16, int bn, bool query, KernelConfig* cfg);
 
