@@ -209,3 +209,39 @@ def test_unsplit_wide_tiles_ragged(M, N, K, G):
     torch.cuda.synchronize()
     rows = synth.sample_rows(M, 96, seed=132)
     check_close(out_to_f64(out)[rows], p.ref(rows=rows), what=f"M={M} N={N} K={K} G={G}")
+
+
+def _tiles(plan):
+    return plan["tiles_n"] * plan["tiles_m"]
+
+
+@pytest.mark.parametrize("a_dtype", ["f16", "bf16"])
+def test_half_tile_tail_identity_rows_bit_exact(a_dtype):
+    # 2 x 80 = 160 tiles on the persistent grid: the 8 tiles past the first full round
+    # run as 16 half tiles (128 tokens each); out[m, n] = RN(w[n, m]) exactly
+    M = K = 512
+    N, G = 10240, 128
+    plan = wq.get_plan(wq.WQ_OP_W4A16, wq.WQ_F16 if a_dtype == "f16" else wq.WQ_BF16, M, N, K, G)
+    assert plan["splits"] == 1 and plan["n_items"] > _tiles(plan)
+    eye = np.eye(K, dtype=np.float32)
+    A = eye.astype(np.float16).view(np.uint16) if a_dtype == "f16" else \
+        torch.from_numpy(eye).to(torch.bfloat16).view(torch.int16).numpy().view(np.uint16)
+    p = Int4Problem(M, N, K, G, a_dtype=a_dtype, seed=140, A_bits=A).pack()
+    out = p.run()
+    torch.cuda.synchronize()
+    w = oracle.dequant_int4(p.wts.w, p.wts.s, K, G).astype(np.float64)
+    rn = oracle.round_f16_array(w.T) if a_dtype == "f16" else oracle.round_bf16_array(w.T)
+    assert np.array_equal(out_bits(out), rn)
+
+
+def test_half_tile_tail_ragged_M():
+    # 2 x 160 = 320 tiles: 16 half tiles in the tail; in the second token tile only
+    # rows 256..299 exist, so its upper half tile lies entirely past M
+    M, N, K, G = 300, 20480, 256, 32
+    plan = wq.get_plan(wq.WQ_OP_W4A16, wq.WQ_F16, M, N, K, G)
+    assert plan["splits"] == 1 and plan["n_items"] > _tiles(plan)
+    p = Int4Problem(M, N, K, G, seed=141).pack()
+    out = p.run()
+    torch.cuda.synchronize()
+    rows = np.unique(np.concatenate([synth.sample_rows(M, 64, seed=142), np.arange(250, 300)]))
+    check_close(out_to_f64(out)[rows], p.ref(rows=rows), what="half-tile tail, ragged M")

@@ -102,6 +102,7 @@ CUtensorMapSwizzle swizzle_for_pitch(int pitch_bytes) {
 struct Plan {
     KernelConfig cfg;
     int tiles_n, tiles_m, nkb, splits, n_items, grid, walk_n_fast;
+    int n_full;    // tile kernel: whole-tile items; the rest are half tiles
     size_t ws_bytes;
     bool decode;   // W4A16 decode kernel (register-resident mma.sync, M <= 16)
 };
@@ -212,7 +213,21 @@ wq_status make_plan(int fmt, bool bf16, int64_t M, int64_t N, int64_t K, int sms
     }
     if (items >= (1LL << 31)) return WQ_ERR_SHAPE;
     p.n_items = (int)items;
+    p.n_full = (int)items;
     p.grid = (int)(items < slots || decode ? items : slots);   // decode: one CTA per item
+    // Tile kernel without split-K: whole tiles in rounds over the persistent CTAs; the
+    // R tiles left after the last full round, if at most half the CTAs, become 2R half
+    // tiles (BN / 2 tokens each), so the last round takes half a tile's time on twice
+    // as many CTAs (e.g. 512 tiles on 152 CTAs: 3.5 instead of 4 tile-times).
+    if (!decode && p.splits == 1 && cfg.bn >= 64 && slots > 0) {
+        const long long n_full = tiles / slots * slots;
+        const long long rem = tiles - n_full;
+        if (rem > 0 && 2 * rem <= slots) {
+            p.n_full = (int)n_full;
+            p.n_items = (int)(n_full + 2 * rem);
+            p.grid = (int)(p.n_items < slots ? p.n_items : slots);
+        }
+    }
     const double w_bytes = (double)N * (double)K * w_bits / 8.0;
     const double a_bytes = (double)M * (double)K * 2.0;
     p.walk_n_fast = w_bytes < a_bytes ? 1 : 0;
@@ -243,9 +258,12 @@ void fill_common(GemmParams& gp, const Plan& pl, int64_t M, int64_t N, int64_t K
     gp.kb_base = pl.nkb / pl.splits;
     gp.kb_rem = pl.nkb % pl.splits;
     gp.n_items = pl.n_items;
+    gp.n_full = pl.n_full;
+    gp.half_bn = pl.cfg.bn / 2;
     gp.walk_n_fast = pl.walk_n_fast;
     gp.w_evict_first = pl.tiles_m == 1 ? 1 : 0;
-    gp.div_walk = make_fastdiv(pl.walk_n_fast ? pl.tiles_n : pl.tiles_m, (uint32_t)(pl.n_items / pl.splits));
+    gp.div_walk = make_fastdiv(pl.walk_n_fast ? pl.tiles_n : pl.tiles_m,
+                               (uint32_t)((long long)pl.tiles_n * pl.tiles_m));
     gp.div_splits = make_fastdiv(pl.splits, (uint32_t)pl.n_items);
     gp.status = status;
     gp.timeout_ns = kTimeoutNs;

@@ -216,12 +216,29 @@ __device__ __forceinline__ float load_16bit(const void* p, size_t idx) {
 
 struct Item {
     int n_tile, m_tile, slice, kb_begin, kb_end;
+    int half;    // 1: a half tile (half_bn tokens starting at m_sub), 0: a whole tile
+    int m_sub;
 };
 
+// Items below p.n_full are whole tiles (or split-K slices of them); the tiles past
+// them -- fewer than half the persistent CTAs -- are each split into two half tiles
+// along the tokens, so that the last round of work is spread over twice as many
+// CTAs without any cross-CTA reduction.
 __device__ __forceinline__ Item decode_item(const GemmParams& p, int item) {
     Item it;
-    const uint32_t t = fastdiv((uint32_t)item, p.div_splits);
-    it.slice = item - (int)t * p.splits;
+    it.half = 0;
+    it.m_sub = 0;
+    uint32_t t;
+    if (item < p.n_full) {
+        t = fastdiv((uint32_t)item, p.div_splits);
+        it.slice = item - (int)t * p.splits;
+    } else {
+        const int j = item - p.n_full;
+        t = (uint32_t)(p.n_full + (j >> 1));
+        it.slice = 0;
+        it.half = 1;
+        it.m_sub = (j & 1) * p.half_bn;
+    }
     if (p.walk_n_fast) {
         const uint32_t mt = fastdiv(t, p.div_walk);
         it.m_tile = (int)mt;
@@ -351,8 +368,8 @@ __global__ void __launch_bounds__(128 * (1 + NWG), (GemmCfg<FMT, BF16, BN, BK, S
                     const uint32_t b_dst = sbase + C::OFF_B + s * C::B_STAGE;
 #pragma unroll
                     for (int j = 0; j < BK / 64; ++j)
-                        ptx::tma_load_2d(b_dst + j * (BN * 128), &p.tmap_a, kb * BK + j * 64, it.m_tile * BN, fb,
-                                         pol_a);
+                        ptx::tma_load_2d(b_dst + j * (BN * 128), &p.tmap_a, kb * BK + j * 64,
+                                         it.m_tile * BN + it.m_sub, fb, pol_a);
                     ++issued;
                     if (++s == STAGES) {
                         s = 0;
@@ -373,7 +390,8 @@ __global__ void __launch_bounds__(128 * (1 + NWG), (GemmCfg<FMT, BF16, BN, BK, S
     } else if (warp == 1) {
         // ------------------------------------------------------------ MMA issuer
         if (lane == 0) {
-            constexpr uint32_t idesc = ptx::make_idesc_f16(BF16, 128, BN);
+            constexpr uint32_t idesc_full = ptx::make_idesc_f16(BF16, 128, BN);
+            constexpr uint32_t idesc_half = ptx::make_idesc_f16(BF16, 128, BN >= 32 ? BN / 2 : BN);
             int s = 0, a = 0;
             uint32_t ph = 0, aph = 0, accph = 0;
             bool ok = true;
@@ -384,6 +402,7 @@ __global__ void __launch_bounds__(128 * (1 + NWG), (GemmCfg<FMT, BF16, BN, BK, S
                     break;
                 }
                 ptx::tc_fence_after();
+                const uint32_t idesc = it.half ? idesc_half : idesc_full;   // half tile: MMA N = BN / 2
                 for (int kb = it.kb_begin; kb < it.kb_end; ++kb) {
                     if (!bounded_wait(afull_bar(a), aph, abort_flag, p.status, DEVICE_TIMEOUT_MMA, p.timeout_ns) ||
                         !bounded_wait(full_bar(s), ph, abort_flag, p.status, DEVICE_TIMEOUT_MMA, p.timeout_ns)) {
@@ -522,9 +541,10 @@ __global__ void __launch_bounds__(128 * (1 + NWG), (GemmCfg<FMT, BF16, BN, BK, S
             ptx::tc_fence_after();
             ptx::grid_dependency_wait();   // outputs and workspace may still be in use by the previous kernel
             const int n = it.n_tile * TILE_N + r;
-            const int m0 = it.m_tile * BN;
-            constexpr int COLS = BN / NWG;         // accumulator columns per warpgroup
-            constexpr int STEP = COLS >= 16 ? 16 : 8;
+            const int m0 = it.m_tile * BN + it.m_sub;
+            // accumulator columns per warpgroup (a half tile has BN / 2 of them)
+            const int COLS = (it.half ? BN / 2 : BN) / NWG;
+            constexpr int STEP = BN / NWG / 2 >= 16 ? 16 : 8;
             const int c_begin = wg * COLS;
             const uint32_t acc_addr = tmem + lane_addr;
             const int tile = it.n_tile + p.tiles_n * it.m_tile;

@@ -6,7 +6,7 @@ namespace wq {
 using F4_16 = GemmLauncher<FMT_FP4, true, 16, 128, 8, 2>;
 using F4_64 = GemmLauncher<FMT_FP4, true, 64, 128, 4, 2>;
 using F4_128 = GemmLauncher<FMT_FP4, true, 128, 128, 2, 2>;
-using F4_256 = GemmLauncher<FMT_FP4, true, 256, 64, 5, 2>;
+using F4_256 = GemmLauncher<FMT_FP4, true, 256, 128, 3, 2>;
 
 bool config_fp4(bool bf16, int bn, bool query, KernelConfig* cfg) {
     if (!bf16) return false;

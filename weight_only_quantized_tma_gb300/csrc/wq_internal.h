@@ -89,7 +89,9 @@ struct GemmParams {
     int nkb;                 // k-blocks
     int a_box_rows;          // activation rows per TMA box (M when one token tile covers M, else BN)
     int kb_base, kb_rem;     // slice s covers kb_base * s + min(s, kb_rem) .. (nkb split as evenly as possible)
-    int n_items;             // tiles_n * tiles_m * splits
+    int n_items;             // work items (tile kernel: n_full whole tiles, then two half tiles per remaining tile)
+    int n_full;              // tile kernel: items below this are whole tiles (or split-K slices)
+    int half_bn;             // tile kernel: tokens of a half tile (BN / 2)
     int walk_n_fast;         // tile walk order: weight rows fastest
     int w_evict_first;       // weights are streamed once (decode)
     int ngroups_pad;         // INT4: padded K / G
