@@ -183,7 +183,7 @@ typedef struct {
     int32_t tiles_n;
     int32_t tiles_m;
     int32_t ctas_per_sm;  /* resident CTAs per SM assumed by the plan */
-    int32_t kernel;       /* WQ_KERNEL_TILE or WQ_KERNEL_DECODE */
+    int32_t kernel;       /* WQ_KERNEL_TILE, WQ_KERNEL_DECODE or WQ_KERNEL_TILE_PAIR */
 } wq_plan;
 
 /* Kernels a plan can pick.  TILE: the tcgen05 kernel (weights dequantized into
@@ -191,6 +191,11 @@ typedef struct {
  * built in registers from the fragment-order layout, group scale applied in fp32. */
 #define WQ_KERNEL_TILE 0
 #define WQ_KERNEL_DECODE 1
+/* TILE_PAIR: W4A16 with large M.  The tile kernel on two-CTA clusters: 256 weight
+ * rows x 256 tokens per tile, each CTA dequantizes its 128 rows and copies half of
+ * the token tile, one tcgen05 MMA of M = 256 spans both SMs.  tiles_n counts
+ * 256-row tiles and grid counts CTAs (two per cluster). */
+#define WQ_KERNEL_TILE_PAIR 2
 
 /* Plan and workspace size for op (a_dtype is ignored for WQ_OP_FP4, G for FP8
  * and FP4).  Either output pointer may be NULL.  Host only. */

@@ -215,18 +215,35 @@ def _tiles(plan):
     return plan["tiles_n"] * plan["tiles_m"]
 
 
+@pytest.fixture(params=["pair", "one_cta"])
+def tile_kernel(request, monkeypatch):
+    """Large-M W4A16 tile kernel under test: the two-CTA pair kernel (the default)
+    or the one-CTA kernel (WQ_DISABLE_PAIR=1)."""
+    if request.param == "one_cta":
+        monkeypatch.setenv("WQ_DISABLE_PAIR", "1")
+    else:
+        monkeypatch.delenv("WQ_DISABLE_PAIR", raising=False)
+    return wq.WQ_KERNEL_TILE_PAIR if request.param == "pair" else wq.WQ_KERNEL_TILE
+
+
+def _identity_bits(K, a_dtype):
+    eye = np.eye(K, dtype=np.float32)
+    if a_dtype == "f16":
+        return eye.astype(np.float16).view(np.uint16)
+    return torch.from_numpy(eye).to(torch.bfloat16).view(torch.int16).numpy().view(np.uint16)
+
+
 @pytest.mark.parametrize("a_dtype", ["f16", "bf16"])
-def test_half_tile_tail_identity_rows_bit_exact(a_dtype):
-    # 2 x 80 = 160 tiles on the persistent grid: the 8 tiles past the first full round
-    # run as 16 half tiles (128 tokens each); out[m, n] = RN(w[n, m]) exactly
+def test_half_tile_tail_identity_rows_bit_exact(a_dtype, tile_kernel):
+    # pair kernel: 40 x 2 = 80 pair tiles on 76 pair slots, the 4 past the first
+    # round run as 8 half tiles; one-CTA kernel: 160 tiles on 152 CTAs, 16 half tiles.
+    # out[m, n] = RN(w[n, m]) exactly
     M = K = 512
     N, G = 10240, 128
     plan = wq.get_plan(wq.WQ_OP_W4A16, wq.WQ_F16 if a_dtype == "f16" else wq.WQ_BF16, M, N, K, G)
+    assert plan["kernel"] == tile_kernel
     assert plan["splits"] == 1 and plan["n_items"] > _tiles(plan)
-    eye = np.eye(K, dtype=np.float32)
-    A = eye.astype(np.float16).view(np.uint16) if a_dtype == "f16" else \
-        torch.from_numpy(eye).to(torch.bfloat16).view(torch.int16).numpy().view(np.uint16)
-    p = Int4Problem(M, N, K, G, a_dtype=a_dtype, seed=140, A_bits=A).pack()
+    p = Int4Problem(M, N, K, G, a_dtype=a_dtype, seed=140, A_bits=_identity_bits(K, a_dtype)).pack()
     out = p.run()
     torch.cuda.synchronize()
     w = oracle.dequant_int4(p.wts.w, p.wts.s, K, G).astype(np.float64)
@@ -234,14 +251,46 @@ def test_half_tile_tail_identity_rows_bit_exact(a_dtype):
     assert np.array_equal(out_bits(out), rn)
 
 
-def test_half_tile_tail_ragged_M():
-    # 2 x 160 = 320 tiles: 16 half tiles in the tail; in the second token tile only
-    # rows 256..299 exist, so its upper half tile lies entirely past M
+def test_half_tile_tail_ragged_M(tile_kernel):
+    # 160 weight tiles x 2 token tiles: half tiles in the tail; in the second token
+    # tile only rows 256..299 exist, so its upper half tile lies entirely past M
     M, N, K, G = 300, 20480, 256, 32
     plan = wq.get_plan(wq.WQ_OP_W4A16, wq.WQ_F16, M, N, K, G)
+    assert plan["kernel"] == tile_kernel
     assert plan["splits"] == 1 and plan["n_items"] > _tiles(plan)
     p = Int4Problem(M, N, K, G, seed=141).pack()
     out = p.run()
     torch.cuda.synchronize()
     rows = np.unique(np.concatenate([synth.sample_rows(M, 64, seed=142), np.arange(250, 300)]))
     check_close(out_to_f64(out)[rows], p.ref(rows=rows), what="half-tile tail, ragged M")
+
+
+@pytest.mark.parametrize("a_dtype,N,G", [("f16", 10240, 128), ("bf16", 10368, 64)])
+def test_pair_identity_rows_bit_exact(a_dtype, N, G):
+    # 256-row pair tiles over 1024 tokens; N = 10368 is 81 weight tiles, so the odd
+    # CTA of the last pair has no weight rows.  out[m, n] = RN(w[n, m]) exactly
+    M = K = 1024
+    plan = wq.get_plan(wq.WQ_OP_W4A16, wq.WQ_F16 if a_dtype == "f16" else wq.WQ_BF16, M, N, K, G)
+    assert plan["kernel"] == wq.WQ_KERNEL_TILE_PAIR and plan["grid"] % 2 == 0
+    assert plan["tiles_n"] == (N // 128 + 1) // 2
+    p = Int4Problem(M, N, K, G, a_dtype=a_dtype, seed=143, A_bits=_identity_bits(K, a_dtype)).pack()
+    out = p.run()
+    torch.cuda.synchronize()
+    w = oracle.dequant_int4(p.wts.w, p.wts.s, K, G).astype(np.float64)
+    rn = oracle.round_f16_array(w.T) if a_dtype == "f16" else oracle.round_bf16_array(w.T)
+    assert np.array_equal(out_bits(out), rn)
+
+
+@pytest.mark.parametrize("M,N,K,G", [(1300, 11008, 4096, 32), (4100, 2304, 768, 256), (2048, 4096, 4096, 128)])
+def test_pair_random(M, N, K, G):
+    # ragged token tiles (rows past M are neither loaded nor stored), Llama-shaped
+    # weights, and the output copied out through the staging area
+    plan = wq.get_plan(wq.WQ_OP_W4A16, wq.WQ_F16, M, N, K, G)
+    assert plan["kernel"] == wq.WQ_KERNEL_TILE_PAIR
+    p = Int4Problem(M, N, K, G, seed=144 + M).pack()
+    out = torch.full((M, N), float("nan"), dtype=torch.float16, device=DEV)
+    p.run(out=out)
+    torch.cuda.synchronize()
+    rows = np.unique(np.concatenate([synth.sample_rows(M, 48, seed=145), np.arange(M - 24, M)]))
+    check_close(out_to_f64(out)[rows], p.ref(rows=rows), what=f"pair M={M} N={N} K={K} G={G}")
+    assert not torch.isnan(out).any()

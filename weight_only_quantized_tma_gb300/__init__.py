@@ -28,6 +28,7 @@ from ._lib import (  # noqa: F401
     WQ_F16,
     WQ_KERNEL_DECODE,
     WQ_KERNEL_TILE,
+    WQ_KERNEL_TILE_PAIR,
     WQ_OP_FP4,
     WQ_OP_FP8,
     WQ_OP_W4A16,

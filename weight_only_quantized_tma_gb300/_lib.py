@@ -20,7 +20,7 @@ LIB_PATH = os.path.join(_HERE, "libwq.so")
 
 WQ_F16, WQ_BF16 = 0, 1
 WQ_OP_W4A16, WQ_OP_FP8, WQ_OP_FP4 = 0, 1, 2
-WQ_KERNEL_TILE, WQ_KERNEL_DECODE = 0, 1
+WQ_KERNEL_TILE, WQ_KERNEL_DECODE, WQ_KERNEL_TILE_PAIR = 0, 1, 2
 STATUS_NAMES = {
     0: "WQ_OK", 1: "WQ_ERR_NULL", 2: "WQ_ERR_SHAPE", 3: "WQ_ERR_GROUP", 4: "WQ_ERR_MISALIGNED",
     5: "WQ_ERR_DTYPE", 6: "WQ_ERR_WORKSPACE", 7: "WQ_ERR_UNSUPPORTED_DEVICE", 8: "WQ_ERR_CUDA",

@@ -7,6 +7,7 @@
 
 #include <atomic>
 #include <cstdint>
+#include <cstdlib>
 #include <cstring>
 #include <mutex>
 
@@ -105,10 +106,12 @@ struct Plan {
     int n_full;    // tile kernel: whole-tile items; the rest are half tiles
     size_t ws_bytes;
     bool decode;   // W4A16 decode kernel (register-resident mma.sync, M <= 16)
+    bool pair;     // tile kernel on two-CTA clusters (256 weight rows per tile)
 };
 
 bool get_config_uncached(int fmt, bool bf16, int bn, bool query, KernelConfig* cfg) {
     if (fmt == FMT_INT4 + 16) return config_int4_decode(bf16, query, cfg);
+    if (fmt == FMT_INT4 + 32) return config_int4_pair(bf16, query, cfg);
     switch (fmt) {
         case FMT_INT4: return config_int4(bf16, bn, query, cfg);
         case FMT_FP8: return config_fp8(bf16, bn, query, cfg);
@@ -121,17 +124,18 @@ bool get_config_uncached(int fmt, bool bf16, int bn, bool query, KernelConfig* c
 // device and instantiation; later calls read the cached answer.
 struct ConfigCache {
     std::mutex mu;
-    bool have[kMaxDevices][4][2][4] = {};
-    bool found[kMaxDevices][4][2][4] = {};
-    KernelConfig cfg[kMaxDevices][4][2][4];
+    bool have[kMaxDevices][5][2][4] = {};
+    bool found[kMaxDevices][5][2][4] = {};
+    KernelConfig cfg[kMaxDevices][5][2][4];
 };
 ConfigCache g_cfg_cache;
 
 bool get_config(int fmt, bool bf16, int bn, bool query, KernelConfig* cfg) {
     const int bi = bn == 16 ? 0 : bn == 64 ? 1 : bn == 128 ? 2 : bn == 256 ? 3 : -1;
-    const int fi = fmt == FMT_INT4 + 16 ? 3 : fmt;     // slot 3: the W4A16 decode kernel
+    // slot 3: the W4A16 decode kernel, slot 4: the W4A16 pair kernel
+    const int fi = fmt == FMT_INT4 + 16 ? 3 : fmt == FMT_INT4 + 32 ? 4 : fmt;
     int dev = 0;
-    if (!query || bi < 0 || fi < 0 || fi > 3 || cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices)
+    if (!query || bi < 0 || fi < 0 || fi > 4 || cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices)
         return get_config_uncached(fmt, bf16, bn, query, cfg);
     std::lock_guard<std::mutex> lock(g_cfg_cache.mu);
     const int b = bf16 ? 1 : 0;
@@ -228,6 +232,35 @@ wq_status make_plan(int fmt, bool bf16, int64_t M, int64_t N, int64_t K, int sms
             p.grid = (int)(p.n_items < slots ? p.n_items : slots);
         }
     }
+    // Large M: 256 x 256 tiles on two-CTA clusters halve the activation bytes each
+    // SM reads per MMA.  Used when the pair tiles fill every pair slot at least once.
+    // (WQ_DISABLE_PAIR=1 in the environment keeps the one-CTA tile kernel, e.g. to
+    // compare the two)
+    const char* no_pair = std::getenv("WQ_DISABLE_PAIR");
+    const bool pair_allowed = !(no_pair && no_pair[0] == '1');
+    if (pair_allowed && !decode && fmt == FMT_INT4 && cfg.bn == 256 && p.splits == 1 && sms > 0 && N % 8 == 0) {
+        KernelConfig pc{};
+        if (get_config(FMT_INT4 + 32, bf16, 256, true, &pc) && pc.max_clusters[2] > 0) {
+            const long long tn2 = (p.tiles_n + 1) / 2;
+            const long long items2 = tn2 * p.tiles_m;
+            const long long pslots = pc.max_clusters[2];
+            if (items2 >= pslots && items2 < (1LL << 30)) {
+                p.cfg = pc;
+                p.pair = true;
+                p.tiles_n = (int)tn2;
+                p.n_items = (int)items2;
+                p.n_full = (int)items2;
+                // the same half-tile tail as the one-CTA walk, over pair slots
+                const long long n_full = items2 / pslots * pslots;
+                const long long rem = items2 - n_full;
+                if (rem > 0 && 2 * rem <= pslots) {
+                    p.n_full = (int)n_full;
+                    p.n_items = (int)(n_full + 2 * rem);
+                }
+                p.grid = 2 * (int)(p.n_items < pslots ? p.n_items : pslots);
+            }
+        }
+    }
     const double w_bytes = (double)N * (double)K * w_bits / 8.0;
     const double a_bytes = (double)M * (double)K * 2.0;
     p.walk_n_fast = w_bytes < a_bytes ? 1 : 0;
@@ -283,11 +316,25 @@ wq_status check_ws(const Plan& pl, const void* ws, size_t ws_bytes) {
 // Activation tensor map.  When one token tile covers all M rows, the box holds only
 // those rows: the tile's remaining rows stay unwritten (they only reach accumulator
 // columns that are never stored) and the copy engine does no out-of-range fill.
+// A second map with boxes half as high serves the half tiles of the last round.
 bool encode_a(GemmParams& gp, const void* A, bool bf16, int64_t M, int64_t K, int bn) {
+    const auto dt = bf16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT16;
     const int rows = M < bn ? (int)M : bn;
+    const int half = M < bn / 2 ? (int)M : bn / 2;
     gp.a_box_rows = rows;
-    return encode_2d(&gp.tmap_a, bf16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT16, A,
-                     (uint64_t)K, (uint64_t)M, (uint64_t)K * 2, 64, (uint32_t)rows, CU_TENSOR_MAP_SWIZZLE_128B);
+    gp.a_box_rows_half = half;
+    return encode_2d(&gp.tmap_a, dt, A, (uint64_t)K, (uint64_t)M, (uint64_t)K * 2, 64, (uint32_t)rows,
+                     CU_TENSOR_MAP_SWIZZLE_128B) &&
+           encode_2d(&gp.tmap_a_half, dt, A, (uint64_t)K, (uint64_t)M, (uint64_t)K * 2, 64, (uint32_t)half,
+                     CU_TENSOR_MAP_SWIZZLE_128B);
+}
+
+// Output map of the pair kernel: out [M][N] 16-bit, boxes of 128 weight rows x 128
+// tokens copied from the shared-memory staging area.  Needs N % 8 == 0 (16-byte
+// row pitch).
+bool encode_out(GemmParams& gp, void* out, bool bf16, int64_t M, int64_t N) {
+    return encode_2d(&gp.tmap_out, bf16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT16, out,
+                     (uint64_t)N, (uint64_t)M, (uint64_t)N * 2, 128, 128, CU_TENSOR_MAP_SWIZZLE_NONE);
 }
 
 // Activation tensor map of the decode kernel: A [M][K] viewed as {64 k, M rows,
@@ -445,7 +492,7 @@ wq_status wq_get_plan(wq_op op, wq_dtype a_dtype, int64_t M, int64_t N, int64_t 
         plan->tiles_n = pl.tiles_n;
         plan->tiles_m = pl.tiles_m;
         plan->ctas_per_sm = pl.cfg.ctas_per_sm;
-        plan->kernel = pl.decode ? WQ_KERNEL_DECODE : WQ_KERNEL_TILE;
+        plan->kernel = pl.decode ? WQ_KERNEL_DECODE : pl.pair ? WQ_KERNEL_TILE_PAIR : WQ_KERNEL_TILE;
     }
     if (ws_bytes) *ws_bytes = (M == 0) ? 0 : pl.ws_bytes;
     return WQ_OK;
@@ -476,8 +523,11 @@ wq_status wq_gemm_w4a16(const void* A, wq_dtype a_dtype, const uint8_t* w_kernel
     if ((st = check_ws(pl, ws, ws_bytes)) != WQ_OK) return st;
     GemmParams gp;
     std::memset(&gp, 0, sizeof(gp));
-    if (pl.decode ? !encode_a_boxes(gp, A, bf16, M, K, pl.cfg.bk) : !encode_a(gp, A, bf16, M, K, pl.cfg.bn))
+    // pair kernel: each CTA copies half of the 256-token tile
+    if (pl.decode ? !encode_a_boxes(gp, A, bf16, M, K, pl.cfg.bk)
+                  : !encode_a(gp, A, bf16, M, K, pl.pair ? pl.cfg.bn / 2 : pl.cfg.bn))
         return WQ_ERR_CUDA;
+    if (pl.pair && !encode_out(gp, out, bf16, M, N)) return WQ_ERR_CUDA;
     gp.w = w_kernel;
     gp.sc = static_cast<const uint8_t*>(s_kernel);
     gp.G = G;
@@ -487,6 +537,7 @@ wq_status wq_gemm_w4a16(const void* A, wq_dtype a_dtype, const uint8_t* w_kernel
     gp.nchunks_pad = (int)(Kp / 32);
     fill_common(gp, pl, M, N, K, out, ws, d->status);
     if (pl.decode) return finish_launch(launch_gemm_int4_decode(gp, bf16, pl.grid, (cudaStream_t)stream));
+    if (pl.pair) return finish_launch(launch_gemm_int4_pair(gp, bf16, pl.grid, (cudaStream_t)stream));
     return finish_launch(launch_gemm_int4(gp, bf16, pl.cfg.bn, pl.grid, (cudaStream_t)stream));
 }
 

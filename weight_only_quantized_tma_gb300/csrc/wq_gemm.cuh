@@ -10,11 +10,26 @@
 // dedicated transform warpgroup converts the weights into TMEM.)
 //
 // Warp roles (128 * (1 + NWG) threads):
-//   warp 0      TMA producer: packed weight tile, its scales, activation tile per
-//               k-block, through a STAGES-deep mbarrier ring;
+//   warp 0      TMA producer of the activation tiles, one per k-block, through a
+//               STAGES-deep mbarrier ring released by the MMA commits;
+//   warp 3      TMA producer of the packed weight tiles and their scales, through
+//               a second STAGES-deep ring released by the transform warps as soon
+//               as they hold the codes in registers;
 //   warp 1      MMA issuer: tcgen05.mma kind::f16, accumulator in TMEM, commits
-//               free the shared-memory stage and the TMEM operand stage;
+//               free the activation stage and the TMEM operand stage;
 //   warp 2      TMEM allocator;
+// The two rings are separate so that the transform of a k-block waits only for
+// its weight bytes: the chain from an MMA completing to the next copy into its
+// activation stage no longer runs through the weight transform.
+//
+// PAIR variant (a cluster of two CTAs on the two SMs of a pair, tcgen05
+// cta_group::2): one output tile is 256 weight rows x BN tokens.  Each CTA
+// dequantizes its own 128 weight rows into its own TMEM and copies only its half
+// of the activation tile (BN / 2 tokens); the even CTA issues MMAs of M = 256 that
+// read both halves, so every SM moves half the activation bytes per MMA.  The odd
+// CTA's MMA warp forwards its activation-landed barrier to the even CTA, its
+// transform warps arrive on the even CTA's operand-full barrier, and the even
+// CTA's commits arrive on the barriers of both CTAs.  No copy is multicast.
 //   warps 4..   transform: unpack / decode + scale into 16-bit operands, then the
 //               epilogue (TMEM -> registers -> alpha/bias -> 16-bit -> global),
 //               including the deterministic split-K reduction.
@@ -39,10 +54,11 @@
 
 namespace wq {
 
-template <int FMT, bool BF16, int BN, int BK, int STAGES, int NWG>
+template <int FMT, bool BF16, int BN, int BK, int STAGES, int NWG, bool PAIR = false>
 struct GemmCfg {
     static constexpr int NT = 128 * (1 + NWG);
-    static constexpr int B_STAGE = BN * BK * 2;                       // activation tile bytes
+    static constexpr int B_ROWS = PAIR ? BN / 2 : BN;                 // tokens this CTA copies per k-block
+    static constexpr int B_STAGE = B_ROWS * BK * 2;                   // activation tile bytes
     static constexpr int W_STAGE = (FMT == FMT_FP8) ? TILE_N * BK : TILE_N * BK / 2;
     static constexpr int SC_STAGE = (FMT == FMT_INT4) ? (BK / 32) * TILE_N * 2
                                   : (FMT == FMT_FP4)  ? TILE_N * BK / 16 : 0;
@@ -55,8 +71,14 @@ struct GemmCfg {
     static constexpr int OFF_B = 0;
     static constexpr int OFF_W = OFF_B + STAGES * B_STAGE;
     static constexpr int OFF_SC = OFF_W + STAGES * W_STAGE;
-    static constexpr int OFF_BAR = (OFF_SC + STAGES * SC_STAGE + 127) / 128 * 128;
-    static constexpr int NBARS = 2 * STAGES + 2 * A_ST + 3;
+    // pair: the epilogue stages the 16-bit output tile [token][weight row] here and
+    // copies it out with TMA, so the accumulator is released before the stores
+    static constexpr bool STAGE_OUT = PAIR;
+    static constexpr int OUT_BOX_M = 128;                             // tokens per output copy
+    static constexpr int OFF_STG = (OFF_SC + STAGES * SC_STAGE + 1023) / 1024 * 1024;
+    static constexpr int STG_BYTES = STAGE_OUT ? BN * TILE_N * 2 : 0;
+    static constexpr int OFF_BAR = (OFF_STG + STG_BYTES + 127) / 128 * 128;
+    static constexpr int NBARS = 4 * STAGES + 2 * A_ST + 4;
     static constexpr int OFF_MISC = OFF_BAR + NBARS * 8;
     static constexpr int SMEM_USED = OFF_MISC + 16;
     static constexpr int SMEM_BYTES = SMEM_USED + 1024;               // alignment slack
@@ -65,9 +87,10 @@ struct GemmCfg {
     static constexpr int W_PITCH = W_STAGE / TILE_N;
     static constexpr uint32_t W_SWZ = (W_PITCH == 128) ? 7u : (W_PITCH == 64) ? 3u : 1u;
     // two CTAs per SM when shared and tensor memory allow it (decode, split-K)
-    static constexpr int MIN_BLOCKS = (2 * (SMEM_BYTES + 1024) <= 228 * 1024 && TMEM_COLS <= 256) ? 2 : 1;
+    static constexpr int MIN_BLOCKS = (!PAIR && 2 * (SMEM_BYTES + 1024) <= 228 * 1024 && TMEM_COLS <= 256) ? 2 : 1;
     static_assert(BK == 64 || BK == 128, "BK");
     static_assert(BN % 16 == 0 && BN >= 16 && BN <= 256, "BN");
+    static_assert(!PAIR || BN == 256, "pair tiles are 256 x 256");
     static_assert(A_ST >= 2, "need at least two TMEM operand stages");
     static_assert(SMEM_BYTES <= 227 * 1024, "shared memory");
     static_assert(B_STAGE % 1024 == 0 && W_STAGE % 1024 == 0, "1024-byte stage alignment");
@@ -81,12 +104,14 @@ __device__ __forceinline__ uint32_t swz(uint32_t a, uint32_t mask) { return a ^ 
 // Returns false if the CTA is aborting or the wait timed out (which starts the
 // abort).  The global timer is slow to read, so it is only consulted every 256
 // failed probes; the abort flag (shared memory) is checked on every probe.
+// CLUSTER: the barrier receives arrivals from the other CTA of a cluster pair.
+template <bool CLUSTER = false>
 __device__ __forceinline__ bool bounded_wait(uint32_t bar, uint32_t parity, volatile uint32_t* abort_flag,
                                              uint32_t* status, uint32_t code, long long timeout_ns) {
-    if (ptx::mbar_try_wait(bar, parity)) return true;
+    if (ptx::mbar_try_wait<CLUSTER>(bar, parity)) return true;
     uint64_t t0 = 0;
     for (uint32_t i = 1;; ++i) {
-        if (ptx::mbar_try_wait(bar, parity)) return true;
+        if (ptx::mbar_try_wait<CLUSTER>(bar, parity)) return true;
         if (*abort_flag) return false;
         if ((i & 255u) == 0u) {
             const uint64_t now = ptx::globaltimer();
@@ -209,6 +234,12 @@ __device__ __forceinline__ void store_out(void* out, size_t idx, float v) {
 }
 
 template <bool BF16>
+__device__ __forceinline__ uint16_t to_16bit(float v) {
+    if (BF16) return __bfloat16_as_ushort(__float2bfloat16_rn(v));
+    return __half_as_ushort(__float2half_rn(v));
+}
+
+template <bool BF16>
 __device__ __forceinline__ float load_16bit(const void* p, size_t idx) {
     if (BF16) return __bfloat162float(reinterpret_cast<const __nv_bfloat16*>(p)[idx]);
     return __half2float(reinterpret_cast<const __half*>(p)[idx]);
@@ -255,21 +286,25 @@ __device__ __forceinline__ Item decode_item(const GemmParams& p, int item) {
     return it;
 }
 
-template <int FMT, bool BF16, int BN, int BK, int STAGES, int NWG>
-__global__ void __launch_bounds__(128 * (1 + NWG), (GemmCfg<FMT, BF16, BN, BK, STAGES, NWG>::MIN_BLOCKS))
+template <int FMT, bool BF16, int BN, int BK, int STAGES, int NWG, bool PAIR>
+__global__ void __launch_bounds__(128 * (1 + NWG), (GemmCfg<FMT, BF16, BN, BK, STAGES, NWG, PAIR>::MIN_BLOCKS))
     wq_gemm_kernel(const __grid_constant__ GemmParams p) {
-    using C = GemmCfg<FMT, BF16, BN, BK, STAGES, NWG>;
+    using C = GemmCfg<FMT, BF16, BN, BK, STAGES, NWG, PAIR>;
+    constexpr int CG = PAIR ? 2 : 1;   // tcgen05 CTA group of every tcgen05 instruction here
     extern __shared__ uint8_t smem_raw[];
     uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
     const uint32_t sbase = ptx::smem_u32(smem);
     const uint32_t bar0 = sbase + C::OFF_BAR;
-    auto full_bar = [&](int s) { return bar0 + 8u * s; };
-    auto empty_bar = [&](int s) { return bar0 + 8u * (STAGES + s); };
-    auto afull_bar = [&](int a) { return bar0 + 8u * (2 * STAGES + a); };
-    auto aempty_bar = [&](int a) { return bar0 + 8u * (2 * STAGES + C::A_ST + a); };
-    const uint32_t accfull_bar = bar0 + 8u * (2 * STAGES + 2 * C::A_ST);
+    auto full_bar = [&](int s) { return bar0 + 8u * s; };                 // activation stage landed
+    auto empty_bar = [&](int s) { return bar0 + 8u * (STAGES + s); };     // activation stage free
+    auto wfull_bar = [&](int s) { return bar0 + 8u * (2 * STAGES + s); }; // weight stage landed
+    auto wempty_bar = [&](int s) { return bar0 + 8u * (3 * STAGES + s); };// weight stage free
+    auto afull_bar = [&](int a) { return bar0 + 8u * (4 * STAGES + a); };
+    auto aempty_bar = [&](int a) { return bar0 + 8u * (4 * STAGES + C::A_ST + a); };
+    const uint32_t accfull_bar = bar0 + 8u * (4 * STAGES + 2 * C::A_ST);
     const uint32_t accempty_bar = accfull_bar + 8u;
     const uint32_t final_bar = accfull_bar + 16u;
+    const uint32_t epi_bar = accfull_bar + 24u;   // staged epilogue: sync of the transform warps
     uint32_t* misc = reinterpret_cast<uint32_t*>(smem + C::OFF_MISC);
     volatile uint32_t* tmem_slot = misc + 0;
     volatile uint32_t* abort_flag = misc + 1;
@@ -277,20 +312,29 @@ __global__ void __launch_bounds__(128 * (1 + NWG), (GemmCfg<FMT, BF16, BN, BK, S
     const int warp = threadIdx.x >> 5;
     const int lane = threadIdx.x & 31;
     const int n_epi = 128 * NWG;
+    // pair: rank 0 issues the MMAs; barriers it waits on count the other CTA too
+    const int rank = PAIR ? (int)ptx::cluster_ctarank() : 0;
+    const bool issuer = (rank == 0);
+    const int ctas = PAIR ? 2 : 1;
 
     if (threadIdx.x == 0) {
         for (int s = 0; s < STAGES; ++s) {
-            ptx::mbar_init(full_bar(s), 1);
+            // pair, rank 0: its own copies plus the forwarded arrival of rank 1's
+            ptx::mbar_init(full_bar(s), (PAIR && issuer) ? 2 : 1);
             ptx::mbar_init(empty_bar(s), 1);
+            ptx::mbar_init(wfull_bar(s), 1);
+            ptx::mbar_init(wempty_bar(s), n_epi / 32);
         }
-        // operand-full and accumulator-empty take one arrival per transform warp
+        // weight-empty, operand-full and accumulator-empty take one arrival per
+        // transform warp (of both CTAs of a pair)
         for (int a = 0; a < C::A_ST; ++a) {
-            ptx::mbar_init(afull_bar(a), n_epi / 32);
+            ptx::mbar_init(afull_bar(a), ctas * n_epi / 32);
             ptx::mbar_init(aempty_bar(a), 1);
         }
         ptx::mbar_init(accfull_bar, 1);
-        ptx::mbar_init(accempty_bar, n_epi / 32);
+        ptx::mbar_init(accempty_bar, ctas * n_epi / 32);
         ptx::mbar_init(final_bar, 1);
+        ptx::mbar_init(epi_bar, n_epi / 32);
         *abort_flag = 0u;
         ptx::fence_barrier_init();
         ptx::fence_proxy_async_smem();
@@ -300,22 +344,36 @@ __global__ void __launch_bounds__(128 * (1 + NWG), (GemmCfg<FMT, BF16, BN, BK, S
         if (FMT != FMT_INT4) ptx::prefetch_tmap(&p.tmap_w);
     }
     if (warp == 2) {
-        ptx::tmem_alloc(sbase + C::OFF_MISC, C::TMEM_COLS);
-        ptx::tmem_relinquish();
+        ptx::tmem_alloc<CG>(sbase + C::OFF_MISC, C::TMEM_COLS);
+        ptx::tmem_relinquish<CG>();
     }
     ptx::tc_fence_before();
     __syncthreads();
+    // pair: both CTAs' barriers are initialised before either CTA signals the other
+    if (PAIR) ptx::cluster_sync();
     ptx::tc_fence_after();
     const uint32_t tmem = *tmem_slot;
+    // a barrier of the issuing CTA / of the other CTA, as a shared::cluster address
+    auto at_issuer = [&](uint32_t bar) { return PAIR ? ptx::mapa_shared(bar, 0) : bar; };
+    auto at_other = [&](uint32_t bar) { return ptx::mapa_shared(bar, (uint32_t)(rank ^ 1)); };
+    // this CTA's 128-row weight tile of an item (pair: two per item)
+    auto w_tile = [&](const Item& it) { return PAIR ? 2 * it.n_tile + rank : it.n_tile; };
+    const int tiles_w = (p.N + TILE_N - 1) / TILE_N;
+    // persistent walk: a pair takes items as one
+    const int item0 = PAIR ? (int)(blockIdx.x >> 1) : (int)blockIdx.x;
+    const int istride = PAIR ? (int)(gridDim.x >> 1) : (int)gridDim.x;
     // The next kernel on the stream may start its own set-up now (programmatic
     // dependent launch); it waits for this grid before touching shared data.
     if (threadIdx.x == 0) ptx::grid_launch_dependents();
 
-    if (warp == 0) {
-        // ------------------------------------------------------------ producer
+    if (warp == 0 || warp == 3) {
+        // ------------------------------------------------------------ producers
+        // warp 0: activation tiles (freed by the MMA commits); warp 3: weight
+        // tiles and scales (freed by the transform warps)
         if (lane == 0) {
-            const uint64_t pol_w = p.w_evict_first ? ptx::policy_evict_first() : ptx::policy_evict_last();
-            const uint64_t pol_a = ptx::policy_evict_last();
+            const bool act = (warp == 0);
+            const uint64_t pol = act ? ptx::policy_evict_last()
+                                     : (p.w_evict_first ? ptx::policy_evict_first() : ptx::policy_evict_last());
             int s = 0;
             uint32_t ph = 0;
             long long issued = 0;
@@ -323,53 +381,59 @@ __global__ void __launch_bounds__(128 * (1 + NWG), (GemmCfg<FMT, BF16, BN, BK, S
             // every global input may have been written by the previous kernel on the
             // stream: wait for it (programmatic dependent launch) before the first copy
             ptx::grid_dependency_wait();
-            for (int item = blockIdx.x; item < p.n_items && ok; item += gridDim.x) {
+            for (int item = item0; item < p.n_items && ok; item += istride) {
                 const Item it = decode_item(p, item);
                 for (int kb = it.kb_begin; kb < it.kb_end; ++kb) {
-                    if (!bounded_wait(empty_bar(s), ph ^ 1u, abort_flag, p.status, DEVICE_TIMEOUT_PRODUCER,
-                                      p.timeout_ns)) {
+                    if (!bounded_wait(act ? empty_bar(s) : wempty_bar(s), ph ^ 1u, abort_flag, p.status,
+                                            DEVICE_TIMEOUT_PRODUCER, p.timeout_ns)) {
                         ok = false;
                         break;
                     }
-                    const uint32_t fb = full_bar(s);
-                    // activation rows >= M are not loaded: they only feed accumulator
-                    // columns that are never stored, and out-of-range rows would cost
-                    // the copy engine a zero fill
-                    uint32_t bytes = (uint32_t)((BK / 64) * p.a_box_rows * 128);
-                    const uint32_t w_dst = sbase + C::OFF_W + s * C::W_STAGE;
-                    const uint32_t sc_dst = sbase + C::OFF_SC + s * C::SC_STAGE;
-                    uint32_t sc_bytes = 0;
-                    if (FMT == FMT_INT4) {
-                        const int gcnt = (p.G >= BK) ? 1 : (BK >> p.g_shift);
-                        sc_bytes = (uint32_t)gcnt * TILE_N * 2;
-                        bytes += C::W_STAGE + sc_bytes;
-                    } else if (FMT == FMT_FP4) {
-                        sc_bytes = (uint32_t)C::SC_STAGE;
-                        bytes += C::W_STAGE + sc_bytes;
-                    } else {
-                        bytes += C::W_STAGE;
-                    }
-                    ptx::mbar_arrive_expect_tx(fb, bytes);
-                    if (FMT == FMT_INT4) {
-                        const uint8_t* wsrc =
-                            p.w + ((size_t)it.n_tile * p.nchunks_pad + (size_t)kb * (BK / 32)) * (TILE_N * 16);
-                        ptx::bulk_load(w_dst, wsrc, C::W_STAGE, fb, pol_w);
-                        const int g0 = (kb * BK) >> p.g_shift;
-                        const uint8_t* ssrc = p.sc + ((size_t)it.n_tile * p.ngroups_pad + g0) * (TILE_N * 2);
-                        ptx::bulk_load(sc_dst, ssrc, sc_bytes, fb, pol_w);
-                    } else if (FMT == FMT_FP4) {
-                        ptx::tma_load_2d(w_dst, &p.tmap_w, kb * (BK / 2), it.n_tile * TILE_N, fb, pol_w);
-                        const uint8_t* ssrc =
-                            p.sc + ((size_t)it.n_tile * p.nchunks_pad + (size_t)kb * (BK / 64)) * (TILE_N * 4);
-                        ptx::bulk_load(sc_dst, ssrc, sc_bytes, fb, pol_w);
-                    } else {
-                        ptx::tma_load_2d(w_dst, &p.tmap_w, kb * BK, it.n_tile * TILE_N, fb, pol_w);
-                    }
-                    const uint32_t b_dst = sbase + C::OFF_B + s * C::B_STAGE;
+                    if (act) {
+                        // activation rows >= M are not loaded: they only feed accumulator
+                        // columns that are never stored, and out-of-range rows would cost
+                        // the copy engine a zero fill
+                        // a half tile copies only its own rows (a box half as high)
+                        const uint32_t fb = full_bar(s);
+                        const void* tmap = it.half ? &p.tmap_a_half : &p.tmap_a;
+                        const int rows = it.half ? p.a_box_rows_half : p.a_box_rows;
+                        ptx::mbar_arrive_expect_tx(fb, (uint32_t)((BK / 64) * rows * 128));
+                        const uint32_t b_dst = sbase + C::OFF_B + s * C::B_STAGE;
+                        // pair: this CTA's half of the tokens (of a half tile: its quarter)
+                        const int row0 = it.m_tile * BN + it.m_sub +
+                                         (PAIR ? rank * (it.half ? BN / 4 : C::B_ROWS) : 0);
 #pragma unroll
-                    for (int j = 0; j < BK / 64; ++j)
-                        ptx::tma_load_2d(b_dst + j * (BN * 128), &p.tmap_a, kb * BK + j * 64,
-                                         it.m_tile * BN + it.m_sub, fb, pol_a);
+                        for (int j = 0; j < BK / 64; ++j)
+                            ptx::tma_load_2d(b_dst + j * (C::B_ROWS * 128), tmap, kb * BK + j * 64, row0, fb, pol);
+                    } else if (PAIR && w_tile(it) >= tiles_w) {
+                        // the odd CTA of a pair past the last weight tile (N / 128 odd):
+                        // nothing to copy; its operand rows only reach output rows >= N
+                        ptx::mbar_arrive(wfull_bar(s));
+                    } else {
+                        const uint32_t fb = wfull_bar(s);
+                        const uint32_t w_dst = sbase + C::OFF_W + s * C::W_STAGE;
+                        const uint32_t sc_dst = sbase + C::OFF_SC + s * C::SC_STAGE;
+                        if (FMT == FMT_INT4) {
+                            const int gcnt = (p.G >= BK) ? 1 : (BK >> p.g_shift);
+                            const uint32_t sc_bytes = (uint32_t)gcnt * TILE_N * 2;
+                            ptx::mbar_arrive_expect_tx(fb, C::W_STAGE + sc_bytes);
+                            const uint8_t* wsrc =
+                                p.w + ((size_t)w_tile(it) * p.nchunks_pad + (size_t)kb * (BK / 32)) * (TILE_N * 16);
+                            ptx::bulk_load(w_dst, wsrc, C::W_STAGE, fb, pol);
+                            const int g0 = (kb * BK) >> p.g_shift;
+                            const uint8_t* ssrc = p.sc + ((size_t)w_tile(it) * p.ngroups_pad + g0) * (TILE_N * 2);
+                            ptx::bulk_load(sc_dst, ssrc, sc_bytes, fb, pol);
+                        } else if (FMT == FMT_FP4) {
+                            ptx::mbar_arrive_expect_tx(fb, C::W_STAGE + C::SC_STAGE);
+                            ptx::tma_load_2d(w_dst, &p.tmap_w, kb * (BK / 2), w_tile(it) * TILE_N, fb, pol);
+                            const uint8_t* ssrc =
+                                p.sc + ((size_t)w_tile(it) * p.nchunks_pad + (size_t)kb * (BK / 64)) * (TILE_N * 4);
+                            ptx::bulk_load(sc_dst, ssrc, C::SC_STAGE, fb, pol);
+                        } else {
+                            ptx::mbar_arrive_expect_tx(fb, C::W_STAGE);
+                            ptx::tma_load_2d(w_dst, &p.tmap_w, kb * BK, w_tile(it) * TILE_N, fb, pol);
+                        }
+                    }
                     ++issued;
                     if (++s == STAGES) {
                         s = 0;
@@ -377,12 +441,49 @@ __global__ void __launch_bounds__(128 * (1 + NWG), (GemmCfg<FMT, BF16, BN, BK, S
                     }
                 }
             }
+            if (ok && act) {
+                // tail: every stage released, i.e. every MMA commit aimed at this
+                // CTA's activation ring has landed before the CTA can exit
+                for (int j = 0; j < STAGES && ok; ++j) {
+                    ok = bounded_wait(empty_bar(s), ph ^ 1u, abort_flag, p.status, DEVICE_TIMEOUT_PRODUCER,
+                                            p.timeout_ns);
+                    if (++s == STAGES) {
+                        s = 0;
+                        ph ^= 1u;
+                    }
+                }
+            }
             if (*abort_flag) {
-                // wait for this CTA's own copies in flight before the CTA can exit
+                // wait for this thread's own copies in flight before the CTA can exit
                 const long long first = issued > STAGES ? issued - STAGES : 0;
                 for (long long j = first; j < issued; ++j) {
-                    if (!drain_wait(full_bar((int)(j % STAGES)), (uint32_t)((j / STAGES) & 1), p.timeout_ns))
+                    const int sj = (int)(j % STAGES);
+                    if (!drain_wait(act ? full_bar(sj) : wfull_bar(sj), (uint32_t)((j / STAGES) & 1), p.timeout_ns))
                         atomicOr(p.status, DEVICE_TIMEOUT_DRAIN);
+                }
+            }
+        }
+        __syncwarp();
+    } else if (warp == 1 && PAIR && !issuer) {
+        // ------------------------------------------------------------ pair, odd CTA: forwarder
+        // The even CTA's MMAs read this CTA's activation half: pass each stage's
+        // landing on to the even CTA's full barrier.
+        if (lane == 0) {
+            int s = 0;
+            uint32_t ph = 0;
+            bool ok = true;
+            for (int item = item0; item < p.n_items && ok; item += istride) {
+                const Item it = decode_item(p, item);
+                for (int kb = it.kb_begin; kb < it.kb_end; ++kb) {
+                    if (!bounded_wait(full_bar(s), ph, abort_flag, p.status, DEVICE_TIMEOUT_MMA, p.timeout_ns)) {
+                        ok = false;
+                        break;
+                    }
+                    ptx::mbar_arrive_cluster(at_issuer(full_bar(s)));
+                    if (++s == STAGES) {
+                        s = 0;
+                        ph ^= 1u;
+                    }
                 }
             }
         }
@@ -390,22 +491,30 @@ __global__ void __launch_bounds__(128 * (1 + NWG), (GemmCfg<FMT, BF16, BN, BK, S
     } else if (warp == 1) {
         // ------------------------------------------------------------ MMA issuer
         if (lane == 0) {
-            constexpr uint32_t idesc_full = ptx::make_idesc_f16(BF16, 128, BN);
-            constexpr uint32_t idesc_half = ptx::make_idesc_f16(BF16, 128, BN >= 32 ? BN / 2 : BN);
+            constexpr uint32_t idesc_full = ptx::make_idesc_f16(BF16, PAIR ? 256 : 128, BN);
+            constexpr uint32_t idesc_half = ptx::make_idesc_f16(BF16, PAIR ? 256 : 128, BN >= 32 ? BN / 2 : BN);
+            // every commit arrives on this CTA's barrier and, in a pair, on the other's
+            auto commit = [&](uint32_t bar) {
+                ptx::mma_commit<CG>(bar);
+                if (PAIR) ptx::mma_commit<CG>(at_other(bar));
+            };
             int s = 0, a = 0;
             uint32_t ph = 0, aph = 0, accph = 0;
             bool ok = true;
-            for (int item = blockIdx.x; item < p.n_items && ok; item += gridDim.x) {
+            for (int item = item0; item < p.n_items && ok; item += istride) {
                 const Item it = decode_item(p, item);
-                if (!bounded_wait(accempty_bar, accph ^ 1u, abort_flag, p.status, DEVICE_TIMEOUT_MMA, p.timeout_ns)) {
+                if (!bounded_wait(accempty_bar, accph ^ 1u, abort_flag, p.status, DEVICE_TIMEOUT_MMA,
+                                        p.timeout_ns)) {
                     ok = false;
                     break;
                 }
                 ptx::tc_fence_after();
                 const uint32_t idesc = it.half ? idesc_half : idesc_full;   // half tile: MMA N = BN / 2
                 for (int kb = it.kb_begin; kb < it.kb_end; ++kb) {
-                    if (!bounded_wait(afull_bar(a), aph, abort_flag, p.status, DEVICE_TIMEOUT_MMA, p.timeout_ns) ||
-                        !bounded_wait(full_bar(s), ph, abort_flag, p.status, DEVICE_TIMEOUT_MMA, p.timeout_ns)) {
+                    if (!bounded_wait(afull_bar(a), aph, abort_flag, p.status, DEVICE_TIMEOUT_MMA,
+                                            p.timeout_ns) ||
+                        !bounded_wait(full_bar(s), ph, abort_flag, p.status, DEVICE_TIMEOUT_MMA,
+                                            p.timeout_ns)) {
                         ok = false;
                         break;
                     }
@@ -414,12 +523,12 @@ __global__ void __launch_bounds__(128 * (1 + NWG), (GemmCfg<FMT, BF16, BN, BK, S
                     const uint32_t a_tmem = tmem + C::A_BASE + a * C::A_COLS;
 #pragma unroll
                     for (int kk = 0; kk < BK / 16; ++kk) {
-                        const uint32_t b_addr = b_base + (kk / 4) * (BN * 128) + (kk % 4) * 32;
-                        ptx::mma_f16_ts(tmem, a_tmem + kk * 8, ptx::make_sdesc_sw128(b_addr), idesc,
-                                        (kb > it.kb_begin || kk > 0) ? 1u : 0u);
+                        const uint32_t b_addr = b_base + (kk / 4) * (C::B_ROWS * 128) + (kk % 4) * 32;
+                        ptx::mma_f16_ts<CG>(tmem, a_tmem + kk * 8, ptx::make_sdesc_sw128(b_addr), idesc,
+                                            (kb > it.kb_begin || kk > 0) ? 1u : 0u);
                     }
-                    ptx::mma_commit(empty_bar(s));
-                    ptx::mma_commit(aempty_bar(a));
+                    commit(empty_bar(s));
+                    commit(aempty_bar(a));
                     if (++s == STAGES) {
                         s = 0;
                         ph ^= 1u;
@@ -430,11 +539,14 @@ __global__ void __launch_bounds__(128 * (1 + NWG), (GemmCfg<FMT, BF16, BN, BK, S
                     }
                 }
                 if (!ok) break;
-                ptx::mma_commit(accfull_bar);
+                commit(accfull_bar);
                 accph ^= 1u;
             }
+            // pair: the last epilogue of both CTAs has arrived here before the CTA exits
+            if (PAIR && ok && !*abort_flag)
+                bounded_wait(accempty_bar, accph ^ 1u, abort_flag, p.status, DEVICE_TIMEOUT_MMA, p.timeout_ns);
             if (*abort_flag) {
-                ptx::mma_commit(final_bar);
+                ptx::mma_commit<CG>(final_bar);
                 if (!drain_wait(final_bar, 0, p.timeout_ns)) atomicOr(p.status, DEVICE_TIMEOUT_DRAIN);
             }
         }
@@ -447,101 +559,119 @@ __global__ void __launch_bounds__(128 * (1 + NWG), (GemmCfg<FMT, BF16, BN, BK, S
         const int r = quarter * 32 + lane;  // weight row inside the tile == TMEM lane
         const uint32_t lane_addr = (uint32_t)(quarter * 32) << 16;
         int s = 0, a = 0;
-        uint32_t ph = 0, aph = 0, accph = 0;
+        uint32_t ph = 0, aph = 0, accph = 0, eph = 0;
         bool ok = true;
+        // all transform warps meet here (bounded, so an aborting warp cannot strand
+        // the others the way a hardware barrier would)
+        auto epi_sync = [&]() -> bool {
+            __syncwarp();
+            if (lane == 0) ptx::mbar_arrive(epi_bar);
+            const bool w = __all_sync(0xffffffffu, bounded_wait(epi_bar, eph, abort_flag, p.status,
+                                                                DEVICE_TIMEOUT_EPILOGUE, p.timeout_ns));
+            eph ^= 1u;
+            return w;
+        };
         ptx::grid_dependency_wait();   // alpha / bias are global inputs too
         const float alpha = (FMT == FMT_INT4) ? 1.0f : __ldg(p.alpha);
-        for (int item = blockIdx.x; item < p.n_items && ok; item += gridDim.x) {
-            const Item it = decode_item(p, item);
-            for (int kb = it.kb_begin; kb < it.kb_end; ++kb) {
-                bool w1 = bounded_wait(full_bar(s), ph, abort_flag, p.status, DEVICE_TIMEOUT_TRANSFORM, p.timeout_ns);
-                bool w2 = w1 && bounded_wait(aempty_bar(a), aph ^ 1u, abort_flag, p.status, DEVICE_TIMEOUT_TRANSFORM,
-                                             p.timeout_ns);
-                if (!__all_sync(0xffffffffu, w2)) {
-                    ok = false;
-                    break;
-                }
-                ptx::tc_fence_after();
-                const uint8_t* wt = smem + C::OFF_W + s * C::W_STAGE;
-                const uint8_t* sct = smem + C::OFF_SC + s * C::SC_STAGE;
-                const uint32_t a_col = tmem + lane_addr + C::A_BASE + a * C::A_COLS;
-                if (FMT == FMT_FP8) {
-                    constexpr int CH = BK / 16;  // 16-byte chunks (16 codes, 8 columns) per row
-#pragma unroll
-                    for (int c = wg * (CH / NWG); c < (wg + 1) * (CH / NWG); ++c) {
-                        const uint4 q = *reinterpret_cast<const uint4*>(wt + swz(r * C::W_PITCH + c * 16, C::W_SWZ));
-                        uint32_t o[8];
-                        fp8_to_operand<BF16>(q, o);
-                        ptx::tmem_st8(a_col + c * 8, o);
-                    }
-                } else {
-                    constexpr int CH = BK / 32;  // 16-byte chunks (32 codes, 16 columns) per row
-                    constexpr int CPW = CH / NWG;  // chunks per transform warpgroup
-                    const int c0 = wg * CPW;
-                    // all shared-memory loads first, then the conversions, then the TMEM
-                    // stores, so the units overlap instead of running back to back
-                    uint2 qi[CPW][4];     // INT4: four lanes' halves per 32-k unit
-                    uint4 q[CPW];         // FP4: one 16-byte chunk per 32-k unit
-                    uint16_t sv[CPW];
-                    const int gr = r >> 4, g8 = r & 7;
-#pragma unroll
-                    for (int i = 0; i < CPW; ++i) {
-                        const int c = c0 + i;
-                        if (FMT == FMT_INT4) {
-                            // unit c: quad c / 2 of the stage, k steps 2 (c % 2) and 2 (c % 2) + 1
-                            const uint8_t* ub = wt + (c >> 1) * 4096 + gr * 512 + (c & 1) * 8;
-#pragma unroll
-                            for (int l = 0; l < 4; ++l)
-                                qi[i][l] = *reinterpret_cast<const uint2*>(ub + int4_slot(4 * g8 + l) * 16);
-                            sv[i] = *reinterpret_cast<const uint16_t*>(sct + (((c * 32) >> p.g_shift) * TILE_N + r) * 2);
-                        } else {
-                            q[i] = *reinterpret_cast<const uint4*>(wt + swz(r * C::W_PITCH + c * 16, C::W_SWZ));
-                            sv[i] = *reinterpret_cast<const uint16_t*>(sct + (c >> 1) * (TILE_N * 4) + r * 4 + (c & 1) * 2);
-                        }
-                    }
-                    uint32_t o[CPW][16];
-#pragma unroll
-                    for (int i = 0; i < CPW; ++i) {
-                        if (FMT == FMT_INT4) {
-                            const Int4RowConsts kc = int4_row_consts((r >> 3) & 1);
-                            if (BF16)
-                                int4_row_to_bf16(qi[i], kc, __half2float(__ushort_as_half(sv[i])), o[i]);
-                            else
-                                int4_row_to_f16(qi[i], kc, (uint32_t)sv[i] | ((uint32_t)sv[i] << 16), o[i]);
-                        } else {
-                            fp4_to_bf16(q[i], sv[i], o[i]);
-                        }
-                    }
-#pragma unroll
-                    for (int i = 0; i < CPW; ++i) ptx::tmem_st16(a_col + (c0 + i) * 16, o[i]);
-                }
-                ptx::tmem_wait_st();
-                ptx::tc_fence_before();
-                __syncwarp();
-                if (lane == 0) ptx::mbar_arrive(afull_bar(a));
-                if (++s == STAGES) {
-                    s = 0;
-                    ph ^= 1u;
-                }
-                if (++a == C::A_ST) {
-                    a = 0;
-                    aph ^= 1u;
-                }
+        // One k-block of the transform: waits for its codes and a free TMEM operand
+        // stage, writes the 16-bit operand there and hands it to the MMA issuer.
+        auto transform_one = [&]() -> bool {
+            bool w1 = bounded_wait(wfull_bar(s), ph, abort_flag, p.status, DEVICE_TIMEOUT_TRANSFORM, p.timeout_ns);
+            bool w2 = w1 && bounded_wait(aempty_bar(a), aph ^ 1u, abort_flag, p.status,
+                                               DEVICE_TIMEOUT_TRANSFORM, p.timeout_ns);
+            if (!__all_sync(0xffffffffu, w2)) {
+                return false;
             }
-            if (!ok) break;
-
-            // ------------------------------------------------ epilogue
+            ptx::tc_fence_after();
+            const uint8_t* wt = smem + C::OFF_W + s * C::W_STAGE;
+            const uint8_t* sct = smem + C::OFF_SC + s * C::SC_STAGE;
+            const uint32_t a_col = tmem + lane_addr + C::A_BASE + a * C::A_COLS;
+            if (FMT == FMT_FP8) {
+                constexpr int CH = BK / 16;  // 16-byte chunks (16 codes, 8 columns) per row
+#pragma unroll
+                for (int c = wg * (CH / NWG); c < (wg + 1) * (CH / NWG); ++c) {
+                    const uint4 q = *reinterpret_cast<const uint4*>(wt + swz(r * C::W_PITCH + c * 16, C::W_SWZ));
+                    uint32_t o[8];
+                    fp8_to_operand<BF16>(q, o);
+                    ptx::tmem_st8(a_col + c * 8, o);
+                }
+                __syncwarp();
+                if (lane == 0) ptx::mbar_arrive(wempty_bar(s));   // codes consumed
+            } else {
+                constexpr int CH = BK / 32;  // 16-byte chunks (32 codes, 16 columns) per row
+                constexpr int CPW = CH / NWG;  // chunks per transform warpgroup
+                const int c0 = wg * CPW;
+                // all shared-memory loads first, then the conversions, then the TMEM
+                // stores, so the units overlap instead of running back to back
+                uint2 qi[CPW][4];     // INT4: four lanes' halves per 32-k unit
+                uint4 q[CPW];         // FP4: one 16-byte chunk per 32-k unit
+                uint16_t sv[CPW];
+                const int gr = r >> 4, g8 = r & 7;
+#pragma unroll
+                for (int i = 0; i < CPW; ++i) {
+                    const int c = c0 + i;
+                    if (FMT == FMT_INT4) {
+                        // unit c: quad c / 2 of the stage, k steps 2 (c % 2) and 2 (c % 2) + 1
+                        const uint8_t* ub = wt + (c >> 1) * 4096 + gr * 512 + (c & 1) * 8;
+#pragma unroll
+                        for (int l = 0; l < 4; ++l)
+                            qi[i][l] = *reinterpret_cast<const uint2*>(ub + int4_slot(4 * g8 + l) * 16);
+                        sv[i] = *reinterpret_cast<const uint16_t*>(sct + (((c * 32) >> p.g_shift) * TILE_N + r) * 2);
+                    } else {
+                        q[i] = *reinterpret_cast<const uint4*>(wt + swz(r * C::W_PITCH + c * 16, C::W_SWZ));
+                        sv[i] = *reinterpret_cast<const uint16_t*>(sct + (c >> 1) * (TILE_N * 4) + r * 4 + (c & 1) * 2);
+                    }
+                }
+                uint32_t o[CPW][16];
+#pragma unroll
+                for (int i = 0; i < CPW; ++i) {
+                    if (FMT == FMT_INT4) {
+                        const Int4RowConsts kc = int4_row_consts((r >> 3) & 1);
+                        if (BF16)
+                            int4_row_to_bf16(qi[i], kc, __half2float(__ushort_as_half(sv[i])), o[i]);
+                        else
+                            int4_row_to_f16(qi[i], kc, (uint32_t)sv[i] | ((uint32_t)sv[i] << 16), o[i]);
+                    } else {
+                        fp4_to_bf16(q[i], sv[i], o[i]);
+                    }
+                }
+                __syncwarp();
+                if (lane == 0) ptx::mbar_arrive(wempty_bar(s));   // codes consumed
+#pragma unroll
+                for (int i = 0; i < CPW; ++i) ptx::tmem_st16(a_col + (c0 + i) * 16, o[i]);
+            }
+            ptx::tmem_wait_st();
+            ptx::tc_fence_before();
+            __syncwarp();
+            if (lane == 0) {
+                if (PAIR && !issuer)
+                    ptx::mbar_arrive_cluster(at_issuer(afull_bar(a)));
+                else
+                    ptx::mbar_arrive(afull_bar(a));
+            }
+            if (++s == STAGES) {
+                s = 0;
+                ph ^= 1u;
+            }
+            if (++a == C::A_ST) {
+                a = 0;
+                aph ^= 1u;
+            }
+            return true;
+        };
+        // Epilogue of one item: accumulator -> output (or split-K partial), then the
+        // accumulator is handed back to the MMA issuer.
+        auto epilogue = [&](const Item& it) -> bool {
             const bool wacc = bounded_wait(accfull_bar, accph, abort_flag, p.status, DEVICE_TIMEOUT_EPILOGUE,
-                                           p.timeout_ns);
+                                                 p.timeout_ns);
             if (!__all_sync(0xffffffffu, wacc)) {
-                ok = false;
-                break;
+                return false;
             }
             accph ^= 1u;
             ptx::tc_fence_after();
             ptx::grid_dependency_wait();   // outputs and workspace may still be in use by the previous kernel
-            const int n = it.n_tile * TILE_N + r;
-            const int m0 = it.m_tile * BN + it.m_sub;
+            const int n = w_tile(it) * TILE_N + r;
+            const int m0 = it.m_tile * BN + it.m_sub;   // pair: accumulator column j is token m0 + j
             // accumulator columns per warpgroup (a half tile has BN / 2 of them)
             const int COLS = (it.half ? BN / 2 : BN) / NWG;
             constexpr int STEP = BN / NWG / 2 >= 16 ? 16 : 8;
@@ -552,24 +682,66 @@ __global__ void __launch_bounds__(128 * (1 + NWG), (GemmCfg<FMT, BF16, BN, BK, S
             float bias_v = 0.0f;
             if (FMT == FMT_FP8 && p.bias != nullptr && nvalid) bias_v = load_16bit<BF16>(p.bias, (size_t)n);
 
-            if (p.splits == 1) {
+            if (C::STAGE_OUT) {
+                // accumulator -> 16-bit -> staging [token][weight row]; the accumulator is
+                // handed back as soon as it is read, then one thread copies the staged
+                // tile out with TMA while the next item runs (rows >= M and columns >= N
+                // are not written by the copy)
+                if (warp == 4 && lane == 0) ptx::bulk_wait_group_read0();   // previous copy-out read it
+                if (!epi_sync()) return false;
+                uint16_t* stg = reinterpret_cast<uint16_t*>(smem + C::OFF_STG);
 #pragma unroll 1
-                for (int cc = c_begin; cc < c_begin + COLS; cc += STEP) {
-                    uint32_t v[16];
-                    if (STEP == 16) {
-                        ptx::tmem_ld16(acc_addr + cc, v);
-                    } else {
-                        uint32_t v8[8];
-                        ptx::tmem_ld8(acc_addr + cc, v8);
-#pragma unroll
-                        for (int j = 0; j < 8; ++j) v[j] = v8[j];
-                    }
+                for (int cc = c_begin; cc < c_begin + COLS; cc += 32) {
+                    uint32_t v[32];
+                    ptx::tmem_ld16(acc_addr + cc, *reinterpret_cast<uint32_t(*)[16]>(v));
+                    ptx::tmem_ld16(acc_addr + cc + 16, *reinterpret_cast<uint32_t(*)[16]>(v + 16));
                     ptx::tmem_wait_ld();
 #pragma unroll
-                    for (int j = 0; j < STEP; ++j) {
-                        const int m = m0 + cc + j;
-                        if (nvalid && m < p.M)
-                            store_out<BF16>(p.out, (size_t)m * p.N + n, alpha * __uint_as_float(v[j]) + bias_v);
+                    for (int j = 0; j < 32; ++j)
+                        stg[(cc + j) * TILE_N + r] = to_16bit<BF16>(alpha * __uint_as_float(v[j]) + bias_v);
+                }
+                ptx::tc_fence_before();
+                ptx::fence_proxy_async_smem();   // staging writes visible to the copy engine
+                __syncwarp();
+                if (lane == 0) {
+                    if (PAIR && !issuer)
+                        ptx::mbar_arrive_cluster(at_issuer(accempty_bar));
+                    else
+                        ptx::mbar_arrive(accempty_bar);
+                }
+                if (!epi_sync()) return false;   // the whole tile is staged
+                if (warp == 4 && lane == 0 && w_tile(it) * TILE_N < p.N) {
+                    const int rows = it.half ? BN / 2 : BN;
+                    for (int h = 0; h < rows && m0 + h < p.M; h += C::OUT_BOX_M)
+                        ptx::tma_store_2d(&p.tmap_out, ptx::smem_u32(stg) + h * TILE_N * 2, w_tile(it) * TILE_N,
+                                          m0 + h);
+                    ptx::bulk_commit_group();
+                }
+                return true;
+            }
+            if (p.splits == 1) {
+                // CH accumulator columns per wait on tensor memory: the loads of a
+                // chunk are issued back to back, so the epilogue pays the TMEM
+                // latency once per chunk instead of once per 16 columns
+                constexpr int CH = (BN / NWG / 2 >= 64) ? 64 : (BN / NWG / 2 >= 8 ? BN / NWG / 2 : 8);
+#pragma unroll 1
+                for (int cc = c_begin; cc < c_begin + COLS; cc += CH) {
+                    uint32_t v[CH];
+                    if (CH >= 16) {
+#pragma unroll
+                        for (int q = 0; q < CH / 16; ++q)
+                            ptx::tmem_ld16(acc_addr + cc + 16 * q, *reinterpret_cast<uint32_t(*)[16]>(v + 16 * q));
+                    } else {
+                        ptx::tmem_ld8(acc_addr + cc, *reinterpret_cast<uint32_t(*)[8]>(v));
+                    }
+                    ptx::tmem_wait_ld();
+                    if (nvalid) {
+#pragma unroll
+                        for (int j = 0; j < CH; ++j) {
+                            const int m = m0 + cc + j;
+                            if (m < p.M)
+                                store_out<BF16>(p.out, (size_t)m * p.N + n, alpha * __uint_as_float(v[j]) + bias_v);
+                        }
                     }
                 }
             } else {
@@ -629,24 +801,69 @@ __global__ void __launch_bounds__(128 * (1 + NWG), (GemmCfg<FMT, BF16, BN, BK, S
             }
             ptx::tc_fence_before();
             __syncwarp();
-            if (lane == 0) ptx::mbar_arrive(accempty_bar);
+            if (lane == 0) {
+                if (PAIR && !issuer)
+                    ptx::mbar_arrive_cluster(at_issuer(accempty_bar));
+                else
+                    ptx::mbar_arrive(accempty_bar);
+            }
+            return true;
+        };
+        // The epilogue of an item runs after the transform of the first A_ST k-blocks
+        // of the next one: those fill the operand stages while the item's last MMAs
+        // run, so the MMA issuer starts the next item as soon as the accumulator is
+        // free instead of waiting for the epilogue and then for a transform.
+        Item pend{};
+        bool has_pend = false;
+        for (int item = item0; item < p.n_items && ok; item += istride) {
+            const Item it = decode_item(p, item);
+            int done = 0;
+            for (int kb = it.kb_begin; kb < it.kb_end && ok; ++kb) {
+                ok = transform_one();
+                if (ok && has_pend && ++done == C::A_ST) {
+                    ok = epilogue(pend);
+                    has_pend = false;
+                }
+            }
+            if (ok && has_pend) {
+                ok = epilogue(pend);
+                has_pend = false;
+            }
+            pend = it;
+            has_pend = true;
         }
-        (void)ok;
+        if (ok && has_pend) ok = epilogue(pend);
+        // the last copies out have completed before the CTA exits
+        if (C::STAGE_OUT && warp == 4 && lane == 0) ptx::bulk_wait_group0();
+        if (ok) {
+            // tail: every MMA commit aimed at this CTA's operand stages has landed
+            for (int j = 0; j < C::A_ST && ok; ++j) {
+                ok = __all_sync(0xffffffffu, bounded_wait(aempty_bar(a), aph ^ 1u, abort_flag, p.status,
+                                                                DEVICE_TIMEOUT_TRANSFORM, p.timeout_ns));
+                if (++a == C::A_ST) {
+                    a = 0;
+                    aph ^= 1u;
+                }
+            }
+        }
     }
 
     ptx::tc_fence_before();
     __syncthreads();
+    // pair: neither CTA leaves (or frees its tensor memory) while the other may
+    // still signal it or run MMAs on its operands
+    if (PAIR) ptx::cluster_sync();
     if (warp == 2) {
         ptx::tc_fence_after();
-        ptx::tmem_dealloc(tmem, C::TMEM_COLS);
+        ptx::tmem_dealloc<CG>(tmem, C::TMEM_COLS);
     }
 }
 
 // Host-side launcher for one instantiation.
-template <int FMT, bool BF16, int BN, int BK, int STAGES, int NWG>
+template <int FMT, bool BF16, int BN, int BK, int STAGES, int NWG, bool PAIR = false>
 struct GemmLauncher {
-    using C = GemmCfg<FMT, BF16, BN, BK, STAGES, NWG>;
-    static constexpr auto kernel = wq_gemm_kernel<FMT, BF16, BN, BK, STAGES, NWG>;
+    using C = GemmCfg<FMT, BF16, BN, BK, STAGES, NWG, PAIR>;
+    static constexpr auto kernel = wq_gemm_kernel<FMT, BF16, BN, BK, STAGES, NWG, PAIR>;
     static cudaError_t prepare() {
         // per device: allow the dynamic shared memory this configuration needs
         static int attr_set[64] = {0};
@@ -687,6 +904,24 @@ struct GemmLauncher {
         if (by_thr < n) n = by_thr;
         if (by_tmem < n) n = by_tmem;
         if (n >= 1) k.ctas_per_sm = n;
+        if (PAIR) {
+            // pairs the GPU holds at once
+            cudaLaunchConfig_t lc = {};
+            lc.gridDim = dim3(2, 1, 1);
+            lc.blockDim = dim3(C::NT, 1, 1);
+            lc.dynamicSmemBytes = C::SMEM_BYTES;
+            cudaLaunchAttribute at[1];
+            at[0].id = cudaLaunchAttributeClusterDimension;
+            at[0].val.clusterDim.x = 2;
+            at[0].val.clusterDim.y = 1;
+            at[0].val.clusterDim.z = 1;
+            lc.attrs = at;
+            lc.numAttrs = 1;
+            int nc = 0;
+            if (cudaOccupancyMaxActiveClusters(&nc, kernel, &lc) == cudaSuccess) k.max_clusters[2] = nc;
+            else (void)cudaGetLastError();
+            k.pair = 1;
+        }
         return k;
     }
     static cudaError_t launch(const GemmParams& p, int grid, cudaStream_t st) {
@@ -698,11 +933,19 @@ struct GemmLauncher {
         cfg.dynamicSmemBytes = C::SMEM_BYTES;
         cfg.stream = st;
         // programmatic dependent launch: set-up overlaps the previous kernel's tail
-        cudaLaunchAttribute attr[1];
+        cudaLaunchAttribute attr[2];
         attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
         attr[0].val.programmaticStreamSerializationAllowed = 1;
         cfg.attrs = attr;
         cfg.numAttrs = 1;
+        if (PAIR) {
+            if (grid % 2 != 0) return cudaErrorInvalidValue;
+            attr[1].id = cudaLaunchAttributeClusterDimension;
+            attr[1].val.clusterDim.x = 2;
+            attr[1].val.clusterDim.y = 1;
+            attr[1].val.clusterDim.z = 1;
+            cfg.numAttrs = 2;
+        }
         return cudaLaunchKernelEx(&cfg, kernel, p);
     }
 };

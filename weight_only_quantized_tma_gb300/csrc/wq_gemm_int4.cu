@@ -14,6 +14,19 @@ using I4F16_128 = GemmLauncher<FMT_INT4, false, 128, 128, 2, 2>;
 using I4F16_256 = GemmLauncher<FMT_INT4, false, 256, 128, 3, 2>;
 using I4BF16_16 = GemmLauncher<FMT_INT4, true, 16, 128, 8, 2>;
 using I4BF16_256 = GemmLauncher<FMT_INT4, true, 256, 128, 3, 2>;
+// Large M: two-CTA clusters, 256 x 256 tiles, each CTA holding half the activation
+// tile; three stages leave room for the 64 KB output staging area.
+using I4F16_P = GemmLauncher<FMT_INT4, false, 256, 128, 3, 2, true>;
+using I4BF16_P = GemmLauncher<FMT_INT4, true, 256, 128, 3, 2, true>;
+
+bool config_int4_pair(bool bf16, bool query, KernelConfig* cfg) {
+    *cfg = bf16 ? I4BF16_P::config(query) : I4F16_P::config(query);
+    return true;
+}
+
+cudaError_t launch_gemm_int4_pair(const GemmParams& p, bool bf16, int grid, cudaStream_t st) {
+    return bf16 ? I4BF16_P::launch(p, grid, st) : I4F16_P::launch(p, grid, st);
+}
 // Decode (M <= 16): register-resident mma.sync kernel, one 8-token column tile for
 // M <= 8, two for M <= 16, and the fold position (k steps per group) fixed at compile
 // time.  All instantiations share shared memory, threads and the cluster limits.

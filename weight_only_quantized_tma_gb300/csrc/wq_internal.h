@@ -73,6 +73,8 @@ __host__ __device__ __forceinline__ uint32_t fastdiv(uint32_t x, const FastDiv& 
 struct GemmParams {
     CUtensorMap tmap_a;      // activations [M][K], 16-bit, box {64, BN}, 128-byte swizzle
     CUtensorMap tmap_w;      // FP8 [N][K] / FP4 [N][K/2] weights (unused for INT4)
+    CUtensorMap tmap_a_half; // activations, box half as high (half tiles)
+    CUtensorMap tmap_out;    // pair kernel: out [M][N], 16-bit, box {128, 128}, no swizzle
     const uint8_t* w;        // INT4 prepacked weight tiles
     const uint8_t* sc;       // INT4 prepacked group scales / FP4 prepacked block scales
     const float* alpha;      // FP8 / FP4 global scale (device), unused for INT4
@@ -84,10 +86,11 @@ struct GemmParams {
     int M, N, K;
     int G;                   // INT4 group size
     int g_shift;             // log2(G)
-    int tiles_n, tiles_m;
+    int tiles_n, tiles_m;    // output tiles along N (pair kernel: 256-row pairs) and M
     int splits;              // split-K slices per output tile
     int nkb;                 // k-blocks
     int a_box_rows;          // activation rows per TMA box (M when one token tile covers M, else BN)
+    int a_box_rows_half;     // rows per box of tmap_a_half
     int kb_base, kb_rem;     // slice s covers kb_base * s + min(s, kb_rem) .. (nkb split as evenly as possible)
     int n_items;             // work items (tile kernel: n_full whole tiles, then two half tiles per remaining tile)
     int n_full;              // tile kernel: items below this are whole tiles (or split-K slices)
@@ -123,7 +126,8 @@ struct KernelConfig {
     int smem_bytes;  // dynamic shared memory
     int tmem_cols;
     int ctas_per_sm;  // resident CTAs per SM (registers, shared and tensor memory)
-    int max_clusters[kMaxDecodeCluster + 1];  // decode kernel: S-CTA clusters held at once (S = 2..16)
+    int max_clusters[kMaxDecodeCluster + 1];  // S-CTA clusters held at once (decode: S = 2..16; pair: S = 2)
+    int pair;        // tile kernel on two-CTA clusters (tcgen05 cta_group::2, 256 weight rows per tile)
 };
 
 // Per-format launch entry points, defined in wq_gemm_{int4,fp8,fp4}.cu.
@@ -140,6 +144,9 @@ bool config_int4(bool bf16, int bn, bool query, KernelConfig* cfg);
 // two-column-tile instantiation; both use the same shared memory and threads.
 bool config_int4_decode(bool bf16, bool query, KernelConfig* cfg);
 cudaError_t launch_gemm_int4_decode(const GemmParams& p, bool bf16, int grid, cudaStream_t st);
+// W4A16 tile kernel on two-CTA clusters (256 weight rows x 256 tokens per tile).
+bool config_int4_pair(bool bf16, bool query, KernelConfig* cfg);
+cudaError_t launch_gemm_int4_pair(const GemmParams& p, bool bf16, int grid, cudaStream_t st);
 bool config_fp8(bool bf16, int bn, bool query, KernelConfig* cfg);
 bool config_fp4(bool bf16, int bn, bool query, KernelConfig* cfg);
 
