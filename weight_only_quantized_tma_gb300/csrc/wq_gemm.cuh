@@ -13,8 +13,8 @@
 //   warp 0      TMA producer of the activation tiles, one per k-block, through a
 //               STAGES-deep mbarrier ring released by the MMA commits;
 //   warp 3      TMA producer of the packed weight tiles and their scales, through
-//               a second STAGES-deep ring released by the transform warps as soon
-//               as they hold the codes in registers;
+//               a second, WSTAGES-deep ring released by the transform warps as
+//               soon as they hold the codes in registers;
 //   warp 1      MMA issuer: tcgen05.mma kind::f16, accumulator in TMEM, commits
 //               free the activation stage and the TMEM operand stage;
 //   warp 2      TMEM allocator;
@@ -54,7 +54,7 @@
 
 namespace wq {
 
-template <int FMT, bool BF16, int BN, int BK, int STAGES, int NWG, bool PAIR = false>
+template <int FMT, bool BF16, int BN, int BK, int STAGES, int NWG, bool PAIR = false, int WSTAGES = STAGES>
 struct GemmCfg {
     static constexpr int NT = 128 * (1 + NWG);
     static constexpr int B_ROWS = PAIR ? BN / 2 : BN;                 // tokens this CTA copies per k-block
@@ -70,15 +70,15 @@ struct GemmCfg {
     // shared memory carve-up (offsets from a 1024-aligned base)
     static constexpr int OFF_B = 0;
     static constexpr int OFF_W = OFF_B + STAGES * B_STAGE;
-    static constexpr int OFF_SC = OFF_W + STAGES * W_STAGE;
+    static constexpr int OFF_SC = OFF_W + WSTAGES * W_STAGE;
     // pair: the epilogue stages the 16-bit output tile [token][weight row] here and
     // copies it out with TMA, so the accumulator is released before the stores
     static constexpr bool STAGE_OUT = PAIR;
     static constexpr int OUT_BOX_M = 128;                             // tokens per output copy
-    static constexpr int OFF_STG = (OFF_SC + STAGES * SC_STAGE + 1023) / 1024 * 1024;
+    static constexpr int OFF_STG = (OFF_SC + WSTAGES * SC_STAGE + 1023) / 1024 * 1024;
     static constexpr int STG_BYTES = STAGE_OUT ? BN * TILE_N * 2 : 0;
     static constexpr int OFF_BAR = (OFF_STG + STG_BYTES + 127) / 128 * 128;
-    static constexpr int NBARS = 4 * STAGES + 2 * A_ST + 4;
+    static constexpr int NBARS = 2 * STAGES + 2 * WSTAGES + 2 * A_ST + 4;
     static constexpr int OFF_MISC = OFF_BAR + NBARS * 8;
     static constexpr int SMEM_USED = OFF_MISC + 16;
     static constexpr int SMEM_BYTES = SMEM_USED + 1024;               // alignment slack
@@ -286,10 +286,10 @@ __device__ __forceinline__ Item decode_item(const GemmParams& p, int item) {
     return it;
 }
 
-template <int FMT, bool BF16, int BN, int BK, int STAGES, int NWG, bool PAIR>
-__global__ void __launch_bounds__(128 * (1 + NWG), (GemmCfg<FMT, BF16, BN, BK, STAGES, NWG, PAIR>::MIN_BLOCKS))
+template <int FMT, bool BF16, int BN, int BK, int STAGES, int NWG, bool PAIR, int WSTAGES>
+__global__ void __launch_bounds__(128 * (1 + NWG), (GemmCfg<FMT, BF16, BN, BK, STAGES, NWG, PAIR, WSTAGES>::MIN_BLOCKS))
     wq_gemm_kernel(const __grid_constant__ GemmParams p) {
-    using C = GemmCfg<FMT, BF16, BN, BK, STAGES, NWG, PAIR>;
+    using C = GemmCfg<FMT, BF16, BN, BK, STAGES, NWG, PAIR, WSTAGES>;
     constexpr int CG = PAIR ? 2 : 1;   // tcgen05 CTA group of every tcgen05 instruction here
     extern __shared__ uint8_t smem_raw[];
     uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
@@ -297,11 +297,11 @@ __global__ void __launch_bounds__(128 * (1 + NWG), (GemmCfg<FMT, BF16, BN, BK, S
     const uint32_t bar0 = sbase + C::OFF_BAR;
     auto full_bar = [&](int s) { return bar0 + 8u * s; };                 // activation stage landed
     auto empty_bar = [&](int s) { return bar0 + 8u * (STAGES + s); };     // activation stage free
-    auto wfull_bar = [&](int s) { return bar0 + 8u * (2 * STAGES + s); }; // weight stage landed
-    auto wempty_bar = [&](int s) { return bar0 + 8u * (3 * STAGES + s); };// weight stage free
-    auto afull_bar = [&](int a) { return bar0 + 8u * (4 * STAGES + a); };
-    auto aempty_bar = [&](int a) { return bar0 + 8u * (4 * STAGES + C::A_ST + a); };
-    const uint32_t accfull_bar = bar0 + 8u * (4 * STAGES + 2 * C::A_ST);
+    auto wfull_bar = [&](int s) { return bar0 + 8u * (2 * STAGES + s); };            // weight stage landed
+    auto wempty_bar = [&](int s) { return bar0 + 8u * (2 * STAGES + WSTAGES + s); }; // weight stage free
+    auto afull_bar = [&](int a) { return bar0 + 8u * (2 * STAGES + 2 * WSTAGES + a); };
+    auto aempty_bar = [&](int a) { return bar0 + 8u * (2 * STAGES + 2 * WSTAGES + C::A_ST + a); };
+    const uint32_t accfull_bar = bar0 + 8u * (2 * STAGES + 2 * WSTAGES + 2 * C::A_ST);
     const uint32_t accempty_bar = accfull_bar + 8u;
     const uint32_t final_bar = accfull_bar + 16u;
     const uint32_t epi_bar = accfull_bar + 24u;   // staged epilogue: sync of the transform warps
@@ -322,6 +322,8 @@ __global__ void __launch_bounds__(128 * (1 + NWG), (GemmCfg<FMT, BF16, BN, BK, S
             // pair, rank 0: its own copies plus the forwarded arrival of rank 1's
             ptx::mbar_init(full_bar(s), (PAIR && issuer) ? 2 : 1);
             ptx::mbar_init(empty_bar(s), 1);
+        }
+        for (int s = 0; s < WSTAGES; ++s) {
             ptx::mbar_init(wfull_bar(s), 1);
             ptx::mbar_init(wempty_bar(s), n_epi / 32);
         }
@@ -372,6 +374,7 @@ __global__ void __launch_bounds__(128 * (1 + NWG), (GemmCfg<FMT, BF16, BN, BK, S
         // tiles and scales (freed by the transform warps)
         if (lane == 0) {
             const bool act = (warp == 0);
+            const int NS = act ? STAGES : WSTAGES;   // depth of this producer's ring
             const uint64_t pol = act ? ptx::policy_evict_last()
                                      : (p.w_evict_first ? ptx::policy_evict_first() : ptx::policy_evict_last());
             int s = 0;
@@ -435,7 +438,7 @@ __global__ void __launch_bounds__(128 * (1 + NWG), (GemmCfg<FMT, BF16, BN, BK, S
                         }
                     }
                     ++issued;
-                    if (++s == STAGES) {
+                    if (++s == NS) {
                         s = 0;
                         ph ^= 1u;
                     }
@@ -455,10 +458,10 @@ __global__ void __launch_bounds__(128 * (1 + NWG), (GemmCfg<FMT, BF16, BN, BK, S
             }
             if (*abort_flag) {
                 // wait for this thread's own copies in flight before the CTA can exit
-                const long long first = issued > STAGES ? issued - STAGES : 0;
+                const long long first = issued > NS ? issued - NS : 0;
                 for (long long j = first; j < issued; ++j) {
-                    const int sj = (int)(j % STAGES);
-                    if (!drain_wait(act ? full_bar(sj) : wfull_bar(sj), (uint32_t)((j / STAGES) & 1), p.timeout_ns))
+                    const int sj = (int)(j % NS);
+                    if (!drain_wait(act ? full_bar(sj) : wfull_bar(sj), (uint32_t)((j / NS) & 1), p.timeout_ns))
                         atomicOr(p.status, DEVICE_TIMEOUT_DRAIN);
                 }
             }
@@ -498,47 +501,70 @@ __global__ void __launch_bounds__(128 * (1 + NWG), (GemmCfg<FMT, BF16, BN, BK, S
                 ptx::mma_commit<CG>(bar);
                 if (PAIR) ptx::mma_commit<CG>(at_other(bar));
             };
+            // The issuing thread runs at most about one MMA ahead of the tensor pipe,
+            // so every instruction between two MMAs is pipe time unless it overlaps an
+            // MMA in flight.  Hence: the next k-block's barriers are probed (without
+            // blocking) before its last MMA is issued, and a k-block's commits go out
+            // after the next k-block's first MMA (they then also cover that MMA, which
+            // frees the stages one MMA later).
+            const uint32_t empty0_o = PAIR ? at_other(empty_bar(0)) : 0u;   // barriers are contiguous
+            const uint32_t aempty0_o = PAIR ? at_other(aempty_bar(0)) : 0u;
+            auto commit_stage = [&](int cs, int ca) {
+                ptx::mma_commit<CG>(empty_bar(cs));
+                ptx::mma_commit<CG>(aempty_bar(ca));
+                if (PAIR) {
+                    ptx::mma_commit<CG>(empty0_o + 8u * cs);
+                    ptx::mma_commit<CG>(aempty0_o + 8u * ca);
+                }
+            };
             int s = 0, a = 0;
             uint32_t ph = 0, aph = 0, accph = 0;
             bool ok = true;
             for (int item = item0; item < p.n_items && ok; item += istride) {
                 const Item it = decode_item(p, item);
                 if (!bounded_wait(accempty_bar, accph ^ 1u, abort_flag, p.status, DEVICE_TIMEOUT_MMA,
-                                        p.timeout_ns)) {
+                                  p.timeout_ns)) {
                     ok = false;
                     break;
                 }
                 ptx::tc_fence_after();
                 const uint32_t idesc = it.half ? idesc_half : idesc_full;   // half tile: MMA N = BN / 2
+                int pend_s = -1, pend_a = 0;   // commits owed for the previous k-block
+                bool ready = false;            // this k-block's operands already seen landed
                 for (int kb = it.kb_begin; kb < it.kb_end; ++kb) {
-                    if (!bounded_wait(afull_bar(a), aph, abort_flag, p.status, DEVICE_TIMEOUT_MMA,
-                                            p.timeout_ns) ||
-                        !bounded_wait(full_bar(s), ph, abort_flag, p.status, DEVICE_TIMEOUT_MMA,
-                                            p.timeout_ns)) {
+                    if (!ready && (!bounded_wait(afull_bar(a), aph, abort_flag, p.status, DEVICE_TIMEOUT_MMA,
+                                                 p.timeout_ns) ||
+                                   !bounded_wait(full_bar(s), ph, abort_flag, p.status, DEVICE_TIMEOUT_MMA,
+                                                 p.timeout_ns))) {
                         ok = false;
                         break;
                     }
                     ptx::tc_fence_after();
                     const uint32_t b_base = sbase + C::OFF_B + s * C::B_STAGE;
                     const uint32_t a_tmem = tmem + C::A_BASE + a * C::A_COLS;
+                    const int s_n = (s + 1 == STAGES) ? 0 : s + 1;
+                    const uint32_t ph_n = (s + 1 == STAGES) ? (ph ^ 1u) : ph;
+                    const int a_n = (a + 1 == C::A_ST) ? 0 : a + 1;
+                    const uint32_t aph_n = (a + 1 == C::A_ST) ? (aph ^ 1u) : aph;
+                    ready = false;
 #pragma unroll
                     for (int kk = 0; kk < BK / 16; ++kk) {
                         const uint32_t b_addr = b_base + (kk / 4) * (C::B_ROWS * 128) + (kk % 4) * 32;
                         ptx::mma_f16_ts<CG>(tmem, a_tmem + kk * 8, ptx::make_sdesc_sw128(b_addr), idesc,
                                             (kb > it.kb_begin || kk > 0) ? 1u : 0u);
+                        if (kk == 0 && pend_s >= 0) commit_stage(pend_s, pend_a);
+                        if (kk == BK / 16 - 2 && kb + 1 < it.kb_end)
+                            ready = ptx::mbar_test_wait(afull_bar(a_n), aph_n) && ptx::mbar_test_wait(full_bar(s_n), ph_n);
                     }
-                    commit(empty_bar(s));
-                    commit(aempty_bar(a));
-                    if (++s == STAGES) {
-                        s = 0;
-                        ph ^= 1u;
-                    }
-                    if (++a == C::A_ST) {
-                        a = 0;
-                        aph ^= 1u;
-                    }
+                    pend_s = s;
+                    pend_a = a;
+                    s = s_n;
+                    ph = ph_n;
+                    a = a_n;
+                    aph = aph_n;
                 }
                 if (!ok) break;
+                if (pend_s >= 0) commit_stage(pend_s, pend_a);
                 commit(accfull_bar);
                 accph ^= 1u;
             }
@@ -610,7 +636,22 @@ __global__ void __launch_bounds__(128 * (1 + NWG), (GemmCfg<FMT, BF16, BN, BK, S
 #pragma unroll
                 for (int i = 0; i < CPW; ++i) {
                     const int c = c0 + i;
-                    if (FMT == FMT_INT4) {
+                    if (FMT == FMT_INT4 && CPW % 2 == 0) {
+                        // units c, c + 1 (c even) are the two 8-byte halves of the same
+                        // 16-byte slots of quad c / 2: one 16-byte load per slot serves both
+                        if (i % 2 == 0) {
+                            const uint8_t* ub = wt + (c >> 1) * 4096 + gr * 512;
+#pragma unroll
+                            for (int l = 0; l < 4; ++l) {
+                                const uint4 v = *reinterpret_cast<const uint4*>(ub + int4_slot(4 * g8 + l) * 16);
+                                qi[i][l] = make_uint2(v.x, v.y);
+                                qi[i + 1][l] = make_uint2(v.z, v.w);
+                            }
+                            sv[i] = *reinterpret_cast<const uint16_t*>(sct + (((c * 32) >> p.g_shift) * TILE_N + r) * 2);
+                            sv[i + 1] = (p.g_shift >= 6) ? sv[i]   // both units in one group (G >= 64)
+                                      : *reinterpret_cast<const uint16_t*>(sct + ((((c + 1) * 32) >> p.g_shift) * TILE_N + r) * 2);
+                        }
+                    } else if (FMT == FMT_INT4) {
                         // unit c: quad c / 2 of the stage, k steps 2 (c % 2) and 2 (c % 2) + 1
                         const uint8_t* ub = wt + (c >> 1) * 4096 + gr * 512 + (c & 1) * 8;
 #pragma unroll
@@ -649,7 +690,7 @@ __global__ void __launch_bounds__(128 * (1 + NWG), (GemmCfg<FMT, BF16, BN, BK, S
                 else
                     ptx::mbar_arrive(afull_bar(a));
             }
-            if (++s == STAGES) {
+            if (++s == WSTAGES) {
                 s = 0;
                 ph ^= 1u;
             }
@@ -860,10 +901,10 @@ __global__ void __launch_bounds__(128 * (1 + NWG), (GemmCfg<FMT, BF16, BN, BK, S
 }
 
 // Host-side launcher for one instantiation.
-template <int FMT, bool BF16, int BN, int BK, int STAGES, int NWG, bool PAIR = false>
+template <int FMT, bool BF16, int BN, int BK, int STAGES, int NWG, bool PAIR = false, int WSTAGES = STAGES>
 struct GemmLauncher {
-    using C = GemmCfg<FMT, BF16, BN, BK, STAGES, NWG, PAIR>;
-    static constexpr auto kernel = wq_gemm_kernel<FMT, BF16, BN, BK, STAGES, NWG, PAIR>;
+    using C = GemmCfg<FMT, BF16, BN, BK, STAGES, NWG, PAIR, WSTAGES>;
+    static constexpr auto kernel = wq_gemm_kernel<FMT, BF16, BN, BK, STAGES, NWG, PAIR, WSTAGES>;
     static cudaError_t prepare() {
         // per device: allow the dynamic shared memory this configuration needs
         static int attr_set[64] = {0};

@@ -15,9 +15,10 @@ using I4F16_256 = GemmLauncher<FMT_INT4, false, 256, 128, 3, 2>;
 using I4BF16_16 = GemmLauncher<FMT_INT4, true, 16, 128, 8, 2>;
 using I4BF16_256 = GemmLauncher<FMT_INT4, true, 256, 128, 3, 2>;
 // Large M: two-CTA clusters, 256 x 256 tiles, each CTA holding half the activation
-// tile; three stages leave room for the 64 KB output staging area.
-using I4F16_P = GemmLauncher<FMT_INT4, false, 256, 128, 3, 2, true>;
-using I4BF16_P = GemmLauncher<FMT_INT4, true, 256, 128, 3, 2, true>;
+// tile: four activation stages (their reload latency bounds the k-block rate), three
+// weight stages and the 64 KB output staging area.
+using I4F16_P = GemmLauncher<FMT_INT4, false, 256, 128, 4, 2, true, 3>;
+using I4BF16_P = GemmLauncher<FMT_INT4, true, 256, 128, 4, 2, true, 3>;
 
 bool config_int4_pair(bool bf16, bool query, KernelConfig* cfg) {
     *cfg = bf16 ? I4BF16_P::config(query) : I4F16_P::config(query);
