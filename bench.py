@@ -20,7 +20,6 @@ runs an independent replica (the decode GEMMs do not shard); rank 0 prints.
 from __future__ import annotations
 
 import argparse
-import glob
 import hashlib
 import json
 import os
@@ -59,18 +58,24 @@ def load_peaks():
         return dict(FALLBACK_PEAKS), "fallback"
 
 
+# The sources the decode kernel is compiled from (its own header, the helpers and PTX
+# wrappers it includes, the shared declarations and the instantiating unit).
+DECODE_KERNEL_SOURCES = ("wq_gemm_mma.cuh", "wq_gemm.cuh", "sm103_ptx.cuh", "wq_internal.h", "wq_gemm_int4.cu")
+
+
 def kernel_source_hash():
     h = hashlib.sha256()
-    for p in sorted(glob.glob(os.path.join(ROOT, "weight_only_quantized_tma_gb300", "csrc", "*"))):
-        with open(p, "rb") as f:
-            h.update(os.path.basename(p).encode())
+    for name in DECODE_KERNEL_SOURCES:
+        with open(os.path.join(ROOT, "weight_only_quantized_tma_gb300", "csrc", name), "rb") as f:
+            h.update(name.encode())
             h.update(f.read())
     return h.hexdigest()[:16]
 
 
-def profiled_traffic():
-    """DRAM bytes per decode launch from the committed ncu summary, if it was taken
-    on the current kernel sources (else None)."""
+def profiled_traffic(plan_of=None):
+    """DRAM bytes per decode launch from the committed ncu summary, if it was taken on
+    the current kernel sources and the captured shape still gets the recorded launch
+    (grid and K slices); else None."""
     path = os.path.join(ROOT, "profiles", "wq_gemm_w4a16_decode_ncu.md")
     try:
         text = open(path).read()
@@ -78,12 +83,17 @@ def profiled_traffic():
         return None
     vals = {}
     for line in text.splitlines():
-        if ":" in line and line.strip().startswith(("- kernel_source_hash", "- traffic_bytes_per_launch")):
+        if ":" in line and line.strip().startswith("- "):
             k, v = line.strip()[2:].split(":", 1)
             vals[k.strip()] = v.strip().strip("`")
     if vals.get("kernel_source_hash") != kernel_source_hash():
         return None
     try:
+        if plan_of is not None:
+            M, N, K, Gc = (int(x) for x in vals["captured_shape"].split(","))
+            plan = plan_of(M, N, K, Gc)
+            if plan["grid"] != int(vals["captured_grid"]) or plan["splits"] != int(vals["captured_splits"]):
+                return None
         return int(vals["traffic_bytes_per_launch"])
     except (KeyError, ValueError):
         return None
@@ -328,7 +338,7 @@ def run_ours(args, rank, world, local_rank):
                          "frac_hbm": round(byts / (mean_us * 1e-6) / 1e9 / peaks["hbm_gbs"], 4),
                          "splits": plan["splits"], "grid": plan["grid"]})
     achieved = tot_bytes / (tot_us * 1e-6) / 1e9
-    traffic = profiled_traffic()
+    traffic = profiled_traffic(lambda M, N, K, Gc: wq.get_plan(wq.WQ_OP_W4A16, wq.WQ_F16, M, N, K, Gc))
 
     # ---------------- prefill extras (M = 4096), L2 flushed between runs
     prefill = []
