@@ -368,6 +368,30 @@ def run_ours(args, rank, world, local_rank):
                             "frac_tensor": round(tflops / peaks["bf16_tflops"], 4)})
         del flush
 
+    # ---------------- quantiser extra: fp16 W (11008 x 4096) -> INT4 codes + fp16 scales
+    quantiser = []
+    if not args.skip_prefill:
+        flush = torch.empty(512 << 20, dtype=torch.uint8, device=dev)
+        for Gq in (32, 128):
+            Nq, Kq = 11008, 4096
+            Wq = torch.randn((Nq, Kq), generator=torch.Generator().manual_seed(77), dtype=torch.float32)
+            Wq = (Wq * 0.02).to(torch.float16).to(dev)
+            times = []
+            with torch.cuda.stream(stream):
+                for it in range(3 + 10):
+                    flush.fill_(it & 0xFF)
+                    a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+                    a.record(stream)
+                    wq.wq_quantize_int4(Wq, Gq)
+                    b.record(stream)
+                    times.append((a, b))
+            torch.cuda.synchronize(dev)
+            us = statistics.median([a.elapsed_time(b) * 1e3 for a, b in times[3:]])
+            qbytes = Nq * Kq * 2 + Nq * Kq // 2 + (Kq // Gq) * Nq * 2
+            quantiser.append({"N": Nq, "K": Kq, "G": Gq, "us": round(us, 2), "GB/s": round(qbytes / (us * 1e-6) / 1e9, 1),
+                              "frac_hbm": round(qbytes / (us * 1e-6) / 1e9 / peaks["hbm_gbs"], 4)})
+        del flush
+
     # ---------------- end to end through the public API (pinned host buffers)
     e2e_steps = max(3, min(args.steps, 50))
     host_in = [[torch.empty(A.shape, dtype=A.dtype, pin_memory=True).copy_(A.cpu()) for (_, _, _, A, *_r) in s]
@@ -414,6 +438,7 @@ def run_ours(args, rank, world, local_rank):
                      "achieved_from": "CUDA events around each launch, per-launch pass after the timed region"},
         "per_gemm": sorted(per_gemm, key=lambda d: (d["M"], d["N"], d["K"])),
         "prefill": prefill,
+        "quantiser": quantiser,
         "e2e": {"value": round(e2e_value, 2), "unit": "GB/s", "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
                 "ms_per_step": round(e2e_s * 1e3, 4),
                 "how": "per step: pinned-host->device copy of every A, wq_gemm_w4a16 via the Python binding, "

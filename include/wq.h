@@ -93,6 +93,22 @@ wq_status wq_int4_packed_bytes(int64_t N, int64_t K, int32_t G, size_t* w_bytes,
 wq_status wq_pack_int4(const uint8_t* w_canon, const void* s_canon, int64_t N, int64_t K, int32_t G,
                        uint8_t* w_kernel, void* s_kernel, wq_stream_t stream);
 
+/* Synthetic group-wise symmetric INT4 quantiser, the step upstream of
+ * wq_pack_int4 ("Low Bit Triton Kernels", GPU MODE lecture 34, hands-on exercise
+ * 1: fp16 weight -> group-wise quantize -> two nibbles per byte; the page fixes no
+ * scale rule, the symmetric one is taken).  For each row n and group g of G
+ * consecutive k:
+ *     s_canon[g][n] = RN16(amax / 7),   amax = max |w[n][k]| over the group
+ *     q[n][k] = clamp(rint(w[n][k] / s) + 8, 0, 15)   (half to even; 8 if s == 0)
+ * decided in fp32 with IEEE division.  w: fp16 [N][K], finite, 16-byte aligned.
+ * Outputs in the canonical layouts wq_pack_int4 reads: w_canon uint8 [N][K/2]
+ * (even k in the low nibble, 4-byte aligned), s_canon fp16 [K/G][N] (2-byte
+ * aligned).  Requirements: N > 0, K % 32 == 0, K % G == 0, G in {32, 64, 128,
+ * 256}.  A group whose amax is below 7 * 2^-14 gets a subnormal fp16 scale, whose
+ * coarser step can clamp codes (at most within 2^-11 of amax). */
+wq_status wq_quantize_int4(const void* w, int64_t N, int64_t K, int32_t G, uint8_t* w_canon, void* s_canon,
+                           wq_stream_t stream);
+
 /* Inverse of wq_pack_int4 (tests, export). */
 wq_status wq_unpack_int4(const uint8_t* w_kernel, const void* s_kernel, int64_t N, int64_t K, int32_t G,
                          uint8_t* w_canon, void* s_canon, wq_stream_t stream);

@@ -75,6 +75,7 @@ def _load():
         lib.oracle_pack_int4.argtypes = [u8p, ctypes.c_int64, ctypes.c_int64, u8p]
         lib.oracle_unpack_int4.argtypes = [u8p, ctypes.c_int64, ctypes.c_int64, u8p]
         lib.oracle_dequant_int4.argtypes = [u8p, u8p, ctypes.c_int64, ctypes.c_int64, ctypes.c_int64, u8p]
+        lib.oracle_quantize_int4.argtypes = [u8p, ctypes.c_int64, ctypes.c_int64, ctypes.c_int64, u8p, u8p]
         lib.oracle_gemm_w4a16.argtypes = [u8p, ctypes.c_int, u8p, u8p, ctypes.c_int64, ctypes.c_int64,
                                           ctypes.c_int64, ctypes.c_int64, u8p, ctypes.c_int64, u8p,
                                           ctypes.c_int64, u8p]
@@ -184,6 +185,20 @@ def unpack_int4(w: np.ndarray, K: int) -> np.ndarray:
     out = np.empty((N, K), dtype=np.uint8)
     _load().oracle_unpack_int4(_ptr(w), N, K, _ptr(out))
     return out
+
+
+def quantize_int4(w_bits: np.ndarray, G: int):
+    """Group-wise symmetric INT4 quantiser ("Low Bit Triton Kernels", hands-on exercise
+    1): fp16 W bits [N][K] -> (canonical packed codes [N][K/2] uint8, fp16 scale bits
+    [K/G][N] uint16), S = RN16(amax / 7), q = clamp(rint(W / S) + 8, 0, 15)."""
+    w_bits = np.ascontiguousarray(w_bits, dtype=np.uint16)
+    N, K = w_bits.shape
+    if K % 2 or K % G:
+        raise ValueError("K must be even and a multiple of G")
+    w = np.empty((N, K // 2), dtype=np.uint8)
+    s = np.empty((K // G, N), dtype=np.uint16)
+    _load().oracle_quantize_int4(_ptr(w_bits), N, K, G, _ptr(w), _ptr(s))
+    return w, s
 
 
 def dequant_int4(w: np.ndarray, s_bits: np.ndarray, K: int, G: int) -> np.ndarray:

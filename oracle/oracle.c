@@ -182,6 +182,46 @@ ORACLE_API void oracle_unpack_int4(const uint8_t* w, int64_t N, int64_t K, uint8
         }
 }
 
+/* Synthetic group-wise symmetric INT4 quantiser, the step upstream of the packing
+ * ("Low Bit Triton Kernels", hands-on exercise 1: fp16 weight -> group-wise
+ * quantize -> two nibbles per byte, checked by a round trip).  The page fixes no
+ * scale rule; the reading taken is the symmetric one whose largest magnitude maps
+ * to +-7:
+ *   amax = max_{k in group} |W[n, k]|,   S[g, n] = RN16(amax / 7)
+ *   q = clamp(rint(W[n, k] / S) + 8, 0, 15)          (rint: half to even)
+ * with q = 8 throughout a group whose scale is 0.  The decisions are taken in fp32
+ * (IEEE division, round half to even), the precision of the GPU kernel; both are
+ * equal to the exact rational roundings: amax / 7 is never within fp32 rounding of
+ * an fp16 tie, and W / S is either exactly a tie (representable) or ~3e-5 away.
+ * W fp16 bits [N][K]; outputs: canonical packed codes [N][K/2] (even k in the low
+ * nibble) and fp16 scale bits [K/G][N]. */
+ORACLE_API void oracle_quantize_int4(const uint16_t* w_f16, int64_t N, int64_t K, int64_t G, uint8_t* w,
+                                     uint16_t* s) {
+    memset(w, 0, (size_t)(N * (K / 2)));
+    for (int64_t n = 0; n < N; ++n)
+        for (int64_t g = 0; g < K / G; ++g) {
+            double amax = 0.0;
+            for (int64_t k = g * G; k < (g + 1) * G; ++k) {
+                const double a = fabs(oracle_f16_to_double(w_f16[n * K + k]));
+                if (a > amax) amax = a;
+            }
+            const float amax32 = (float)amax;                     /* exact: an fp16 value */
+            const uint16_t sb = oracle_round_f16((double)(amax32 / 7.0f));
+            s[g * N + n] = sb;
+            const float sv = (float)oracle_f16_to_double(sb);
+            for (int64_t k = g * G; k < (g + 1) * G; ++k) {
+                int q = 8;
+                if (sv != 0.0f) {
+                    const float x = (float)oracle_f16_to_double(w_f16[n * K + k]) / sv;
+                    q = (int)rintf(x) + 8;
+                    if (q < 0) q = 0;
+                    if (q > 15) q = 15;
+                }
+                w[n * (K / 2) + k / 2] |= (uint8_t)((k % 2 == 0) ? q : (q << 4));
+            }
+        }
+}
+
 /* One dequantized INT4 weight: (q - 8) * S[k / G, n], S fp16 [K/G][N]. */
 static double int4_weight(const uint8_t* w, const uint16_t* s, int64_t N, int64_t K, int64_t G,
                           int64_t n, int64_t k) {

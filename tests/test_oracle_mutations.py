@@ -61,6 +61,21 @@ MUTATIONS = {
     "f16_subnormal_scale": (
         "v = ldexp((double)m, -24);                 /* subnormal: m * 2^-24 */",
         "v = ldexp((double)m, -25);                 /* subnormal: m * 2^-24 */"),
+    "quant_divisor": (
+        "oracle_round_f16((double)(amax32 / 7.0f));",
+        "oracle_round_f16((double)(amax32 / 8.0f));"),
+    "quant_round_half_up": (
+        "q = (int)rintf(x) + 8;",
+        "q = (int)floorf(x + 0.5f) + 8;"),
+    "quant_offset": (
+        "q = (int)rintf(x) + 8;",
+        "q = (int)rintf(x) + 7;"),
+    "quant_scale_layout": (
+        "s[g * N + n] = sb;",
+        "s[n * (K / G) + g] = sb;"),
+    "quant_nibble_order": (
+        "w[n * (K / 2) + k / 2] |= (uint8_t)((k % 2 == 0) ? q : (q << 4));",
+        "w[n * (K / 2) + k / 2] |= (uint8_t)((k % 2 == 1) ? q : (q << 4));"),
     "pack_nibbles_swapped": (
         "w[n * (K / 2) + j] = (uint8_t)(lo | (hi << 4));",
         "w[n * (K / 2) + j] = (uint8_t)(hi | (lo << 4));"),

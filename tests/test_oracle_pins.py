@@ -362,3 +362,54 @@ def test_metrics_definition():
     rmax, rmean = oracle.rel_errors(out, ref)
     assert rmax == pytest.approx(0.02 / 4.0)
     assert rmean == pytest.approx((0.03 / 4) / (7.5 / 4))
+
+
+# ------------------------------------------------- quantiser (upstream of the packing)
+
+def test_quantiser_worked_example():
+    g = _golden("int4_quantiser_worked_example.json")
+    w, s = oracle.quantize_int4(_f16_bits(g["W"]), g["G"])
+    assert w.tolist() == g["packed"]
+    assert s.view(np.float16).astype(np.float64).tolist() == g["scales"]
+    assert oracle.unpack_int4(w, g["K"]).tolist() == g["q"]
+    assert oracle.dequant_int4(w, s, g["K"], g["G"]).astype(np.float64).tolist() == g["dequant"]
+
+
+@pytest.mark.parametrize("G", [32, 64, 128, 256])
+def test_quantiser_error_within_half_a_step(G):
+    # Rounding to the nearest step: |W - (q - 8) S| <= S / 2 for every weight, and the
+    # largest magnitude of a group lands on q - 8 = +-7 (groups with a normal fp16 scale;
+    # a subnormal scale is coarser than amax / 7 and may clamp).  An all-zero group gets
+    # S = 0 and q = 8.
+    rng = np.random.default_rng(300 + G)
+    N, K = 64, 1024
+    W = (rng.standard_normal((N, K)) * 0.02).astype(np.float16)
+    W[3, :G] = 0
+    W[5, G:2 * G] *= np.float16(1e-3)
+    w, s = oracle.quantize_int4(W.view(np.uint16), G)
+    q = oracle.unpack_int4(w, K).astype(np.int64)
+    S = s.view(np.float16).astype(np.float64)               # [K/G][N]
+    Sk = np.repeat(S.T, G, axis=1)                          # [N][K]
+    Wd = W.astype(np.float64)
+    normal = np.repeat((S.T >= 2.0 ** -14), G, axis=1)
+    err = np.abs(Wd - (q - 8) * Sk)
+    assert np.all(err[normal] <= Sk[normal] / 2)
+    assert np.all(q[3, :G] == 8) and S[0, 3] == 0
+    absw = np.abs(Wd).reshape(N, K // G, G)
+    top = np.take_along_axis(q.reshape(N, K // G, G), absw.argmax(axis=2)[..., None], axis=2)[..., 0]
+    assert np.all(np.abs(top[S.T >= 2.0 ** -14] - 8) == 7)
+
+
+def test_quantiser_reproduces_exactly_representable_weights():
+    # W = (q - 8) S with a code of +-7 in every group and scales of at most 8 significant
+    # bits, so every weight is an fp16 value: quantising W gives q and S back exactly
+    rng = np.random.default_rng(310)
+    N, K, G = 16, 512, 64
+    q = rng.integers(1, 16, size=(N, K))
+    q.reshape(N, K // G, G)[:, :, 0] = rng.choice([1, 15], size=(N, K // G))
+    S = rng.integers(128, 256, size=(K // G, N)) * 2.0 ** (rng.integers(-12, -4, size=(K // G, N)) - 7)
+    W = (q - 8) * np.repeat(S.T, G, axis=1)
+    assert np.array_equal(W.astype(np.float16).astype(np.float64), W)
+    w, s = oracle.quantize_int4(W.astype(np.float16).view(np.uint16), G)
+    assert np.array_equal(oracle.unpack_int4(w, K), q)
+    assert np.array_equal(s.view(np.float16).astype(np.float64), S)

@@ -23,6 +23,7 @@ from ._lib import (  # noqa: F401
     wq_int4_packed_bytes,
     wq_pack_fp4_sf,
     wq_pack_int4,
+    wq_quantize_int4,
     wq_unpack_int4,
     WQ_BF16,
     WQ_F16,

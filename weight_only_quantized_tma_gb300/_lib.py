@@ -55,6 +55,7 @@ _SIGNATURES = {
     "wq_status_string": (ctypes.c_char_p, [ctypes.c_int]),
     "wq_int4_packed_bytes": (ctypes.c_int, [_i64, _i64, _i32, ctypes.POINTER(_sz), ctypes.POINTER(_sz)]),
     "wq_pack_int4": (ctypes.c_int, [_vp, _vp, _i64, _i64, _i32, _vp, _vp, _vp]),
+    "wq_quantize_int4": (ctypes.c_int, [_vp, _i64, _i64, _i32, _vp, _vp, _vp]),
     "wq_unpack_int4": (ctypes.c_int, [_vp, _vp, _i64, _i64, _i32, _vp, _vp, _vp]),
     "wq_debug_dequant_int4": (ctypes.c_int, [_vp, _vp, _i64, _i64, _i32, _vp, _vp]),
     "wq_gemm_w4a16": (ctypes.c_int, [_vp, ctypes.c_int, _vp, _vp, _i64, _i64, _i64, _i32, _vp, _vp, _sz, _vp]),
@@ -180,6 +181,19 @@ def wq_pack_int4(w_canon: torch.Tensor, s_canon: torch.Tensor, N: int, K: int, G
     _check(lib().wq_pack_int4(_ptr(w_canon), _ptr(s_canon), N, K, G, _ptr(wk), _ptr(sk), _stream(w_canon)),
            "wq_pack_int4")
     return wk, sk
+
+
+def wq_quantize_int4(w: torch.Tensor, G: int):
+    """fp16 weight [N, K] -> canonical uint8 codes [N, K/2] + fp16 scales [K/G, N]
+    (group-wise symmetric: S = RN16(amax / 7), q = clamp(rint(w / S) + 8, 0, 15))."""
+    if w.dtype != torch.float16 or w.dim() != 2:
+        raise ValueError("wq_quantize_int4: w must be a 2-D float16 tensor")
+    w = w.contiguous()
+    N, K = w.shape
+    w_canon = torch.empty((N, K // 2), dtype=torch.uint8, device=w.device)
+    s_canon = torch.empty((K // G, N), dtype=torch.float16, device=w.device)
+    _check(lib().wq_quantize_int4(_ptr(w), N, K, G, _ptr(w_canon), _ptr(s_canon), _stream(w)), "wq_quantize_int4")
+    return w_canon, s_canon
 
 
 def wq_unpack_int4(w_kernel: torch.Tensor, s_kernel: torch.Tensor, N: int, K: int, G: int):

@@ -408,6 +408,19 @@ wq_status wq_pack_int4(const uint8_t* w_canon, const void* s_canon, int64_t N, i
                                           static_cast<uint16_t*>(s_kernel), (cudaStream_t)stream));
 }
 
+wq_status wq_quantize_int4(const void* w, int64_t N, int64_t K, int32_t G, uint8_t* w_canon, void* s_canon,
+                           wq_stream_t stream) {
+    if (!w || !w_canon || !s_canon) return WQ_ERR_NULL;
+    if (N <= 0 || K <= 0 || N > kMaxDim || K > kMaxDim || K % 32 != 0) return WQ_ERR_SHAPE;
+    if (!valid_group(G) || K % G != 0) return WQ_ERR_GROUP;
+    if (!aligned(w, 16) || !aligned(w_canon, 4) || !aligned(s_canon, 2)) return WQ_ERR_MISALIGNED;
+    DeviceInfo* d = nullptr;
+    wq_status st = device_info(&d);
+    if (st != WQ_OK) return st;
+    return finish_launch(launch_quantize_int4(static_cast<const uint16_t*>(w), N, K, G, w_canon,
+                                              static_cast<uint16_t*>(s_canon), (cudaStream_t)stream));
+}
+
 wq_status wq_unpack_int4(const uint8_t* w_kernel, const void* s_kernel, int64_t N, int64_t K, int32_t G,
                          uint8_t* w_canon, void* s_canon, wq_stream_t stream) {
     wq_status st = check_pack_args(w_kernel, s_kernel, w_canon, s_canon, N, K, G);

@@ -150,6 +150,10 @@ cudaError_t launch_gemm_int4_pair(const GemmParams& p, bool bf16, int grid, cuda
 bool config_fp8(bool bf16, int bn, bool query, KernelConfig* cfg);
 bool config_fp4(bool bf16, int bn, bool query, KernelConfig* cfg);
 
+// Synthetic INT4 quantiser (fp16 [N][K] -> canonical codes and scales), wq_quant.cu.
+cudaError_t launch_quantize_int4(const uint16_t* w, int64_t N, int64_t K, int G, uint8_t* wq, uint16_t* s,
+                                 cudaStream_t st);
+
 // Layout transforms, defined in wq_pack.cu.
 cudaError_t launch_pack_int4(const uint8_t* w, const uint16_t* s, int64_t N, int64_t K, int G, uint8_t* wk,
                              uint16_t* sk, cudaStream_t st);
