@@ -368,6 +368,73 @@ def run_ours(args, rank, world, local_rank):
                             "frac_tensor": round(tflops / peaks["bf16_tflops"], 4)})
         del flush
 
+    # ---------------- FP8 / FP4 extras (L2 flushed between runs): the config shapes, fp16
+    # and bf16 activations, the bias epilogue, and FP4 at the FP4 page's own shape
+    fp8_fp4 = []
+    if not args.skip_prefill:
+        flush = torch.empty(512 << 20, dtype=torch.uint8, device=dev)
+
+        def time_call(fn, reps=10):
+            times = []
+            with torch.cuda.stream(stream):
+                for it in range(3 + reps):
+                    flush.fill_(it & 0xFF)
+                    a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+                    a.record(stream)
+                    fn()
+                    b.record(stream)
+                    times.append((a, b))
+            torch.cuda.synchronize(dev)
+            return statistics.median([a.elapsed_time(b) * 1e3 for a, b in times[3:]])
+
+        def entry(op, M, N, K, adt, us, byts, extra=None):
+            d = {"op": op, "M": M, "N": N, "K": K, "A": adt, "us": round(us, 2),
+                 "TFLOP/s": round(2.0 * M * N * K / (us * 1e-6) / 1e12, 1),
+                 "frac_tensor": round(2.0 * M * N * K / (us * 1e-6) / 1e12 / peaks["bf16_tflops"], 4),
+                 "GB/s": round(byts / (us * 1e-6) / 1e9, 1),
+                 "frac_hbm": round(byts / (us * 1e-6) / 1e9 / peaks["hbm_gbs"], 4)}
+            d.update(extra or {})
+            fp8_fp4.append(d)
+
+        fp8_cases = [(32768, 3200, 5120, "bf16", False), (16384, 12800, 5120, "bf16", False),
+                     (8192, 10240, 5120, "bf16", False), (8192, 10240, 5120, "f16", False),
+                     (8192, 10240, 5120, "f16", True), (1, 10240, 5120, "bf16", False),
+                     (16, 10240, 5120, "bf16", False), (64, 10240, 5120, "bf16", False),
+                     (16, 10240, 5120, "f16", True)]
+        for (M, N, K, adt, with_bias) in fp8_cases:
+            seed = 4000 + M
+            Ax = torch.from_numpy(synth.activations(M, K, adt, seed).view(np.int16)).to(dev).view(
+                torch.bfloat16 if adt == "bf16" else torch.float16)
+            w8 = synth.fp8_weights(N, K, seed + 1)
+            wd = torch.from_numpy(w8.w).to(dev)
+            alpha = torch.tensor([w8.scale], dtype=torch.float32, device=dev)
+            bias = (torch.from_numpy(synth.bias(N, adt, seed + 2).view(np.int16)).to(dev).view(Ax.dtype)
+                    if with_bias else None)
+            outx = torch.empty((M, N), dtype=Ax.dtype, device=dev)
+            wsx = torch.zeros(wq.get_plan(wq.WQ_OP_FP8, wq.WQ_F16 if adt == "f16" else wq.WQ_BF16, M, N, K, 0)
+                             ["ws_bytes"] + 16, dtype=torch.uint8, device=dev)
+            us = time_call(lambda: wq.wq_gemm_w8a16_fp8(Ax, wd, alpha, bias=bias, out=outx, ws=wsx))
+            entry("fp8", M, N, K, adt, us, N * K + M * K * 2 + M * N * 2, {"bias": with_bias})
+            del Ax, wd, outx, wsx
+        fp4_cases = [(1, 12800, 5120, None), (128, 12800, 5120, None), (8192, 12800, 5120, None),
+                     (128, 6656, 19968, "FP4 page (#4466) quotes 43.90 us for its cute-dsl kernel at this shape, "
+                                        "SM100-class GPU, SKU not stated")]
+        for (M, N, K, note) in fp4_cases:
+            seed = 5000 + M
+            Ax = torch.from_numpy(synth.activations(M, K, "bf16", seed).view(np.int16)).to(dev).view(torch.bfloat16)
+            w4 = synth.fp4_weights(N, K, seed + 1)
+            wd = torch.from_numpy(w4.w).to(dev)
+            sfk = wq.wq_pack_fp4_sf(torch.from_numpy(w4.sf).to(dev), N, K)
+            alpha = torch.tensor([w4.alpha], dtype=torch.float32, device=dev)
+            outx = torch.empty((M, N), dtype=torch.bfloat16, device=dev)
+            wsx = torch.zeros(wq.get_plan(wq.WQ_OP_FP4, wq.WQ_BF16, M, N, K, 0)["ws_bytes"] + 16,
+                             dtype=torch.uint8, device=dev)
+            us = time_call(lambda: wq.wq_gemm_bf16_fp4(Ax, wd, sfk, alpha, out=outx, ws=wsx))
+            entry("fp4", M, N, K, "bf16", us, N * K // 2 + N * K // 16 + M * K * 2 + M * N * 2,
+                  {"context": note} if note else None)
+            del Ax, wd, outx, wsx
+        del flush
+
     # ---------------- quantiser extra: fp16 W (11008 x 4096) -> INT4 codes + fp16 scales
     quantiser = []
     if not args.skip_prefill:
@@ -439,6 +506,7 @@ def run_ours(args, rank, world, local_rank):
         "per_gemm": sorted(per_gemm, key=lambda d: (d["M"], d["N"], d["K"])),
         "prefill": prefill,
         "quantiser": quantiser,
+        "fp8_fp4": fp8_fp4,
         "e2e": {"value": round(e2e_value, 2), "unit": "GB/s", "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
                 "ms_per_step": round(e2e_s * 1e3, 4),
                 "how": "per step: pinned-host->device copy of every A, wq_gemm_w4a16 via the Python binding, "

@@ -219,3 +219,70 @@ def test_bounded_wait_gives_up_and_reports():
     out = p.run()
     torch.cuda.synchronize()
     check_close(out_to_f64(out), p.ref(), out_dtype="bf16", what="after probe")
+
+
+# ------------------------------------------------------- large M: pair and one-CTA kernels
+
+@pytest.fixture(params=["pair", "one_cta"])
+def tile_kernel(request, monkeypatch):
+    """The large-M tile kernel under test: two-CTA pair (default) or one CTA per tile."""
+    if request.param == "one_cta":
+        monkeypatch.setenv("WQ_DISABLE_PAIR", "1")
+    else:
+        monkeypatch.delenv("WQ_DISABLE_PAIR", raising=False)
+    return wq.WQ_KERNEL_TILE_PAIR if request.param == "pair" else wq.WQ_KERNEL_TILE
+
+
+@pytest.mark.parametrize("a_dtype", ["bf16", "f16"])
+def test_fp8_large_M_identity_bit_exact(a_dtype, tile_kernel):
+    # M = K = 1024 tokens of identity over 80 weight tiles (40 pair tiles): out = RN(w),
+    # through the staged epilogue on the pair kernel.  Compared as values: a weight of
+    # e4m3 -0 yields +0 (its product plus the +0 products of the other tokens)
+    M = K = 1024
+    N = 10240
+    plan = wq.get_plan(wq.WQ_OP_FP8, wq.WQ_F16 if a_dtype == "f16" else wq.WQ_BF16, M, N, K, 0)
+    assert plan["kernel"] == tile_kernel
+    p = Fp8Problem(M, N, K, a_dtype=a_dtype, seed=210)
+    p.A = synth._to_bits(np.eye(K, dtype=np.float32), a_dtype)
+    p.A_d = to_dev_f16bits(p.A, a_dtype)
+    one = torch.ones(1, dtype=torch.float32, device=DEV)
+    out = p.run(alpha=one)
+    torch.cuda.synchronize()
+    w = oracle.dequant_fp8(p.wts.w).astype(np.float64).T
+    want = oracle.bf16_bits_to_double_array(oracle.round_bf16_array(w)) if a_dtype == "bf16" else \
+        oracle.f16_bits_to_double_array(oracle.round_f16_array(w))
+    assert np.array_equal(out_to_f64(out), want)
+
+
+def test_fp8_large_M_fp16_with_bias(tile_kernel):
+    M, N, K = 2100, 3200, 2048
+    plan = wq.get_plan(wq.WQ_OP_FP8, wq.WQ_F16, M, N, K, 0)
+    assert plan["kernel"] == tile_kernel
+    p = Fp8Problem(M, N, K, a_dtype="f16", seed=215, with_bias=True)
+    out = p.run()
+    torch.cuda.synchronize()
+    rows = np.unique(np.concatenate([synth.sample_rows(M, 64, seed=216), np.arange(M - 20, M)]))
+    check_close(out_to_f64(out)[rows], p.ref(rows=rows), out_dtype="f16", what="fp8 f16 + bias, large M")
+
+
+def test_fp8_large_M_random(tile_kernel):
+    M, N, K = 2100, 3200, 5120
+    plan = wq.get_plan(wq.WQ_OP_FP8, wq.WQ_BF16, M, N, K, 0)
+    assert plan["kernel"] == tile_kernel
+    p = Fp8Problem(M, N, K, seed=211)
+    out = p.run()
+    cast = _cast_copy_fp8(p.A_d, p.w_d, p.wts.scale, torch.bfloat16)
+    torch.cuda.synchronize()
+    rows = np.unique(np.concatenate([synth.sample_rows(M, 64, seed=212), np.arange(M - 20, M)]))
+    _gate_vs_cast_copy(out_to_f64(out)[rows], out_to_f64(cast)[rows], p.ref(rows=rows), "fp8 large M")
+
+
+def test_fp4_large_M(tile_kernel):
+    M, N, K = 2100, 4224, 2048
+    plan = wq.get_plan(wq.WQ_OP_FP4, wq.WQ_BF16, M, N, K, 0)
+    assert plan["kernel"] == tile_kernel
+    p = Fp4Problem(M, N, K, seed=213)
+    out = p.run()
+    torch.cuda.synchronize()
+    rows = np.unique(np.concatenate([synth.sample_rows(M, 64, seed=214), np.arange(M - 20, M)]))
+    check_close(out_to_f64(out)[rows], p.ref(rows=rows), out_dtype="bf16", what="fp4 large M")

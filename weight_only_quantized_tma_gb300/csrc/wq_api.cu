@@ -112,6 +112,8 @@ struct Plan {
 bool get_config_uncached(int fmt, bool bf16, int bn, bool query, KernelConfig* cfg) {
     if (fmt == FMT_INT4 + 16) return config_int4_decode(bf16, query, cfg);
     if (fmt == FMT_INT4 + 32) return config_int4_pair(bf16, query, cfg);
+    if (fmt == FMT_FP8 + 32) return config_fp8_pair(bf16, query, cfg);
+    if (fmt == FMT_FP4 + 32) return bf16 && config_fp4_pair(query, cfg);
     switch (fmt) {
         case FMT_INT4: return config_int4(bf16, bn, query, cfg);
         case FMT_FP8: return config_fp8(bf16, bn, query, cfg);
@@ -124,18 +126,18 @@ bool get_config_uncached(int fmt, bool bf16, int bn, bool query, KernelConfig* c
 // device and instantiation; later calls read the cached answer.
 struct ConfigCache {
     std::mutex mu;
-    bool have[kMaxDevices][5][2][4] = {};
-    bool found[kMaxDevices][5][2][4] = {};
-    KernelConfig cfg[kMaxDevices][5][2][4];
+    bool have[kMaxDevices][7][2][4] = {};
+    bool found[kMaxDevices][7][2][4] = {};
+    KernelConfig cfg[kMaxDevices][7][2][4];
 };
 ConfigCache g_cfg_cache;
 
 bool get_config(int fmt, bool bf16, int bn, bool query, KernelConfig* cfg) {
     const int bi = bn == 16 ? 0 : bn == 64 ? 1 : bn == 128 ? 2 : bn == 256 ? 3 : -1;
-    // slot 3: the W4A16 decode kernel, slot 4: the W4A16 pair kernel
-    const int fi = fmt == FMT_INT4 + 16 ? 3 : fmt == FMT_INT4 + 32 ? 4 : fmt;
+    // slot 3: the W4A16 decode kernel, slots 4-6: the pair kernels (W4A16, FP8, FP4)
+    const int fi = fmt == FMT_INT4 + 16 ? 3 : fmt >= 32 ? 4 + (fmt - 32) : fmt;
     int dev = 0;
-    if (!query || bi < 0 || fi < 0 || fi > 4 || cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices)
+    if (!query || bi < 0 || fi < 0 || fi > 6 || cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices)
         return get_config_uncached(fmt, bf16, bn, query, cfg);
     std::lock_guard<std::mutex> lock(g_cfg_cache.mu);
     const int b = bf16 ? 1 : 0;
@@ -238,15 +240,16 @@ wq_status make_plan(int fmt, bool bf16, int64_t M, int64_t N, int64_t K, int sms
     // compare the two)
     const char* no_pair = std::getenv("WQ_DISABLE_PAIR");
     const bool pair_allowed = !(no_pair && no_pair[0] == '1');
-    if (pair_allowed && !decode && fmt == FMT_INT4 && cfg.bn == 256 && p.splits == 1 && sms > 0 && N % 8 == 0) {
+    if (pair_allowed && !decode && cfg.bn == 256 && p.splits == 1 && sms > 0 && N % 8 == 0) {
         KernelConfig pc{};
-        if (get_config(FMT_INT4 + 32, bf16, 256, true, &pc) && pc.max_clusters[2] > 0) {
+        if (get_config(fmt + 32, bf16, 256, true, &pc) && pc.max_clusters[2] > 0) {
             const long long tn2 = (p.tiles_n + 1) / 2;
             const long long items2 = tn2 * p.tiles_m;
             const long long pslots = pc.max_clusters[2];
             if (items2 >= pslots && items2 < (1LL << 30)) {
                 p.cfg = pc;
                 p.pair = true;
+                p.nkb = (int)((K + pc.bk - 1) / pc.bk);   // the pair kernel's k-block may differ
                 p.tiles_n = (int)tn2;
                 p.n_items = (int)items2;
                 p.n_full = (int)items2;
@@ -575,7 +578,8 @@ wq_status wq_gemm_w8a16_fp8(const void* A, wq_dtype a_dtype, const uint8_t* w_e4
     if ((st = check_ws(pl, ws, ws_bytes)) != WQ_OK) return st;
     GemmParams gp;
     std::memset(&gp, 0, sizeof(gp));
-    if (!encode_a(gp, A, bf16, M, K, pl.cfg.bn)) return WQ_ERR_CUDA;
+    if (!encode_a(gp, A, bf16, M, K, pl.pair ? pl.cfg.bn / 2 : pl.cfg.bn)) return WQ_ERR_CUDA;
+    if (pl.pair && !encode_out(gp, out, bf16, M, N)) return WQ_ERR_CUDA;
     const int bk = pl.cfg.bk;
     if (!encode_2d(&gp.tmap_w, CU_TENSOR_MAP_DATA_TYPE_UINT8, w_e4m3, (uint64_t)K, (uint64_t)N, (uint64_t)K,
                    (uint32_t)bk, TILE_N, swizzle_for_pitch(bk)))
@@ -583,6 +587,7 @@ wq_status wq_gemm_w8a16_fp8(const void* A, wq_dtype a_dtype, const uint8_t* w_e4
     gp.alpha = alpha;
     gp.bias = bias;
     fill_common(gp, pl, M, N, K, out, ws, d->status);
+    if (pl.pair) return finish_launch(launch_gemm_fp8_pair(gp, bf16, pl.grid, (cudaStream_t)stream));
     return finish_launch(launch_gemm_fp8(gp, bf16, pl.cfg.bn, pl.grid, (cudaStream_t)stream));
 }
 
@@ -605,7 +610,8 @@ wq_status wq_gemm_bf16_fp4(const void* A, const uint8_t* w_e2m1, const uint8_t* 
     if ((st = check_ws(pl, ws, ws_bytes)) != WQ_OK) return st;
     GemmParams gp;
     std::memset(&gp, 0, sizeof(gp));
-    if (!encode_a(gp, A, true, M, K, pl.cfg.bn)) return WQ_ERR_CUDA;
+    if (!encode_a(gp, A, true, M, K, pl.pair ? pl.cfg.bn / 2 : pl.cfg.bn)) return WQ_ERR_CUDA;
+    if (pl.pair && !encode_out(gp, out, true, M, N)) return WQ_ERR_CUDA;
     const int pitch = pl.cfg.bk / 2;
     if (!encode_2d(&gp.tmap_w, CU_TENSOR_MAP_DATA_TYPE_UINT8, w_e2m1, (uint64_t)(K / 2), (uint64_t)N,
                    (uint64_t)(K / 2), (uint32_t)pitch, TILE_N, swizzle_for_pitch(pitch)))
@@ -614,6 +620,7 @@ wq_status wq_gemm_bf16_fp4(const void* A, const uint8_t* w_e2m1, const uint8_t* 
     gp.alpha = alpha;
     gp.nchunks_pad = (int)(round_up(K, KPAD_FP4SF) / 64);
     fill_common(gp, pl, M, N, K, out, ws, d->status);
+    if (pl.pair) return finish_launch(launch_gemm_fp4_pair(gp, pl.grid, (cudaStream_t)stream));
     return finish_launch(launch_gemm_fp4(gp, true, pl.cfg.bn, pl.grid, (cudaStream_t)stream));
 }
 

@@ -7,6 +7,15 @@ using F4_16 = GemmLauncher<FMT_FP4, true, 16, 128, 8, 2>;
 using F4_64 = GemmLauncher<FMT_FP4, true, 64, 128, 4, 2>;
 using F4_128 = GemmLauncher<FMT_FP4, true, 128, 128, 2, 2>;
 using F4_256 = GemmLauncher<FMT_FP4, true, 256, 128, 3, 2>;
+// Large M: two-CTA clusters (as the W4A16 pair kernel).
+using F4_P = GemmLauncher<FMT_FP4, true, 256, 128, 4, 2, true, 3>;
+
+bool config_fp4_pair(bool query, KernelConfig* cfg) {
+    *cfg = F4_P::config(query);
+    return true;
+}
+
+cudaError_t launch_gemm_fp4_pair(const GemmParams& p, int grid, cudaStream_t st) { return F4_P::launch(p, grid, st); }
 
 bool config_fp4(bool bf16, int bn, bool query, KernelConfig* cfg) {
     if (!bf16) return false;

@@ -148,6 +148,11 @@ cudaError_t launch_gemm_int4_decode(const GemmParams& p, bool bf16, int grid, cu
 bool config_int4_pair(bool bf16, bool query, KernelConfig* cfg);
 cudaError_t launch_gemm_int4_pair(const GemmParams& p, bool bf16, int grid, cudaStream_t st);
 bool config_fp8(bool bf16, int bn, bool query, KernelConfig* cfg);
+// FP8 / FP4 tile kernels on two-CTA clusters (as the W4A16 pair kernel).
+bool config_fp8_pair(bool bf16, bool query, KernelConfig* cfg);
+cudaError_t launch_gemm_fp8_pair(const GemmParams& p, bool bf16, int grid, cudaStream_t st);
+bool config_fp4_pair(bool query, KernelConfig* cfg);
+cudaError_t launch_gemm_fp4_pair(const GemmParams& p, int grid, cudaStream_t st);
 bool config_fp4(bool bf16, int bn, bool query, KernelConfig* cfg);
 
 // Synthetic INT4 quantiser (fp16 [N][K] -> canonical codes and scales), wq_quant.cu.
