@@ -76,6 +76,10 @@ def _load():
         lib.oracle_unpack_int4.argtypes = [u8p, ctypes.c_int64, ctypes.c_int64, u8p]
         lib.oracle_dequant_int4.argtypes = [u8p, u8p, ctypes.c_int64, ctypes.c_int64, ctypes.c_int64, u8p]
         lib.oracle_quantize_int4.argtypes = [u8p, ctypes.c_int64, ctypes.c_int64, ctypes.c_int64, u8p, u8p]
+        lib.oracle_dequant_int4_zp.argtypes = [u8p, u8p, u8p, ctypes.c_int64, ctypes.c_int64, ctypes.c_int64, u8p]
+        lib.oracle_gemm_w4a16_zp.argtypes = [u8p, ctypes.c_int, u8p, u8p, u8p, ctypes.c_int64, ctypes.c_int64,
+                                             ctypes.c_int64, ctypes.c_int64, u8p, ctypes.c_int64, u8p,
+                                             ctypes.c_int64, u8p]
         lib.oracle_gemm_w4a16.argtypes = [u8p, ctypes.c_int, u8p, u8p, ctypes.c_int64, ctypes.c_int64,
                                           ctypes.c_int64, ctypes.c_int64, u8p, ctypes.c_int64, u8p,
                                           ctypes.c_int64, u8p]
@@ -221,6 +225,31 @@ def gemm_w4a16(a_bits, a_is_bf16, w, s_bits, M, N, K, G, rows=None, cols=None) -
     out = np.empty((nr, nc), dtype=np.float64)
     _load().oracle_gemm_w4a16(_ptr(a_bits), int(bool(a_is_bf16)), _ptr(w), _ptr(s_bits), M, N, K, G,
                               _ptr(r), nr, _ptr(c), nc, _ptr(out))
+    return out
+
+
+def dequant_int4_zp(w: np.ndarray, s_bits: np.ndarray, z: np.ndarray, K: int, G: int) -> np.ndarray:
+    """Asymmetric INT4: fp32 [N][K] = (q - Z[k // G, n]) * S[k // G, n], Z uint8 [K/G][N] in 0..15."""
+    w = _c(w, np.uint8)
+    s_bits = _c(s_bits, np.uint16)
+    z = _c(z, np.uint8)
+    N = w.shape[0]
+    out = np.empty((N, K), dtype=np.float32)
+    _load().oracle_dequant_int4_zp(_ptr(w), _ptr(s_bits), _ptr(z), N, K, G, _ptr(out))
+    return out
+
+
+def gemm_w4a16_zp(a_bits, a_is_bf16, w, s_bits, z, M, N, K, G, rows=None, cols=None) -> np.ndarray:
+    """float64 out[rows, cols] = A[rows] . ((q - Z) * S)[cols]^T (zero point per group and row)."""
+    a_bits = _c(a_bits, np.uint16)
+    w = _c(w, np.uint8)
+    s_bits = _c(s_bits, np.uint16)
+    z = _c(z, np.uint8)
+    r, nr = _index(rows, M)
+    c, nc = _index(cols, N)
+    out = np.empty((nr, nc), dtype=np.float64)
+    _load().oracle_gemm_w4a16_zp(_ptr(a_bits), int(bool(a_is_bf16)), _ptr(w), _ptr(s_bits), _ptr(z), M, N, K, G,
+                                 _ptr(r), nr, _ptr(c), nc, _ptr(out))
     return out
 
 

@@ -222,11 +222,17 @@ ORACLE_API void oracle_quantize_int4(const uint16_t* w_f16, int64_t N, int64_t K
         }
 }
 
+/* The 4-bit code of weight (n, k) in the canonical packing [N][K/2]. */
+static int int4_code(const uint8_t* w, int64_t K, int64_t n, int64_t k) {
+    uint8_t byte = w[n * (K / 2) + k / 2];
+    int q = (k % 2 == 0) ? (byte & 0xF) : ((byte >> 4) & 0xF);
+    return q;
+}
+
 /* One dequantized INT4 weight: (q - 8) * S[k / G, n], S fp16 [K/G][N]. */
 static double int4_weight(const uint8_t* w, const uint16_t* s, int64_t N, int64_t K, int64_t G,
                           int64_t n, int64_t k) {
-    uint8_t byte = w[n * (K / 2) + k / 2];
-    int q = (k % 2 == 0) ? (byte & 0xF) : ((byte >> 4) & 0xF);
+    int q = int4_code(w, K, n, k);
     int64_t g = k / G;
     double scale = oracle_f16_to_double(s[g * N + n]);
     return (double)(q - 8) * scale;
@@ -239,6 +245,47 @@ ORACLE_API void oracle_dequant_int4(const uint8_t* w, const uint16_t* s, int64_t
     for (int64_t n = 0; n < N; ++n)
         for (int64_t k = 0; k < K; ++k)
             out[n * K + k] = (float)int4_weight(w, s, N, K, G, n, k);
+}
+
+/* Asymmetric INT4 (zero point per group and row): (q - Z[k / G, n]) * S[k / G, n],
+ * Z uint8 [K/G][N] holding integers 0..15.  The pages name group-scaled 4-bit formats
+ * with zero points (GPTQ / AWQ / HQQ, "Low Bit Triton Kernels" §02) but print none;
+ * the integer zero point is the reading taken. */
+static double int4_weight_zp(const uint8_t* w, const uint16_t* s, const uint8_t* z, int64_t N, int64_t K,
+                             int64_t G, int64_t n, int64_t k) {
+    int q = int4_code(w, K, n, k);
+    int64_t grp = k / G;
+    double scale = oracle_f16_to_double(s[grp * N + n]);
+    int zero = z[grp * N + n];
+    return (double)(q - zero) * scale;
+}
+
+ORACLE_API void oracle_dequant_int4_zp(const uint8_t* w, const uint16_t* s, const uint8_t* z, int64_t N, int64_t K,
+                                       int64_t G, float* out) {
+    for (int64_t n = 0; n < N; ++n)
+        for (int64_t k = 0; k < K; ++k)
+            out[n * K + k] = (float)int4_weight_zp(w, s, z, N, K, G, n, k);
+}
+
+ORACLE_API void oracle_gemm_w4a16_zp(const uint16_t* A, int a_is_bf16, const uint8_t* w, const uint16_t* s,
+                                     const uint8_t* z, int64_t M, int64_t N, int64_t K, int64_t G,
+                                     const int64_t* rows, int64_t nrows, const int64_t* cols, int64_t ncols,
+                                     double* out) {
+    if (!rows) nrows = M;
+    if (!cols) ncols = N;
+#pragma omp parallel for schedule(dynamic, 1)
+    for (int64_t j = 0; j < ncols; ++j) {
+        const int64_t n = cols ? cols[j] : j;
+        double* wrow = (double*)malloc((size_t)K * sizeof(double));
+        for (int64_t k = 0; k < K; ++k) wrow[k] = int4_weight_zp(w, s, z, N, K, G, n, k);
+        for (int64_t i = 0; i < nrows; ++i) {
+            const int64_t m = rows ? rows[i] : i;
+            double dot = 0.0;
+            for (int64_t k = 0; k < K; ++k) dot += wrow[k] * act_value(A, a_is_bf16, m * K + k);
+            out[i * ncols + j] = dot;
+        }
+        free(wrow);
+    }
 }
 
 /* out[i][j] = sum_k A[rows[i], k] * w[cols[j], k].  rows/cols may be NULL

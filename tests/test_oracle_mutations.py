@@ -76,6 +76,15 @@ MUTATIONS = {
     "quant_nibble_order": (
         "w[n * (K / 2) + k / 2] |= (uint8_t)((k % 2 == 0) ? q : (q << 4));",
         "w[n * (K / 2) + k / 2] |= (uint8_t)((k % 2 == 1) ? q : (q << 4));"),
+    "zp_index_transposed": (
+        "int zero = z[grp * N + n];",
+        "int zero = z[n * (K / G) + grp];"),
+    "zp_A_transposed": (
+        "dot += wrow[k] * act_value(A, a_is_bf16, m * K + k);",
+        "dot += wrow[k] * act_value(A, a_is_bf16, (k * M + m) % (M * K));"),
+    "zp_ignored": (
+        "return (double)(q - zero) * scale;",
+        "return (double)(q - 8) * scale;"),
     "pack_nibbles_swapped": (
         "w[n * (K / 2) + j] = (uint8_t)(lo | (hi << 4));",
         "w[n * (K / 2) + j] = (uint8_t)(hi | (lo << 4));"),

@@ -413,3 +413,52 @@ def test_quantiser_reproduces_exactly_representable_weights():
     w, s = oracle.quantize_int4(W.astype(np.float16).view(np.uint16), G)
     assert np.array_equal(oracle.unpack_int4(w, K), q)
     assert np.array_equal(s.view(np.float16).astype(np.float64), S)
+
+
+# ------------------------------------------------------------- zero-point INT4
+
+def test_zero_point_worked_example():
+    g = _golden("int4_zero_point_worked_example.json")
+    w = np.array(g["packed"], dtype=np.uint8)
+    s = _f16_bits(g["scales"])
+    z = np.array(g["zeros"], dtype=np.uint8)
+    assert oracle.dequant_int4_zp(w, s, z, g["K"], g["G"]).astype(np.float64).tolist() == g["w"]
+    A = _f16_bits(g["A"])
+    out = oracle.gemm_w4a16_zp(A, False, w, s, z, g["M"], g["N"], g["K"], g["G"])
+    assert out.tolist() == g["out"]
+
+
+def test_zero_point_eight_is_the_symmetric_format():
+    # Z = 8 everywhere is exactly the symmetric (q - 8) * S format
+    rng = np.random.default_rng(320)
+    M, N, K, G = 3, 40, 256, 64
+    q = rng.integers(0, 16, size=(N, K)).astype(np.uint8)
+    w = oracle.pack_int4(q)
+    s = _f16_bits(rng.uniform(0.005, 0.02, size=(K // G, N)))
+    A = _f16_bits(rng.standard_normal((M, K)))
+    z = np.full((K // G, N), 8, dtype=np.uint8)
+    assert np.array_equal(oracle.dequant_int4_zp(w, s, z, K, G), oracle.dequant_int4(w, s, K, G))
+    assert np.array_equal(oracle.gemm_w4a16_zp(A, False, w, s, z, M, N, K, G), oracle.gemm_w4a16(A, False, w, s, M, N, K, G))
+
+
+def test_zero_point_brute_force():
+    # a pure-Python triple loop on a tiny case, zero points and scales varying per group and row
+    rng = np.random.default_rng(321)
+    M, N, K, G = 2, 5, 64, 32
+    q = rng.integers(0, 16, size=(N, K))
+    z = rng.integers(0, 16, size=(K // G, N)).astype(np.uint8)
+    sv = rng.uniform(0.01, 0.1, size=(K // G, N))
+    s = _f16_bits(sv)
+    sd = s.view(np.float16).astype(np.float64)
+    Av = rng.standard_normal((M, K))
+    A = _f16_bits(Av)
+    Ad = A.view(np.float16).astype(np.float64)
+    want = np.zeros((M, N))
+    for m in range(M):
+        for n in range(N):
+            acc = 0.0
+            for k in range(K):
+                acc += Ad[m, k] * (int(q[n, k]) - int(z[k // G, n])) * sd[k // G, n]
+            want[m, n] = acc
+    got = oracle.gemm_w4a16_zp(A, False, oracle.pack_int4(q.astype(np.uint8)), s, z, M, N, K, G)
+    assert np.allclose(got, want, rtol=1e-12, atol=1e-12)
