@@ -371,6 +371,7 @@ def run_ours(args, rank, world, local_rank):
     # ---------------- FP8 / FP4 extras (L2 flushed between runs): the config shapes, fp16
     # and bf16 activations, the bias epilogue, and FP4 at the FP4 page's own shape
     fp8_fp4 = []
+    zero_point = []
     if not args.skip_prefill:
         flush = torch.empty(512 << 20, dtype=torch.uint8, device=dev)
 
@@ -387,14 +388,14 @@ def run_ours(args, rank, world, local_rank):
             torch.cuda.synchronize(dev)
             return statistics.median([a.elapsed_time(b) * 1e3 for a, b in times[3:]])
 
-        def entry(op, M, N, K, adt, us, byts, extra=None):
+        def entry(op, M, N, K, adt, us, byts, extra=None, into=None):
             d = {"op": op, "M": M, "N": N, "K": K, "A": adt, "us": round(us, 2),
                  "TFLOP/s": round(2.0 * M * N * K / (us * 1e-6) / 1e12, 1),
                  "frac_tensor": round(2.0 * M * N * K / (us * 1e-6) / 1e12 / peaks["bf16_tflops"], 4),
                  "GB/s": round(byts / (us * 1e-6) / 1e9, 1),
                  "frac_hbm": round(byts / (us * 1e-6) / 1e9 / peaks["hbm_gbs"], 4)}
             d.update(extra or {})
-            fp8_fp4.append(d)
+            (fp8_fp4 if into is None else into).append(d)
 
         fp8_cases = [(32768, 3200, 5120, "bf16", False), (16384, 12800, 5120, "bf16", False),
                      (8192, 10240, 5120, "bf16", False), (8192, 10240, 5120, "f16", False),
@@ -433,6 +434,30 @@ def run_ours(args, rank, world, local_rank):
             entry("fp4", M, N, K, "bf16", us, N * K // 2 + N * K // 16 + M * K * 2 + M * N * 2,
                   {"context": note} if note else None)
             del Ax, wd, outx, wsx
+        # zero-point INT4 beside the symmetric format at the same shapes (the zero-point
+        # path runs on the tile kernels at every M)
+        for (M, N, K, Gz) in [(16, 4096, 4096, 128), (128, 4096, 4096, 128), (4096, 4096, 4096, 128),
+                              (8192, 8192, 8192, 128)]:
+            seed = 6000 + M
+            Ax = torch.from_numpy(synth.activations(M, K, "f16", seed).view(np.int16)).to(dev).view(torch.float16)
+            wz = synth.int4_weights(N, K, Gz, seed + 1)
+            wkz, skz = wq.wq_pack_int4(torch.from_numpy(wz.w).to(dev),
+                                       torch.from_numpy(wz.s.view(np.int16)).to(dev).view(torch.float16), N, K, Gz)
+            zkz = wq.wq_pack_int4_zeros(torch.from_numpy(synth.int4_zeros(N, K, Gz, seed + 2)).to(dev), N, K, Gz)
+            outx = torch.empty((M, N), dtype=torch.float16, device=dev)
+            byts = N * K // 2 + (K // Gz) * N * 3 + M * K * 2 + M * N * 2
+            for op in ("w4a16_zp", "w4a16"):
+                opid = wq.WQ_OP_W4A16_ZP if op == "w4a16_zp" else wq.WQ_OP_W4A16
+                plan = wq.get_plan(opid, wq.WQ_F16, M, N, K, Gz)
+                wsx = torch.zeros(plan["ws_bytes"] + 16, dtype=torch.uint8, device=dev)
+                if op == "w4a16_zp":
+                    us = time_call(lambda: wq.wq_gemm_w4a16_zp(Ax, wkz, skz, zkz, N, K, Gz, out=outx, ws=wsx))
+                else:
+                    us = time_call(lambda: wq.wq_gemm_w4a16(Ax, wkz, skz, N, K, Gz, out=outx, ws=wsx))
+                entry(op, M, N, K, "f16", us, byts if op == "w4a16_zp" else byts - (K // Gz) * N,
+                      {"G": Gz, "kernel": plan["kernel"]}, into=zero_point)
+                del wsx
+            del Ax, wkz, skz, zkz, outx
         del flush
 
     # ---------------- quantiser extra: fp16 W (11008 x 4096) -> INT4 codes + fp16 scales
@@ -507,6 +532,7 @@ def run_ours(args, rank, world, local_rank):
         "prefill": prefill,
         "quantiser": quantiser,
         "fp8_fp4": fp8_fp4,
+        "zero_point": zero_point,
         "e2e": {"value": round(e2e_value, 2), "unit": "GB/s", "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
                 "ms_per_step": round(e2e_s * 1e3, 4),
                 "how": "per step: pinned-host->device copy of every A, wq_gemm_w4a16 via the Python binding, "

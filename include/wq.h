@@ -49,7 +49,7 @@ typedef struct CUstream_st* wq_stream_t; /* same type as cudaStream_t */
 
 typedef enum { WQ_F16 = 0, WQ_BF16 = 1 } wq_dtype;
 
-typedef enum { WQ_OP_W4A16 = 0, WQ_OP_FP8 = 1, WQ_OP_FP4 = 2 } wq_op;
+typedef enum { WQ_OP_W4A16 = 0, WQ_OP_FP8 = 1, WQ_OP_FP4 = 2, WQ_OP_W4A16_ZP = 3 } wq_op;
 
 typedef enum {
     WQ_OK = 0,
@@ -140,6 +140,36 @@ wq_status wq_debug_dequant_int4(const uint8_t* w_kernel, const void* s_kernel, i
 wq_status wq_gemm_w4a16(const void* A, wq_dtype a_dtype, const uint8_t* w_kernel, const void* s_kernel,
                         int64_t M, int64_t N, int64_t K, int32_t G, void* out, void* ws, size_t ws_bytes,
                         wq_stream_t stream);
+
+/* ---------------------------------------------------------- INT4 zero point */
+
+/* Asymmetric (zero-point) INT4: w[n][k] = (q[n][k] - Z[k/G][n]) * S[k/G][n], one
+ * integer zero point 0..15 per group and row beside the scale.  "Low Bit Triton
+ * Kernels" (GPU MODE lecture 34), §02, names the group-scaled 4-bit formats of
+ * GPTQ, AWQ and HQQ, which carry zero points, but prints no zero-point encoding;
+ * an integer zero point in the code range is the reading taken.  With Z = 8 it is
+ * the symmetric format.  Codes and scales pack with wq_pack_int4 as before.
+ *
+ * Size of the kernel-order zero-point buffer: N padded to 128, K to 256, one byte
+ * per (group, row).  Host only. */
+wq_status wq_int4_packed_zeros_bytes(int64_t N, int64_t K, int32_t G, size_t* z_bytes);
+
+/* Layout transform of the zero points: z_canon uint8 [K/G][N] (values 0..15) to
+ * z_kernel [N/128][Kp/G][128], the order of the packed scales; padding gets 8.
+ * z_kernel: 16-byte aligned, wq_int4_packed_zeros_bytes long.  Values above 15
+ * are not checked (the kernel reads them as given). */
+wq_status wq_pack_int4_zeros(const uint8_t* z_canon, int64_t N, int64_t K, int32_t G, uint8_t* z_kernel,
+                             wq_stream_t stream);
+
+/* W4A16 GEMM with zero points: out[M][N] = A[M][K] . ((q - Z) * S)^T.  Arguments as
+ * for wq_gemm_w4a16 plus z_kernel (wq_pack_int4_zeros output, 16-byte aligned), the
+ * workspace sized for WQ_OP_W4A16_ZP.  The operand is RN((q - Z) * s) in the type of
+ * A (q - Z is exact), accumulated in fp32; every M runs on the tile kernels (the
+ * M <= 16 register kernel has no zero-point path).  The same rule on the kernel
+ * before the call holds, now for z_kernel as well. */
+wq_status wq_gemm_w4a16_zp(const void* A, wq_dtype a_dtype, const uint8_t* w_kernel, const void* s_kernel,
+                           const uint8_t* z_kernel, int64_t M, int64_t N, int64_t K, int32_t G, void* out, void* ws,
+                           size_t ws_bytes, wq_stream_t stream);
 
 /* ------------------------------------------------------------------ FP8 */
 

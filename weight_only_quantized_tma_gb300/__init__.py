@@ -19,10 +19,13 @@ from ._lib import (  # noqa: F401
     wq_gemm_bf16_fp4,
     wq_gemm_w4a16,
     wq_gemm_w4a16_noalloc,
+    wq_gemm_w4a16_zp,
     wq_gemm_w8a16_fp8,
     wq_int4_packed_bytes,
+    wq_int4_packed_zeros_bytes,
     wq_pack_fp4_sf,
     wq_pack_int4,
+    wq_pack_int4_zeros,
     wq_quantize_int4,
     wq_unpack_int4,
     WQ_BF16,
@@ -33,4 +36,5 @@ from ._lib import (  # noqa: F401
     WQ_OP_FP4,
     WQ_OP_FP8,
     WQ_OP_W4A16,
+    WQ_OP_W4A16_ZP,
 )

@@ -19,7 +19,7 @@ _HERE = os.path.dirname(os.path.abspath(__file__))
 LIB_PATH = os.path.join(_HERE, "libwq.so")
 
 WQ_F16, WQ_BF16 = 0, 1
-WQ_OP_W4A16, WQ_OP_FP8, WQ_OP_FP4 = 0, 1, 2
+WQ_OP_W4A16, WQ_OP_FP8, WQ_OP_FP4, WQ_OP_W4A16_ZP = 0, 1, 2, 3
 WQ_KERNEL_TILE, WQ_KERNEL_DECODE, WQ_KERNEL_TILE_PAIR = 0, 1, 2
 STATUS_NAMES = {
     0: "WQ_OK", 1: "WQ_ERR_NULL", 2: "WQ_ERR_SHAPE", 3: "WQ_ERR_GROUP", 4: "WQ_ERR_MISALIGNED",
@@ -59,6 +59,10 @@ _SIGNATURES = {
     "wq_unpack_int4": (ctypes.c_int, [_vp, _vp, _i64, _i64, _i32, _vp, _vp, _vp]),
     "wq_debug_dequant_int4": (ctypes.c_int, [_vp, _vp, _i64, _i64, _i32, _vp, _vp]),
     "wq_gemm_w4a16": (ctypes.c_int, [_vp, ctypes.c_int, _vp, _vp, _i64, _i64, _i64, _i32, _vp, _vp, _sz, _vp]),
+    "wq_int4_packed_zeros_bytes": (ctypes.c_int, [_i64, _i64, _i32, ctypes.POINTER(_sz)]),
+    "wq_pack_int4_zeros": (ctypes.c_int, [_vp, _i64, _i64, _i32, _vp, _vp]),
+    "wq_gemm_w4a16_zp": (ctypes.c_int, [_vp, ctypes.c_int, _vp, _vp, _vp, _i64, _i64, _i64, _i32, _vp, _vp, _sz,
+                                        _vp]),
     "wq_debug_dequant_fp8": (ctypes.c_int, [_vp, _i64, _i64, ctypes.c_int, _vp, _vp]),
     "wq_gemm_w8a16_fp8": (ctypes.c_int, [_vp, ctypes.c_int, _vp, _vp, _vp, _i64, _i64, _i64, _vp, _vp, _sz, _vp]),
     "wq_fp4_packed_sf_bytes": (ctypes.c_int, [_i64, _i64, ctypes.POINTER(_sz)]),
@@ -230,6 +234,43 @@ def wq_gemm_w4a16(A: torch.Tensor, w_kernel: torch.Tensor, s_kernel: torch.Tenso
         ws_bytes = ws.numel() * ws.element_size()
     _check(lib().wq_gemm_w4a16(_ptr(A), a_dtype, _ptr(w_kernel), _ptr(s_kernel), M, N, K, G, _ptr(out), _ptr(ws),
                                ws_bytes, _stream(A)), "wq_gemm_w4a16")
+    return out
+
+
+def wq_int4_packed_zeros_bytes(N: int, K: int, G: int) -> int:
+    zb = _sz(0)
+    _check(lib().wq_int4_packed_zeros_bytes(N, K, G, ctypes.byref(zb)), "wq_int4_packed_zeros_bytes")
+    return zb.value
+
+
+def wq_pack_int4_zeros(z_canon: torch.Tensor, N: int, K: int, G: int) -> torch.Tensor:
+    """Canonical uint8 zero points [K/G, N] (0..15) -> kernel-order buffer."""
+    _need(z_canon, "z_canon", torch.uint8, (K // G, N))
+    zk = torch.empty(wq_int4_packed_zeros_bytes(N, K, G), dtype=torch.uint8, device=z_canon.device)
+    _check(lib().wq_pack_int4_zeros(_ptr(z_canon), N, K, G, _ptr(zk), _stream(z_canon)), "wq_pack_int4_zeros")
+    return zk
+
+
+def wq_gemm_w4a16_zp(A: torch.Tensor, w_kernel: torch.Tensor, s_kernel: torch.Tensor, z_kernel: torch.Tensor,
+                     N: int, K: int, G: int, out: torch.Tensor = None, ws: torch.Tensor = None) -> torch.Tensor:
+    """out[M, N] = A[M, K] . ((q - Z) * S)^T, out in the dtype of A."""
+    a_dtype = _adtype(A)
+    _need(A, "A", A.dtype)
+    if A.dim() != 2 or A.shape[1] != K:
+        raise ValueError(f"A must be [M, {K}]")
+    M = A.shape[0]
+    _need(w_kernel, "w_kernel", torch.uint8)
+    _need(s_kernel, "s_kernel", torch.float16)
+    _need(z_kernel, "z_kernel", torch.uint8)
+    if out is None:
+        out = torch.empty((M, N), dtype=A.dtype, device=A.device)
+    _need(out, "out", A.dtype, (M, N))
+    if ws is None:
+        ws, ws_bytes = workspace(WQ_OP_W4A16_ZP, a_dtype, M, N, K, G, A.device)
+    else:
+        ws_bytes = ws.numel() * ws.element_size()
+    _check(lib().wq_gemm_w4a16_zp(_ptr(A), a_dtype, _ptr(w_kernel), _ptr(s_kernel), _ptr(z_kernel), M, N, K, G,
+                                  _ptr(out), _ptr(ws), ws_bytes, _stream(A)), "wq_gemm_w4a16_zp")
     return out
 
 

@@ -173,13 +173,13 @@ size_t split_ws_bytes(int tiles, int splits, int bn) {
 //    the weight is the smaller operand, walk weight-row tiles fastest so the
 //    activation panel being reused stays in L2, else walk token tiles fastest.
 wq_status make_plan(int fmt, bool bf16, int64_t M, int64_t N, int64_t K, int sms, int w_bits, Plan* plan,
-                    int G = 0) {
+                    int G = 0, bool allow_decode = true) {
     static const int kTiles[4] = {16, 64, 128, 256};
     KernelConfig cfg{};
     bool found = false;
     // decode (M <= 16): the register-resident kernel; its activation copy views A
     // as 64-wide boxes, so it needs K % 64 == 0
-    const bool decode = fmt == FMT_INT4 && M <= 16 && K % 64 == 0;
+    const bool decode = allow_decode && fmt == FMT_INT4 && M <= 16 && K % 64 == 0;
     if (decode) found = get_config(FMT_INT4 + 16, bf16, 16, sms > 0, &cfg);
     for (int i = 0; i < 4 && !found; ++i) {
         if (M <= kTiles[i] || i == 3) found = get_config(fmt, bf16, kTiles[i], sms > 0, &cfg);
@@ -274,11 +274,11 @@ wq_status make_plan(int fmt, bool bf16, int64_t M, int64_t N, int64_t K, int sms
 
 int w_bits_of(int fmt) { return fmt == FMT_INT4 ? 4 : fmt == FMT_FP8 ? 8 : 4; }
 
-wq_status plan_for(int fmt, bool bf16, int64_t M, int64_t N, int64_t K, Plan* plan, int G) {
+wq_status plan_for(int fmt, bool bf16, int64_t M, int64_t N, int64_t K, Plan* plan, int G, bool allow_decode) {
     DeviceInfo* d = nullptr;
     wq_status st = device_info(&d);
     if (st != WQ_OK) return st;
-    return make_plan(fmt, bf16, M, N, K, d->sms, w_bits_of(fmt), plan, G);
+    return make_plan(fmt, bf16, M, N, K, d->sms, w_bits_of(fmt), plan, G, allow_decode);
 }
 
 void fill_common(GemmParams& gp, const Plan& pl, int64_t M, int64_t N, int64_t K, void* out, void* ws,
@@ -411,6 +411,23 @@ wq_status wq_pack_int4(const uint8_t* w_canon, const void* s_canon, int64_t N, i
                                           static_cast<uint16_t*>(s_kernel), (cudaStream_t)stream));
 }
 
+wq_status wq_int4_packed_zeros_bytes(int64_t N, int64_t K, int32_t G, size_t* z_bytes) {
+    size_t s_bytes = 0;
+    const wq_status st = wq_int4_packed_bytes(N, K, G, nullptr, &s_bytes);
+    if (st == WQ_OK && z_bytes) *z_bytes = s_bytes / 2;   // one byte per (group, row) instead of two
+    return st;
+}
+
+wq_status wq_pack_int4_zeros(const uint8_t* z_canon, int64_t N, int64_t K, int32_t G, uint8_t* z_kernel,
+                             wq_stream_t stream) {
+    wq_status st = check_pack_args(z_canon, z_kernel, z_canon, z_kernel, N, K, G);
+    if (st != WQ_OK) return st;
+    if (!aligned(z_kernel, 16)) return WQ_ERR_MISALIGNED;
+    DeviceInfo* d = nullptr;
+    if ((st = device_info(&d)) != WQ_OK) return st;
+    return finish_launch(launch_pack_int4_zeros(z_canon, N, K, G, z_kernel, (cudaStream_t)stream));
+}
+
 wq_status wq_quantize_int4(const void* w, int64_t N, int64_t K, int32_t G, uint8_t* w_canon, void* s_canon,
                            wq_stream_t stream) {
     if (!w || !w_canon || !s_canon) return WQ_ERR_NULL;
@@ -488,12 +505,14 @@ wq_status wq_debug_dequant_fp8(const uint8_t* w_e4m3, int64_t N, int64_t K, wq_d
 wq_status wq_get_plan(wq_op op, wq_dtype a_dtype, int64_t M, int64_t N, int64_t K, int32_t G, wq_plan* plan,
                       size_t* ws_bytes) {
     if (M < 0 || N <= 0 || K <= 0 || M > kMaxDim || N > kMaxDim || K > kMaxDim) return WQ_ERR_SHAPE;
-    if (op != WQ_OP_W4A16 && op != WQ_OP_FP8 && op != WQ_OP_FP4) return WQ_ERR_SHAPE;
-    if (op == WQ_OP_W4A16 && (!valid_group(G) || K % G != 0)) return WQ_ERR_GROUP;
+    if (op != WQ_OP_W4A16 && op != WQ_OP_FP8 && op != WQ_OP_FP4 && op != WQ_OP_W4A16_ZP) return WQ_ERR_SHAPE;
+    const bool int4 = op == WQ_OP_W4A16 || op == WQ_OP_W4A16_ZP;
+    if (int4 && (!valid_group(G) || K % G != 0)) return WQ_ERR_GROUP;
     if (a_dtype != WQ_F16 && a_dtype != WQ_BF16) return WQ_ERR_DTYPE;
     const bool bf16 = (op == WQ_OP_FP4) ? true : (a_dtype == WQ_BF16);
     Plan pl{};
-    wq_status st = plan_for((int)op, bf16, M > 0 ? M : 1, N, K, &pl, op == WQ_OP_W4A16 ? G : 0);
+    wq_status st = plan_for(int4 ? FMT_INT4 : (int)op, bf16, M > 0 ? M : 1, N, K, &pl, int4 ? G : 0,
+                            op != WQ_OP_W4A16_ZP);
     if (st != WQ_OK) return st;
     if (plan) {
         plan->bn = pl.cfg.bn;
@@ -519,15 +538,18 @@ wq_status wq_workspace_bytes(wq_op op, wq_dtype a_dtype, int64_t M, int64_t N, i
     return wq_get_plan(op, a_dtype, M, N, K, G, nullptr, bytes);
 }
 
-wq_status wq_gemm_w4a16(const void* A, wq_dtype a_dtype, const uint8_t* w_kernel, const void* s_kernel, int64_t M,
-                        int64_t N, int64_t K, int32_t G, void* out, void* ws, size_t ws_bytes, wq_stream_t stream) {
+// W4A16 with the symmetric zero point 8 (z_kernel null) or packed zero points.
+static wq_status gemm_int4(const void* A, wq_dtype a_dtype, const uint8_t* w_kernel, const void* s_kernel,
+                           const uint8_t* z_kernel, int64_t M, int64_t N, int64_t K, int32_t G, void* out, void* ws,
+                           size_t ws_bytes, wq_stream_t stream) {
     if (M == 0 && N > 0 && K > 0) return WQ_OK;   // empty problem: A and out may be NULL
     if (!A || !w_kernel || !s_kernel || !out) return WQ_ERR_NULL;
     if (M < 0 || N <= 0 || K <= 0 || M > kMaxDim || N > kMaxDim || K > kMaxDim) return WQ_ERR_SHAPE;
     if (K % 32 != 0 || N % 8 != 0) return WQ_ERR_SHAPE;
     if (!valid_group(G) || K % G != 0) return WQ_ERR_GROUP;
     if (a_dtype != WQ_F16 && a_dtype != WQ_BF16) return WQ_ERR_DTYPE;
-    if (!aligned(A, 16) || !aligned(w_kernel, 16) || !aligned(s_kernel, 16) || !aligned(out, 16))
+    if (!aligned(A, 16) || !aligned(w_kernel, 16) || !aligned(s_kernel, 16) || !aligned(out, 16) ||
+        !aligned(z_kernel, 16))
         return WQ_ERR_MISALIGNED;
     DeviceInfo* d = nullptr;
     wq_status st = device_info(&d);
@@ -535,7 +557,7 @@ wq_status wq_gemm_w4a16(const void* A, wq_dtype a_dtype, const uint8_t* w_kernel
     if (M == 0) return WQ_OK;
     const bool bf16 = a_dtype == WQ_BF16;
     Plan pl{};
-    if ((st = make_plan(FMT_INT4, bf16, M, N, K, d->sms, 4, &pl, G)) != WQ_OK) return st;
+    if ((st = make_plan(FMT_INT4, bf16, M, N, K, d->sms, 4, &pl, G, z_kernel == nullptr)) != WQ_OK) return st;
     if ((st = check_ws(pl, ws, ws_bytes)) != WQ_OK) return st;
     GemmParams gp;
     std::memset(&gp, 0, sizeof(gp));
@@ -546,6 +568,7 @@ wq_status wq_gemm_w4a16(const void* A, wq_dtype a_dtype, const uint8_t* w_kernel
     if (pl.pair && !encode_out(gp, out, bf16, M, N)) return WQ_ERR_CUDA;
     gp.w = w_kernel;
     gp.sc = static_cast<const uint8_t*>(s_kernel);
+    gp.zp = z_kernel;
     gp.G = G;
     gp.g_shift = G == 32 ? 5 : G == 64 ? 6 : G == 128 ? 7 : 8;
     const int64_t Kp = round_up(K, KPAD_INT4);
@@ -555,6 +578,19 @@ wq_status wq_gemm_w4a16(const void* A, wq_dtype a_dtype, const uint8_t* w_kernel
     if (pl.decode) return finish_launch(launch_gemm_int4_decode(gp, bf16, pl.grid, (cudaStream_t)stream));
     if (pl.pair) return finish_launch(launch_gemm_int4_pair(gp, bf16, pl.grid, (cudaStream_t)stream));
     return finish_launch(launch_gemm_int4(gp, bf16, pl.cfg.bn, pl.grid, (cudaStream_t)stream));
+}
+
+wq_status wq_gemm_w4a16(const void* A, wq_dtype a_dtype, const uint8_t* w_kernel, const void* s_kernel, int64_t M,
+                        int64_t N, int64_t K, int32_t G, void* out, void* ws, size_t ws_bytes, wq_stream_t stream) {
+    return gemm_int4(A, a_dtype, w_kernel, s_kernel, nullptr, M, N, K, G, out, ws, ws_bytes, stream);
+}
+
+wq_status wq_gemm_w4a16_zp(const void* A, wq_dtype a_dtype, const uint8_t* w_kernel, const void* s_kernel,
+                           const uint8_t* z_kernel, int64_t M, int64_t N, int64_t K, int32_t G, void* out, void* ws,
+                           size_t ws_bytes, wq_stream_t stream) {
+    if (M == 0 && N > 0 && K > 0) return WQ_OK;
+    if (!z_kernel) return WQ_ERR_NULL;
+    return gemm_int4(A, a_dtype, w_kernel, s_kernel, z_kernel, M, N, K, G, out, ws, ws_bytes, stream);
 }
 
 wq_status wq_gemm_w8a16_fp8(const void* A, wq_dtype a_dtype, const uint8_t* w_e4m3, const float* alpha,

@@ -75,7 +75,10 @@ struct GemmCfg {
     // copies it out with TMA, so the accumulator is released before the stores
     static constexpr bool STAGE_OUT = PAIR;
     static constexpr int OUT_BOX_M = 128;                             // tokens per output copy
-    static constexpr int OFF_STG = (OFF_SC + WSTAGES * SC_STAGE + 1023) / 1024 * 1024;
+    // INT4 zero points of the stage's groups (uint8, up to BK / 32 groups of 128 rows)
+    static constexpr int ZP_STAGE = (FMT == FMT_INT4) ? (BK / 32) * TILE_N : 0;
+    static constexpr int OFF_ZP = OFF_SC + WSTAGES * SC_STAGE;
+    static constexpr int OFF_STG = (OFF_ZP + WSTAGES * ZP_STAGE + 1023) / 1024 * 1024;
     static constexpr int STG_BYTES = STAGE_OUT ? BN * TILE_N * 2 : 0;
     static constexpr int OFF_BAR = (OFF_STG + STG_BYTES + 127) / 128 * 128;
     static constexpr int NBARS = 2 * STAGES + 2 * WSTAGES + 2 * A_ST + 4;
@@ -419,13 +422,18 @@ __global__ void __launch_bounds__(128 * (1 + NWG), (GemmCfg<FMT, BF16, BN, BK, S
                         if (FMT == FMT_INT4) {
                             const int gcnt = (p.G >= BK) ? 1 : (BK >> p.g_shift);
                             const uint32_t sc_bytes = (uint32_t)gcnt * TILE_N * 2;
-                            ptx::mbar_arrive_expect_tx(fb, C::W_STAGE + sc_bytes);
+                            const uint32_t zp_bytes = p.zp ? (uint32_t)gcnt * TILE_N : 0u;
+                            ptx::mbar_arrive_expect_tx(fb, C::W_STAGE + sc_bytes + zp_bytes);
                             const uint8_t* wsrc =
                                 p.w + ((size_t)w_tile(it) * p.nchunks_pad + (size_t)kb * (BK / 32)) * (TILE_N * 16);
                             ptx::bulk_load(w_dst, wsrc, C::W_STAGE, fb, pol);
                             const int g0 = (kb * BK) >> p.g_shift;
                             const uint8_t* ssrc = p.sc + ((size_t)w_tile(it) * p.ngroups_pad + g0) * (TILE_N * 2);
                             ptx::bulk_load(sc_dst, ssrc, sc_bytes, fb, pol);
+                            if (p.zp)
+                                ptx::bulk_load(sbase + C::OFF_ZP + s * C::ZP_STAGE,
+                                               p.zp + ((size_t)w_tile(it) * p.ngroups_pad + g0) * TILE_N, zp_bytes, fb,
+                                               pol);
                         } else if (FMT == FMT_FP4) {
                             ptx::mbar_arrive_expect_tx(fb, C::W_STAGE + C::SC_STAGE);
                             ptx::tma_load_2d(w_dst, &p.tmap_w, kb * (BK / 2), w_tile(it) * TILE_N, fb, pol);
@@ -667,7 +675,15 @@ __global__ void __launch_bounds__(128 * (1 + NWG), (GemmCfg<FMT, BF16, BN, BK, S
 #pragma unroll
                 for (int i = 0; i < CPW; ++i) {
                     if (FMT == FMT_INT4) {
-                        const Int4RowConsts kc = int4_row_consts((r >> 3) & 1);
+                        Int4RowConsts kc = int4_row_consts((r >> 3) & 1);
+                        if (p.zp) {
+                            // zero point z of this unit's group and row: subtract b + z (b = 1024
+                            // or 64 by row half) instead of b + 8, exactly as above
+                            const uint8_t* zst = smem + C::OFF_ZP + s * C::ZP_STAGE;
+                            const uint32_t z = zst[(((c0 + i) * 32) >> p.g_shift) * TILE_N + r];
+                            const uint32_t b = ((r >> 3) & 1) ? (0x5400u + (z << 4)) : (0x6400u + z);
+                            kc.bias = b | (b << 16);
+                        }
                         if (BF16)
                             int4_row_to_bf16(qi[i], kc, __half2float(__ushort_as_half(sv[i])), o[i]);
                         else

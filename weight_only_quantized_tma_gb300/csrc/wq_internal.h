@@ -77,6 +77,7 @@ struct GemmParams {
     CUtensorMap tmap_out;    // pair kernel: out [M][N], 16-bit, box {128, 128}, no swizzle
     const uint8_t* w;        // INT4 prepacked weight tiles
     const uint8_t* sc;       // INT4 prepacked group scales / FP4 prepacked block scales
+    const uint8_t* zp;       // INT4 prepacked zero points (uint8, the scales' layout) or null: zero point 8
     const float* alpha;      // FP8 / FP4 global scale (device), unused for INT4
     const void* bias;        // FP8 optional bias [N], same 16-bit type as A
     void* out;               // [M][N], 16-bit
@@ -164,6 +165,7 @@ cudaError_t launch_pack_int4(const uint8_t* w, const uint16_t* s, int64_t N, int
                              uint16_t* sk, cudaStream_t st);
 cudaError_t launch_unpack_int4(const uint8_t* wk, const uint16_t* sk, int64_t N, int64_t K, int G, uint8_t* w,
                                uint16_t* s, cudaStream_t st);
+cudaError_t launch_pack_int4_zeros(const uint8_t* z, int64_t N, int64_t K, int G, uint8_t* zk, cudaStream_t st);
 cudaError_t launch_dequant_int4(const uint8_t* wk, const uint16_t* sk, int64_t N, int64_t K, int G, float* out,
                                 cudaStream_t st);
 cudaError_t launch_pack_fp4_sf(const uint8_t* sf, int64_t N, int64_t K, uint8_t* sfk, cudaStream_t st);

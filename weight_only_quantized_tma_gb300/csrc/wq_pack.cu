@@ -241,6 +241,31 @@ cudaError_t launch_pack_int4(const uint8_t* w, const uint16_t* s, int64_t N, int
     return cudaGetLastError();
 }
 
+// Zero points: canonical uint8 [K/G][N] -> [N/128][Kp/G][128], the layout of the packed
+// scales; padding gets 8 (with scale 0 the weight is 0 either way).
+__global__ void pack_int4_z_kernel(const uint8_t* __restrict__ z, int64_t N, int64_t groups, int64_t groups_pad,
+                                   int64_t total, uint8_t* __restrict__ zk) {
+    for (int64_t u = blockIdx.x * (int64_t)blockDim.x + threadIdx.x; u < total;
+         u += (int64_t)gridDim.x * blockDim.x) {
+        const int64_t r = u % TILE_N;
+        const int64_t t = u / TILE_N;
+        const int64_t g = t % groups_pad;
+        const int64_t nt = t / groups_pad;
+        const int64_t n = nt * TILE_N + r;
+        zk[u] = (n < N && g < groups) ? z[g * N + n] : (uint8_t)8;
+    }
+}
+
+cudaError_t launch_pack_int4_zeros(const uint8_t* z, int64_t N, int64_t K, int G, uint8_t* zk, cudaStream_t st) {
+    const int64_t Np = round_up(N, TILE_N), Kp = round_up(K, KPAD_INT4);
+    const int64_t groups_pad = Kp / G, total = (Np / TILE_N) * groups_pad * TILE_N;
+    pack_int4_z_kernel<<<grid_for(total), kThreads, 0, st>>>(z, N, K / G, groups_pad, total, zk);
+    cudaError_t e = cudaGetLastError();
+    if (e != cudaSuccess) return e;
+    stream_fence_kernel<<<1, 32, 0, st>>>();   // as after the weight packing
+    return cudaGetLastError();
+}
+
 cudaError_t launch_unpack_int4(const uint8_t* wk, const uint16_t* sk, int64_t N, int64_t K, int G, uint8_t* w,
                                uint16_t* s, cudaStream_t st) {
     const int64_t Kp = round_up(K, KPAD_INT4);

@@ -78,6 +78,11 @@ def int4_weights(N: int, K: int, G: int, seed: int, scale_lo: float = 0.005,
     return Int4Weights(w=w, s=_to_bits(s, "f16"), N=N, K=K, G=G)
 
 
+def int4_zeros(N: int, K: int, G: int, seed: int) -> np.ndarray:
+    """Zero points uint8 [K/G, N], uniform over the codes 0..15."""
+    return _rng(seed).integers(0, 16, size=(K // G, N), dtype=np.uint8)
+
+
 @dataclass
 class Fp8Weights:
     w: np.ndarray        # uint8 e4m3 codes [N, K]
