@@ -13,6 +13,11 @@ the definitions on the source pages:
   accumulator.
 * BF16 x FP4 -- "FlashInfer SM100 BF16 x FP4 GEMM" (PR #4466), §2: e2m1 weight
   [N, K/2], e4m3 block scale per 16 along K, global alpha.
+* INT4 codebook (NF4-style) -- "Low Bit Triton Kernels", the passage on choosing
+  the 16 values of a 4-bit weight: ``LUT[q] * S[k // G, n]`` with a 16-entry fp16
+  table supplied by the caller.
+* INT2 W2A16 -- "Bitblas -- Mixed-Precision GEMM with the Ladder Compiler",
+  hands-on item 6: ``(q - 2) * S[k // G, n]``, four codes per byte along K.
 
 This module only marshals numpy arrays into the C functions and builds the
 shared object with gcc on first use.
@@ -81,6 +86,16 @@ def _load():
                                              ctypes.c_int64, ctypes.c_int64, u8p, ctypes.c_int64, u8p,
                                              ctypes.c_int64, u8p]
         lib.oracle_gemm_w4a16.argtypes = [u8p, ctypes.c_int, u8p, u8p, ctypes.c_int64, ctypes.c_int64,
+                                          ctypes.c_int64, ctypes.c_int64, u8p, ctypes.c_int64, u8p,
+                                          ctypes.c_int64, u8p]
+        lib.oracle_dequant_int4_lut.argtypes = [u8p, u8p, u8p, ctypes.c_int64, ctypes.c_int64, ctypes.c_int64, u8p]
+        lib.oracle_gemm_w4a16_lut.argtypes = [u8p, ctypes.c_int, u8p, u8p, u8p, ctypes.c_int64, ctypes.c_int64,
+                                              ctypes.c_int64, ctypes.c_int64, u8p, ctypes.c_int64, u8p,
+                                              ctypes.c_int64, u8p]
+        lib.oracle_pack_int2.argtypes = [u8p, ctypes.c_int64, ctypes.c_int64, u8p]
+        lib.oracle_unpack_int2.argtypes = [u8p, ctypes.c_int64, ctypes.c_int64, u8p]
+        lib.oracle_dequant_int2.argtypes = [u8p, u8p, ctypes.c_int64, ctypes.c_int64, ctypes.c_int64, u8p]
+        lib.oracle_gemm_w2a16.argtypes = [u8p, ctypes.c_int, u8p, u8p, ctypes.c_int64, ctypes.c_int64,
                                           ctypes.c_int64, ctypes.c_int64, u8p, ctypes.c_int64, u8p,
                                           ctypes.c_int64, u8p]
         lib.oracle_dequant_fp8.argtypes = [u8p, ctypes.c_int64, ctypes.c_int64, u8p]
@@ -250,6 +265,81 @@ def gemm_w4a16_zp(a_bits, a_is_bf16, w, s_bits, z, M, N, K, G, rows=None, cols=N
     out = np.empty((nr, nc), dtype=np.float64)
     _load().oracle_gemm_w4a16_zp(_ptr(a_bits), int(bool(a_is_bf16)), _ptr(w), _ptr(s_bits), _ptr(z), M, N, K, G,
                                  _ptr(r), nr, _ptr(c), nc, _ptr(out))
+    return out
+
+
+# ------------------------------------------------------------------ INT4 codebook (NF4-style)
+
+def dequant_int4_lut(w: np.ndarray, s_bits: np.ndarray, lut_bits: np.ndarray, K: int, G: int) -> np.ndarray:
+    """Codebook INT4: fp32 [N][K] = LUT[q] * S[k // G, n], LUT fp16 bits [16]."""
+    w = _c(w, np.uint8)
+    s_bits = _c(s_bits, np.uint16)
+    lut_bits = _c(lut_bits, np.uint16)
+    if lut_bits.size != 16:
+        raise ValueError("the codebook has 16 entries")
+    N = w.shape[0]
+    out = np.empty((N, K), dtype=np.float32)
+    _load().oracle_dequant_int4_lut(_ptr(w), _ptr(s_bits), _ptr(lut_bits), N, K, G, _ptr(out))
+    return out
+
+
+def gemm_w4a16_lut(a_bits, a_is_bf16, w, s_bits, lut_bits, M, N, K, G, rows=None, cols=None) -> np.ndarray:
+    """float64 out[rows, cols] = A[rows] . (LUT[q] * S)[cols]^T."""
+    a_bits = _c(a_bits, np.uint16)
+    w = _c(w, np.uint8)
+    s_bits = _c(s_bits, np.uint16)
+    lut_bits = _c(lut_bits, np.uint16)
+    if lut_bits.size != 16:
+        raise ValueError("the codebook has 16 entries")
+    r, nr = _index(rows, M)
+    c, nc = _index(cols, N)
+    out = np.empty((nr, nc), dtype=np.float64)
+    _load().oracle_gemm_w4a16_lut(_ptr(a_bits), int(bool(a_is_bf16)), _ptr(w), _ptr(s_bits), _ptr(lut_bits),
+                                  M, N, K, G, _ptr(r), nr, _ptr(c), nc, _ptr(out))
+    return out
+
+
+# ------------------------------------------------------------------ INT2 (W2A16)
+
+def pack_int2(q: np.ndarray) -> np.ndarray:
+    """Canonical INT2 packing: uint8 [N][K/4], code k at bits 2 (k % 4) .. +1."""
+    q = _c(q, np.uint8)
+    N, K = q.shape
+    if K % 4:
+        raise ValueError("K must be a multiple of 4")
+    w = np.empty((N, K // 4), dtype=np.uint8)
+    _load().oracle_pack_int2(_ptr(q), N, K, _ptr(w))
+    return w
+
+
+def unpack_int2(w: np.ndarray, K: int) -> np.ndarray:
+    w = _c(w, np.uint8)
+    N = w.shape[0]
+    q = np.empty((N, K), dtype=np.uint8)
+    _load().oracle_unpack_int2(_ptr(w), N, K, _ptr(q))
+    return q
+
+
+def dequant_int2(w: np.ndarray, s_bits: np.ndarray, K: int, G: int) -> np.ndarray:
+    """INT2: fp32 [N][K] = (q - 2) * S[k // G, n]."""
+    w = _c(w, np.uint8)
+    s_bits = _c(s_bits, np.uint16)
+    N = w.shape[0]
+    out = np.empty((N, K), dtype=np.float32)
+    _load().oracle_dequant_int2(_ptr(w), _ptr(s_bits), N, K, G, _ptr(out))
+    return out
+
+
+def gemm_w2a16(a_bits, a_is_bf16, w, s_bits, M, N, K, G, rows=None, cols=None) -> np.ndarray:
+    """float64 out[rows, cols] = A[rows] . ((q - 2) * S)[cols]^T."""
+    a_bits = _c(a_bits, np.uint16)
+    w = _c(w, np.uint8)
+    s_bits = _c(s_bits, np.uint16)
+    r, nr = _index(rows, M)
+    c, nc = _index(cols, N)
+    out = np.empty((nr, nc), dtype=np.float64)
+    _load().oracle_gemm_w2a16(_ptr(a_bits), int(bool(a_is_bf16)), _ptr(w), _ptr(s_bits), M, N, K, G,
+                              _ptr(r), nr, _ptr(c), nc, _ptr(out))
     return out
 
 

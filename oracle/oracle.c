@@ -24,6 +24,14 @@
  *       accumulator, no 16-bit weight copy is made.  The bias term follows the
  *       optional `bias` argument of mm_bf16_fp8 in §2 (public API).
  *
+ *   INT4 codebook: w[n, k] = LUT[q[n, k]] * S[k / G, n]      (NF4-style, LUT an input)
+ *       Source: "Low Bit Triton Kernels", the passage on choosing the 16 values of a
+ *       4-bit weight (uniform INT4 / non-uniform NF4 / FP4) and NF4's table lookup.
+ *
+ *   INT2 (W2A16):  w[n, k] = (q[n, k] - 2) * S[k / G, n], four codes per byte
+ *       Source: "Bitblas -- Mixed-Precision GEMM with the Ladder Compiler", hands-on
+ *       sequence item 6 (W2A16); the layout and offset are the readings stated below.
+ *
  *   FP4:           out[m, n] = alpha * sum_k A[m, k] * e2m1(W[n, k]) * e4m3(SF[n, k / 16])
  *       Source: "FlashInfer SM100 BF16 x FP4 GEMM" (PR #4466), §2: the weight is a
  *       uint8 [N, K/2] array (k = 2 * shape[1]) with one e4m3 scale factor per
@@ -310,6 +318,115 @@ ORACLE_API void oracle_gemm_w4a16(const uint16_t* A, int a_is_bf16, const uint8_
             out[i * ncols + j] = acc;
         }
         free(wrow);
+    }
+}
+
+/* ---------------------------------------------------------------- INT4 codebook */
+
+/* Non-uniform 4-bit format: the code picks one of 16 fp16 codebook values, which
+ * the group scale then multiplies ("Low Bit Triton Kernels", the passage on how
+ * the 16 values of a 4-bit weight are chosen -- a uniform grid (INT4), a
+ * non-uniform one (NF4) or a floating-point one (FP4) -- and on NF4's dequant
+ * being a table lookup held in registers).  The page prints no table, so the
+ * codebook is an input:
+ *   w[n, k] = LUT[q[n, k]] * S[k / G, n]      LUT fp16 [16], S fp16 [K/G][N]
+ * with the codes in the canonical INT4 packing.  LUT[q] * S has at most 11 + 11
+ * significant bits and stays inside the fp32 range, so its fp32 value is exact. */
+static double lut4_weight(const uint8_t* w, const uint16_t* s, const uint16_t* lut, int64_t N, int64_t K,
+                          int64_t G, int64_t n, int64_t k) {
+    int code = int4_code(w, K, n, k);
+    double entry = oracle_f16_to_double(lut[code]);
+    double scale = oracle_f16_to_double(s[(k / G) * N + n]);
+    return entry * scale;
+}
+
+ORACLE_API void oracle_dequant_int4_lut(const uint8_t* w, const uint16_t* s, const uint16_t* lut, int64_t N,
+                                        int64_t K, int64_t G, float* out) {
+    for (int64_t n = 0; n < N; ++n)
+        for (int64_t k = 0; k < K; ++k)
+            out[n * K + k] = (float)lut4_weight(w, s, lut, N, K, G, n, k);
+}
+
+ORACLE_API void oracle_gemm_w4a16_lut(const uint16_t* A, int a_is_bf16, const uint8_t* w, const uint16_t* s,
+                                      const uint16_t* lut, int64_t M, int64_t N, int64_t K, int64_t G,
+                                      const int64_t* rows, int64_t nrows, const int64_t* cols, int64_t ncols,
+                                      double* out) {
+    if (!rows) nrows = M;
+    if (!cols) ncols = N;
+#pragma omp parallel for schedule(dynamic, 1)
+    for (int64_t j = 0; j < ncols; ++j) {
+        const int64_t n = cols ? cols[j] : j;
+        double* wv = (double*)malloc((size_t)K * sizeof(double));
+        for (int64_t k = 0; k < K; ++k) wv[k] = lut4_weight(w, s, lut, N, K, G, n, k);
+        for (int64_t i = 0; i < nrows; ++i) {
+            const int64_t m = rows ? rows[i] : i;
+            double sum = 0.0;
+            for (int64_t k = 0; k < K; ++k) sum += act_value(A, a_is_bf16, m * K + k) * wv[k];
+            out[i * ncols + j] = sum;
+        }
+        free(wv);
+    }
+}
+
+/* ---------------------------------------------------------------- INT2 */
+
+/* W2A16: 2-bit codes ("Bitblas -- Mixed-Precision GEMM with the Ladder Compiler",
+ * hands-on sequence item 6: the W2A16 (INT2 weight) dtype combination, its
+ * accuracy loss and its speed-up).  The page gives no formula; the reading taken
+ * follows the INT4 format one size down: four codes per byte along K, code k at
+ * bits 2 (k % 4) .. 2 (k % 4) + 1 (the smallest k in the lowest bits), symmetric
+ * offset 2 (half the code range, as 8 is for INT4) and fp16 group scales:
+ *   w[n, k] = (q[n, k] - 2) * S[k / G, n]                 q in 0..3 */
+ORACLE_API void oracle_pack_int2(const uint8_t* q, int64_t N, int64_t K, uint8_t* w) {
+    for (int64_t n = 0; n < N; ++n)
+        for (int64_t j = 0; j < K / 4; ++j) {
+            uint8_t byte = 0;
+            for (int i = 0; i < 4; ++i) byte |= (uint8_t)((q[n * K + 4 * j + i] & 0x3) << (2 * i));
+            w[n * (K / 4) + j] = byte;
+        }
+}
+
+static int int2_code(const uint8_t* w, int64_t K, int64_t n, int64_t k) {
+    uint8_t byte = w[n * (K / 4) + k / 4];
+    return (byte >> (2 * (k % 4))) & 0x3;
+}
+
+ORACLE_API void oracle_unpack_int2(const uint8_t* w, int64_t N, int64_t K, uint8_t* q) {
+    for (int64_t n = 0; n < N; ++n)
+        for (int64_t k = 0; k < K; ++k) q[n * K + k] = (uint8_t)int2_code(w, K, n, k);
+}
+
+static double int2_weight(const uint8_t* w, const uint16_t* s, int64_t N, int64_t K, int64_t G, int64_t n,
+                          int64_t k) {
+    int q = int2_code(w, K, n, k);
+    double scale = oracle_f16_to_double(s[(k / G) * N + n]);
+    return (double)(q - 2) * scale;
+}
+
+/* (q - 2) * s has at most 2 + 11 significant bits: the fp32 value is exact. */
+ORACLE_API void oracle_dequant_int2(const uint8_t* w, const uint16_t* s, int64_t N, int64_t K, int64_t G,
+                                    float* out) {
+    for (int64_t n = 0; n < N; ++n)
+        for (int64_t k = 0; k < K; ++k) out[n * K + k] = (float)int2_weight(w, s, N, K, G, n, k);
+}
+
+ORACLE_API void oracle_gemm_w2a16(const uint16_t* A, int a_is_bf16, const uint8_t* w, const uint16_t* s,
+                                  int64_t M, int64_t N, int64_t K, int64_t G, const int64_t* rows, int64_t nrows,
+                                  const int64_t* cols, int64_t ncols, double* out) {
+    if (!rows) nrows = M;
+    if (!cols) ncols = N;
+#pragma omp parallel for schedule(dynamic, 1)
+    for (int64_t j = 0; j < ncols; ++j) {
+        const int64_t n = cols ? cols[j] : j;
+        double* wv = (double*)malloc((size_t)K * sizeof(double));
+        for (int64_t k = 0; k < K; ++k) wv[k] = int2_weight(w, s, N, K, G, n, k);
+        for (int64_t i = 0; i < nrows; ++i) {
+            const int64_t m = rows ? rows[i] : i;
+            double total = 0.0;
+            for (int64_t k = 0; k < K; ++k) total += wv[k] * act_value(A, a_is_bf16, m * K + k);
+            out[i * ncols + j] = total;
+        }
+        free(wv);
     }
 }
 

@@ -85,6 +85,33 @@ MUTATIONS = {
     "zp_ignored": (
         "return (double)(q - zero) * scale;",
         "return (double)(q - 8) * scale;"),
+    "lut_index_reversed": (
+        "double entry = oracle_f16_to_double(lut[code]);",
+        "double entry = oracle_f16_to_double(lut[15 - code]);"),
+    "lut_scale_dropped": (
+        "    return entry * scale;",
+        "    return entry;"),
+    "lut_scale_transposed": (
+        "double scale = oracle_f16_to_double(s[(k / G) * N + n]);\n    return entry * scale;",
+        "double scale = oracle_f16_to_double(s[n * (K / G) + k / G]);\n    return entry * scale;"),
+    "lut_A_transposed": (
+        "sum += act_value(A, a_is_bf16, m * K + k) * wv[k];",
+        "sum += act_value(A, a_is_bf16, (k * M + m) % (M * K)) * wv[k];"),
+    "int2_offset": (
+        "return (double)(q - 2) * scale;",
+        "return (double)(q - 1) * scale;"),
+    "int2_code_order": (
+        "return (byte >> (2 * (k % 4))) & 0x3;",
+        "return (byte >> (2 * (3 - k % 4))) & 0x3;"),
+    "int2_pack_order": (
+        "byte |= (uint8_t)((q[n * K + 4 * j + i] & 0x3) << (2 * i));",
+        "byte |= (uint8_t)((q[n * K + 4 * j + i] & 0x3) << (6 - 2 * i));"),
+    "int2_group_of_k": (
+        "double scale = oracle_f16_to_double(s[(k / G) * N + n]);\n    return (double)(q - 2) * scale;",
+        "double scale = oracle_f16_to_double(s[(k % (K / G)) * N + n]);\n    return (double)(q - 2) * scale;"),
+    "int2_A_transposed": (
+        "total += wv[k] * act_value(A, a_is_bf16, m * K + k);",
+        "total += wv[k] * act_value(A, a_is_bf16, (k * M + m) % (M * K));"),
     "pack_nibbles_swapped": (
         "w[n * (K / 2) + j] = (uint8_t)(lo | (hi << 4));",
         "w[n * (K / 2) + j] = (uint8_t)(hi | (lo << 4));"),

@@ -462,3 +462,130 @@ def test_zero_point_brute_force():
             want[m, n] = acc
     got = oracle.gemm_w4a16_zp(A, False, oracle.pack_int4(q.astype(np.uint8)), s, z, M, N, K, G)
     assert np.allclose(got, want, rtol=1e-12, atol=1e-12)
+
+
+# ------------------------------------------------------------- INT4 codebook (NF4-style)
+
+def test_codebook_worked_example():
+    g = _golden("int4_codebook_worked_example.json")
+    q = np.array(g["q"], dtype=np.uint8)
+    w = np.array(g["packed"], dtype=np.uint8)
+    assert np.array_equal(oracle.pack_int4(q), w)
+    s = _f16_bits(g["scales"])
+    lut = _f16_bits(g["lut"])
+    assert oracle.dequant_int4_lut(w, s, lut, g["K"], g["G"]).astype(np.float64).tolist() == g["w"]
+    A = _f16_bits(g["A"])
+    assert oracle.gemm_w4a16_lut(A, False, w, s, lut, g["M"], g["N"], g["K"], g["G"]).tolist() == g["out"]
+
+
+def test_codebook_of_the_uniform_grid_is_the_symmetric_format():
+    # LUT[q] = q - 8 turns the codebook format into the symmetric INT4 format
+    rng = np.random.default_rng(330)
+    M, N, K, G = 3, 24, 256, 32
+    w = rng.integers(0, 256, size=(N, K // 2), dtype=np.uint8)
+    s = _f16_bits(rng.uniform(0.005, 0.02, size=(K // G, N)))
+    A = _f16_bits(rng.standard_normal((M, K)))
+    lut = _f16_bits(np.arange(16) - 8.0)
+    assert np.array_equal(oracle.dequant_int4_lut(w, s, lut, K, G), oracle.dequant_int4(w, s, K, G))
+    for bf in (False, True):
+        Ab = synth.activations(M, K, "bf16", 331) if bf else A
+        assert np.array_equal(oracle.gemm_w4a16_lut(Ab, bf, w, s, lut, M, N, K, G),
+                              oracle.gemm_w4a16(Ab, bf, w, s, M, N, K, G))
+
+
+def test_codebook_brute_force():
+    # a pure-Python triple loop, a random table and scales varying per group and row
+    rng = np.random.default_rng(332)
+    M, N, K, G = 2, 5, 64, 32
+    q = rng.integers(0, 16, size=(N, K))
+    lut = synth.random_codebook(333)
+    lutd = lut.view(np.float16).astype(np.float64)
+    s = _f16_bits(rng.uniform(0.01, 0.1, size=(K // G, N)))
+    sd = s.view(np.float16).astype(np.float64)
+    A = _f16_bits(rng.standard_normal((M, K)))
+    Ad = A.view(np.float16).astype(np.float64)
+    want = np.zeros((M, N))
+    for m in range(M):
+        for n in range(N):
+            acc = 0.0
+            for k in range(K):
+                acc += Ad[m, k] * lutd[q[n, k]] * sd[k // G, n]
+            want[m, n] = acc
+    got = oracle.gemm_w4a16_lut(A, False, oracle.pack_int4(q.astype(np.uint8)), s, lut, M, N, K, G)
+    assert np.allclose(got, want, rtol=1e-12, atol=1e-12)
+
+
+def test_codebook_identity_activations_return_the_weight():
+    # A = I: out = w^T exactly (one non-zero product per output)
+    rng = np.random.default_rng(334)
+    N, K, G = 8, 64, 32
+    w = rng.integers(0, 256, size=(N, K // 2), dtype=np.uint8)
+    s = _f16_bits(rng.uniform(0.005, 0.02, size=(K // G, N)))
+    lut = synth.normal_quantile_codebook()
+    A = _f16_bits(np.eye(K))
+    out = oracle.gemm_w4a16_lut(A, False, w, s, lut, K, N, K, G)
+    assert np.array_equal(out, oracle.dequant_int4_lut(w, s, lut, K, G).astype(np.float64).T)
+
+
+def test_normal_quantile_codebook_shape():
+    # the generator's table: 16 ascending fp16 values in [-1, 1] with an exact zero
+    v = synth.normal_quantile_codebook().view(np.float16).astype(np.float64)
+    assert v.shape == (16,) and np.all(np.diff(v) > 0)
+    assert v[0] == -1.0 and v[15] == 1.0 and v[7] == 0.0
+
+
+# ------------------------------------------------------------- INT2 (W2A16)
+
+def test_int2_worked_example():
+    g = _golden("int2_worked_example.json")
+    q = np.array(g["q"], dtype=np.uint8)
+    w = oracle.pack_int2(q)
+    assert w.tolist() == g["packed"]
+    assert np.array_equal(oracle.unpack_int2(w, g["K"]), q)
+    s = _f16_bits(g["scales"])
+    assert oracle.dequant_int2(w, s, g["K"], g["G"]).astype(np.float64).tolist() == g["w"]
+    A = _f16_bits(g["A"])
+    assert oracle.gemm_w2a16(A, False, w, s, g["M"], g["N"], g["K"], g["G"]).tolist() == g["out"]
+
+
+def test_int2_pack_round_trip():
+    rng = np.random.default_rng(340)
+    q = rng.integers(0, 4, size=(7, 96), dtype=np.uint8)
+    w = oracle.pack_int2(q)
+    assert w.shape == (7, 24)
+    assert np.array_equal(oracle.unpack_int2(w, 96), q)
+    # every byte value decodes to four codes that re-pack to it
+    allb = np.arange(256, dtype=np.uint8).reshape(1, 256)
+    assert np.array_equal(oracle.pack_int2(oracle.unpack_int2(allb, 1024)), allb)
+
+
+def test_int2_is_int4_shifted_by_six():
+    # an INT2 code q has the value of the INT4 code q + 6: (q + 6) - 8 = q - 2
+    rng = np.random.default_rng(341)
+    M, N, K, G = 3, 16, 128, 32
+    q = rng.integers(0, 4, size=(N, K), dtype=np.uint8)
+    s = _f16_bits(rng.uniform(0.005, 0.02, size=(K // G, N)))
+    A = _f16_bits(rng.standard_normal((M, K)))
+    w2 = oracle.pack_int2(q)
+    w4 = oracle.pack_int4((q + 6).astype(np.uint8))
+    assert np.array_equal(oracle.dequant_int2(w2, s, K, G), oracle.dequant_int4(w4, s, K, G))
+    assert np.array_equal(oracle.gemm_w2a16(A, False, w2, s, M, N, K, G), oracle.gemm_w4a16(A, False, w4, s, M, N, K, G))
+
+
+def test_int2_brute_force():
+    rng = np.random.default_rng(342)
+    M, N, K, G = 2, 5, 64, 32
+    q = rng.integers(0, 4, size=(N, K))
+    s = _f16_bits(rng.uniform(0.01, 0.1, size=(K // G, N)))
+    sd = s.view(np.float16).astype(np.float64)
+    A = _f16_bits(rng.standard_normal((M, K)))
+    Ad = A.view(np.float16).astype(np.float64)
+    want = np.zeros((M, N))
+    for m in range(M):
+        for n in range(N):
+            acc = 0.0
+            for k in range(K):
+                acc += Ad[m, k] * (int(q[n, k]) - 2) * sd[k // G, n]
+            want[m, n] = acc
+    got = oracle.gemm_w2a16(A, False, oracle.pack_int2(q.astype(np.uint8)), s, M, N, K, G)
+    assert np.allclose(got, want, rtol=1e-12, atol=1e-12)

@@ -14,6 +14,9 @@ measure:
   group scales ~ U[0.005, 0.02] rounded to fp16, laid out [K/G, N].
 * FP8 W8A16 -- activations ~ N(0, 1) in bf16; a weight W ~ N(0, 0.02) is encoded
   as e4m3(clamp(W / s, +-448)) with one per-tensor fp32 scale s = max|W| / 448.
+* INT4 codebook -- INT4 codes and scales as above; the 16-entry fp16 table is an
+  NF4-style normal-quantile codebook or 16 draws from N(0, 1).
+* INT2 W2A16 -- codes uniform over 0..3, four per byte along K; scales as INT4.
 * BF16 x FP4 -- activations ~ N(0, 1) in bf16; e2m1 codes uniform over all 16
   values, two per byte along K; one e4m3 block scale ~ U[0.25, 2] per 16 values
   along K, laid out [N, K/16]; global alpha = 0.01.
@@ -81,6 +84,42 @@ def int4_weights(N: int, K: int, G: int, seed: int, scale_lo: float = 0.005,
 def int4_zeros(N: int, K: int, G: int, seed: int) -> np.ndarray:
     """Zero points uint8 [K/G, N], uniform over the codes 0..15."""
     return _rng(seed).integers(0, 16, size=(K // G, N), dtype=np.uint8)
+
+
+def normal_quantile_codebook() -> np.ndarray:
+    """An NF4-style 16-entry codebook as fp16 bits, ascending: quantiles of N(0, 1)
+    at evenly spaced probabilities (7 below the median, 8 above, offset 0.03 from
+    the tails), an exact zero at index 7, scaled so the largest magnitude is 1.
+    The pages name NF4 as the non-uniform 4-bit choice but print no table; any 16
+    values are valid input to the codebook GEMM."""
+    from scipy.special import ndtri
+    neg = ndtri(np.linspace(0.03, 0.5, 8)[:-1])
+    pos = ndtri(np.linspace(0.5, 0.97, 9)[1:])
+    v = np.concatenate([neg / -neg[0], [0.0], pos / pos[-1]]).astype(np.float32)
+    return _to_bits(v, "f16")
+
+
+def random_codebook(seed: int) -> np.ndarray:
+    """16 codebook entries ~ N(0, 1) as fp16 bits (an arbitrary table)."""
+    return _to_bits(_rng(seed).standard_normal(16, dtype=np.float32), "f16")
+
+
+@dataclass
+class Int2Weights:
+    w: np.ndarray        # uint8 [N, K/4], canonical: code k at bits 2 (k % 4)
+    s: np.ndarray        # uint16 fp16 bits [K/G, N]
+    N: int
+    K: int
+    G: int
+
+
+def int2_weights(N: int, K: int, G: int, seed: int, scale_lo: float = 0.005,
+                 scale_hi: float = 0.02) -> Int2Weights:
+    """Codes uniform over 0..3, four per byte along K (so bytes uniform over 0..255)."""
+    rng = _rng(seed)
+    w = rng.integers(0, 256, size=(N, K // 4), dtype=np.uint8)
+    s = rng.uniform(scale_lo, scale_hi, size=(K // G, N)).astype(np.float32)
+    return Int2Weights(w=w, s=_to_bits(s, "f16"), N=N, K=K, G=G)
 
 
 @dataclass
