@@ -372,6 +372,7 @@ def run_ours(args, rank, world, local_rank):
     # and bf16 activations, the bias epilogue, and FP4 at the FP4 page's own shape
     fp8_fp4 = []
     zero_point = []
+    codebook_int2 = []
     if not args.skip_prefill:
         flush = torch.empty(512 << 20, dtype=torch.uint8, device=dev)
 
@@ -458,6 +459,31 @@ def run_ours(args, rank, world, local_rank):
                       {"G": Gz, "kernel": plan["kernel"]}, into=zero_point)
                 del wsx
             del Ax, wkz, skz, zkz, outx
+        # codebook INT4 (NF4-style table) and INT2 W2A16 on the tile kernels
+        for (M, N, K, Gc) in [(16, 4096, 4096, 128), (4096, 4096, 4096, 128), (8192, 8192, 8192, 128)]:
+            seed = 7000 + M
+            Ax = torch.from_numpy(synth.activations(M, K, "f16", seed).view(np.int16)).to(dev).view(torch.float16)
+            outx = torch.empty((M, N), dtype=torch.float16, device=dev)
+            io = M * K * 2 + M * N * 2 + (K // Gc) * N * 2
+            wc = synth.int4_weights(N, K, Gc, seed + 1)
+            s_dev = torch.from_numpy(wc.s.view(np.int16)).to(dev).view(torch.float16)
+            wkc, skc = wq.wq_pack_int4(torch.from_numpy(wc.w).to(dev), s_dev, N, K, Gc)
+            lut = torch.from_numpy(synth.normal_quantile_codebook().view(np.int16)).to(dev).view(torch.float16)
+            plan = wq.get_plan(wq.WQ_OP_W4A16_LUT, wq.WQ_F16, M, N, K, Gc)
+            wsx = torch.zeros(plan["ws_bytes"] + 16, dtype=torch.uint8, device=dev)
+            us = time_call(lambda: wq.wq_gemm_w4a16_lut(Ax, wkc, skc, lut, N, K, Gc, out=outx, ws=wsx))
+            entry("w4a16_lut", M, N, K, "f16", us, N * K // 2 + io + 32, {"G": Gc, "kernel": plan["kernel"]},
+                  into=codebook_int2)
+            del wkc, skc, wsx
+            w2 = synth.int2_weights(N, K, Gc, seed + 2)
+            w2d = torch.from_numpy(w2.w).to(dev)
+            sk2 = wq.wq_pack_int2_scales(torch.from_numpy(w2.s.view(np.int16)).to(dev).view(torch.float16), N, K, Gc)
+            plan = wq.get_plan(wq.WQ_OP_W2A16, wq.WQ_F16, M, N, K, Gc)
+            wsx = torch.zeros(plan["ws_bytes"] + 16, dtype=torch.uint8, device=dev)
+            us = time_call(lambda: wq.wq_gemm_w2a16(Ax, w2d, sk2, N, K, Gc, out=outx, ws=wsx))
+            entry("w2a16", M, N, K, "f16", us, N * K // 4 + io, {"G": Gc, "kernel": plan["kernel"]},
+                  into=codebook_int2)
+            del Ax, w2d, sk2, wsx, outx, s_dev
         del flush
 
     # ---------------- quantiser extra: fp16 W (11008 x 4096) -> INT4 codes + fp16 scales
@@ -533,6 +559,7 @@ def run_ours(args, rank, world, local_rank):
         "quantiser": quantiser,
         "fp8_fp4": fp8_fp4,
         "zero_point": zero_point,
+        "codebook_int2": codebook_int2,
         "e2e": {"value": round(e2e_value, 2), "unit": "GB/s", "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
                 "ms_per_step": round(e2e_s * 1e3, 4),
                 "how": "per step: pinned-host->device copy of every A, wq_gemm_w4a16 via the Python binding, "

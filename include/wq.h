@@ -49,7 +49,14 @@ typedef struct CUstream_st* wq_stream_t; /* same type as cudaStream_t */
 
 typedef enum { WQ_F16 = 0, WQ_BF16 = 1 } wq_dtype;
 
-typedef enum { WQ_OP_W4A16 = 0, WQ_OP_FP8 = 1, WQ_OP_FP4 = 2, WQ_OP_W4A16_ZP = 3 } wq_op;
+typedef enum {
+    WQ_OP_W4A16 = 0,
+    WQ_OP_FP8 = 1,
+    WQ_OP_FP4 = 2,
+    WQ_OP_W4A16_ZP = 3,
+    WQ_OP_W4A16_LUT = 4,
+    WQ_OP_W2A16 = 5
+} wq_op;
 
 typedef enum {
     WQ_OK = 0,
@@ -170,6 +177,69 @@ wq_status wq_pack_int4_zeros(const uint8_t* z_canon, int64_t N, int64_t K, int32
 wq_status wq_gemm_w4a16_zp(const void* A, wq_dtype a_dtype, const uint8_t* w_kernel, const void* s_kernel,
                            const uint8_t* z_kernel, int64_t M, int64_t N, int64_t K, int32_t G, void* out, void* ws,
                            size_t ws_bytes, wq_stream_t stream);
+
+/* ------------------------------------------------------------- INT4 codebook */
+
+/* Codebook (NF4-style) INT4: w[n][k] = LUT[q[n][k]] * S[k/G][n], the 4-bit code
+ * selecting one of 16 fp16 values.  "Low Bit Triton Kernels" (GPU MODE lecture 34),
+ * the passage on choosing the 16 values of a 4-bit weight: a uniform grid (INT4), a
+ * non-uniform one (NF4) or a floating-point one (FP4), NF4's dequant being a lookup
+ * table held in registers at about twice the instructions of the INT4 shift-and-mask.
+ * The page prints no table, so the table is an argument: any 16 finite fp16 values
+ * (with LUT[q] = q - 8 this is the symmetric format).  Codes and scales pack with
+ * wq_pack_int4 as for W4A16.
+ *
+ * W4A16 GEMM with a codebook: out[M][N] = A[M][K] . (LUT[q] * S)^T.  Arguments as
+ * for wq_gemm_w4a16 plus lut: 16 fp16 values in device memory, 16-byte aligned (read
+ * as two 16-byte vectors); the workspace is sized for WQ_OP_W4A16_LUT.  The operand
+ * is RN(LUT[q] * s) in the type of A (the product of two fp16 values is exact in
+ * fp32), accumulated in fp32; every M runs on the tile kernels.  lut is read after
+ * the kernel waits for the kernel before it on the stream, so it may be written by
+ * that kernel. */
+wq_status wq_gemm_w4a16_lut(const void* A, wq_dtype a_dtype, const uint8_t* w_kernel, const void* s_kernel,
+                            const void* lut, int64_t M, int64_t N, int64_t K, int32_t G, void* out, void* ws,
+                            size_t ws_bytes, wq_stream_t stream);
+
+/* Debug export: the exact dequantized codebook weight LUT[q] * s as fp32 [N][K],
+ * read from the prepacked buffers (lut: 16 fp16 values, 2-byte aligned). */
+wq_status wq_debug_dequant_int4_lut(const uint8_t* w_kernel, const void* s_kernel, const void* lut, int64_t N,
+                                    int64_t K, int32_t G, float* w_f32, wq_stream_t stream);
+
+/* ------------------------------------------------------------------ INT2 */
+
+/* W2A16: w[n][k] = (q[n][k] - 2) * S[k/G][n], 2-bit codes q in 0..3.  "Bitblas --
+ * Mixed-Precision GEMM with the Ladder Compiler" (GPU MODE lecture 33), hands-on
+ * sequence item 6, names the W2A16 (INT2 weight) combination without a formula; the
+ * reading taken is the INT4 format one size down: four codes per byte along K with
+ * code k at bits 2 (k % 4) .. 2 (k % 4) + 1 of byte k / 4 (w_canon uint8 [N][K/4]),
+ * symmetric offset 2, fp16 group scales S[K/G][N].  The codes are read canonical
+ * (TMA rows of K/4 bytes); only the scales are reordered.
+ *
+ * Size of the kernel-order scale buffer (N padded to 128, K to 256).  Requirements:
+ * N > 0, K % 64 == 0 (16-byte code rows), K % G == 0, G in {32, 64, 128, 256}.
+ * Host only. */
+wq_status wq_int2_packed_scales_bytes(int64_t N, int64_t K, int32_t G, size_t* s_bytes);
+
+/* Layout transform of the scales: s_canon fp16 [K/G][N] (2-byte aligned) to s_kernel
+ * [N/128][Kp/G][128] (16-byte aligned, wq_int2_packed_scales_bytes long), padding
+ * zero.  Ends with an ordinary launch, as wq_pack_int4. */
+wq_status wq_pack_int2_scales(const void* s_canon, int64_t N, int64_t K, int32_t G, void* s_kernel,
+                              wq_stream_t stream);
+
+/* Debug export: the exact dequantized weight (q - 2) * s as fp32 [N][K] (at most 13
+ * significant bits), from the canonical codes and the packed scales. */
+wq_status wq_debug_dequant_int2(const uint8_t* w_canon, const void* s_kernel, int64_t N, int64_t K, int32_t G,
+                                float* w_f32, wq_stream_t stream);
+
+/* W2A16 GEMM: out[M][N] (type of A) = A[M][K] . ((q - 2) * S)^T.  A: a_dtype [M][K],
+ * 16-byte aligned.  w_canon: uint8 [N][K/4], 16-byte aligned.  s_kernel: output of
+ * wq_pack_int2_scales.  out: 16-byte aligned, N % 8 == 0.  ws: workspace sized for
+ * WQ_OP_W2A16 (the rules of wq_gemm_w4a16's workspace apply).  The operand is
+ * RN((q - 2) * s) in the type of A, accumulated in fp32; every M runs on the tile
+ * kernels.  Every input is read after the kernel waits for the kernel before it on
+ * the stream. */
+wq_status wq_gemm_w2a16(const void* A, wq_dtype a_dtype, const uint8_t* w_canon, const void* s_kernel, int64_t M,
+                        int64_t N, int64_t K, int32_t G, void* out, void* ws, size_t ws_bytes, wq_stream_t stream);
 
 /* ------------------------------------------------------------------ FP8 */
 

@@ -19,7 +19,7 @@ _HERE = os.path.dirname(os.path.abspath(__file__))
 LIB_PATH = os.path.join(_HERE, "libwq.so")
 
 WQ_F16, WQ_BF16 = 0, 1
-WQ_OP_W4A16, WQ_OP_FP8, WQ_OP_FP4, WQ_OP_W4A16_ZP = 0, 1, 2, 3
+WQ_OP_W4A16, WQ_OP_FP8, WQ_OP_FP4, WQ_OP_W4A16_ZP, WQ_OP_W4A16_LUT, WQ_OP_W2A16 = 0, 1, 2, 3, 4, 5
 WQ_KERNEL_TILE, WQ_KERNEL_DECODE, WQ_KERNEL_TILE_PAIR = 0, 1, 2
 STATUS_NAMES = {
     0: "WQ_OK", 1: "WQ_ERR_NULL", 2: "WQ_ERR_SHAPE", 3: "WQ_ERR_GROUP", 4: "WQ_ERR_MISALIGNED",
@@ -63,6 +63,13 @@ _SIGNATURES = {
     "wq_pack_int4_zeros": (ctypes.c_int, [_vp, _i64, _i64, _i32, _vp, _vp]),
     "wq_gemm_w4a16_zp": (ctypes.c_int, [_vp, ctypes.c_int, _vp, _vp, _vp, _i64, _i64, _i64, _i32, _vp, _vp, _sz,
                                         _vp]),
+    "wq_gemm_w4a16_lut": (ctypes.c_int, [_vp, ctypes.c_int, _vp, _vp, _vp, _i64, _i64, _i64, _i32, _vp, _vp, _sz,
+                                         _vp]),
+    "wq_debug_dequant_int4_lut": (ctypes.c_int, [_vp, _vp, _vp, _i64, _i64, _i32, _vp, _vp]),
+    "wq_int2_packed_scales_bytes": (ctypes.c_int, [_i64, _i64, _i32, ctypes.POINTER(_sz)]),
+    "wq_pack_int2_scales": (ctypes.c_int, [_vp, _i64, _i64, _i32, _vp, _vp]),
+    "wq_debug_dequant_int2": (ctypes.c_int, [_vp, _vp, _i64, _i64, _i32, _vp, _vp]),
+    "wq_gemm_w2a16": (ctypes.c_int, [_vp, ctypes.c_int, _vp, _vp, _i64, _i64, _i64, _i32, _vp, _vp, _sz, _vp]),
     "wq_debug_dequant_fp8": (ctypes.c_int, [_vp, _i64, _i64, ctypes.c_int, _vp, _vp]),
     "wq_gemm_w8a16_fp8": (ctypes.c_int, [_vp, ctypes.c_int, _vp, _vp, _vp, _i64, _i64, _i64, _vp, _vp, _sz, _vp]),
     "wq_fp4_packed_sf_bytes": (ctypes.c_int, [_i64, _i64, ctypes.POINTER(_sz)]),
@@ -271,6 +278,82 @@ def wq_gemm_w4a16_zp(A: torch.Tensor, w_kernel: torch.Tensor, s_kernel: torch.Te
         ws_bytes = ws.numel() * ws.element_size()
     _check(lib().wq_gemm_w4a16_zp(_ptr(A), a_dtype, _ptr(w_kernel), _ptr(s_kernel), _ptr(z_kernel), M, N, K, G,
                                   _ptr(out), _ptr(ws), ws_bytes, _stream(A)), "wq_gemm_w4a16_zp")
+    return out
+
+
+def wq_gemm_w4a16_lut(A: torch.Tensor, w_kernel: torch.Tensor, s_kernel: torch.Tensor, lut: torch.Tensor,
+                      N: int, K: int, G: int, out: torch.Tensor = None, ws: torch.Tensor = None) -> torch.Tensor:
+    """out[M, N] = A[M, K] . (LUT[q] * S)^T with a 16-entry fp16 codebook, out in the dtype of A."""
+    a_dtype = _adtype(A)
+    _need(A, "A", A.dtype)
+    if A.dim() != 2 or A.shape[1] != K:
+        raise ValueError(f"A must be [M, {K}]")
+    M = A.shape[0]
+    _need(w_kernel, "w_kernel", torch.uint8)
+    _need(s_kernel, "s_kernel", torch.float16)
+    _need(lut, "lut", torch.float16, (16,))
+    if out is None:
+        out = torch.empty((M, N), dtype=A.dtype, device=A.device)
+    _need(out, "out", A.dtype, (M, N))
+    if ws is None:
+        ws, ws_bytes = workspace(WQ_OP_W4A16_LUT, a_dtype, M, N, K, G, A.device)
+    else:
+        ws_bytes = ws.numel() * ws.element_size()
+    _check(lib().wq_gemm_w4a16_lut(_ptr(A), a_dtype, _ptr(w_kernel), _ptr(s_kernel), _ptr(lut), M, N, K, G,
+                                   _ptr(out), _ptr(ws), ws_bytes, _stream(A)), "wq_gemm_w4a16_lut")
+    return out
+
+
+def wq_debug_dequant_int4_lut(w_kernel: torch.Tensor, s_kernel: torch.Tensor, lut: torch.Tensor, N: int, K: int,
+                              G: int) -> torch.Tensor:
+    _need(lut, "lut", torch.float16, (16,))
+    out = torch.empty((N, K), dtype=torch.float32, device=w_kernel.device)
+    _check(lib().wq_debug_dequant_int4_lut(_ptr(w_kernel), _ptr(s_kernel), _ptr(lut), N, K, G, _ptr(out),
+                                           _stream(w_kernel)), "wq_debug_dequant_int4_lut")
+    return out
+
+
+def wq_int2_packed_scales_bytes(N: int, K: int, G: int) -> int:
+    sb = _sz(0)
+    _check(lib().wq_int2_packed_scales_bytes(N, K, G, ctypes.byref(sb)), "wq_int2_packed_scales_bytes")
+    return sb.value
+
+
+def wq_pack_int2_scales(s_canon: torch.Tensor, N: int, K: int, G: int) -> torch.Tensor:
+    """fp16 scales [K/G, N] -> the kernel-order scale buffer of the INT2 GEMM."""
+    _need(s_canon, "s_canon", torch.float16, (K // G, N))
+    sk = torch.empty(wq_int2_packed_scales_bytes(N, K, G) // 2, dtype=torch.float16, device=s_canon.device)
+    _check(lib().wq_pack_int2_scales(_ptr(s_canon), N, K, G, _ptr(sk), _stream(s_canon)), "wq_pack_int2_scales")
+    return sk
+
+
+def wq_debug_dequant_int2(w_canon: torch.Tensor, s_kernel: torch.Tensor, N: int, K: int, G: int) -> torch.Tensor:
+    _need(w_canon, "w_canon", torch.uint8, (N, K // 4))
+    out = torch.empty((N, K), dtype=torch.float32, device=w_canon.device)
+    _check(lib().wq_debug_dequant_int2(_ptr(w_canon), _ptr(s_kernel), N, K, G, _ptr(out), _stream(w_canon)),
+           "wq_debug_dequant_int2")
+    return out
+
+
+def wq_gemm_w2a16(A: torch.Tensor, w_canon: torch.Tensor, s_kernel: torch.Tensor, N: int, K: int, G: int,
+                  out: torch.Tensor = None, ws: torch.Tensor = None) -> torch.Tensor:
+    """out[M, N] = A[M, K] . ((q - 2) * S)^T, 2-bit codes [N, K/4], out in the dtype of A."""
+    a_dtype = _adtype(A)
+    _need(A, "A", A.dtype)
+    if A.dim() != 2 or A.shape[1] != K:
+        raise ValueError(f"A must be [M, {K}]")
+    M = A.shape[0]
+    _need(w_canon, "w_canon", torch.uint8, (N, K // 4))
+    _need(s_kernel, "s_kernel", torch.float16)
+    if out is None:
+        out = torch.empty((M, N), dtype=A.dtype, device=A.device)
+    _need(out, "out", A.dtype, (M, N))
+    if ws is None:
+        ws, ws_bytes = workspace(WQ_OP_W2A16, a_dtype, M, N, K, G, A.device)
+    else:
+        ws_bytes = ws.numel() * ws.element_size()
+    _check(lib().wq_gemm_w2a16(_ptr(A), a_dtype, _ptr(w_canon), _ptr(s_kernel), M, N, K, G, _ptr(out), _ptr(ws),
+                               ws_bytes, _stream(A)), "wq_gemm_w2a16")
     return out
 
 

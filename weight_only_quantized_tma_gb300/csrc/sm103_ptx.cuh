@@ -386,6 +386,20 @@ __device__ __forceinline__ uint32_t lop3_and_or(uint32_t a, uint32_t mask, uint3
     asm("lop3.b32 %0, %1, %2, %3, 0xEA;" : "=r"(r) : "r"(a), "r"(mask), "r"(magic));
     return r;
 }
+// Byte permute in PTX's default mode: byte i of the result is byte (c >> 4i) & 7 of
+// {b:a} (a = bytes 0-3), or, when bit 3 of that selector nibble is set, that byte's
+// sign bit copied into all 8 bits.
+__device__ __forceinline__ uint32_t prmt(uint32_t a, uint32_t b, uint32_t c) {
+    uint32_t r;
+    asm("prmt.b32 %0, %1, %2, %3;" : "=r"(r) : "r"(a), "r"(b), "r"(c));
+    return r;
+}
+// (a & ~m) | (b & m): bitwise select
+__device__ __forceinline__ uint32_t lop3_select(uint32_t a, uint32_t b, uint32_t m) {
+    uint32_t r;
+    asm("lop3.b32 %0, %1, %2, %3, 0xD8;" : "=r"(r) : "r"(a), "r"(b), "r"(m));   // 0xD8 = (F0 & ~AA) | (CC & AA)
+    return r;
+}
 // Two fp32 -> bf16x2 (lo from `lo`), round to nearest even.
 __device__ __forceinline__ uint32_t f32x2_to_bf16x2(float lo, float hi) {
     uint32_t r;

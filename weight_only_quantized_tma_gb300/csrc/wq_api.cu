@@ -114,30 +114,36 @@ bool get_config_uncached(int fmt, bool bf16, int bn, bool query, KernelConfig* c
     if (fmt == FMT_INT4 + 32) return config_int4_pair(bf16, query, cfg);
     if (fmt == FMT_FP8 + 32) return config_fp8_pair(bf16, query, cfg);
     if (fmt == FMT_FP4 + 32) return bf16 && config_fp4_pair(query, cfg);
+    if (fmt == FMT_LUT4 + 32) return config_lut4_pair(bf16, query, cfg);
+    if (fmt == FMT_INT2 + 32) return config_int2_pair(bf16, query, cfg);
     switch (fmt) {
         case FMT_INT4: return config_int4(bf16, bn, query, cfg);
         case FMT_FP8: return config_fp8(bf16, bn, query, cfg);
         case FMT_FP4: return config_fp4(bf16, bn, query, cfg);
+        case FMT_LUT4: return config_lut4(bf16, bn, query, cfg);
+        case FMT_INT2: return config_int2(bf16, bn, query, cfg);
     }
     return false;
 }
 
 // The device query behind a configuration (attributes, residency) is done once per
 // device and instantiation; later calls read the cached answer.
+// Slots: the tile formats 0 .. kNumFmts - 1, the W4A16 decode kernel, the pair kernels.
+constexpr int kCfgSlots = 2 * kNumFmts + 1;
 struct ConfigCache {
     std::mutex mu;
-    bool have[kMaxDevices][7][2][4] = {};
-    bool found[kMaxDevices][7][2][4] = {};
-    KernelConfig cfg[kMaxDevices][7][2][4];
+    bool have[kMaxDevices][kCfgSlots][2][4] = {};
+    bool found[kMaxDevices][kCfgSlots][2][4] = {};
+    KernelConfig cfg[kMaxDevices][kCfgSlots][2][4];
 };
 ConfigCache g_cfg_cache;
 
 bool get_config(int fmt, bool bf16, int bn, bool query, KernelConfig* cfg) {
     const int bi = bn == 16 ? 0 : bn == 64 ? 1 : bn == 128 ? 2 : bn == 256 ? 3 : -1;
-    // slot 3: the W4A16 decode kernel, slots 4-6: the pair kernels (W4A16, FP8, FP4)
-    const int fi = fmt == FMT_INT4 + 16 ? 3 : fmt >= 32 ? 4 + (fmt - 32) : fmt;
+    const int fi = fmt == FMT_INT4 + 16 ? kNumFmts : fmt >= 32 ? kNumFmts + 1 + (fmt - 32) : fmt;
     int dev = 0;
-    if (!query || bi < 0 || fi < 0 || fi > 6 || cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices)
+    if (!query || bi < 0 || fi < 0 || fi >= kCfgSlots || cudaGetDevice(&dev) != cudaSuccess || dev < 0 ||
+        dev >= kMaxDevices)
         return get_config_uncached(fmt, bf16, bn, query, cfg);
     std::lock_guard<std::mutex> lock(g_cfg_cache.mu);
     const int b = bf16 ? 1 : 0;
@@ -272,7 +278,7 @@ wq_status make_plan(int fmt, bool bf16, int64_t M, int64_t N, int64_t K, int sms
     return WQ_OK;
 }
 
-int w_bits_of(int fmt) { return fmt == FMT_INT4 ? 4 : fmt == FMT_FP8 ? 8 : 4; }
+int w_bits_of(int fmt) { return fmt == FMT_FP8 ? 8 : fmt == FMT_INT2 ? 2 : 4; }
 
 wq_status plan_for(int fmt, bool bf16, int64_t M, int64_t N, int64_t K, Plan* plan, int G, bool allow_decode) {
     DeviceInfo* d = nullptr;
@@ -459,7 +465,21 @@ wq_status wq_debug_dequant_int4(const uint8_t* w_kernel, const void* s_kernel, i
     if (!aligned(w_kernel, 16) || !aligned(s_kernel, 16) || !aligned(w_f32, 4)) return WQ_ERR_MISALIGNED;
     DeviceInfo* d = nullptr;
     if ((st = device_info(&d)) != WQ_OK) return st;
-    return finish_launch(launch_dequant_int4(w_kernel, static_cast<const uint16_t*>(s_kernel), N, K, G, w_f32,
+    return finish_launch(launch_dequant_int4(w_kernel, static_cast<const uint16_t*>(s_kernel), nullptr, N, K, G,
+                                             w_f32, (cudaStream_t)stream));
+}
+
+wq_status wq_debug_dequant_int4_lut(const uint8_t* w_kernel, const void* s_kernel, const void* lut, int64_t N,
+                                    int64_t K, int32_t G, float* w_f32, wq_stream_t stream) {
+    if (!lut) return WQ_ERR_NULL;
+    wq_status st = check_pack_args(w_kernel, s_kernel, w_f32, w_f32, N, K, G);
+    if (st != WQ_OK) return st;
+    if (!aligned(w_kernel, 16) || !aligned(s_kernel, 16) || !aligned(w_f32, 4) || !aligned(lut, 2))
+        return WQ_ERR_MISALIGNED;
+    DeviceInfo* d = nullptr;
+    if ((st = device_info(&d)) != WQ_OK) return st;
+    return finish_launch(launch_dequant_int4(w_kernel, static_cast<const uint16_t*>(s_kernel),
+                                             static_cast<const uint16_t*>(lut), N, K, G, w_f32,
                                              (cudaStream_t)stream));
 }
 
@@ -505,14 +525,21 @@ wq_status wq_debug_dequant_fp8(const uint8_t* w_e4m3, int64_t N, int64_t K, wq_d
 wq_status wq_get_plan(wq_op op, wq_dtype a_dtype, int64_t M, int64_t N, int64_t K, int32_t G, wq_plan* plan,
                       size_t* ws_bytes) {
     if (M < 0 || N <= 0 || K <= 0 || M > kMaxDim || N > kMaxDim || K > kMaxDim) return WQ_ERR_SHAPE;
-    if (op != WQ_OP_W4A16 && op != WQ_OP_FP8 && op != WQ_OP_FP4 && op != WQ_OP_W4A16_ZP) return WQ_ERR_SHAPE;
-    const bool int4 = op == WQ_OP_W4A16 || op == WQ_OP_W4A16_ZP;
-    if (int4 && (!valid_group(G) || K % G != 0)) return WQ_ERR_GROUP;
+    int fmt = -1;
+    switch (op) {
+        case WQ_OP_W4A16: case WQ_OP_W4A16_ZP: fmt = FMT_INT4; break;
+        case WQ_OP_FP8: fmt = FMT_FP8; break;
+        case WQ_OP_FP4: fmt = FMT_FP4; break;
+        case WQ_OP_W4A16_LUT: fmt = FMT_LUT4; break;
+        case WQ_OP_W2A16: fmt = FMT_INT2; break;
+    }
+    if (fmt < 0) return WQ_ERR_SHAPE;
+    const bool grouped = group_scaled(fmt);
+    if (grouped && (!valid_group(G) || K % G != 0)) return WQ_ERR_GROUP;
     if (a_dtype != WQ_F16 && a_dtype != WQ_BF16) return WQ_ERR_DTYPE;
     const bool bf16 = (op == WQ_OP_FP4) ? true : (a_dtype == WQ_BF16);
     Plan pl{};
-    wq_status st = plan_for(int4 ? FMT_INT4 : (int)op, bf16, M > 0 ? M : 1, N, K, &pl, int4 ? G : 0,
-                            op != WQ_OP_W4A16_ZP);
+    wq_status st = plan_for(fmt, bf16, M > 0 ? M : 1, N, K, &pl, grouped ? G : 0, op == WQ_OP_W4A16);
     if (st != WQ_OK) return st;
     if (plan) {
         plan->bn = pl.cfg.bn;
@@ -538,10 +565,12 @@ wq_status wq_workspace_bytes(wq_op op, wq_dtype a_dtype, int64_t M, int64_t N, i
     return wq_get_plan(op, a_dtype, M, N, K, G, nullptr, bytes);
 }
 
-// W4A16 with the symmetric zero point 8 (z_kernel null) or packed zero points.
+// W4A16 with the symmetric zero point 8 (z_kernel and lut null), packed zero points,
+// or a 16-entry codebook.  Only the symmetric format has the M <= 16 register kernel.
 static wq_status gemm_int4(const void* A, wq_dtype a_dtype, const uint8_t* w_kernel, const void* s_kernel,
-                           const uint8_t* z_kernel, int64_t M, int64_t N, int64_t K, int32_t G, void* out, void* ws,
-                           size_t ws_bytes, wq_stream_t stream) {
+                           const uint8_t* z_kernel, const uint16_t* lut, int64_t M, int64_t N, int64_t K, int32_t G,
+                           void* out, void* ws, size_t ws_bytes, wq_stream_t stream) {
+    const int fmt = lut ? FMT_LUT4 : FMT_INT4;
     if (M == 0 && N > 0 && K > 0) return WQ_OK;   // empty problem: A and out may be NULL
     if (!A || !w_kernel || !s_kernel || !out) return WQ_ERR_NULL;
     if (M < 0 || N <= 0 || K <= 0 || M > kMaxDim || N > kMaxDim || K > kMaxDim) return WQ_ERR_SHAPE;
@@ -549,7 +578,7 @@ static wq_status gemm_int4(const void* A, wq_dtype a_dtype, const uint8_t* w_ker
     if (!valid_group(G) || K % G != 0) return WQ_ERR_GROUP;
     if (a_dtype != WQ_F16 && a_dtype != WQ_BF16) return WQ_ERR_DTYPE;
     if (!aligned(A, 16) || !aligned(w_kernel, 16) || !aligned(s_kernel, 16) || !aligned(out, 16) ||
-        !aligned(z_kernel, 16))
+        !aligned(z_kernel, 16) || !aligned(lut, 16))
         return WQ_ERR_MISALIGNED;
     DeviceInfo* d = nullptr;
     wq_status st = device_info(&d);
@@ -557,7 +586,7 @@ static wq_status gemm_int4(const void* A, wq_dtype a_dtype, const uint8_t* w_ker
     if (M == 0) return WQ_OK;
     const bool bf16 = a_dtype == WQ_BF16;
     Plan pl{};
-    if ((st = make_plan(FMT_INT4, bf16, M, N, K, d->sms, 4, &pl, G, z_kernel == nullptr)) != WQ_OK) return st;
+    if ((st = make_plan(fmt, bf16, M, N, K, d->sms, 4, &pl, G, z_kernel == nullptr)) != WQ_OK) return st;
     if ((st = check_ws(pl, ws, ws_bytes)) != WQ_OK) return st;
     GemmParams gp;
     std::memset(&gp, 0, sizeof(gp));
@@ -569,6 +598,7 @@ static wq_status gemm_int4(const void* A, wq_dtype a_dtype, const uint8_t* w_ker
     gp.w = w_kernel;
     gp.sc = static_cast<const uint8_t*>(s_kernel);
     gp.zp = z_kernel;
+    gp.lut = lut;
     gp.G = G;
     gp.g_shift = G == 32 ? 5 : G == 64 ? 6 : G == 128 ? 7 : 8;
     const int64_t Kp = round_up(K, KPAD_INT4);
@@ -576,13 +606,16 @@ static wq_status gemm_int4(const void* A, wq_dtype a_dtype, const uint8_t* w_ker
     gp.nchunks_pad = (int)(Kp / 32);
     fill_common(gp, pl, M, N, K, out, ws, d->status);
     if (pl.decode) return finish_launch(launch_gemm_int4_decode(gp, bf16, pl.grid, (cudaStream_t)stream));
+    if (fmt == FMT_LUT4)
+        return finish_launch(pl.pair ? launch_gemm_lut4_pair(gp, bf16, pl.grid, (cudaStream_t)stream)
+                                     : launch_gemm_lut4(gp, bf16, pl.cfg.bn, pl.grid, (cudaStream_t)stream));
     if (pl.pair) return finish_launch(launch_gemm_int4_pair(gp, bf16, pl.grid, (cudaStream_t)stream));
     return finish_launch(launch_gemm_int4(gp, bf16, pl.cfg.bn, pl.grid, (cudaStream_t)stream));
 }
 
 wq_status wq_gemm_w4a16(const void* A, wq_dtype a_dtype, const uint8_t* w_kernel, const void* s_kernel, int64_t M,
                         int64_t N, int64_t K, int32_t G, void* out, void* ws, size_t ws_bytes, wq_stream_t stream) {
-    return gemm_int4(A, a_dtype, w_kernel, s_kernel, nullptr, M, N, K, G, out, ws, ws_bytes, stream);
+    return gemm_int4(A, a_dtype, w_kernel, s_kernel, nullptr, nullptr, M, N, K, G, out, ws, ws_bytes, stream);
 }
 
 wq_status wq_gemm_w4a16_zp(const void* A, wq_dtype a_dtype, const uint8_t* w_kernel, const void* s_kernel,
@@ -590,7 +623,88 @@ wq_status wq_gemm_w4a16_zp(const void* A, wq_dtype a_dtype, const uint8_t* w_ker
                            size_t ws_bytes, wq_stream_t stream) {
     if (M == 0 && N > 0 && K > 0) return WQ_OK;
     if (!z_kernel) return WQ_ERR_NULL;
-    return gemm_int4(A, a_dtype, w_kernel, s_kernel, z_kernel, M, N, K, G, out, ws, ws_bytes, stream);
+    return gemm_int4(A, a_dtype, w_kernel, s_kernel, z_kernel, nullptr, M, N, K, G, out, ws, ws_bytes, stream);
+}
+
+wq_status wq_gemm_w4a16_lut(const void* A, wq_dtype a_dtype, const uint8_t* w_kernel, const void* s_kernel,
+                            const void* lut, int64_t M, int64_t N, int64_t K, int32_t G, void* out, void* ws,
+                            size_t ws_bytes, wq_stream_t stream) {
+    if (M == 0 && N > 0 && K > 0) return WQ_OK;
+    if (!lut) return WQ_ERR_NULL;
+    return gemm_int4(A, a_dtype, w_kernel, s_kernel, nullptr, static_cast<const uint16_t*>(lut), M, N, K, G, out,
+                     ws, ws_bytes, stream);
+}
+
+// ------------------------------------------------------------------ INT2
+
+static wq_status check_int2_shape(int64_t N, int64_t K, int32_t G) {
+    if (N <= 0 || K <= 0 || N > kMaxDim || K > kMaxDim || K % 64 != 0) return WQ_ERR_SHAPE;
+    if (!valid_group(G) || K % G != 0) return WQ_ERR_GROUP;
+    return WQ_OK;
+}
+
+wq_status wq_int2_packed_scales_bytes(int64_t N, int64_t K, int32_t G, size_t* s_bytes) {
+    wq_status st = check_int2_shape(N, K, G);
+    if (st != WQ_OK) return st;
+    if (s_bytes) *s_bytes = (size_t)(round_up(N, TILE_N) * (round_up(K, KPAD_INT4) / G) * 2);
+    return WQ_OK;
+}
+
+wq_status wq_pack_int2_scales(const void* s_canon, int64_t N, int64_t K, int32_t G, void* s_kernel,
+                              wq_stream_t stream) {
+    if (!s_canon || !s_kernel) return WQ_ERR_NULL;
+    wq_status st = check_int2_shape(N, K, G);
+    if (st != WQ_OK) return st;
+    if (!aligned(s_canon, 2) || !aligned(s_kernel, 16)) return WQ_ERR_MISALIGNED;
+    DeviceInfo* d = nullptr;
+    if ((st = device_info(&d)) != WQ_OK) return st;
+    return finish_launch(launch_pack_group_scales(static_cast<const uint16_t*>(s_canon), N, K, G,
+                                                  static_cast<uint16_t*>(s_kernel), (cudaStream_t)stream));
+}
+
+wq_status wq_debug_dequant_int2(const uint8_t* w_canon, const void* s_kernel, int64_t N, int64_t K, int32_t G,
+                                float* w_f32, wq_stream_t stream) {
+    if (!w_canon || !s_kernel || !w_f32) return WQ_ERR_NULL;
+    wq_status st = check_int2_shape(N, K, G);
+    if (st != WQ_OK) return st;
+    if (!aligned(s_kernel, 16) || !aligned(w_f32, 4)) return WQ_ERR_MISALIGNED;
+    DeviceInfo* d = nullptr;
+    if ((st = device_info(&d)) != WQ_OK) return st;
+    return finish_launch(launch_dequant_int2(w_canon, static_cast<const uint16_t*>(s_kernel), N, K, G, w_f32,
+                                             (cudaStream_t)stream));
+}
+
+wq_status wq_gemm_w2a16(const void* A, wq_dtype a_dtype, const uint8_t* w_canon, const void* s_kernel, int64_t M,
+                        int64_t N, int64_t K, int32_t G, void* out, void* ws, size_t ws_bytes, wq_stream_t stream) {
+    if (M == 0 && N > 0 && K > 0) return WQ_OK;   // empty problem: A and out may be NULL
+    if (!A || !w_canon || !s_kernel || !out) return WQ_ERR_NULL;
+    if (M < 0 || M > kMaxDim || N % 8 != 0) return WQ_ERR_SHAPE;
+    wq_status st = check_int2_shape(N, K, G);
+    if (st != WQ_OK) return st;
+    if (a_dtype != WQ_F16 && a_dtype != WQ_BF16) return WQ_ERR_DTYPE;
+    if (!aligned(A, 16) || !aligned(w_canon, 16) || !aligned(s_kernel, 16) || !aligned(out, 16))
+        return WQ_ERR_MISALIGNED;
+    DeviceInfo* d = nullptr;
+    if ((st = device_info(&d)) != WQ_OK) return st;
+    const bool bf16 = a_dtype == WQ_BF16;
+    Plan pl{};
+    if ((st = make_plan(FMT_INT2, bf16, M, N, K, d->sms, 2, &pl, G)) != WQ_OK) return st;
+    if ((st = check_ws(pl, ws, ws_bytes)) != WQ_OK) return st;
+    GemmParams gp;
+    std::memset(&gp, 0, sizeof(gp));
+    if (!encode_a(gp, A, bf16, M, K, pl.pair ? pl.cfg.bn / 2 : pl.cfg.bn)) return WQ_ERR_CUDA;
+    if (pl.pair && !encode_out(gp, out, bf16, M, N)) return WQ_ERR_CUDA;
+    const int pitch = pl.cfg.bk / 4;   // bytes of one row's codes per k-block
+    if (!encode_2d(&gp.tmap_w, CU_TENSOR_MAP_DATA_TYPE_UINT8, w_canon, (uint64_t)(K / 4), (uint64_t)N,
+                   (uint64_t)(K / 4), (uint32_t)pitch, TILE_N, swizzle_for_pitch(pitch)))
+        return WQ_ERR_CUDA;
+    gp.sc = static_cast<const uint8_t*>(s_kernel);
+    gp.G = G;
+    gp.g_shift = G == 32 ? 5 : G == 64 ? 6 : G == 128 ? 7 : 8;
+    gp.ngroups_pad = (int)(round_up(K, KPAD_INT4) / G);
+    fill_common(gp, pl, M, N, K, out, ws, d->status);
+    if (pl.pair) return finish_launch(launch_gemm_int2_pair(gp, bf16, pl.grid, (cudaStream_t)stream));
+    return finish_launch(launch_gemm_int2(gp, bf16, pl.cfg.bn, pl.grid, (cudaStream_t)stream));
 }
 
 wq_status wq_gemm_w8a16_fp8(const void* A, wq_dtype a_dtype, const uint8_t* w_e4m3, const float* alpha,

@@ -37,6 +37,9 @@
 // Dequantization per format (all exact until the final rounding to the operand
 // type, see the conversion helpers below):
 //   INT4  w = RN((q - 8) * s[k / G, n])           ("Low Bit Triton Kernels", §03)
+//   LUT4  w = RN(LUT[q] * s[k / G, n])            (the same page: NF4's 16 non-uniform
+//                                                  values as a lookup table)
+//   INT2  w = RN((q - 2) * s[k / G, n])           ("Bitblas", hands-on item 6: W2A16)
 //   FP8   w = e4m3(code)       (scale on the fp32 accumulator, PR #7495 intro)
 //   FP4   w = e2m1(code) * e4m3(sf[n, k / 16])    (alpha on the accumulator, PR #4466 §2)
 //
@@ -59,8 +62,8 @@ struct GemmCfg {
     static constexpr int NT = 128 * (1 + NWG);
     static constexpr int B_ROWS = PAIR ? BN / 2 : BN;                 // tokens this CTA copies per k-block
     static constexpr int B_STAGE = B_ROWS * BK * 2;                   // activation tile bytes
-    static constexpr int W_STAGE = (FMT == FMT_FP8) ? TILE_N * BK : TILE_N * BK / 2;
-    static constexpr int SC_STAGE = (FMT == FMT_INT4) ? (BK / 32) * TILE_N * 2
+    static constexpr int W_STAGE = (FMT == FMT_FP8) ? TILE_N * BK : (FMT == FMT_INT2) ? TILE_N * BK / 4 : TILE_N * BK / 2;
+    static constexpr int SC_STAGE = group_scaled(FMT) ? (BK / 32) * TILE_N * 2
                                   : (FMT == FMT_FP4)  ? TILE_N * BK / 16 : 0;
     static constexpr int TMEM_COLS = (BN <= 128) ? 256 : 512;
     static constexpr int A_BASE = (BN < 64) ? 64 : BN;                // first TMEM column of operand stages
@@ -92,6 +95,7 @@ struct GemmCfg {
     // two CTAs per SM when shared and tensor memory allow it (decode, split-K)
     static constexpr int MIN_BLOCKS = (!PAIR && 2 * (SMEM_BYTES + 1024) <= 228 * 1024 && TMEM_COLS <= 256) ? 2 : 1;
     static_assert(BK == 64 || BK == 128, "BK");
+    static_assert(FMT != FMT_INT2 || (BK == 128 && NWG == 2), "INT2 transform: two 32-code units per warpgroup");
     static_assert(BN % 16 == 0 && BN >= 16 && BN <= 256, "BN");
     static_assert(!PAIR || BN == 256, "pair tiles are 256 x 256");
     static_assert(A_ST >= 2, "need at least two TMEM operand stages");
@@ -188,6 +192,130 @@ __device__ __forceinline__ void int4_row_to_bf16(const uint2 (&w)[4], const Int4
             const float2 fh = __half22float2(*reinterpret_cast<const __half2*>(&hi));
             o[8 * t + c] = ptx::f32x2_to_bf16x2(fl.x * s, fl.y * s);
             o[8 * t + 4 + c] = ptx::f32x2_to_bf16x2(fh.x * s, fh.y * s);
+        }
+    }
+}
+
+// INT4 codebook ("Low Bit Triton Kernels": NF4's 16 non-uniform values are a
+// lookup table held in registers).  The 16 fp16 entries are split into their low
+// bytes (lo[i] byte j = low byte of entry 4i + j) and high bytes, so that byte
+// permutes look up four codes at once: one permute over an 8-byte half of a table
+// per code range 0-7 / 8-15, a select by bit 3 of each code, and two permutes that
+// interleave low and high bytes into fp16 pairs.
+struct Lut16 {
+    uint32_t lo[4], hi[4];
+};
+__device__ __forceinline__ Lut16 lut16_load(const uint16_t* lut) {
+    const uint4 a = __ldg(reinterpret_cast<const uint4*>(lut));       // entries 0-7
+    const uint4 b = __ldg(reinterpret_cast<const uint4*>(lut) + 1);   // entries 8-15
+    const uint32_t e[8] = {a.x, a.y, a.z, a.w, b.x, b.y, b.z, b.w};   // word i: entries 2i, 2i + 1
+    Lut16 t;
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+        t.lo[i] = ptx::prmt(e[2 * i], e[2 * i + 1], 0x6420u);
+        t.hi[i] = ptx::prmt(e[2 * i], e[2 * i + 1], 0x7531u);
+    }
+    return t;
+}
+
+// The four codes of one row in one fragment-order word (bits 0-3 / 16-19 / 8-11 /
+// 24-27 for k, k + 1, k + 8, k + 9 in the lower row half; 4 bits higher in the
+// upper half, hshift = 4) -> the fp16 pairs LUT(k, k + 1) and LUT(k + 8, k + 9).
+__device__ __forceinline__ void lut16_word(uint32_t w, uint32_t hshift, const Lut16& t, uint32_t& p_lo,
+                                           uint32_t& p_hi) {
+    const uint32_t u = w >> hshift;                                     // the row's codes in low nibbles
+    const uint32_t sel = ((u & 0x0F0Fu) | ((u >> 12) & 0xF0F0u)) & 0x7777u;   // k, k+1, k+8, k+9 (3 bits)
+    // 0xFF in the result bytes whose code is >= 8: the sign of word bytes 0, 2, 1, 3
+    // after moving each code's bit 3 to bit 7
+    const uint32_t m = ptx::prmt(u << 4, 0u, 0xB9A8u);
+    const uint32_t lo = ptx::lop3_select(ptx::prmt(t.lo[0], t.lo[1], sel), ptx::prmt(t.lo[2], t.lo[3], sel), m);
+    const uint32_t hi = ptx::lop3_select(ptx::prmt(t.hi[0], t.hi[1], sel), ptx::prmt(t.hi[2], t.hi[3], sel), m);
+    p_lo = ptx::prmt(lo, hi, 0x5140u);
+    p_hi = ptx::prmt(lo, hi, 0x7362u);
+}
+
+// A row's 32 values of one unit (the gather of int4_row_to_f16) through the
+// codebook, times the group scale: RN16(LUT[q] * s) (the fp16 product of two fp16
+// values is one rounding of the exact product).
+__device__ __forceinline__ void lut16_row_to_f16(const uint2 (&w)[4], uint32_t hshift, const Lut16& t, uint32_t s2,
+                                                 uint32_t (&o)[16]) {
+#pragma unroll
+    for (int c = 0; c < 4; ++c) {
+        const uint32_t wt[2] = {w[c].x, w[c].y};
+#pragma unroll
+        for (int k = 0; k < 2; ++k) {
+            uint32_t lo, hi;
+            lut16_word(wt[k], hshift, t, lo, hi);
+            o[8 * k + c] = ptx::hmul2_u32(lo, s2);
+            o[8 * k + 4 + c] = ptx::hmul2_u32(hi, s2);
+        }
+    }
+}
+
+// bf16 operands: LUT[q] * s is exact in fp32 (11 + 11 significant bits), one
+// rounding to bf16.
+__device__ __forceinline__ void lut16_row_to_bf16(const uint2 (&w)[4], uint32_t hshift, const Lut16& t, float s,
+                                                  uint32_t (&o)[16]) {
+#pragma unroll
+    for (int c = 0; c < 4; ++c) {
+        const uint32_t wt[2] = {w[c].x, w[c].y};
+#pragma unroll
+        for (int k = 0; k < 2; ++k) {
+            uint32_t lo, hi;
+            lut16_word(wt[k], hshift, t, lo, hi);
+            const float2 fl = __half22float2(*reinterpret_cast<const __half2*>(&lo));
+            const float2 fh = __half22float2(*reinterpret_cast<const __half2*>(&hi));
+            o[8 * k + c] = ptx::f32x2_to_bf16x2(fl.x * s, fl.y * s);
+            o[8 * k + 4 + c] = ptx::f32x2_to_bf16x2(fh.x * s, fh.y * s);
+        }
+    }
+}
+
+// INT2 (W2A16): 32 codes of a row, two canonical words (code k at bits 2 (k % 16)
+// of word k / 16) -> 16 pairs (k = 2p, 2p + 1) in o[p].  Per word, the even and the
+// odd codes are separated into the low and the high halves (AND, shift-AND, two byte
+// permutes), so that code pair p sits at bits 4p' / 16 + 4p' of a word; the fp16
+// "magic number" for that position (exponent 2^10, 2^6, 2^2: mantissa unit 1, 1/16,
+// 1/256 shifted by 0, 4, 8 bits) turns it into b + q with one AND-OR, and the fourth
+// pair of each half is shifted down first.  Subtracting b + 2 gives q - 2 exactly;
+// one multiply by the group scale rounds once: RN16((q - 2) * s).
+__device__ __forceinline__ void int2_word_to_pairs(uint32_t w, uint32_t (&h)[8]) {
+    const uint32_t ev = w & 0x33333333u;            // codes 2p at bits 4p
+    const uint32_t od = (w >> 2) & 0x33333333u;     // codes 2p + 1 at bits 4p
+    const uint32_t x = ptx::prmt(ev, od, 0x5410u);  // pairs 0-3: even in the low half, odd in the high
+    const uint32_t y = ptx::prmt(ev, od, 0x7632u);  // pairs 4-7
+    const uint32_t src[2] = {x, y};
+#pragma unroll
+    for (int j = 0; j < 2; ++j) {
+        const uint32_t v = src[j];
+        h[4 * j + 0] = ptx::hsub2_u32(ptx::lop3_and_or(v, 0x00030003u, 0x64006400u), 0x64026402u);   // 1024 + q
+        h[4 * j + 1] = ptx::hsub2_u32(ptx::lop3_and_or(v, 0x00300030u, 0x54005400u), 0x54205420u);   // 64 + q
+        h[4 * j + 2] = ptx::hsub2_u32(ptx::lop3_and_or(v, 0x03000300u, 0x44004400u), 0x46004600u);   // 4 + q
+        h[4 * j + 3] = ptx::hsub2_u32(ptx::lop3_and_or(v >> 12, 0x00030003u, 0x64006400u), 0x64026402u);
+    }
+}
+
+__device__ __forceinline__ void int2_row_to_f16(const uint2& w, uint32_t s2, uint32_t (&o)[16]) {
+    uint32_t h[8];
+    int2_word_to_pairs(w.x, h);
+#pragma unroll
+    for (int p = 0; p < 8; ++p) o[p] = ptx::hmul2_u32(h[p], s2);
+    int2_word_to_pairs(w.y, h);
+#pragma unroll
+    for (int p = 0; p < 8; ++p) o[8 + p] = ptx::hmul2_u32(h[p], s2);
+}
+
+// bf16 operands: (q - 2) * s is exact in fp32, one rounding to bf16.
+__device__ __forceinline__ void int2_row_to_bf16(const uint2& w, float s, uint32_t (&o)[16]) {
+    const uint32_t wv[2] = {w.x, w.y};
+#pragma unroll
+    for (int j = 0; j < 2; ++j) {
+        uint32_t h[8];
+        int2_word_to_pairs(wv[j], h);
+#pragma unroll
+        for (int p = 0; p < 8; ++p) {
+            const float2 f = __half22float2(*reinterpret_cast<const __half2*>(&h[p]));
+            o[8 * j + p] = ptx::f32x2_to_bf16x2(f.x * s, f.y * s);
         }
     }
 }
@@ -346,7 +474,7 @@ __global__ void __launch_bounds__(128 * (1 + NWG), (GemmCfg<FMT, BF16, BN, BK, S
     }
     if (warp == 0 && lane == 0) {
         ptx::prefetch_tmap(&p.tmap_a);
-        if (FMT != FMT_INT4) ptx::prefetch_tmap(&p.tmap_w);
+        if (!int4_layout(FMT)) ptx::prefetch_tmap(&p.tmap_w);
     }
     if (warp == 2) {
         ptx::tmem_alloc<CG>(sbase + C::OFF_MISC, C::TMEM_COLS);
@@ -419,10 +547,10 @@ __global__ void __launch_bounds__(128 * (1 + NWG), (GemmCfg<FMT, BF16, BN, BK, S
                         const uint32_t fb = wfull_bar(s);
                         const uint32_t w_dst = sbase + C::OFF_W + s * C::W_STAGE;
                         const uint32_t sc_dst = sbase + C::OFF_SC + s * C::SC_STAGE;
-                        if (FMT == FMT_INT4) {
+                        if (int4_layout(FMT)) {
                             const int gcnt = (p.G >= BK) ? 1 : (BK >> p.g_shift);
                             const uint32_t sc_bytes = (uint32_t)gcnt * TILE_N * 2;
-                            const uint32_t zp_bytes = p.zp ? (uint32_t)gcnt * TILE_N : 0u;
+                            const uint32_t zp_bytes = (FMT == FMT_INT4 && p.zp) ? (uint32_t)gcnt * TILE_N : 0u;
                             ptx::mbar_arrive_expect_tx(fb, C::W_STAGE + sc_bytes + zp_bytes);
                             const uint8_t* wsrc =
                                 p.w + ((size_t)w_tile(it) * p.nchunks_pad + (size_t)kb * (BK / 32)) * (TILE_N * 16);
@@ -430,10 +558,20 @@ __global__ void __launch_bounds__(128 * (1 + NWG), (GemmCfg<FMT, BF16, BN, BK, S
                             const int g0 = (kb * BK) >> p.g_shift;
                             const uint8_t* ssrc = p.sc + ((size_t)w_tile(it) * p.ngroups_pad + g0) * (TILE_N * 2);
                             ptx::bulk_load(sc_dst, ssrc, sc_bytes, fb, pol);
-                            if (p.zp)
+                            if (FMT == FMT_INT4 && p.zp)
                                 ptx::bulk_load(sbase + C::OFF_ZP + s * C::ZP_STAGE,
                                                p.zp + ((size_t)w_tile(it) * p.ngroups_pad + g0) * TILE_N, zp_bytes, fb,
                                                pol);
+                        } else if (FMT == FMT_INT2) {
+                            // canonical 2-bit rows through TMA (BK / 4 bytes per row), group
+                            // scales as for INT4
+                            const int gcnt = (p.G >= BK) ? 1 : (BK >> p.g_shift);
+                            const uint32_t sc_bytes = (uint32_t)gcnt * TILE_N * 2;
+                            ptx::mbar_arrive_expect_tx(fb, C::W_STAGE + sc_bytes);
+                            ptx::tma_load_2d(w_dst, &p.tmap_w, kb * (BK / 4), w_tile(it) * TILE_N, fb, pol);
+                            const int g0 = (kb * BK) >> p.g_shift;
+                            const uint8_t* ssrc = p.sc + ((size_t)w_tile(it) * p.ngroups_pad + g0) * (TILE_N * 2);
+                            ptx::bulk_load(sc_dst, ssrc, sc_bytes, fb, pol);
                         } else if (FMT == FMT_FP4) {
                             ptx::mbar_arrive_expect_tx(fb, C::W_STAGE + C::SC_STAGE);
                             ptx::tma_load_2d(w_dst, &p.tmap_w, kb * (BK / 2), w_tile(it) * TILE_N, fb, pol);
@@ -606,7 +744,7 @@ __global__ void __launch_bounds__(128 * (1 + NWG), (GemmCfg<FMT, BF16, BN, BK, S
             return w;
         };
         ptx::grid_dependency_wait();   // alpha / bias are global inputs too
-        const float alpha = (FMT == FMT_INT4) ? 1.0f : __ldg(p.alpha);
+        const float alpha = group_scaled(FMT) ? 1.0f : __ldg(p.alpha);
         // One k-block of the transform: waits for its codes and a free TMEM operand
         // stage, writes the 16-bit operand there and hands it to the MMA issuer.
         auto transform_one = [&]() -> bool {
@@ -644,7 +782,7 @@ __global__ void __launch_bounds__(128 * (1 + NWG), (GemmCfg<FMT, BF16, BN, BK, S
 #pragma unroll
                 for (int i = 0; i < CPW; ++i) {
                     const int c = c0 + i;
-                    if (FMT == FMT_INT4 && CPW % 2 == 0) {
+                    if (int4_layout(FMT) && CPW % 2 == 0) {
                         // units c, c + 1 (c even) are the two 8-byte halves of the same
                         // 16-byte slots of quad c / 2: one 16-byte load per slot serves both
                         if (i % 2 == 0) {
@@ -659,19 +797,50 @@ __global__ void __launch_bounds__(128 * (1 + NWG), (GemmCfg<FMT, BF16, BN, BK, S
                             sv[i + 1] = (p.g_shift >= 6) ? sv[i]   // both units in one group (G >= 64)
                                       : *reinterpret_cast<const uint16_t*>(sct + ((((c + 1) * 32) >> p.g_shift) * TILE_N + r) * 2);
                         }
-                    } else if (FMT == FMT_INT4) {
+                    } else if (int4_layout(FMT)) {
                         // unit c: quad c / 2 of the stage, k steps 2 (c % 2) and 2 (c % 2) + 1
                         const uint8_t* ub = wt + (c >> 1) * 4096 + gr * 512 + (c & 1) * 8;
 #pragma unroll
                         for (int l = 0; l < 4; ++l)
                             qi[i][l] = *reinterpret_cast<const uint2*>(ub + int4_slot(4 * g8 + l) * 16);
                         sv[i] = *reinterpret_cast<const uint16_t*>(sct + (((c * 32) >> p.g_shift) * TILE_N + r) * 2);
+                    } else if (FMT == FMT_INT2) {
+                        // unit c: bytes 8c .. 8c + 7 of the row (32 codes); units c, c + 1
+                        // (c even) share one 16-byte chunk
+                        if (i % 2 == 0) {
+                            const uint4 v = *reinterpret_cast<const uint4*>(wt + swz(r * C::W_PITCH + (c >> 1) * 16, C::W_SWZ));
+                            qi[i][0] = make_uint2(v.x, v.y);
+                            qi[i + 1][0] = make_uint2(v.z, v.w);
+                            sv[i] = *reinterpret_cast<const uint16_t*>(sct + (((c * 32) >> p.g_shift) * TILE_N + r) * 2);
+                            sv[i + 1] = (p.g_shift >= 6) ? sv[i]
+                                      : *reinterpret_cast<const uint16_t*>(sct + ((((c + 1) * 32) >> p.g_shift) * TILE_N + r) * 2);
+                        }
                     } else {
                         q[i] = *reinterpret_cast<const uint4*>(wt + swz(r * C::W_PITCH + c * 16, C::W_SWZ));
                         sv[i] = *reinterpret_cast<const uint16_t*>(sct + (c >> 1) * (TILE_N * 4) + r * 4 + (c & 1) * 2);
                     }
                 }
                 uint32_t o[CPW][16];
+                if (FMT == FMT_LUT4) {
+                    // codebook: LUT[q] * s
+                    const Lut16 tab = lut16_load(p.lut);
+                    const uint32_t hshift = (uint32_t)((r >> 3) & 1) * 4u;
+#pragma unroll
+                    for (int i = 0; i < CPW; ++i) {
+                        if (BF16)
+                            lut16_row_to_bf16(qi[i], hshift, tab, __half2float(__ushort_as_half(sv[i])), o[i]);
+                        else
+                            lut16_row_to_f16(qi[i], hshift, tab, (uint32_t)sv[i] | ((uint32_t)sv[i] << 16), o[i]);
+                    }
+                } else if (FMT == FMT_INT2) {
+#pragma unroll
+                    for (int i = 0; i < CPW; ++i) {
+                        if (BF16)
+                            int2_row_to_bf16(qi[i][0], __half2float(__ushort_as_half(sv[i])), o[i]);
+                        else
+                            int2_row_to_f16(qi[i][0], (uint32_t)sv[i] | ((uint32_t)sv[i] << 16), o[i]);
+                    }
+                } else {
 #pragma unroll
                 for (int i = 0; i < CPW; ++i) {
                     if (FMT == FMT_INT4) {
@@ -691,6 +860,7 @@ __global__ void __launch_bounds__(128 * (1 + NWG), (GemmCfg<FMT, BF16, BN, BK, S
                     } else {
                         fp4_to_bf16(q[i], sv[i], o[i]);
                     }
+                }
                 }
                 __syncwarp();
                 if (lane == 0) ptx::mbar_arrive(wempty_bar(s));   // codes consumed

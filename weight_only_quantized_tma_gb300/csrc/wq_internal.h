@@ -9,7 +9,15 @@
 
 namespace wq {
 
-enum WFmt : int { FMT_INT4 = 0, FMT_FP8 = 1, FMT_FP4 = 2 };
+// Weight formats of the tile kernel.  FMT_LUT4 is the INT4 layout with a 16-entry
+// codebook in place of q - 8; FMT_INT2 holds canonical 2-bit codes [N][K/4] with
+// the INT4 group-scale layout.
+enum WFmt : int { FMT_INT4 = 0, FMT_FP8 = 1, FMT_FP4 = 2, FMT_LUT4 = 3, FMT_INT2 = 4 };
+constexpr int kNumFmts = 5;
+// the prepacked fragment-order INT4 code layout (wq_pack_int4)
+__host__ __device__ constexpr bool int4_layout(int f) { return f == FMT_INT4 || f == FMT_LUT4; }
+// fp16 group scales in the prepacked [N/128][Kp/G][128] layout, applied before the MMA
+__host__ __device__ constexpr bool group_scaled(int f) { return f == FMT_INT4 || f == FMT_LUT4 || f == FMT_INT2; }
 
 // Weight rows per CTA tile (the MMA M dimension: dequantized weight rows are the
 // tcgen05 A operand, tokens are the N dimension).
@@ -78,6 +86,7 @@ struct GemmParams {
     const uint8_t* w;        // INT4 prepacked weight tiles
     const uint8_t* sc;       // INT4 prepacked group scales / FP4 prepacked block scales
     const uint8_t* zp;       // INT4 prepacked zero points (uint8, the scales' layout) or null: zero point 8
+    const uint16_t* lut;     // FMT_LUT4 codebook: 16 fp16 values, value LUT[q] * s
     const float* alpha;      // FP8 / FP4 global scale (device), unused for INT4
     const void* bias;        // FP8 optional bias [N], same 16-bit type as A
     void* out;               // [M][N], 16-bit
@@ -155,6 +164,15 @@ cudaError_t launch_gemm_fp8_pair(const GemmParams& p, bool bf16, int grid, cudaS
 bool config_fp4_pair(bool query, KernelConfig* cfg);
 cudaError_t launch_gemm_fp4_pair(const GemmParams& p, int grid, cudaStream_t st);
 bool config_fp4(bool bf16, int bn, bool query, KernelConfig* cfg);
+// Codebook INT4 (FMT_LUT4) and INT2 tile kernels, one-CTA and pair.
+bool config_lut4(bool bf16, int bn, bool query, KernelConfig* cfg);
+cudaError_t launch_gemm_lut4(const GemmParams& p, bool bf16, int bn, int grid, cudaStream_t st);
+bool config_lut4_pair(bool bf16, bool query, KernelConfig* cfg);
+cudaError_t launch_gemm_lut4_pair(const GemmParams& p, bool bf16, int grid, cudaStream_t st);
+bool config_int2(bool bf16, int bn, bool query, KernelConfig* cfg);
+cudaError_t launch_gemm_int2(const GemmParams& p, bool bf16, int bn, int grid, cudaStream_t st);
+bool config_int2_pair(bool bf16, bool query, KernelConfig* cfg);
+cudaError_t launch_gemm_int2_pair(const GemmParams& p, bool bf16, int grid, cudaStream_t st);
 
 // Synthetic INT4 quantiser (fp16 [N][K] -> canonical codes and scales), wq_quant.cu.
 cudaError_t launch_quantize_int4(const uint16_t* w, int64_t N, int64_t K, int G, uint8_t* wq, uint16_t* s,
@@ -166,8 +184,11 @@ cudaError_t launch_pack_int4(const uint8_t* w, const uint16_t* s, int64_t N, int
 cudaError_t launch_unpack_int4(const uint8_t* wk, const uint16_t* sk, int64_t N, int64_t K, int G, uint8_t* w,
                                uint16_t* s, cudaStream_t st);
 cudaError_t launch_pack_int4_zeros(const uint8_t* z, int64_t N, int64_t K, int G, uint8_t* zk, cudaStream_t st);
-cudaError_t launch_dequant_int4(const uint8_t* wk, const uint16_t* sk, int64_t N, int64_t K, int G, float* out,
+cudaError_t launch_pack_group_scales(const uint16_t* s, int64_t N, int64_t K, int G, uint16_t* sk, cudaStream_t st);
+cudaError_t launch_dequant_int2(const uint8_t* w, const uint16_t* sk, int64_t N, int64_t K, int G, float* out,
                                 cudaStream_t st);
+cudaError_t launch_dequant_int4(const uint8_t* wk, const uint16_t* sk, const uint16_t* lut, int64_t N, int64_t K,
+                                int G, float* out, cudaStream_t st);
 cudaError_t launch_pack_fp4_sf(const uint8_t* sf, int64_t N, int64_t K, uint8_t* sfk, cudaStream_t st);
 cudaError_t launch_dequant_fp4(const uint8_t* w, const uint8_t* sfk, int64_t N, int64_t K, float* out,
                                cudaStream_t st);

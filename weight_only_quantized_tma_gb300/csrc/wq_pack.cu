@@ -115,15 +115,18 @@ __global__ void unpack_int4_s_kernel(const uint16_t* __restrict__ sk, int64_t N,
     }
 }
 
-__global__ void dequant_int4_kernel(const uint8_t* __restrict__ wk, const uint16_t* __restrict__ sk, int64_t N,
-                                    int64_t K, int G, int64_t nkb, int64_t groups_pad, float* __restrict__ out) {
+// (q - 8) * s, or LUT[q] * s with a codebook; both products are exact in fp32.
+__global__ void dequant_int4_kernel(const uint8_t* __restrict__ wk, const uint16_t* __restrict__ sk,
+                                    const uint16_t* __restrict__ lut, int64_t N, int64_t K, int G, int64_t nkb,
+                                    int64_t groups_pad, float* __restrict__ out) {
     const int64_t total = N * K;
     for (int64_t u = blockIdx.x * (int64_t)blockDim.x + threadIdx.x; u < total;
          u += (int64_t)gridDim.x * blockDim.x) {
         const int64_t n = u / K, k = u % K;
         const int q = (int)packed_code(wk, nkb, n, k);
         const uint16_t sb = sk[((n / TILE_N) * groups_pad + k / G) * TILE_N + (n % TILE_N)];
-        out[u] = (float)(q - 8) * __half2float(__ushort_as_half(sb));
+        const float v = lut ? __half2float(__ushort_as_half(lut[q])) : (float)(q - 8);
+        out[u] = v * __half2float(__ushort_as_half(sb));
     }
 }
 
@@ -241,6 +244,38 @@ cudaError_t launch_pack_int4(const uint8_t* w, const uint16_t* s, int64_t N, int
     return cudaGetLastError();
 }
 
+// Group scales alone (INT2: the codes stay canonical), in the INT4 scale layout;
+// ends with an ordinary launch for the same reason as launch_pack_int4.
+cudaError_t launch_pack_group_scales(const uint16_t* s, int64_t N, int64_t K, int G, uint16_t* sk, cudaStream_t st) {
+    const int64_t Np = round_up(N, TILE_N), Kp = round_up(K, KPAD_INT4);
+    const int64_t groups_pad = Kp / G, total = (Np / TILE_N) * groups_pad * TILE_N;
+    pack_int4_s_kernel<<<grid_for(total), kThreads, 0, st>>>(s, N, K / G, groups_pad, total, sk);
+    cudaError_t e = cudaGetLastError();
+    if (e != cudaSuccess) return e;
+    stream_fence_kernel<<<1, 32, 0, st>>>();
+    return cudaGetLastError();
+}
+
+// INT2 debug export: (q - 2) * s from canonical codes [N][K/4] and packed scales.
+__global__ void dequant_int2_kernel(const uint8_t* __restrict__ w, const uint16_t* __restrict__ sk, int64_t N,
+                                    int64_t K, int G, int64_t groups_pad, float* __restrict__ out) {
+    const int64_t total = N * K;
+    for (int64_t u = blockIdx.x * (int64_t)blockDim.x + threadIdx.x; u < total;
+         u += (int64_t)gridDim.x * blockDim.x) {
+        const int64_t n = u / K, k = u % K;
+        const int q = (w[n * (K / 4) + k / 4] >> (2 * (k % 4))) & 0x3;
+        const uint16_t sb = sk[((n / TILE_N) * groups_pad + k / G) * TILE_N + (n % TILE_N)];
+        out[u] = (float)(q - 2) * __half2float(__ushort_as_half(sb));
+    }
+}
+
+cudaError_t launch_dequant_int2(const uint8_t* w, const uint16_t* sk, int64_t N, int64_t K, int G, float* out,
+                                cudaStream_t st) {
+    const int64_t Kp = round_up(K, KPAD_INT4);
+    dequant_int2_kernel<<<grid_for(N * K), kThreads, 0, st>>>(w, sk, N, K, G, Kp / G, out);
+    return cudaGetLastError();
+}
+
 // Zero points: canonical uint8 [K/G][N] -> [N/128][Kp/G][128], the layout of the packed
 // scales; padding gets 8 (with scale 0 the weight is 0 either way).
 __global__ void pack_int4_z_kernel(const uint8_t* __restrict__ z, int64_t N, int64_t groups, int64_t groups_pad,
@@ -276,10 +311,10 @@ cudaError_t launch_unpack_int4(const uint8_t* wk, const uint16_t* sk, int64_t N,
     return cudaGetLastError();
 }
 
-cudaError_t launch_dequant_int4(const uint8_t* wk, const uint16_t* sk, int64_t N, int64_t K, int G, float* out,
-                                cudaStream_t st) {
+cudaError_t launch_dequant_int4(const uint8_t* wk, const uint16_t* sk, const uint16_t* lut, int64_t N, int64_t K,
+                                int G, float* out, cudaStream_t st) {
     const int64_t Kp = round_up(K, KPAD_INT4);
-    dequant_int4_kernel<<<grid_for(N * K), kThreads, 0, st>>>(wk, sk, N, K, G, Kp / 128, Kp / G, out);
+    dequant_int4_kernel<<<grid_for(N * K), kThreads, 0, st>>>(wk, sk, lut, N, K, G, Kp / 128, Kp / G, out);
     return cudaGetLastError();
 }
 
