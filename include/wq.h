@@ -300,6 +300,10 @@ typedef struct {
     int32_t tiles_m;
     int32_t ctas_per_sm;  /* resident CTAs per SM assumed by the plan */
     int32_t kernel;       /* WQ_KERNEL_TILE, WQ_KERNEL_DECODE or WQ_KERNEL_TILE_PAIR */
+    int32_t cluster_split; /* 1: the split-K slices of a tile run as one thread-block cluster and
+                              are reduced through distributed shared memory (no workspace) */
+    int32_t cluster_capacity; /* splits-CTA clusters of this kernel the device holds at once
+                                 (0 when not applicable); cluster_split needs tiles <= it */
 } wq_plan;
 
 /* Kernels a plan can pick.  TILE: the tcgen05 kernel (weights dequantized into
@@ -318,7 +322,11 @@ typedef struct {
 wq_status wq_get_plan(wq_op op, wq_dtype a_dtype, int64_t M, int64_t N, int64_t K, int32_t G, wq_plan* plan,
                       size_t* ws_bytes);
 
-/* Workspace bytes an op needs (0 when no split-K is used).  Host only. */
+/* Workspace bytes an op needs: 0 when no split-K is used or when the split-K
+ * slices are reduced inside a thread-block cluster (wq_plan.cluster_split; the
+ * tile kernel does this for S <= 16 slices).  WQ_SPLITK_WORKSPACE=1 in the
+ * environment keeps the workspace reduction (last arriver sums the slices), e.g.
+ * to compare the two.  Host only. */
 wq_status wq_workspace_bytes(wq_op op, wq_dtype a_dtype, int64_t M, int64_t N, int64_t K, int32_t G,
                              size_t* bytes);
 

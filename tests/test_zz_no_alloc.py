@@ -30,17 +30,21 @@ def _call(L, p, out):
                                    ctypes.c_void_p(out.data_ptr()), stream)
 
 
-@pytest.mark.parametrize("M,N,K,scratch", [(32, 4096, 1024, True), (20, 1024, 2048, True), (1, 11008, 4096, False),
-                                           (16, 4096, 4096, False)])
-def test_noalloc_matches_workspace_entry_on_two_calls(M, N, K, scratch):
+@pytest.mark.parametrize("M,N,K,scratch", [(32, 4096, 1024, True), (20, 1024, 2048, True), (32, 4096, 1024, False),
+                                           (1, 11008, 4096, False), (16, 4096, 4096, False)])
+def test_noalloc_matches_workspace_entry_on_two_calls(M, N, K, scratch, monkeypatch):
     G = 128
+    if scratch:
+        # tile-kernel split-K with the workspace reduction (the tile kernel otherwise
+        # reduces its slices inside a cluster): the built-in scratch is really exercised
+        monkeypatch.setenv("WQ_SPLITK_WORKSPACE", "1")
     plan = wq.get_plan(wq.WQ_OP_W4A16, wq.WQ_F16, M, N, K, G)
     if scratch:
-        # tile-kernel split-K: the built-in scratch is really exercised
         assert plan["splits"] > 1 and 0 < plan["ws_bytes"] <= _lib.WQ_NOALLOC_SCRATCH_BYTES
+        assert plan["cluster_split"] == 0
     else:
-        # the decode kernel reduces split-K inside a cluster and needs no scratch
-        assert plan["kernel"] == wq.WQ_KERNEL_DECODE and plan["ws_bytes"] == 0
+        # the decode kernel and the tile kernel's cluster split-K need no scratch
+        assert plan["ws_bytes"] == 0
     p = Int4Problem(M, N, K, G, seed=901 + M).pack()
     expected = p.run()                       # the entry point with a caller workspace
     torch.cuda.synchronize()
@@ -53,7 +57,8 @@ def test_noalloc_matches_workspace_entry_on_two_calls(M, N, K, scratch):
         check_close(out_to_f64(out), p.ref(), what="noalloc vs oracle")
 
 
-def test_noalloc_rejects_problems_beyond_its_scratch():
+def test_noalloc_rejects_problems_beyond_its_scratch(monkeypatch):
+    monkeypatch.setenv("WQ_SPLITK_WORKSPACE", "1")
     M, N, K, G = 256, 2048, 4096, 128
     plan = wq.get_plan(wq.WQ_OP_W4A16, wq.WQ_F16, M, N, K, G)
     assert plan["ws_bytes"] > _lib.WQ_NOALLOC_SCRATCH_BYTES

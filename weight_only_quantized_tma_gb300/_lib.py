@@ -45,7 +45,7 @@ class WQError(RuntimeError):
 class WqPlan(ctypes.Structure):
     _fields_ = [(n, ctypes.c_int32) for n in (
         "bn", "bk", "stages", "splits", "grid", "threads", "smem_bytes", "n_items", "walk_n_fast",
-        "tiles_n", "tiles_m", "ctas_per_sm", "kernel")]
+        "tiles_n", "tiles_m", "ctas_per_sm", "kernel", "cluster_split", "cluster_capacity")]
 
     def as_dict(self):
         return {n: getattr(self, n) for n, _ in self._fields_}

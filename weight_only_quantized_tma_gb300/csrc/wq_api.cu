@@ -107,6 +107,7 @@ struct Plan {
     size_t ws_bytes;
     bool decode;   // W4A16 decode kernel (register-resident mma.sync, M <= 16)
     bool pair;     // tile kernel on two-CTA clusters (256 weight rows per tile)
+    bool csplit;   // tile kernel split-K reduced inside thread-block clusters (no workspace)
 };
 
 bool get_config_uncached(int fmt, bool bf16, int bn, bool query, KernelConfig* cfg) {
@@ -270,10 +271,36 @@ wq_status make_plan(int fmt, bool bf16, int64_t M, int64_t N, int64_t K, int sms
             }
         }
     }
+    // Split-K on the one-CTA tile kernel with token tiles of 64 or 128: the S slices of
+    // a tile form one thread-block cluster and reduce through distributed shared
+    // memory (one item per CTA).  In the workspace reduction one warp reads S partial
+    // columns for each of its 32-64 output columns, several microseconds at these
+    // tiles.  All clusters must be resident at once (a second wave would double the
+    // time), and the device holds fewer S-CTA clusters of this kernel than slots / S
+    // (about one CTA per SM), so S is the largest count with tiles <= max_clusters[S];
+    // the cluster grid must still cover at least 4/5 of the SMs, else the workspace
+    // reduction on the full grid is faster (measured on GB300: 4096 x 4096 at M = 128,
+    // 30.5 us with 4 slices in clusters against 37.7 us with 9 through the workspace;
+    // 6656 x 19968 at M = 128, 79 us with 2 slices in 104 CTAs against 62 us with 5).
+    // At BN = 256 the cluster reduction measured slower at equal slice counts.
+    // WQ_SPLITK_WORKSPACE=1 keeps the workspace reduction.
+    if (!decode && !p.pair && p.splits > 1 && cfg.csplit_ok && cfg.bn >= 64 && cfg.bn <= 128 &&
+        p.grid == p.n_items && sms > 0) {
+        const char* ws_env = std::getenv("WQ_SPLITK_WORKSPACE");
+        int best = 0;
+        for (int S = 2; S <= p.splits && S <= kMaxDecodeCluster; ++S)
+            if (tiles <= cfg.max_clusters[S] && p.nkb >= 2 * S) best = S;
+        if (best >= 2 && 5 * tiles * best >= 4LL * sms && !(ws_env && ws_env[0] == '1')) {
+            p.csplit = true;
+            p.splits = best;
+            splits = best;
+            p.n_items = p.n_full = p.grid = (int)(tiles * best);
+        }
+    }
     const double w_bytes = (double)N * (double)K * w_bits / 8.0;
     const double a_bytes = (double)M * (double)K * 2.0;
     p.walk_n_fast = w_bytes < a_bytes ? 1 : 0;
-    p.ws_bytes = decode ? 0 : split_ws_bytes((int)tiles, splits, cfg.bn);
+    p.ws_bytes = (decode || p.csplit) ? 0 : split_ws_bytes((int)tiles, splits, cfg.bn);
     *plan = p;
     return WQ_OK;
 }
@@ -307,6 +334,7 @@ void fill_common(GemmParams& gp, const Plan& pl, int64_t M, int64_t N, int64_t K
     gp.div_walk = make_fastdiv(pl.walk_n_fast ? pl.tiles_n : pl.tiles_m,
                                (uint32_t)((long long)pl.tiles_n * pl.tiles_m));
     gp.div_splits = make_fastdiv(pl.splits, (uint32_t)pl.n_items);
+    gp.csplit = pl.csplit ? 1 : 0;
     gp.status = status;
     gp.timeout_ns = kTimeoutNs;
     if (pl.ws_bytes > 0) {
@@ -555,6 +583,9 @@ wq_status wq_get_plan(wq_op op, wq_dtype a_dtype, int64_t M, int64_t N, int64_t 
         plan->tiles_m = pl.tiles_m;
         plan->ctas_per_sm = pl.cfg.ctas_per_sm;
         plan->kernel = pl.decode ? WQ_KERNEL_DECODE : pl.pair ? WQ_KERNEL_TILE_PAIR : WQ_KERNEL_TILE;
+        plan->cluster_split = pl.csplit ? 1 : 0;
+        plan->cluster_capacity =
+            (pl.splits >= 2 && pl.splits <= kMaxDecodeCluster && !pl.pair) ? pl.cfg.max_clusters[pl.splits] : 0;
     }
     if (ws_bytes) *ws_bytes = (M == 0) ? 0 : pl.ws_bytes;
     return WQ_OK;

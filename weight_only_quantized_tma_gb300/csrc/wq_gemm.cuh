@@ -92,6 +92,13 @@ struct GemmCfg {
     // and the matching swizzle; the XOR mask applies to 16-byte chunk indices.
     static constexpr int W_PITCH = W_STAGE / TILE_N;
     static constexpr uint32_t W_SWZ = (W_PITCH == 128) ? 7u : (W_PITCH == 64) ? 3u : 1u;
+    // Split-K inside a cluster: after the main loop the stage memory [0, OFF_STG) of
+    // every CTA is an inbox for the fp32 partial rows the other slices send it,
+    // [slice][row][BN + 1] (the odd pitch keeps a warp's 32 rows on 32 banks); at most
+    // S * ceil(128 / S) <= 143 rows for S <= 16.
+    static constexpr int CS_PITCH = BN + 1;
+    static constexpr int CS_INBOX = (TILE_N + 15) * CS_PITCH * 4;
+    static constexpr bool CSPLIT_OK = !PAIR && CS_INBOX <= OFF_STG;
     // two CTAs per SM when shared and tensor memory allow it (decode, split-K)
     static constexpr int MIN_BLOCKS = (!PAIR && 2 * (SMEM_BYTES + 1024) <= 228 * 1024 && TMEM_COLS <= 256) ? 2 : 1;
     static_assert(BK == 64 || BK == 128, "BK");
@@ -1007,22 +1014,40 @@ __global__ void __launch_bounds__(128 * (1 + NWG), (GemmCfg<FMT, BF16, BN, BK, S
                 if (last) {
                     __threadfence();
                     const float* base = p.ws_part + (size_t)(tile * p.splits) * BN * TILE_N;
-                    // all slices of a column are loaded before any is added (one L2 round
-                    // trip instead of one per slice), then summed in slice order 0..S-1
-                    constexpr int MAX_SPLITS = 16;
+                    // CB columns at a time, two slices per round: 2 CB independent loads
+                    // in flight per thread (one L2 round trip per round instead of one
+                    // per column), each column summed in slice order 0..S-1
+                    constexpr int CB = 8;
+                    const int ncols = min(COLS, p.M - (m0 + c_begin));
 #pragma unroll 1
-                    for (int cc = c_begin; cc < c_begin + COLS; ++cc) {
-                        const int m = m0 + cc;
-                        if (m >= p.M) break;
-                        float v[MAX_SPLITS];
+                    for (int c0 = 0; c0 < ncols; c0 += CB) {
+                        float acc[CB];
 #pragma unroll
-                        for (int sl = 0; sl < MAX_SPLITS; ++sl)
-                            v[sl] = sl < p.splits ? __ldcg(base + ((size_t)sl * BN + cc) * TILE_N + r) : 0.0f;
-                        float acc = 0.0f;
+                        for (int j = 0; j < CB; ++j) acc[j] = 0.0f;
+#pragma unroll 1
+                        for (int sl = 0; sl < p.splits; sl += 2) {
+                            const bool two = sl + 1 < p.splits;
+                            float v0[CB], v1[CB];
 #pragma unroll
-                        for (int sl = 0; sl < MAX_SPLITS; ++sl)
-                            if (sl < p.splits) acc += v[sl];
-                        if (nvalid) store_out<BF16>(p.out, (size_t)m * p.N + n, alpha * acc + bias_v);
+                            for (int j = 0; j < CB; ++j) {
+                                const bool in = c0 + j < ncols;
+                                const size_t col = (size_t)(c_begin + c0 + j);
+                                v0[j] = in ? __ldcg(base + ((size_t)sl * BN + col) * TILE_N + r) : 0.0f;
+                                v1[j] = (in && two) ? __ldcg(base + ((size_t)(sl + 1) * BN + col) * TILE_N + r) : 0.0f;
+                            }
+#pragma unroll
+                            for (int j = 0; j < CB; ++j) {
+                                acc[j] += v0[j];
+                                if (two) acc[j] += v1[j];
+                            }
+                        }
+                        if (nvalid) {
+#pragma unroll
+                            for (int j = 0; j < CB; ++j)
+                                if (c0 + j < ncols)
+                                    store_out<BF16>(p.out, (size_t)(m0 + c_begin + c0 + j) * p.N + n,
+                                                    alpha * acc[j] + bias_v);
+                        }
                     }
                 }
             }
@@ -1059,7 +1084,17 @@ __global__ void __launch_bounds__(128 * (1 + NWG), (GemmCfg<FMT, BF16, BN, BK, S
             pend = it;
             has_pend = true;
         }
-        if (ok && has_pend) ok = epilogue(pend);
+        if (ok && has_pend) {
+            if (!PAIR && p.csplit) {
+                // split-K inside a cluster: the accumulator is read after the cluster
+                // barrier below, once every slice of the tile has finished its main loop
+                ok = __all_sync(0xffffffffu, bounded_wait(accfull_bar, accph, abort_flag, p.status,
+                                                          DEVICE_TIMEOUT_EPILOGUE, p.timeout_ns));
+                accph ^= 1u;
+            } else {
+                ok = epilogue(pend);
+            }
+        }
         // the last copies out have completed before the CTA exits
         if (C::STAGE_OUT && warp == 4 && lane == 0) ptx::bulk_wait_group0();
         if (ok) {
@@ -1077,6 +1112,74 @@ __global__ void __launch_bounds__(128 * (1 + NWG), (GemmCfg<FMT, BF16, BN, BK, S
 
     ptx::tc_fence_before();
     __syncthreads();
+    if (!PAIR && p.csplit) {
+        // Deterministic split-K inside a thread-block cluster (one CTA per slice, one
+        // item per CTA, slice = rank).  Every thread of every CTA of the cluster passes
+        // both cluster barriers, also after an abort, so no CTA can strand a peer.
+        // (1) every slice is past its main loop: the peers' stage memory is free;
+        // (2) each CTA sends its accumulator rows to the CTA that owns them (rows
+        //     [q R, q R + R) belong to rank q, R = ceil(128 / S)) as remote
+        //     shared-memory stores; (3) each CTA adds its own rows over the slices in
+        //     order 0..S-1 and stores them.
+        const bool good = *abort_flag == 0u;
+        const int S = p.splits;
+        const int R = (TILE_N + S - 1) / S;
+        const int q = (int)ptx::cluster_ctarank();
+        const Item it = decode_item(p, (int)blockIdx.x);
+        const int m0 = it.m_tile * BN;
+        ptx::cluster_sync();
+        if (good && warp >= 4) {
+            ptx::tc_fence_after();
+            const int ew = warp - 4, wg = ew >> 2, quarter = warp & 3;
+            const int r = quarter * 32 + lane;
+            const int owner = r / R;
+            const uint32_t dst = ptx::mapa_shared(
+                sbase + (uint32_t)(((q * R + (r - owner * R)) * C::CS_PITCH) * 4), (uint32_t)owner);
+            constexpr int COLS = BN / NWG;
+            constexpr int STEP = COLS >= 16 ? 16 : 8;
+            const uint32_t acc_addr = tmem + ((uint32_t)(quarter * 32) << 16) + (uint32_t)(wg * COLS);
+#pragma unroll 1
+            for (int cc = 0; cc < COLS; cc += STEP) {
+                uint32_t v[16];
+                if (STEP == 16) {
+                    ptx::tmem_ld16(acc_addr + cc, v);
+                } else {
+                    uint32_t v8[8];
+                    ptx::tmem_ld8(acc_addr + cc, v8);
+#pragma unroll
+                    for (int j = 0; j < 8; ++j) v[j] = v8[j];
+                }
+                ptx::tmem_wait_ld();
+#pragma unroll
+                for (int j = 0; j < STEP; ++j)
+                    ptx::st_shared_cluster_f32(dst + (uint32_t)(wg * COLS + cc + j) * 4u, __uint_as_float(v[j]));
+            }
+        }
+        ptx::tc_fence_before();
+        ptx::cluster_sync();
+        if (good) {
+            ptx::grid_dependency_wait();   // outputs may still be in use by the previous kernel
+            const float alpha = group_scaled(FMT) ? 1.0f : __ldg(p.alpha);
+            const int row0 = q * R;
+            const int rows = min(TILE_N, row0 + R) - row0;
+            const int mval = min(BN, p.M - m0);
+            const float* box = reinterpret_cast<const float*>(smem);
+            const int nbase = it.n_tile * TILE_N + row0;
+            // consecutive threads take consecutive weight rows: conflict-free inbox
+            // reads (odd pitch) and coalesced output stores
+            for (int e = threadIdx.x; e < rows * mval; e += C::NT) {
+                const int j = e % rows, cc = e / rows;
+                const int n = nbase + j;
+                float acc = 0.0f;
+                for (int sl = 0; sl < S; ++sl) acc += box[(sl * R + j) * C::CS_PITCH + cc];
+                if (n < p.N) {
+                    float b = 0.0f;
+                    if (FMT == FMT_FP8 && p.bias != nullptr) b = load_16bit<BF16>(p.bias, (size_t)n);
+                    store_out<BF16>(p.out, (size_t)(m0 + cc) * p.N + n, alpha * acc + b);
+                }
+            }
+        }
+    }
     // pair: neither CTA leaves (or frees its tensor memory) while the other may
     // still signal it or run MMAs on its operands
     if (PAIR) ptx::cluster_sync();
@@ -1104,6 +1207,9 @@ struct GemmLauncher {
         if (e == cudaSuccess)
             e = cudaFuncSetAttribute(kernel,
                                      cudaFuncAttributePreferredSharedMemoryCarveout, 100);
+        // split-K clusters of up to 16 CTAs (non-portable size)
+        if (e == cudaSuccess && C::CSPLIT_OK)
+            e = cudaFuncSetAttribute(kernel, cudaFuncAttributeNonPortableClusterSizeAllowed, 1);
         if (e == cudaSuccess && dev < 64) attr_set[dev] = 1;
         return e;
     }
@@ -1149,6 +1255,29 @@ struct GemmLauncher {
             else (void)cudaGetLastError();
             k.pair = 1;
         }
+        if (C::CSPLIT_OK) {
+            // split-K clusters of S = 2..16 CTAs the GPU holds at once (0: not launchable)
+            for (int S = 2; S <= kMaxDecodeCluster; ++S) {
+                cudaLaunchConfig_t lc = {};
+                lc.gridDim = dim3((unsigned)S, 1, 1);
+                lc.blockDim = dim3(C::NT, 1, 1);
+                lc.dynamicSmemBytes = C::SMEM_BYTES;
+                cudaLaunchAttribute at[1];
+                at[0].id = cudaLaunchAttributeClusterDimension;
+                at[0].val.clusterDim.x = (unsigned)S;
+                at[0].val.clusterDim.y = 1;
+                at[0].val.clusterDim.z = 1;
+                lc.attrs = at;
+                lc.numAttrs = 1;
+                int nc = 0;
+                if (cudaOccupancyMaxActiveClusters(&nc, kernel, &lc) != cudaSuccess) {
+                    (void)cudaGetLastError();
+                    nc = 0;
+                }
+                k.max_clusters[S] = nc;
+            }
+            k.csplit_ok = 1;
+        }
         return k;
     }
     static cudaError_t launch(const GemmParams& p, int grid, cudaStream_t st) {
@@ -1169,6 +1298,16 @@ struct GemmLauncher {
             if (grid % 2 != 0) return cudaErrorInvalidValue;
             attr[1].id = cudaLaunchAttributeClusterDimension;
             attr[1].val.clusterDim.x = 2;
+            attr[1].val.clusterDim.y = 1;
+            attr[1].val.clusterDim.z = 1;
+            cfg.numAttrs = 2;
+        } else if (p.csplit) {
+            // one CTA per (tile, slice), the slices of a tile one cluster
+            if (!C::CSPLIT_OK || p.splits < 2 || p.splits > kMaxDecodeCluster || grid != p.n_items ||
+                grid % p.splits != 0)
+                return cudaErrorInvalidValue;
+            attr[1].id = cudaLaunchAttributeClusterDimension;
+            attr[1].val.clusterDim.x = (unsigned)p.splits;
             attr[1].val.clusterDim.y = 1;
             attr[1].val.clusterDim.z = 1;
             cfg.numAttrs = 2;

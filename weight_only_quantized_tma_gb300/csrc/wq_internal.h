@@ -90,6 +90,7 @@ struct GemmParams {
     const float* alpha;      // FP8 / FP4 global scale (device), unused for INT4
     const void* bias;        // FP8 optional bias [N], same 16-bit type as A
     void* out;               // [M][N], 16-bit
+    int csplit;              // split-K slices of a tile are one thread-block cluster (no workspace)
     float* ws_part;          // split-K partials
     uint32_t* ws_count;      // split-K arrival tickets, one per output tile
     uint32_t* status;        // device status word (WQ_DEVICE_* bits)
@@ -138,6 +139,7 @@ struct KernelConfig {
     int ctas_per_sm;  // resident CTAs per SM (registers, shared and tensor memory)
     int max_clusters[kMaxDecodeCluster + 1];  // S-CTA clusters held at once (decode: S = 2..16; pair: S = 2)
     int pair;        // tile kernel on two-CTA clusters (tcgen05 cta_group::2, 256 weight rows per tile)
+    int csplit_ok;   // tile kernel: split-K slices can be reduced inside a cluster (max_clusters[S])
 };
 
 // Per-format launch entry points, defined in wq_gemm_{int4,fp8,fp4}.cu.
