@@ -171,9 +171,10 @@ wq_status wq_pack_int4_zeros(const uint8_t* z_canon, int64_t N, int64_t K, int32
 /* W4A16 GEMM with zero points: out[M][N] = A[M][K] . ((q - Z) * S)^T.  Arguments as
  * for wq_gemm_w4a16 plus z_kernel (wq_pack_int4_zeros output, 16-byte aligned), the
  * workspace sized for WQ_OP_W4A16_ZP.  The operand is RN((q - Z) * s) in the type of
- * A (q - Z is exact), accumulated in fp32; every M runs on the tile kernels (the
- * M <= 16 register kernel has no zero-point path).  The same rule on the kernel
- * before the call holds, now for z_kernel as well. */
+ * A (q - Z is exact), accumulated in fp32, on the tile kernels; for M <= 16 with
+ * K % 64 == 0 the register decode kernel forms s * (sum_k A (q - 8) + (8 - Z) sum_k A)
+ * per group in fp32 instead (exact products, no operand rounding).  The same rule on
+ * the kernel before the call holds, now for z_kernel as well. */
 wq_status wq_gemm_w4a16_zp(const void* A, wq_dtype a_dtype, const uint8_t* w_kernel, const void* s_kernel,
                            const uint8_t* z_kernel, int64_t M, int64_t N, int64_t K, int32_t G, void* out, void* ws,
                            size_t ws_bytes, wq_stream_t stream);

@@ -108,11 +108,12 @@ def test_lut_identity_A_pair_kernel_bit_exact(a_dtype):
 
 
 @pytest.mark.parametrize("a_dtype", ["f16", "bf16"])
-@pytest.mark.parametrize("M", [4, 200, 4096])
-def test_lut_uniform_grid_matches_int4_bitwise(M, a_dtype):
+@pytest.mark.parametrize("M,K,G", [(4, 1056, 32), (200, 1024, 128), (4096, 1024, 128)])
+def test_lut_uniform_grid_matches_int4_bitwise(M, K, G, a_dtype):
     # LUT[q] = q - 8 gives the symmetric operand RN((q - 8) * s): the same bits as the
-    # zero-point kernel with Z = 8 (tile kernels at every M, the same tiling)
-    N, K, G = 512, 1024, 128
+    # zero-point tile kernel with Z = 8 (K % 64 != 0 keeps M = 4 off the register
+    # decode kernel, which the zero-point entry takes for M <= 16)
+    N = 512
     p = LutProblem(M, N, K, G, a_dtype=a_dtype, seed=706, lut=(np.arange(16) - 8.0).astype(np.float16).view(np.uint16))
     got = p.run()
     z = wq.wq_pack_int4_zeros(torch.full((K // G, N), 8, dtype=torch.uint8, device=DEV), N, K, G)
@@ -223,8 +224,8 @@ def test_int2_identity_A_pair_kernel_bit_exact(a_dtype):
 @pytest.mark.parametrize("M", [4, 200, 4096])
 def test_int2_matches_int4_shifted_codes_bitwise(M, a_dtype):
     # an INT2 code q has the operand of the INT4 code q + 6; the tile kernels tile both
-    # formats alike, so the outputs agree bit for bit (INT4 through the zero-point
-    # entry with Z = 8, which takes the tile kernels at every M)
+    # formats alike, so the outputs agree bit for bit (INT4 through the codebook entry
+    # with the uniform-grid table LUT[q] = q - 8, which takes the tile kernels at every M)
     N, K, G = 512, 1024, 64
     rng = np.random.default_rng(723)
     q = rng.integers(0, 4, size=(N, K), dtype=np.uint8)
@@ -232,8 +233,8 @@ def test_int2_matches_int4_shifted_codes_bitwise(M, a_dtype):
     got = p.run()
     w4 = torch.from_numpy(oracle.pack_int4((q + 6).astype(np.uint8))).to(DEV)
     wk, sk = wq.wq_pack_int4(w4, p.s_d, N, K, G)
-    z = wq.wq_pack_int4_zeros(torch.full((K // G, N), 8, dtype=torch.uint8, device=DEV), N, K, G)
-    ref = wq.wq_gemm_w4a16_zp(p.A_d, wk, sk, z, N, K, G)
+    grid = to_dev_f16bits((np.arange(16) - 8.0).astype(np.float16).view(np.uint16), "f16")
+    ref = wq.wq_gemm_w4a16_lut(p.A_d, wk, sk, grid, N, K, G)
     torch.cuda.synchronize()
     assert torch.equal(got.view(torch.int16), ref.view(torch.int16))
 

@@ -113,7 +113,8 @@ def test_zero_point_eight_matches_symmetric_bitwise(a_dtype):
 def test_random_vs_oracle(M, N, K, G, a_dtype):
     p = ZpProblem(M, N, K, G, a_dtype=a_dtype, seed=604 + M + K)
     plan = wq.get_plan(wq.WQ_OP_W4A16_ZP, wq.WQ_BF16 if a_dtype == "bf16" else wq.WQ_F16, M, N, K, G)
-    assert plan["kernel"] != wq.WQ_KERNEL_DECODE
+    # M <= 16 with K % 64 == 0 takes the register decode kernel, the rest the tile kernels
+    assert (plan["kernel"] == wq.WQ_KERNEL_DECODE) == (M <= 16 and K % 64 == 0)
     out = p.run()
     torch.cuda.synchronize()
     _check(p, out, None, f"zp M{M} N{N} K{K} G{G}")
@@ -143,3 +144,44 @@ def test_bad_arguments():
     assert st == 3   # WQ_ERR_GROUP
     st = lib.wq_pack_int4_zeros(p.zk.data_ptr(), N, K, G, p.zk.data_ptr() + 1, None)
     assert st == 4   # WQ_ERR_MISALIGNED
+
+
+# ------------------------------------------------------------------ decode kernel (M <= 16)
+
+@pytest.mark.parametrize("a_dtype", ["f16", "bf16"])
+@pytest.mark.parametrize("M,G", [(1, 128), (5, 32), (16, 64), (9, 256)])
+def test_decode_zero_point_eight_matches_symmetric_bitwise(M, G, a_dtype):
+    # Z = 8: the fold adds (8 - z) S_g = 0 exactly, so the bits equal the symmetric
+    # decode kernel's
+    N, K = 1024, 2048
+    z = np.full((K // G, N), 8, dtype=np.uint8)
+    p = ZpProblem(M, N, K, G, a_dtype=a_dtype, seed=610 + M, z=z)
+    assert wq.get_plan(wq.WQ_OP_W4A16_ZP, wq.WQ_BF16 if a_dtype == "bf16" else wq.WQ_F16, M, N, K, G)["kernel"] \
+        == wq.WQ_KERNEL_DECODE
+    got = p.run()
+    sym = wq.wq_gemm_w4a16(p.A_d, p.wk, p.sk, N, K, G)
+    torch.cuda.synchronize()
+    assert torch.equal(got.view(torch.int16), sym.view(torch.int16))
+
+
+@pytest.mark.parametrize("a_dtype", ["f16", "bf16"])
+@pytest.mark.parametrize("G", [32, 64, 128, 256])
+def test_decode_identity_rows_bit_exact(G, a_dtype):
+    # A = the first 16 rows of the identity: out[m, n] = RN((q[n, m] - z) * s) exactly
+    # (one non-zero product, and the fold's (b + z) S_g terms are exact integers times 1)
+    M, N, K = 16, 384, 512
+    A = _eye_bits(K, a_dtype)[:M].copy()
+    p = ZpProblem(M, N, K, G, a_dtype=a_dtype, seed=611, A_bits=A)
+    out = p.run()
+    torch.cuda.synchronize()
+    w = oracle.dequant_int4_zp(p.wts.w, p.wts.s, p.z, K, G).astype(np.float64)
+    rn = oracle.round_f16_array(w.T[:M]) if a_dtype == "f16" else oracle.round_bf16_array(w.T[:M])
+    assert np.array_equal(out_bits(out), rn)
+
+
+@pytest.mark.parametrize("case", synth.DECODE, ids=lambda c: f"M{c.M}_N{c.N}_K{c.K}")
+def test_decode_configs_with_zero_points(case):
+    p = ZpProblem(case.M, case.N, case.K, case.G, seed=612 + case.M + case.N)
+    out = p.run()
+    torch.cuda.synchronize()
+    _check(p, out, None, f"zp decode {case}")

@@ -112,6 +112,7 @@ struct Plan {
 
 bool get_config_uncached(int fmt, bool bf16, int bn, bool query, KernelConfig* cfg) {
     if (fmt == FMT_INT4 + 16) return config_int4_decode(bf16, query, cfg);
+    if (fmt == FMT_INT4 + 17) return config_int4_decode_zp(bf16, query, cfg);
     if (fmt == FMT_INT4 + 32) return config_int4_pair(bf16, query, cfg);
     if (fmt == FMT_FP8 + 32) return config_fp8_pair(bf16, query, cfg);
     if (fmt == FMT_FP4 + 32) return bf16 && config_fp4_pair(query, cfg);
@@ -129,8 +130,9 @@ bool get_config_uncached(int fmt, bool bf16, int bn, bool query, KernelConfig* c
 
 // The device query behind a configuration (attributes, residency) is done once per
 // device and instantiation; later calls read the cached answer.
-// Slots: the tile formats 0 .. kNumFmts - 1, the W4A16 decode kernel, the pair kernels.
-constexpr int kCfgSlots = 2 * kNumFmts + 1;
+// Slots: the tile formats 0 .. kNumFmts - 1, the W4A16 decode kernels (symmetric, zero
+// point), the pair kernels.
+constexpr int kCfgSlots = 2 * kNumFmts + 2;
 struct ConfigCache {
     std::mutex mu;
     bool have[kMaxDevices][kCfgSlots][2][4] = {};
@@ -141,7 +143,7 @@ ConfigCache g_cfg_cache;
 
 bool get_config(int fmt, bool bf16, int bn, bool query, KernelConfig* cfg) {
     const int bi = bn == 16 ? 0 : bn == 64 ? 1 : bn == 128 ? 2 : bn == 256 ? 3 : -1;
-    const int fi = fmt == FMT_INT4 + 16 ? kNumFmts : fmt >= 32 ? kNumFmts + 1 + (fmt - 32) : fmt;
+    const int fi = (fmt >= 16 && fmt < 32) ? kNumFmts + (fmt - 16) : fmt >= 32 ? kNumFmts + 2 + (fmt - 32) : fmt;
     int dev = 0;
     if (!query || bi < 0 || fi < 0 || fi >= kCfgSlots || cudaGetDevice(&dev) != cudaSuccess || dev < 0 ||
         dev >= kMaxDevices)
@@ -180,14 +182,15 @@ size_t split_ws_bytes(int tiles, int splits, int bn) {
 //    the weight is the smaller operand, walk weight-row tiles fastest so the
 //    activation panel being reused stays in L2, else walk token tiles fastest.
 wq_status make_plan(int fmt, bool bf16, int64_t M, int64_t N, int64_t K, int sms, int w_bits, Plan* plan,
-                    int G = 0, bool allow_decode = true) {
+                    int G = 0, int decode_kind = 0) {
     static const int kTiles[4] = {16, 64, 128, 256};
     KernelConfig cfg{};
     bool found = false;
     // decode (M <= 16): the register-resident kernel; its activation copy views A
     // as 64-wide boxes, so it needs K % 64 == 0
-    const bool decode = allow_decode && fmt == FMT_INT4 && M <= 16 && K % 64 == 0;
-    if (decode) found = get_config(FMT_INT4 + 16, bf16, 16, sms > 0, &cfg);
+    // decode_kind: 0 symmetric, 1 zero points, -1 no decode kernel
+    const bool decode = decode_kind >= 0 && fmt == FMT_INT4 && M <= 16 && K % 64 == 0;
+    if (decode) found = get_config(FMT_INT4 + 16 + decode_kind, bf16, 16, sms > 0, &cfg);
     for (int i = 0; i < 4 && !found; ++i) {
         if (M <= kTiles[i] || i == 3) found = get_config(fmt, bf16, kTiles[i], sms > 0, &cfg);
     }
@@ -307,11 +310,11 @@ wq_status make_plan(int fmt, bool bf16, int64_t M, int64_t N, int64_t K, int sms
 
 int w_bits_of(int fmt) { return fmt == FMT_FP8 ? 8 : fmt == FMT_INT2 ? 2 : 4; }
 
-wq_status plan_for(int fmt, bool bf16, int64_t M, int64_t N, int64_t K, Plan* plan, int G, bool allow_decode) {
+wq_status plan_for(int fmt, bool bf16, int64_t M, int64_t N, int64_t K, Plan* plan, int G, int decode_kind) {
     DeviceInfo* d = nullptr;
     wq_status st = device_info(&d);
     if (st != WQ_OK) return st;
-    return make_plan(fmt, bf16, M, N, K, d->sms, w_bits_of(fmt), plan, G, allow_decode);
+    return make_plan(fmt, bf16, M, N, K, d->sms, w_bits_of(fmt), plan, G, decode_kind);
 }
 
 void fill_common(GemmParams& gp, const Plan& pl, int64_t M, int64_t N, int64_t K, void* out, void* ws,
@@ -567,7 +570,8 @@ wq_status wq_get_plan(wq_op op, wq_dtype a_dtype, int64_t M, int64_t N, int64_t 
     if (a_dtype != WQ_F16 && a_dtype != WQ_BF16) return WQ_ERR_DTYPE;
     const bool bf16 = (op == WQ_OP_FP4) ? true : (a_dtype == WQ_BF16);
     Plan pl{};
-    wq_status st = plan_for(fmt, bf16, M > 0 ? M : 1, N, K, &pl, grouped ? G : 0, op == WQ_OP_W4A16);
+    wq_status st = plan_for(fmt, bf16, M > 0 ? M : 1, N, K, &pl, grouped ? G : 0,
+                            op == WQ_OP_W4A16 ? 0 : op == WQ_OP_W4A16_ZP ? 1 : -1);
     if (st != WQ_OK) return st;
     if (plan) {
         plan->bn = pl.cfg.bn;
@@ -617,7 +621,7 @@ static wq_status gemm_int4(const void* A, wq_dtype a_dtype, const uint8_t* w_ker
     if (M == 0) return WQ_OK;
     const bool bf16 = a_dtype == WQ_BF16;
     Plan pl{};
-    if ((st = make_plan(fmt, bf16, M, N, K, d->sms, 4, &pl, G, z_kernel == nullptr)) != WQ_OK) return st;
+    if ((st = make_plan(fmt, bf16, M, N, K, d->sms, 4, &pl, G, z_kernel ? 1 : 0)) != WQ_OK) return st;
     if ((st = check_ws(pl, ws, ws_bytes)) != WQ_OK) return st;
     GemmParams gp;
     std::memset(&gp, 0, sizeof(gp));
@@ -636,7 +640,9 @@ static wq_status gemm_int4(const void* A, wq_dtype a_dtype, const uint8_t* w_ker
     gp.ngroups_pad = (int)(Kp / G);
     gp.nchunks_pad = (int)(Kp / 32);
     fill_common(gp, pl, M, N, K, out, ws, d->status);
-    if (pl.decode) return finish_launch(launch_gemm_int4_decode(gp, bf16, pl.grid, (cudaStream_t)stream));
+    if (pl.decode)
+        return finish_launch(z_kernel ? launch_gemm_int4_decode_zp(gp, bf16, pl.grid, (cudaStream_t)stream)
+                                      : launch_gemm_int4_decode(gp, bf16, pl.grid, (cudaStream_t)stream));
     if (fmt == FMT_LUT4)
         return finish_launch(pl.pair ? launch_gemm_lut4_pair(gp, bf16, pl.grid, (cudaStream_t)stream)
                                      : launch_gemm_lut4(gp, bf16, pl.cfg.bn, pl.grid, (cudaStream_t)stream));

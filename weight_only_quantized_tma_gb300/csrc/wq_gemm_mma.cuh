@@ -41,7 +41,7 @@
 
 namespace wq {
 
-template <int BK, int STAGES>
+template <int BK, int STAGES, bool ZP = false>
 struct MmaDecodeCfg {
     static constexpr int NCW = 4;                             // compute warps
     static constexpr int RGW = TILE_N / 16 / NCW;             // 16-row groups per compute warp
@@ -55,7 +55,11 @@ struct MmaDecodeCfg {
     static constexpr int W_STAGE = TILE_N * BK / 2;
     static constexpr int SC_OFF = W_STAGE;
     static constexpr int S_OFF = SC_OFF + (BK / 32) * TILE_N * 2;
-    static constexpr int WS_STAGE = S_OFF + (BK / 32) * 2 * 16 * 4;   // -(b + 8) S_g[m], fp32 [BK / 32][2][16]
+    // zero-point variant: the stage's zero points (uint8 [BK / 32][128]) and the plain
+    // activation sums S_g[m] (fp32 [BK / 32][16])
+    static constexpr int Z_OFF = S_OFF + (BK / 32) * 2 * 16 * 4;   // after -(b + 8) S_g[m], fp32 [BK / 32][2][16]
+    static constexpr int SR_OFF = Z_OFF + (ZP ? (BK / 32) * TILE_N : 0);
+    static constexpr int WS_STAGE = SR_OFF + (ZP ? (BK / 32) * 16 * 4 : 0);
     static constexpr int A_STAGE = 16 * 128 * NZ;             // up to 16 token rows of 128 bytes per box
     static constexpr int A_BASE = (STAGES * WS_STAGE + 1023) / 1024 * 1024;
     // split-K inbox: the partial sums the S CTAs of a cluster send to the CTA that
@@ -124,9 +128,9 @@ __device__ __forceinline__ void int4_word_to_frag(uint32_t w, uint32_t (&a)[4]) 
 // steps per scale group inside a 128-value stage (2, 4 or 8; G >= 128 folds once per
 // stage).  One CTA per item (tile, K slice): gridDim.x == n_items, and the slices of
 // a tile form one cluster of p.splits CTAs.
-template <bool BF16, int NT, int GSTEPS, int BK, int STAGES>
+template <bool BF16, int NT, int GSTEPS, int BK, int STAGES, bool ZP = false>
 __global__ void __launch_bounds__(192) wq_decode_mma_kernel(const __grid_constant__ GemmParams p) {
-    using C = MmaDecodeCfg<BK, STAGES>;
+    using C = MmaDecodeCfg<BK, STAGES, ZP>;
     constexpr int NZ = C::NZ;
     constexpr int NCW = C::NCW;
     constexpr int RGW = C::RGW;
@@ -207,16 +211,20 @@ __global__ void __launch_bounds__(192) wq_decode_mma_kernel(const __grid_constan
             const uint64_t pol_a = ptx::policy_evict_last();
             const int gcnt = (p.G >= BK) ? 1 : (BK >> p.g_shift);
             const uint32_t sc_bytes = (uint32_t)gcnt * TILE_N * 2;
+            const uint32_t zp_bytes = ZP ? (uint32_t)gcnt * TILE_N : 0u;
             auto load_w = [&](int s, int kb) {
                 const uint32_t fb = full_bar(s);
                 const uint32_t st = sbase + s * C::WS_STAGE;
-                ptx::mbar_arrive_expect_tx(fb, (uint32_t)C::W_STAGE + sc_bytes + a_bytes);
+                ptx::mbar_arrive_expect_tx(fb, (uint32_t)C::W_STAGE + sc_bytes + zp_bytes + a_bytes);
                 const uint8_t* wsrc =
                     p.w + ((size_t)tile * p.nchunks_pad + (size_t)kb * (BK / 32)) * (TILE_N * 16);
                 ptx::bulk_load(st, wsrc, C::W_STAGE, fb, pol_w);
                 const int g0 = (kb * BK) >> p.g_shift;
                 const uint8_t* ssrc = p.sc + ((size_t)tile * p.ngroups_pad + g0) * (TILE_N * 2);
                 ptx::bulk_load(st + C::SC_OFF, ssrc, sc_bytes, fb, pol_w);
+                if (ZP)
+                    ptx::bulk_load(st + C::Z_OFF, p.zp + ((size_t)tile * p.ngroups_pad + g0) * TILE_N, zp_bytes, fb,
+                                   pol_w);
             };
             for (int i = 0; i < pre; ++i) load_w(i, it.kb_begin + i);
             ptx::grid_dependency_wait();
@@ -295,6 +303,10 @@ __global__ void __launch_bounds__(192) wq_decode_mma_kernel(const __grid_constan
                         *reinterpret_cast<float2*>(dst + m) = make_float2(-CORR_LO * sacc[nt][0], -CORR_LO * sacc[nt][1]);
                         *reinterpret_cast<float2*>(dst + 16 + m) =
                             make_float2(-CORR_HI * sacc[nt][0], -CORR_HI * sacc[nt][1]);
+                        if (ZP) {
+                            float* raw = reinterpret_cast<float*>(smem + s * C::WS_STAGE + C::SR_OFF) + (t / GSTEPS) * 16;
+                            *reinterpret_cast<float2*>(raw + m) = make_float2(sacc[nt][0], sacc[nt][1]);
+                        }
                     }
                 }
             }
@@ -371,19 +383,32 @@ __global__ void __launch_bounds__(192) wq_decode_mma_kernel(const __grid_constan
                     for (int nt = 0; nt < NT; ++nt) mma_16816(tmp[j][t % SETS][nt], a, b[nt][0], b[nt][1], BF16);
                 }
                 if ((t + 1) % GSTEPS == 0) {
-                    // acc += s * (D - (b + 8) S_g)
+                    // acc += s * (D - (b + 8) S_g); with zero points z per row,
+                    // D - (b + z) S_g = (D - (b + 8) S_g) + (8 - z) S_g
                     const int gi = t / GSTEPS;
 #pragma unroll
                     for (int j = 0; j < RGW; ++j) {
                         const uint16_t* sp = sc + gi * TILE_N + (warp * RGW + j) * 16 + g;
                         const float s_lo = __half2float(__ushort_as_half(sp[0]));
                         const float s_hi = __half2float(__ushort_as_half(sp[8]));
+                        float dz_lo = 0.0f, dz_hi = 0.0f;
+                        float2 sraw[NT];
+                        if constexpr (ZP) {
+                            const uint8_t* zp = stp + C::Z_OFF + gi * TILE_N + (warp * RGW + j) * 16 + g;
+                            dz_lo = (float)(8 - (int)zp[0]);
+                            dz_hi = (float)(8 - (int)zp[8]);
+                            const float* raw = reinterpret_cast<const float*>(stp + C::SR_OFF) + gi * 16;
+#pragma unroll
+                            for (int nt = 0; nt < NT; ++nt)
+                                sraw[nt] = *reinterpret_cast<const float2*>(raw + nt * 8 + 2 * c);
+                        }
 #pragma unroll
                         for (int nt = 0; nt < NT; ++nt)
 #pragma unroll
                             for (int e = 0; e < 4; ++e) {
                                 float d = tmp[j][0][nt][e];
                                 if constexpr (SETS == 2) d += tmp[j][1][nt][e];
+                                if constexpr (ZP) d = fmaf((e < 2) ? dz_lo : dz_hi, (e & 1) ? sraw[nt].y : sraw[nt].x, d);
                                 acc[j][nt][e] = fmaf((e < 2) ? s_lo : s_hi, d, acc[j][nt][e]);
                             }
                     }
@@ -464,10 +489,10 @@ __global__ void __launch_bounds__(192) wq_decode_mma_kernel(const __grid_constan
     }
 }
 
-template <bool BF16, int NT, int GSTEPS, int BK, int STAGES>
+template <bool BF16, int NT, int GSTEPS, int BK, int STAGES, bool ZP = false>
 struct MmaDecodeLauncher {
-    using C = MmaDecodeCfg<BK, STAGES>;
-    static constexpr auto kernel = wq_decode_mma_kernel<BF16, NT, GSTEPS, BK, STAGES>;
+    using C = MmaDecodeCfg<BK, STAGES, ZP>;
+    static constexpr auto kernel = wq_decode_mma_kernel<BF16, NT, GSTEPS, BK, STAGES, ZP>;
     static cudaError_t prepare() {
         static int attr_set[64] = {0};
         int dev = 0;

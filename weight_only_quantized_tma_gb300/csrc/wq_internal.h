@@ -156,6 +156,9 @@ bool config_int4(bool bf16, int bn, bool query, KernelConfig* cfg);
 // two-column-tile instantiation; both use the same shared memory and threads.
 bool config_int4_decode(bool bf16, bool query, KernelConfig* cfg);
 cudaError_t launch_gemm_int4_decode(const GemmParams& p, bool bf16, int grid, cudaStream_t st);
+// The same decode kernel with per-(group, row) zero points (wq_gemm_zp_decode.cu).
+bool config_int4_decode_zp(bool bf16, bool query, KernelConfig* cfg);
+cudaError_t launch_gemm_int4_decode_zp(const GemmParams& p, bool bf16, int grid, cudaStream_t st);
 // W4A16 tile kernel on two-CTA clusters (256 weight rows x 256 tokens per tile).
 bool config_int4_pair(bool bf16, bool query, KernelConfig* cfg);
 cudaError_t launch_gemm_int4_pair(const GemmParams& p, bool bf16, int grid, cudaStream_t st);
