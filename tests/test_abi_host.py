@@ -118,3 +118,52 @@ def test_python_binding_rejects_bad_tensors():
     with pytest.raises(ValueError):
         wq.wq_gemm_w4a16(torch.zeros(4, 64, dtype=torch.float32), torch.zeros(1, dtype=torch.uint8),
                          torch.zeros(1, dtype=torch.float16), 128, 64, 32)
+
+
+def test_gemm_lut_validation(L):
+    f = L.wq_gemm_w4a16_lut
+    assert f(P, 0, P, P, None, 4, 512, 1024, 128, P, None, 0, None) == NULL        # the table
+    assert f(P, 0, P, P, P, 4, 512, 1000, 128, P, None, 0, None) == SHAPE          # K % 32
+    assert f(P, 0, P, P, P, 4, 512, 1024, 96, P, None, 0, None) == GROUP
+    assert f(P, 0, P, P, P + 2, 4, 512, 1024, 128, P, None, 0, None) == MISALIGNED  # two 16-byte vectors
+    # an empty problem is valid and touches nothing
+    assert f(None, 0, None, None, None, 0, 512, 1024, 128, None, None, 0, None) == OK
+    d = L.wq_debug_dequant_int4_lut
+    assert d(P, P, None, 512, 1024, 128, P, None) == NULL
+    assert d(P, P, P + 1, 512, 1024, 128, P, None) == MISALIGNED
+
+
+def test_int2_sizes_and_validation(L):
+    b = ctypes.c_size_t()
+    assert L.wq_int2_packed_scales_bytes(4096, 4096, 128, ctypes.byref(b)) == OK
+    assert b.value == 4096 * 32 * 2
+    assert L.wq_int2_packed_scales_bytes(200, 192, 64, ctypes.byref(b)) == OK
+    assert b.value == 256 * (256 // 64) * 2          # N -> 256, K -> 256
+    assert L.wq_int2_packed_scales_bytes(128, 96, 32, ctypes.byref(b)) == SHAPE    # K % 64
+    assert L.wq_int2_packed_scales_bytes(128, 256, 48, ctypes.byref(b)) == GROUP
+    f = L.wq_gemm_w2a16
+    assert f(P, 0, None, P, 4, 512, 1024, 128, P, None, 0, None) == NULL
+    assert f(P, 0, P, P, 4, 512, 1056, 32, P, None, 0, None) == SHAPE              # K % 64
+    assert f(P, 0, P, P, 4, 500, 1024, 128, P, None, 0, None) == SHAPE             # N % 8
+    assert f(P, 0, P, P, 4, 512, 1024, 96, P, None, 0, None) == GROUP
+    assert f(P, 5, P, P, 4, 512, 1024, 128, P, None, 0, None) == DTYPE
+    assert f(P, 0, P + 4, P, 4, 512, 1024, 128, P, None, 0, None) == MISALIGNED
+    assert f(None, 0, None, None, 0, 512, 1024, 128, None, None, 0, None) == OK
+    assert L.wq_pack_int2_scales(None, 128, 256, 128, P, None) == NULL
+    assert L.wq_pack_int2_scales(P, 128, 256, 128, P + 8, None) == MISALIGNED
+    assert L.wq_debug_dequant_int2(P, P, 128, 200, 40, P, None) == SHAPE
+
+
+def test_gemm_zp_validation(L):
+    f = L.wq_gemm_w4a16_zp
+    assert f(P, 0, P, P, None, 4, 512, 1024, 128, P, None, 0, None) == NULL
+    assert f(P, 0, P, P, P + 8, 4, 512, 1024, 128, P, None, 0, None) == MISALIGNED
+    assert f(None, 0, None, None, None, 0, 512, 1024, 128, None, None, 0, None) == OK
+
+
+def test_plan_ops_are_validated(L):
+    plan = _lib.WqPlan()
+    n = ctypes.c_size_t()
+    assert L.wq_get_plan(9, 0, 4, 512, 1024, 128, ctypes.byref(plan), ctypes.byref(n)) == SHAPE
+    assert L.wq_get_plan(_lib.WQ_OP_W2A16, 0, 4, 512, 1024, 100, ctypes.byref(plan), ctypes.byref(n)) == GROUP
+    assert L.wq_get_plan(_lib.WQ_OP_W4A16_LUT, 3, 4, 512, 1024, 128, ctypes.byref(plan), ctypes.byref(n)) == DTYPE
