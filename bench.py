@@ -190,6 +190,16 @@ def cpu_oracle_decode(step_fraction_cols, min_seconds, seed_base=1000):
     return byts / elapsed / 1e9, elapsed, oracle.num_threads(), sample
 
 
+def max_over_ranks(x, world, device="cpu"):
+    """The largest value over all ranks (the slowest rank's time); x itself on one rank."""
+    if world <= 1:
+        return float(x)
+    import torch
+    t = torch.tensor([float(x)], dtype=torch.float64, device=device)
+    torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
+    return float(t.item())
+
+
 def run_reference(args, rank, world):
     if rank != 0:
         return
@@ -302,11 +312,8 @@ def run_ours(args, rank, world, local_rank):
             ev1.record(stream)
         torch.cuda.synchronize(dev)
         barrier()
-    step_ms = ev0.elapsed_time(ev1) / args.steps
-    if world > 1:
-        t = torch.tensor([step_ms], device=dev)
-        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
-        step_ms = float(t.item())
+    step_ms = max_over_ranks(ev0.elapsed_time(ev1) / args.steps, world, dev)
+    # whole job: every rank (an independent replica) streams step_bytes per step
     value = step_bytes * world / (step_ms * 1e-3) / 1e9
 
     # ---------------- per-launch durations (CUDA events on the launching stream)
