@@ -60,7 +60,7 @@ def load_peaks():
 
 # The sources the decode kernel is compiled from (its own header, the helpers and PTX
 # wrappers it includes, the shared declarations and the instantiating unit).
-DECODE_KERNEL_SOURCES = ("wq_gemm_mma.cuh", "wq_gemm.cuh", "sm103_ptx.cuh", "wq_internal.h", "wq_gemm_int4.cu")
+DECODE_KERNEL_SOURCES = ("wq_gemm_mma.cuh", "wq_common.cuh", "sm103_ptx.cuh", "wq_internal.h", "wq_gemm_int4.cu")
 
 
 def kernel_source_hash():

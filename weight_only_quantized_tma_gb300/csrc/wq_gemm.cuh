@@ -53,6 +53,7 @@
 #include <cuda_fp16.h>
 
 #include "sm103_ptx.cuh"
+#include "wq_common.cuh"
 #include "wq_internal.h"
 
 namespace wq {
@@ -94,9 +95,10 @@ struct GemmCfg {
     static constexpr uint32_t W_SWZ = (W_PITCH == 128) ? 7u : (W_PITCH == 64) ? 3u : 1u;
     // Split-K inside a cluster: after the main loop the stage memory [0, OFF_STG) of
     // every CTA is an inbox for the fp32 partial rows the other slices send it,
-    // [slice][row][BN + 1] (the odd pitch keeps a warp's 32 rows on 32 banks); at most
+    // [slice][row][BN + 4] (16-byte rows for vector stores and loads; a warp's 32
+    // rows then fall on 8 bank quads, the minimum for 16-byte accesses); at most
     // S * ceil(128 / S) <= 143 rows for S <= 16.
-    static constexpr int CS_PITCH = BN + 1;
+    static constexpr int CS_PITCH = BN + 4;
     static constexpr int CS_INBOX = (TILE_N + 15) * CS_PITCH * 4;
     static constexpr bool CSPLIT_OK = !PAIR && CS_INBOX <= OFF_STG;
     // two CTAs per SM when shared and tensor memory allow it (decode, split-K)
@@ -109,45 +111,6 @@ struct GemmCfg {
     static_assert(SMEM_BYTES <= 227 * 1024, "shared memory");
     static_assert(B_STAGE % 1024 == 0 && W_STAGE % 1024 == 0, "1024-byte stage alignment");
 };
-
-// Physical byte offset of a logical offset inside a TMA-swizzled tile whose base
-// is 1024-byte aligned (16-byte chunk index XOR the 128-byte row index bits).
-__device__ __forceinline__ uint32_t swz(uint32_t a, uint32_t mask) { return a ^ (((a >> 7) & mask) << 4); }
-
-// Bounded wait on an mbarrier phase, executed by every lane that calls it.
-// Returns false if the CTA is aborting or the wait timed out (which starts the
-// abort).  The global timer is slow to read, so it is only consulted every 256
-// failed probes; the abort flag (shared memory) is checked on every probe.
-// CLUSTER: the barrier receives arrivals from the other CTA of a cluster pair.
-template <bool CLUSTER = false>
-__device__ __forceinline__ bool bounded_wait(uint32_t bar, uint32_t parity, volatile uint32_t* abort_flag,
-                                             uint32_t* status, uint32_t code, long long timeout_ns) {
-    if (ptx::mbar_try_wait<CLUSTER>(bar, parity)) return true;
-    uint64_t t0 = 0;
-    for (uint32_t i = 1;; ++i) {
-        if (ptx::mbar_try_wait<CLUSTER>(bar, parity)) return true;
-        if (*abort_flag) return false;
-        if ((i & 255u) == 0u) {
-            const uint64_t now = ptx::globaltimer();
-            if (t0 == 0) {
-                t0 = now;
-            } else if ((long long)(now - t0) > timeout_ns) {
-                *abort_flag = 1u;
-                atomicOr(status, code);
-                return false;
-            }
-        }
-    }
-}
-
-// Wait used while draining after an abort: ignores the abort flag.
-__device__ __forceinline__ bool drain_wait(uint32_t bar, uint32_t parity, long long timeout_ns) {
-    const uint64_t t0 = ptx::globaltimer();
-    for (uint32_t i = 1; !ptx::mbar_try_wait(bar, parity); ++i) {
-        if ((i & 255u) == 0u && (long long)(ptx::globaltimer() - t0) > timeout_ns) return false;
-    }
-    return true;
-}
 
 // ---------------------------------------------------------------- conversions
 
@@ -361,67 +324,6 @@ __device__ __forceinline__ void fp4_to_bf16(const uint4& q, uint16_t sf_pair, ui
 #pragma unroll
         for (int i = 0; i < 4; ++i) o[4 * j + i] = ptx::f16x2_to_bf16x2_exact(ptx::hmul2_u32(h[i], s2));
     }
-}
-
-template <bool BF16>
-__device__ __forceinline__ void store_out(void* out, size_t idx, float v) {
-    if (BF16)
-        reinterpret_cast<__nv_bfloat16*>(out)[idx] = __float2bfloat16_rn(v);
-    else
-        reinterpret_cast<__half*>(out)[idx] = __float2half_rn(v);
-}
-
-template <bool BF16>
-__device__ __forceinline__ uint16_t to_16bit(float v) {
-    if (BF16) return __bfloat16_as_ushort(__float2bfloat16_rn(v));
-    return __half_as_ushort(__float2half_rn(v));
-}
-
-template <bool BF16>
-__device__ __forceinline__ float load_16bit(const void* p, size_t idx) {
-    if (BF16) return __bfloat162float(reinterpret_cast<const __nv_bfloat16*>(p)[idx]);
-    return __half2float(reinterpret_cast<const __half*>(p)[idx]);
-}
-
-struct Item {
-    int n_tile, m_tile, slice, kb_begin, kb_end;
-    int half;    // 1: a half tile (half_bn tokens starting at m_sub), 0: a whole tile
-    int m_sub;
-};
-
-// Items below p.n_full are whole tiles (or split-K slices of them); the tiles past
-// them -- fewer than half the persistent CTAs -- are each split into two half tiles
-// along the tokens, so that the last round of work is spread over twice as many
-// CTAs without any cross-CTA reduction.
-__device__ __forceinline__ Item decode_item(const GemmParams& p, int item) {
-    Item it;
-    it.half = 0;
-    it.m_sub = 0;
-    uint32_t t;
-    if (item < p.n_full) {
-        t = fastdiv((uint32_t)item, p.div_splits);
-        it.slice = item - (int)t * p.splits;
-    } else {
-        const int j = item - p.n_full;
-        t = (uint32_t)(p.n_full + (j >> 1));
-        it.slice = 0;
-        it.half = 1;
-        it.m_sub = (j & 1) * p.half_bn;
-    }
-    if (p.walk_n_fast) {
-        const uint32_t mt = fastdiv(t, p.div_walk);
-        it.m_tile = (int)mt;
-        it.n_tile = (int)t - (int)mt * p.tiles_n;
-    } else {
-        const uint32_t nt = fastdiv(t, p.div_walk);
-        it.n_tile = (int)nt;
-        it.m_tile = (int)t - (int)nt * p.tiles_m;
-    }
-    // no division on the device: nkb = kb_base * splits + kb_rem, the first kb_rem
-    // slices take one extra k-block
-    it.kb_begin = it.slice * p.kb_base + min(it.slice, p.kb_rem);
-    it.kb_end = it.kb_begin + p.kb_base + (it.slice < p.kb_rem ? 1 : 0);
-    return it;
 }
 
 template <int FMT, bool BF16, int BN, int BK, int STAGES, int NWG, bool PAIR, int WSTAGES>
@@ -1151,8 +1053,10 @@ __global__ void __launch_bounds__(128 * (1 + NWG), (GemmCfg<FMT, BF16, BN, BK, S
                 }
                 ptx::tmem_wait_ld();
 #pragma unroll
-                for (int j = 0; j < STEP; ++j)
-                    ptx::st_shared_cluster_f32(dst + (uint32_t)(wg * COLS + cc + j) * 4u, __uint_as_float(v[j]));
+                for (int j = 0; j < STEP; j += 4)
+                    ptx::st_shared_cluster_v4f32(dst + (uint32_t)(wg * COLS + cc + j) * 4u, __uint_as_float(v[j]),
+                                                 __uint_as_float(v[j + 1]), __uint_as_float(v[j + 2]),
+                                                 __uint_as_float(v[j + 3]));
             }
         }
         ptx::tc_fence_before();
@@ -1165,17 +1069,28 @@ __global__ void __launch_bounds__(128 * (1 + NWG), (GemmCfg<FMT, BF16, BN, BK, S
             const int mval = min(BN, p.M - m0);
             const float* box = reinterpret_cast<const float*>(smem);
             const int nbase = it.n_tile * TILE_N + row0;
-            // consecutive threads take consecutive weight rows: conflict-free inbox
-            // reads (odd pitch) and coalesced output stores
-            for (int e = threadIdx.x; e < rows * mval; e += C::NT) {
-                const int j = e % rows, cc = e / rows;
+            const int groups = (mval + 3) / 4;
+            // consecutive threads take consecutive weight rows (coalesced output
+            // stores), each four tokens with one 16-byte load per slice; every column
+            // is summed in slice order 0..S-1
+            for (int e = threadIdx.x; e < rows * groups; e += C::NT) {
+                const int j = e % rows, c4 = (e / rows) * 4;
                 const int n = nbase + j;
-                float acc = 0.0f;
-                for (int sl = 0; sl < S; ++sl) acc += box[(sl * R + j) * C::CS_PITCH + cc];
+                float4 acc = make_float4(0.0f, 0.0f, 0.0f, 0.0f);
+                for (int sl = 0; sl < S; ++sl) {
+                    const float4 v = *reinterpret_cast<const float4*>(box + (sl * R + j) * C::CS_PITCH + c4);
+                    acc.x += v.x;
+                    acc.y += v.y;
+                    acc.z += v.z;
+                    acc.w += v.w;
+                }
                 if (n < p.N) {
                     float b = 0.0f;
                     if (FMT == FMT_FP8 && p.bias != nullptr) b = load_16bit<BF16>(p.bias, (size_t)n);
-                    store_out<BF16>(p.out, (size_t)(m0 + cc) * p.N + n, alpha * acc + b);
+                    const float a4[4] = {acc.x, acc.y, acc.z, acc.w};
+#pragma unroll
+                    for (int i = 0; i < 4; ++i)
+                        if (c4 + i < mval) store_out<BF16>(p.out, (size_t)(m0 + c4 + i) * p.N + n, alpha * a4[i] + b);
                 }
             }
         }

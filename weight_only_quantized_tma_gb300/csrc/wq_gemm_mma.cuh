@@ -37,7 +37,7 @@
 // are touched only after that wait.
 #pragma once
 
-#include "wq_gemm.cuh"
+#include "wq_common.cuh"
 
 namespace wq {
 

@@ -2,7 +2,6 @@
 // INT4: each group's fold adds (8 - z) S_g[m] per row, with the zero points streamed
 // beside the scales.  Same shapes and instantiation grid as the symmetric decode
 // kernel in wq_gemm_int4.cu.
-#include "wq_gemm.cuh"
 #include "wq_gemm_mma.cuh"
 
 namespace wq {
