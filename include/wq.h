@@ -325,9 +325,11 @@ wq_status wq_get_plan(wq_op op, wq_dtype a_dtype, int64_t M, int64_t N, int64_t 
 
 /* Workspace bytes an op needs: 0 when no split-K is used or when the split-K
  * slices are reduced inside a thread-block cluster (wq_plan.cluster_split; the
- * tile kernel does this for S <= 16 slices).  WQ_SPLITK_WORKSPACE=1 in the
- * environment keeps the workspace reduction (last arriver sums the slices), e.g.
- * to compare the two.  Host only. */
+ * tile kernel chooses this for token tiles of 64 or more when a cost estimate
+ * favours it).  In the environment, WQ_SPLITK_WORKSPACE=1 keeps the workspace
+ * reduction (the last arriver sums the slices) and WQ_SPLITK_CLUSTER=1 takes the
+ * cluster reduction whenever its clusters fit in one wave, e.g. to compare the two.
+ * Host only. */
 wq_status wq_workspace_bytes(wq_op op, wq_dtype a_dtype, int64_t M, int64_t N, int64_t K, int32_t G,
                              size_t* bytes);
 

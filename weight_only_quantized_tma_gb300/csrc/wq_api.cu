@@ -274,26 +274,36 @@ wq_status make_plan(int fmt, bool bf16, int64_t M, int64_t N, int64_t K, int sms
             }
         }
     }
-    // Split-K on the one-CTA tile kernel with token tiles of 64 or 128: the S slices of
-    // a tile form one thread-block cluster and reduce through distributed shared
-    // memory (one item per CTA).  In the workspace reduction one warp reads S partial
-    // columns for each of its 32-64 output columns, several microseconds at these
-    // tiles.  All clusters must be resident at once (a second wave would double the
-    // time), and the device holds fewer S-CTA clusters of this kernel than slots / S
-    // (about one CTA per SM), so S is the largest count with tiles <= max_clusters[S];
-    // the cluster grid must still cover at least 4/5 of the SMs, else the workspace
-    // reduction on the full grid is faster (measured on GB300: 4096 x 4096 at M = 128,
-    // 30.5 us with 4 slices in clusters against 37.7 us with 9 through the workspace;
-    // 6656 x 19968 at M = 128, 79 us with 2 slices in 104 CTAs against 62 us with 5).
-    // At BN = 256 the cluster reduction measured slower at equal slice counts.
-    // WQ_SPLITK_WORKSPACE=1 keeps the workspace reduction.
-    if (!decode && !p.pair && p.splits > 1 && cfg.csplit_ok && cfg.bn >= 64 && cfg.bn <= 128 &&
-        p.grid == p.n_items && sms > 0) {
+    // Split-K on the one-CTA tile kernel with token tiles of 64 or more: the S slices
+    // of a tile can form one thread-block cluster and reduce through distributed
+    // shared memory (one item per CTA, no workspace).  The device holds fewer S-CTA
+    // clusters of this kernel than slots / S (about one CTA per SM), and all clusters
+    // must be resident at once, so the cluster path runs S_c <= S slices: the largest
+    // count with tiles <= max_clusters[S_c].  It is taken when a cost estimate in
+    // quarter microseconds, from per-CTA globaltimer traces and timings on GB300,
+    // favours it:
+    //   workspace: 3 per k-block of a slice (two CTAs share an SM) plus, for the last
+    //              arriving warp, 2 per round of 8 columns x 2 slices;
+    //   cluster:   2 per k-block (about one CTA per SM) plus 6 for the exchange.
+    // (Measured: 4096 x 4096 at M = 128, 20.7 us with 4 slices in clusters against
+    // 37 us with 9 through the workspace; 2048 x 8192 at M = 128, 22.5 against 47 us;
+    // 6656 x 19968 at M = 128, 71 us with 2 slices in clusters against 61 us with 5.)
+    // WQ_SPLITK_WORKSPACE=1 keeps the workspace reduction; WQ_SPLITK_CLUSTER=1 takes the
+    // cluster reduction whenever the clusters fit in one wave (any token tile), e.g. to
+    // compare the two.
+    const char* cl_env = std::getenv("WQ_SPLITK_CLUSTER");
+    const bool force_cluster = cl_env && cl_env[0] == '1';
+    if (!decode && !p.pair && p.splits > 1 && cfg.csplit_ok && p.grid == p.n_items && sms > 0 &&
+        (force_cluster || cfg.bn >= 64)) {
         const char* ws_env = std::getenv("WQ_SPLITK_WORKSPACE");
         int best = 0;
         for (int S = 2; S <= p.splits && S <= kMaxDecodeCluster; ++S)
             if (tiles <= cfg.max_clusters[S] && p.nkb >= 2 * S) best = S;
-        if (best >= 2 && 5 * tiles * best >= 4LL * sms && !(ws_env && ws_env[0] == '1')) {
+        const int cols = cfg.bn / (cfg.nwg > 0 ? cfg.nwg : 2);   // output columns per epilogue warp
+        const long long est_ws = 3LL * ((p.nkb + p.splits - 1) / p.splits) +
+                                 2LL * ((p.splits + 1) / 2) * ((cols + 7) / 8);
+        const long long est_cl = best >= 2 ? 2LL * ((p.nkb + best - 1) / best) + 6 : 0;
+        if (best >= 2 && (force_cluster || est_cl < est_ws) && !(ws_env && ws_env[0] == '1')) {
             p.csplit = true;
             p.splits = best;
             splits = best;
