@@ -32,7 +32,11 @@
 // CTA's commits arrive on the barriers of both CTAs.  No copy is multicast.
 //   warps 4..   transform: unpack / decode + scale into 16-bit operands, then the
 //               epilogue (TMEM -> registers -> alpha/bias -> 16-bit -> global),
-//               including the deterministic split-K reduction.
+//               including the deterministic split-K reduction: through a workspace
+//               (each slice writes fp32 partials, the last arriver of a warp's strip
+//               sums them), or, when the slices of a tile are one thread-block
+//               cluster (p.csplit), through the other slices' shared memory after
+//               the main loop (all warps of the cluster meet at two cluster barriers).
 //
 // Dequantization per format (all exact until the final rounding to the operand
 // type, see the conversion helpers below):
