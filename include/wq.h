@@ -18,6 +18,10 @@
  *           SM100 BF16 x FP4 GEMM" (PR #4466), §2 (uint8 weight of shape [N, K/2],
  *           block scale factors reordered by an offline preparation step) and §3
  *           (the kernel takes weight, weight scale, activation, alpha, output).
+ *   W4A16 variants on the same packed codes: an integer zero point per group and
+ *           row, (q - Z) * S (wq_gemm_w4a16_zp), and a 16-entry fp16 codebook,
+ *           LUT[q] * S (NF4-style, wq_gemm_w4a16_lut).
+ *   W2A16   2-bit codes, four per byte along K, (q - 2) * S (wq_gemm_w2a16).
  *
  * Conventions for every entry point:
  *   - All arrays are row-major and live in device memory unless stated.  The
