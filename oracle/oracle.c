@@ -168,6 +168,22 @@ static double act_value(const uint16_t* A, int a_is_bf16, int64_t idx) {
     return a_is_bf16 ? oracle_bf16_to_double(A[idx]) : oracle_f16_to_double(A[idx]);
 }
 
+/* The activation rows a GEMM reads, decoded once: row i of the result holds
+ * A[rows[i], 0..K-1] (rows NULL: all M rows) as float64.  Only the decoding moves
+ * out of the dot products; every product and every k-ascending sum below is the
+ * same.  The caller frees the array. */
+static double* act_rows(const uint16_t* A, int a_is_bf16, int64_t M, int64_t K, const int64_t* rows,
+                        int64_t nrows) {
+    double* ad = (double*)malloc(sizeof(double) * (size_t)(nrows * K > 0 ? nrows * K : 1));
+#pragma omp parallel for schedule(static)
+    for (int64_t i = 0; i < nrows; ++i) {
+        const int64_t m = rows ? rows[i] : i;
+        for (int64_t k = 0; k < K; ++k) ad[i * K + k] = act_value(A, a_is_bf16, m * K + k);
+    }
+    (void)M;
+    return ad;
+}
+
 /* ---------------------------------------------------------------- INT4 */
 
 /* Canonical packing: byte (n, j) holds code q[n, 2j] in its low nibble and
@@ -281,19 +297,21 @@ ORACLE_API void oracle_gemm_w4a16_zp(const uint16_t* A, int a_is_bf16, const uin
                                      double* out) {
     if (!rows) nrows = M;
     if (!cols) ncols = N;
+    double* ad = act_rows(A, a_is_bf16, M, K, rows, nrows);
 #pragma omp parallel for schedule(dynamic, 1)
     for (int64_t j = 0; j < ncols; ++j) {
         const int64_t n = cols ? cols[j] : j;
         double* wrow = (double*)malloc((size_t)K * sizeof(double));
         for (int64_t k = 0; k < K; ++k) wrow[k] = int4_weight_zp(w, s, z, N, K, G, n, k);
         for (int64_t i = 0; i < nrows; ++i) {
-            const int64_t m = rows ? rows[i] : i;
+            const double* arow = ad + i * K;
             double dot = 0.0;
-            for (int64_t k = 0; k < K; ++k) dot += wrow[k] * act_value(A, a_is_bf16, m * K + k);
+            for (int64_t k = 0; k < K; ++k) dot += wrow[k] * arow[k];
             out[i * ncols + j] = dot;
         }
         free(wrow);
     }
+    free(ad);
 }
 
 /* out[i][j] = sum_k A[rows[i], k] * w[cols[j], k].  rows/cols may be NULL
@@ -304,6 +322,7 @@ ORACLE_API void oracle_gemm_w4a16(const uint16_t* A, int a_is_bf16, const uint8_
                                   int64_t ncols, double* out) {
     if (!rows) nrows = M;
     if (!cols) ncols = N;
+    double* ad = act_rows(A, a_is_bf16, M, K, rows, nrows);
 #pragma omp parallel for schedule(dynamic, 1)
     for (int64_t j = 0; j < ncols; ++j) {
         int64_t n = cols ? cols[j] : j;
@@ -311,14 +330,14 @@ ORACLE_API void oracle_gemm_w4a16(const uint16_t* A, int a_is_bf16, const uint8_
         for (int64_t k = 0; k < K; ++k)
             wrow[k] = int4_weight(w, s, N, K, G, n, k);
         for (int64_t i = 0; i < nrows; ++i) {
-            int64_t m = rows ? rows[i] : i;
             double acc = 0.0;
             for (int64_t k = 0; k < K; ++k)
-                acc += act_value(A, a_is_bf16, m * K + k) * wrow[k];
+                acc += ad[i * K + k] * wrow[k];
             out[i * ncols + j] = acc;
         }
         free(wrow);
     }
+    free(ad);
 }
 
 /* ---------------------------------------------------------------- INT4 codebook */
@@ -353,19 +372,20 @@ ORACLE_API void oracle_gemm_w4a16_lut(const uint16_t* A, int a_is_bf16, const ui
                                       double* out) {
     if (!rows) nrows = M;
     if (!cols) ncols = N;
+    double* ad = act_rows(A, a_is_bf16, M, K, rows, nrows);
 #pragma omp parallel for schedule(dynamic, 1)
     for (int64_t j = 0; j < ncols; ++j) {
         const int64_t n = cols ? cols[j] : j;
         double* wv = (double*)malloc((size_t)K * sizeof(double));
         for (int64_t k = 0; k < K; ++k) wv[k] = lut4_weight(w, s, lut, N, K, G, n, k);
         for (int64_t i = 0; i < nrows; ++i) {
-            const int64_t m = rows ? rows[i] : i;
             double sum = 0.0;
-            for (int64_t k = 0; k < K; ++k) sum += act_value(A, a_is_bf16, m * K + k) * wv[k];
+            for (int64_t k = 0; k < K; ++k) sum += ad[K * i + k] * wv[k];
             out[i * ncols + j] = sum;
         }
         free(wv);
     }
+    free(ad);
 }
 
 /* ---------------------------------------------------------------- INT2 */
@@ -415,19 +435,21 @@ ORACLE_API void oracle_gemm_w2a16(const uint16_t* A, int a_is_bf16, const uint8_
                                   const int64_t* cols, int64_t ncols, double* out) {
     if (!rows) nrows = M;
     if (!cols) ncols = N;
+    double* ad = act_rows(A, a_is_bf16, M, K, rows, nrows);
 #pragma omp parallel for schedule(dynamic, 1)
     for (int64_t j = 0; j < ncols; ++j) {
         const int64_t n = cols ? cols[j] : j;
         double* wv = (double*)malloc((size_t)K * sizeof(double));
         for (int64_t k = 0; k < K; ++k) wv[k] = int2_weight(w, s, N, K, G, n, k);
         for (int64_t i = 0; i < nrows; ++i) {
-            const int64_t m = rows ? rows[i] : i;
+            const double* xa = ad + i * K;
             double total = 0.0;
-            for (int64_t k = 0; k < K; ++k) total += wv[k] * act_value(A, a_is_bf16, m * K + k);
+            for (int64_t k = 0; k < K; ++k) total += wv[k] * xa[k];
             out[i * ncols + j] = total;
         }
         free(wv);
     }
+    free(ad);
 }
 
 /* ---------------------------------------------------------------- FP8 */
@@ -446,6 +468,7 @@ ORACLE_API void oracle_gemm_w8a16_fp8(const uint16_t* A, int a_is_bf16, const ui
                                       const int64_t* cols, int64_t ncols, double* out) {
     if (!rows) nrows = M;
     if (!cols) ncols = N;
+    double* ad = act_rows(A, a_is_bf16, M, K, rows, nrows);
 #pragma omp parallel for schedule(dynamic, 1)
     for (int64_t j = 0; j < ncols; ++j) {
         int64_t n = cols ? cols[j] : j;
@@ -454,14 +477,15 @@ ORACLE_API void oracle_gemm_w8a16_fp8(const uint16_t* A, int a_is_bf16, const ui
             wrow[k] = oracle_e4m3_to_double(w[n * K + k]);
         double b = bias ? act_value(bias, a_is_bf16, n) : 0.0;
         for (int64_t i = 0; i < nrows; ++i) {
-            int64_t m = rows ? rows[i] : i;
+            const double* a8 = ad + i * K;
             double acc = 0.0;
             for (int64_t k = 0; k < K; ++k)
-                acc += act_value(A, a_is_bf16, m * K + k) * wrow[k];
+                acc += a8[k] * wrow[k];
             out[i * ncols + j] = alpha * acc + b;
         }
         free(wrow);
     }
+    free(ad);
 }
 
 /* ---------------------------------------------------------------- FP4 */
@@ -489,6 +513,7 @@ ORACLE_API void oracle_gemm_bf16_fp4(const uint16_t* A, const uint8_t* w, const 
                                      int64_t ncols, double* out) {
     if (!rows) nrows = M;
     if (!cols) ncols = N;
+    double* ad = act_rows(A, 1, M, K, rows, nrows);
 #pragma omp parallel for schedule(dynamic, 1)
     for (int64_t j = 0; j < ncols; ++j) {
         int64_t n = cols ? cols[j] : j;
@@ -496,14 +521,15 @@ ORACLE_API void oracle_gemm_bf16_fp4(const uint16_t* A, const uint8_t* w, const 
         for (int64_t k = 0; k < K; ++k)
             wrow[k] = fp4_weight(w, sf, K, n, k);
         for (int64_t i = 0; i < nrows; ++i) {
-            int64_t m = rows ? rows[i] : i;
+            const double* a4 = ad + i * K;
             double acc = 0.0;
             for (int64_t k = 0; k < K; ++k)
-                acc += oracle_bf16_to_double(A[m * K + k]) * wrow[k];
+                acc += a4[k] * wrow[k];
             out[i * ncols + j] = alpha * acc;
         }
         free(wrow);
     }
+    free(ad);
 }
 
 /* Number of OpenMP threads the GEMM loops use (1 without OpenMP). */

@@ -53,8 +53,17 @@ MUTATIONS = {
         "out[i * ncols + j] = alpha * acc;",
         "out[i * ncols + j] = acc;"),
     "A_transposed": (
-        "acc += act_value(A, a_is_bf16, m * K + k) * wrow[k];\n            out[i * ncols + j] = acc;",
-        "acc += act_value(A, a_is_bf16, (k * M + m) % (M * K)) * wrow[k];\n            out[i * ncols + j] = acc;"),
+        "acc += ad[i * K + k] * wrow[k];",
+        "acc += ad[(k * nrows + i) % (nrows * K)] * wrow[k];"),
+    "act_rows_transposed": (
+        "ad[i * K + k] = act_value(A, a_is_bf16, m * K + k);",
+        "ad[i * K + k] = act_value(A, a_is_bf16, (k * M + m) % (M * K));"),
+    "fp8_A_transposed": (
+        "acc += a8[k] * wrow[k];",
+        "acc += ad[(k * nrows + i) % (nrows * K)] * wrow[k];"),
+    "fp4_A_transposed": (
+        "acc += a4[k] * wrow[k];",
+        "acc += ad[(k * nrows + i) % (nrows * K)] * wrow[k];"),
     "round_ties_away": (
         "if (diff > 0.5 || (diff == 0.5 && fmod(fl, 2.0) != 0.0))",
         "if (diff >= 0.5)"),
@@ -80,8 +89,8 @@ MUTATIONS = {
         "int zero = z[grp * N + n];",
         "int zero = z[n * (K / G) + grp];"),
     "zp_A_transposed": (
-        "dot += wrow[k] * act_value(A, a_is_bf16, m * K + k);",
-        "dot += wrow[k] * act_value(A, a_is_bf16, (k * M + m) % (M * K));"),
+        "dot += wrow[k] * arow[k];",
+        "dot += wrow[k] * ad[(k * nrows + i) % (nrows * K)];"),
     "zp_ignored": (
         "return (double)(q - zero) * scale;",
         "return (double)(q - 8) * scale;"),
@@ -95,8 +104,8 @@ MUTATIONS = {
         "double scale = oracle_f16_to_double(s[(k / G) * N + n]);\n    return entry * scale;",
         "double scale = oracle_f16_to_double(s[n * (K / G) + k / G]);\n    return entry * scale;"),
     "lut_A_transposed": (
-        "sum += act_value(A, a_is_bf16, m * K + k) * wv[k];",
-        "sum += act_value(A, a_is_bf16, (k * M + m) % (M * K)) * wv[k];"),
+        "sum += ad[K * i + k] * wv[k];",
+        "sum += ad[(k * nrows + i) % (nrows * K)] * wv[k];"),
     "int2_offset": (
         "return (double)(q - 2) * scale;",
         "return (double)(q - 1) * scale;"),
@@ -110,8 +119,8 @@ MUTATIONS = {
         "double scale = oracle_f16_to_double(s[(k / G) * N + n]);\n    return (double)(q - 2) * scale;",
         "double scale = oracle_f16_to_double(s[(k % (K / G)) * N + n]);\n    return (double)(q - 2) * scale;"),
     "int2_A_transposed": (
-        "total += wv[k] * act_value(A, a_is_bf16, m * K + k);",
-        "total += wv[k] * act_value(A, a_is_bf16, (k * M + m) % (M * K));"),
+        "total += wv[k] * xa[k];",
+        "total += wv[k] * ad[(k * nrows + i) % (nrows * K)];"),
     "pack_nibbles_swapped": (
         "w[n * (K / 2) + j] = (uint8_t)(lo | (hi << 4));",
         "w[n * (K / 2) + j] = (uint8_t)(hi | (lo << 4));"),
