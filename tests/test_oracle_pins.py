@@ -589,3 +589,83 @@ def test_int2_brute_force():
             want[m, n] = acc
     got = oracle.gemm_w2a16(A, False, oracle.pack_int2(q.astype(np.uint8)), s, M, N, K, G)
     assert np.allclose(got, want, rtol=1e-12, atol=1e-12)
+
+
+# ------------------------------------------------------------- row / column subsets
+#
+# The large-M GPU tests compare sampled output rows (and the CPU baseline sampled
+# columns) against the oracle called with `rows` / `cols`.  Each format's subset path
+# must give exactly the entries of the full product, for unsorted and repeated
+# indices, first and last rows and columns included.
+
+_SUB_ROWS = [8, 0, 4, 4, 10]
+_SUB_COLS = [19, 3, 0, 7, 7, 12]
+
+
+def _check_subsets(call, M, N):
+    full = call(None, None)
+    assert full.shape == (M, N)
+    rows_only = call(_SUB_ROWS, None)
+    cols_only = call(None, _SUB_COLS)
+    both = call(_SUB_ROWS, _SUB_COLS)
+    assert np.array_equal(rows_only, full[_SUB_ROWS, :])
+    assert np.array_equal(cols_only, full[:, _SUB_COLS])
+    assert np.array_equal(both, full[np.ix_(_SUB_ROWS, _SUB_COLS)])
+    # a single entry equals the full product's entry (no dependence on the other indices)
+    assert call([10], [19])[0, 0] == full[10, 19]
+
+
+@pytest.mark.parametrize("a_dtype", ["f16", "bf16"])
+def test_fp8_row_and_column_subsets(a_dtype):
+    M, N, K = 11, 20, 128
+    A = synth.activations(M, K, a_dtype, seed=40)
+    wts = synth.fp8_weights(N, K, seed=41)
+    bias = synth.bias(N, a_dtype, seed=42)
+    _check_subsets(lambda r, c: oracle.gemm_w8a16_fp8(A, a_dtype == "bf16", wts.w, float(wts.scale), M, N, K,
+                                                      bias_bits=bias, rows=r, cols=c), M, N)
+
+
+def test_fp4_row_and_column_subsets():
+    M, N, K = 11, 20, 96
+    A = synth.activations(M, K, "bf16", seed=43)
+    wts = synth.fp4_weights(N, K, seed=44)
+    _check_subsets(lambda r, c: oracle.gemm_bf16_fp4(A, wts.w, wts.sf, float(wts.alpha), M, N, K, rows=r, cols=c),
+                   M, N)
+    # and the subset entries against the independent brute-force loop
+    want = _brute_force_fp4(A, wts.w, wts.sf, float(wts.alpha), M, N, K)
+    got = oracle.gemm_bf16_fp4(A, wts.w, wts.sf, float(wts.alpha), M, N, K, rows=_SUB_ROWS, cols=_SUB_COLS)
+    assert np.allclose(got, want[np.ix_(_SUB_ROWS, _SUB_COLS)], rtol=1e-14, atol=1e-15)
+
+
+def test_zero_point_row_and_column_subsets():
+    M, N, K, G = 11, 20, 128, 32
+    A = synth.activations(M, K, "f16", seed=45)
+    wts = synth.int4_weights(N, K, G, seed=46)
+    z = synth.int4_zeros(N, K, G, seed=47)
+    _check_subsets(lambda r, c: oracle.gemm_w4a16_zp(A, False, wts.w, wts.s, z, M, N, K, G, rows=r, cols=c), M, N)
+
+
+def test_codebook_row_and_column_subsets():
+    M, N, K, G = 11, 20, 128, 64
+    A = synth.activations(M, K, "bf16", seed=48)
+    wts = synth.int4_weights(N, K, G, seed=49)
+    lut = synth.random_codebook(50)
+    _check_subsets(lambda r, c: oracle.gemm_w4a16_lut(A, True, wts.w, wts.s, lut, M, N, K, G, rows=r, cols=c),
+                   M, N)
+
+
+def test_int2_row_and_column_subsets():
+    M, N, K, G = 11, 20, 128, 32
+    A = synth.activations(M, K, "f16", seed=51)
+    wts = synth.int2_weights(N, K, G, seed=52)
+    _check_subsets(lambda r, c: oracle.gemm_w2a16(A, False, wts.w, wts.s, M, N, K, G, rows=r, cols=c), M, N)
+
+
+def test_int4_subsets_against_brute_force():
+    M, N, K, G = 11, 20, 64, 32
+    A = synth.activations(M, K, "f16", seed=53)
+    wts = synth.int4_weights(N, K, G, seed=54)
+    _check_subsets(lambda r, c: oracle.gemm_w4a16(A, False, wts.w, wts.s, M, N, K, G, rows=r, cols=c), M, N)
+    want = _brute_force_int4(A, wts.w, wts.s, M, N, K, G)
+    got = oracle.gemm_w4a16(A, False, wts.w, wts.s, M, N, K, G, rows=_SUB_ROWS, cols=_SUB_COLS)
+    assert np.allclose(got, want[np.ix_(_SUB_ROWS, _SUB_COLS)], rtol=0, atol=1e-12)
