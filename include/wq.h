@@ -300,7 +300,9 @@ typedef struct {
     int32_t threads;      /* threads per CTA */
     int32_t smem_bytes;   /* dynamic shared memory per CTA */
     int32_t n_items;      /* tiles x splits */
-    int32_t walk_n_fast;  /* 1: weight-row tiles are walked fastest */
+    int32_t walk_n_fast;  /* 1: weight-row tiles are walked fastest (when the weight is the
+                             smaller operand); WQ_WALK=n / WQ_WALK=m in the environment
+                             forces either order, e.g. to measure both */
     int32_t tiles_n;
     int32_t tiles_m;
     int32_t ctas_per_sm;  /* resident CTAs per SM assumed by the plan */
@@ -337,6 +339,19 @@ wq_status wq_get_plan(wq_op op, wq_dtype a_dtype, int64_t M, int64_t N, int64_t 
 wq_status wq_workspace_bytes(wq_op op, wq_dtype a_dtype, int64_t M, int64_t N, int64_t K, int32_t G,
                              size_t* bytes);
 
+/* Host-side check of the launch planner's division by a runtime constant (the tile
+ * walk and the split-K item decode divide work-item indices by tile and slice
+ * counts with a multiply-shift).  "FlashInfer W8A16 GEMM (mm_bf16_fp8) analysis",
+ * §3(b): a divisor-1 magic number of 2^40 overflowed int64 in that page's kernel;
+ * the planner falls back to the plain division whenever the largest dividend times
+ * the magic number would not fit in 63 bits.  For divisor d and largest dividend
+ * x_max (the planner's bound), writes q[i] = x[i] / d computed exactly as the
+ * kernels do, and *uses_multiply = 1 when the multiply-shift path is taken (0: the
+ * plain division).  Requires d >= 1, every x[i] <= x_max, n >= 0.  Host only: no
+ * GPU, no CUDA call.  Returns WQ_ERR_NULL / WQ_ERR_SHAPE on bad arguments. */
+wq_status wq_debug_fastdiv(uint32_t d, uint32_t x_max, const uint32_t* x, int64_t n, uint32_t* q,
+                           int32_t* uses_multiply);
+
 /* ------------------------------------------------------------------ no caller workspace */
 
 /* Bytes of split-K scratch built into the library for wq_gemm_w4a16_noalloc. */
@@ -351,7 +366,8 @@ wq_status wq_workspace_bytes(wq_op op, wq_dtype a_dtype, int64_t M, int64_t N, i
  * library, held on every GPU that loads the library until the process exits; a
  * problem whose scratch would not fit returns WQ_ERR_WORKSPACE and launches nothing.
  * The first call on a device looks up the array's device address (once per device,
- * with that device current): make that first call before any stream capture.  Each
+ * with that device current): make that first call before any stream capture.  A
+ * lookup that fails returns WQ_ERR_CUDA and is tried again by the next call.  Each
  * call clears the array's 16 KiB of arrival counters on `stream`, then runs the GEMM.
  * All calls share the array and it keeps the last call's contents, so calls that
  * overlap on the GPU (unordered streams) race; order them on one stream. */

@@ -167,3 +167,73 @@ def test_plan_ops_are_validated(L):
     assert L.wq_get_plan(9, 0, 4, 512, 1024, 128, ctypes.byref(plan), ctypes.byref(n)) == SHAPE
     assert L.wq_get_plan(_lib.WQ_OP_W2A16, 0, 4, 512, 1024, 100, ctypes.byref(plan), ctypes.byref(n)) == GROUP
     assert L.wq_get_plan(_lib.WQ_OP_W4A16_LUT, 3, 4, 512, 1024, 128, ctypes.byref(plan), ctypes.byref(n)) == DTYPE
+
+
+# ------------------------------------------------------------- division by a runtime constant
+#
+# The tile walk and the split-K item decode divide work-item indices with a
+# multiply-shift ("FlashInfer W8A16 GEMM (mm_bf16_fp8) analysis", §3(b): the
+# divisor-1 magic number 2^40 overflowed int64 there).  The host copy of that
+# division is checked here against plain integer division at its edges.
+
+def _fastdiv(L, d, x_max, xs):
+    import numpy as np
+    x = np.ascontiguousarray(np.asarray(xs, dtype=np.uint32))
+    q = np.zeros_like(x)
+    used = ctypes.c_int32(-1)
+    st = L.wq_debug_fastdiv(d, x_max, x.ctypes.data, x.size, q.ctypes.data, ctypes.byref(used))
+    return st, q, used.value
+
+
+def _edge_dividends(x_max, d):
+    xs = {0, 1, 2, x_max, max(0, x_max - 1), max(0, x_max - d), max(0, x_max - d + 1)}
+    for k in (1, 2, 3, 7):
+        for base in (k * d, (x_max // d) * d):
+            for off in (-1, 0, 1):
+                v = base + off
+                if 0 <= v <= x_max:
+                    xs.add(v)
+    return sorted(v for v in xs if v <= x_max)
+
+
+@pytest.mark.parametrize("d", [1, 2, 3, 7, 128, 152, 304, 1000, 65535, 65536, (1 << 20) + 1, (1 << 31) - 1])
+@pytest.mark.parametrize("x_max", [1, 1000, 123456, (1 << 20), (1 << 31) - 1])
+def test_fastdiv_matches_integer_division(L, d, x_max):
+    import random
+    rnd = random.Random(d * 7919 + x_max)
+    xs = _edge_dividends(x_max, d) + [rnd.randint(0, x_max) for _ in range(2000)]
+    st, q, used = _fastdiv(L, d, x_max, xs)
+    assert st == OK
+    assert [int(v) for v in q] == [x // d for x in xs]
+    assert used in (0, 1)
+
+
+def test_fastdiv_overflow_guard_falls_back(L):
+    # the guard: the multiply-shift is used only while x_max * magic fits in 63 bits.
+    # For the largest divisors the magic number is just under 2^32:
+    for d in [(1 << 30) + 1, (1 << 30) + 12345, (1 << 31) - 3, (1 << 31) - 1]:
+        for x_max in [(1 << 31) - 1, 1 << 30, 3]:
+            xs = _edge_dividends(x_max, d)
+            st, q, used = _fastdiv(L, d, x_max, xs)
+            assert st == OK
+            assert [int(v) for v in q] == [x // d for x in xs]
+            # magic = ceil(2^(31+l) / d) <= 2^32, so x_max * magic < 2^63 for every
+            # x_max < 2^31: the multiply path is safe and must be the one taken
+            assert used == 1
+    # divisor 1 has magic 2^31 exactly: 2^31 * x_max < 2^62, multiply path, exact
+    st, q, used = _fastdiv(L, 1, (1 << 31) - 1, [0, 1, (1 << 31) - 1])
+    assert st == OK and [int(v) for v in q] == [0, 1, (1 << 31) - 1] and used == 1
+    # dividends or divisors at or beyond 2^31 are outside the multiply-shift's range:
+    # plain division, still exact
+    st, q, used = _fastdiv(L, 3, (1 << 32) - 1, [(1 << 32) - 1, 1 << 31])
+    assert st == OK and [int(v) for v in q] == [((1 << 32) - 1) // 3, (1 << 31) // 3] and used == 0
+    st, q, used = _fastdiv(L, (1 << 31) + 5, (1 << 32) - 1, [(1 << 32) - 1])
+    assert st == OK and int(q[0]) == ((1 << 32) - 1) // ((1 << 31) + 5) and used == 0
+
+
+def test_fastdiv_argument_checks(L):
+    used = ctypes.c_int32()
+    assert L.wq_debug_fastdiv(0, 10, None, 0, None, ctypes.byref(used)) == SHAPE
+    assert L.wq_debug_fastdiv(3, 10, None, 1, None, ctypes.byref(used)) == NULL
+    st, _, _ = _fastdiv(L, 3, 10, [11])
+    assert st == SHAPE

@@ -84,6 +84,7 @@ _SIGNATURES = {
     "wq_clear_device_status": (ctypes.c_int, []),
     "wq_debug_wait_probe": (ctypes.c_int, [_i64, _vp]),
     "wq_gemm_w4a16_noalloc": (ctypes.c_int, [_vp, ctypes.c_int, _vp, _vp, _i64, _i64, _i64, _i32, _vp, _vp]),
+    "wq_debug_fastdiv": (ctypes.c_int, [ctypes.c_uint32, ctypes.c_uint32, _vp, _i64, _vp, ctypes.POINTER(_i32)]),
 }
 
 WQ_NOALLOC_SCRATCH_BYTES = 8 << 20
@@ -360,10 +361,16 @@ def wq_gemm_w2a16(A: torch.Tensor, w_canon: torch.Tensor, s_kernel: torch.Tensor
 def wq_gemm_w4a16_noalloc(A: torch.Tensor, w_kernel: torch.Tensor, s_kernel: torch.Tensor, N: int, K: int, G: int,
                           out: torch.Tensor = None) -> torch.Tensor:
     """wq_gemm_w4a16 without a workspace argument, for callers that cannot allocate
-    device memory (the split-K scratch is a fixed array inside the library)."""
+    device memory (the split-K scratch is a fixed array inside the library).  The C
+    entry point allocates nothing; pass `out` as well for the whole call to allocate
+    nothing (when `out` is None this wrapper creates it with torch.empty)."""
     a_dtype = _adtype(A)
     _need(A, "A", A.dtype)
+    if A.dim() != 2 or A.shape[1] != K:
+        raise ValueError(f"A must be [M, {K}]")
     M = A.shape[0]
+    _need(w_kernel, "w_kernel", torch.uint8)
+    _need(s_kernel, "s_kernel", torch.float16)
     if out is None:
         out = torch.empty((M, N), dtype=A.dtype, device=A.device)
     _need(out, "out", A.dtype, (M, N))

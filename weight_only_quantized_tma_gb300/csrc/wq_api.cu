@@ -158,16 +158,12 @@ bool get_config(int fmt, bool bf16, int bn, bool query, KernelConfig* cfg) {
     return g_cfg_cache.found[dev][fi][b][bi];
 }
 
-// Split-K workspace: a fixed region of arrival counters (8 per output tile, room
-// for kMaxSplitTiles tiles) followed by the fp32 partials.  Keeping the counters
-// at a fixed place lets calls of different shapes share one workspace: every
-// call leaves the counters zero again.
-constexpr int kMaxSplitTiles = 512;
-constexpr size_t kCounterBytes = (size_t)kMaxSplitTiles * 8 * sizeof(uint32_t);
-
+// Split-K workspace: the arrival counters (kSplitCounterBytes) followed by the fp32
+// partials.  Keeping the counters at a fixed place lets calls of different shapes
+// share one workspace: every call leaves the counters zero again.
 size_t split_ws_bytes(int tiles, int splits, int bn) {
     if (splits <= 1) return 0;
-    return kCounterBytes + (size_t)tiles * splits * bn * TILE_N * sizeof(float);
+    return kSplitCounterBytes + (size_t)tiles * splits * bn * TILE_N * sizeof(float);
 }
 
 // Deterministic in (fmt, dtype, M, N, K) and the device's SM count.
@@ -313,6 +309,11 @@ wq_status make_plan(int fmt, bool bf16, int64_t M, int64_t N, int64_t K, int sms
     const double w_bytes = (double)N * (double)K * w_bits / 8.0;
     const double a_bytes = (double)M * (double)K * 2.0;
     p.walk_n_fast = w_bytes < a_bytes ? 1 : 0;
+    // WQ_WALK=n (weight-row tiles fastest) or WQ_WALK=m (token tiles fastest) in the
+    // environment overrides the rule, e.g. to measure both orders on one shape
+    const char* walk_env = std::getenv("WQ_WALK");
+    if (walk_env && walk_env[0] == 'n' && walk_env[1] == '\0') p.walk_n_fast = 1;
+    if (walk_env && walk_env[0] == 'm' && walk_env[1] == '\0') p.walk_n_fast = 0;
     p.ws_bytes = (decode || p.csplit) ? 0 : split_ws_bytes((int)tiles, splits, cfg.bn);
     *plan = p;
     return WQ_OK;
@@ -352,7 +353,7 @@ void fill_common(GemmParams& gp, const Plan& pl, int64_t M, int64_t N, int64_t K
     gp.timeout_ns = kTimeoutNs;
     if (pl.ws_bytes > 0) {
         gp.ws_count = static_cast<uint32_t*>(ws);
-        gp.ws_part = reinterpret_cast<float*>(static_cast<uint8_t*>(ws) + kCounterBytes);
+        gp.ws_part = reinterpret_cast<float*>(static_cast<uint8_t*>(ws) + kSplitCounterBytes);
     }
 }
 
@@ -819,6 +820,18 @@ wq_status wq_gemm_bf16_fp4(const void* A, const uint8_t* w_e2m1, const uint8_t* 
     fill_common(gp, pl, M, N, K, out, ws, d->status);
     if (pl.pair) return finish_launch(launch_gemm_fp4_pair(gp, pl.grid, (cudaStream_t)stream));
     return finish_launch(launch_gemm_fp4(gp, true, pl.cfg.bn, pl.grid, (cudaStream_t)stream));
+}
+
+wq_status wq_debug_fastdiv(uint32_t d, uint32_t x_max, const uint32_t* x, int64_t n, uint32_t* q,
+                           int32_t* uses_multiply) {
+    if (!uses_multiply || (n > 0 && (!x || !q))) return WQ_ERR_NULL;
+    if (d == 0 || n < 0) return WQ_ERR_SHAPE;
+    for (int64_t i = 0; i < n; ++i)
+        if (x[i] > x_max) return WQ_ERR_SHAPE;
+    const FastDiv f = make_fastdiv(d, x_max);
+    *uses_multiply = f.magic != 0 ? 1 : 0;
+    for (int64_t i = 0; i < n; ++i) q[i] = fastdiv(x[i], f);
+    return WQ_OK;
 }
 
 wq_status wq_device_status(uint32_t* bits) {
