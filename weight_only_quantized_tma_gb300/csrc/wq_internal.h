@@ -40,6 +40,12 @@ __host__ __device__ __forceinline__ int int4_slot(int lane) {
     const int g = lane >> 2, c = lane & 3;
     return 4 * g + (c ^ ((g >> 1) & 3));
 }
+// Split-K workspace of the tile kernel: a fixed region of arrival counters (8 per
+// output tile, room for kMaxSplitTiles tiles) at its start, then the fp32 partials.
+// The counters must read zero when a call starts; every call leaves them zero.
+constexpr int kMaxSplitTiles = 512;
+constexpr size_t kSplitCounterBytes = (size_t)kMaxSplitTiles * 8 * sizeof(uint32_t);
+
 // Padding granularity of the prepacked INT4 / FP4-scale layouts along K.
 constexpr int KPAD_INT4 = 256;
 constexpr int KPAD_FP4SF = 128;  // covers a whole k-block of the largest BK

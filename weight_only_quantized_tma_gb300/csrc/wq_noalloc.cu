@@ -16,31 +16,41 @@
 #include <mutex>
 
 #include "../../include/wq.h"
+#include "wq_internal.h"
 
 namespace {
 
 static __device__ __align__(256) unsigned char g_noalloc_scratch[WQ_NOALLOC_SCRATCH_BYTES];
 
-// The first 16 KiB of any split-K workspace are arrival counters that must read
+// The start of any split-K workspace holds the arrival counters, which must read
 // zero when a call starts (see wq_gemm_w4a16 in include/wq.h).
-constexpr size_t kCounterBytes = 16384;
+constexpr size_t kCounterBytes = wq::kSplitCounterBytes;
+static_assert(kCounterBytes <= (size_t)WQ_NOALLOC_SCRATCH_BYTES, "counters fit in the scratch array");
 constexpr int kMaxDevices = 64;
 
 struct ScratchSlot {
-    std::once_flag once;
+    std::mutex mu;
     void* ptr = nullptr;
-    cudaError_t err = cudaSuccess;
 };
 ScratchSlot g_slots[kMaxDevices];
 
-// Device address of the scratch array on the current device (set-up on first use).
+// Device address of the scratch array on the current device.  Looked up on first use
+// and kept only once the lookup succeeds: a lookup that fails (for instance one made
+// while the stream is being captured) is tried again on the next call.
 wq_status scratch_address(void** out) {
     int dev = 0;
     if (cudaGetDevice(&dev) != cudaSuccess) return WQ_ERR_CUDA;
     if (dev < 0 || dev >= kMaxDevices) return WQ_ERR_UNSUPPORTED_DEVICE;
     ScratchSlot& s = g_slots[dev];
-    std::call_once(s.once, [&]() { s.err = cudaGetSymbolAddress(&s.ptr, g_noalloc_scratch); });
-    if (s.err != cudaSuccess || s.ptr == nullptr) return WQ_ERR_CUDA;
+    std::lock_guard<std::mutex> lock(s.mu);
+    if (s.ptr == nullptr) {
+        void* p = nullptr;
+        if (cudaGetSymbolAddress(&p, g_noalloc_scratch) != cudaSuccess || p == nullptr) {
+            (void)cudaGetLastError();   // leave no sticky error behind for the caller
+            return WQ_ERR_CUDA;
+        }
+        s.ptr = p;
+    }
     *out = s.ptr;
     return WQ_OK;
 }
