@@ -101,13 +101,12 @@ def test_ragged_shapes(N, K, G):
 
 
 @pytest.mark.parametrize("case", synth.PREFILL, ids=lambda c: f"G{c.G}")
-def test_prefill_configs_sampled_rows(case):
+def test_prefill_configs_all_rows(case):
+    # the W4A16 prefill config checked on every output element (4096 x 4096)
     p = Int4Problem(case.M, case.N, case.K, case.G, seed=synth.seed_for(2, synth.PREFILL.index(case))).pack()
     out = p.run()
     torch.cuda.synchronize()
-    rows = synth.sample_rows(case.M, 128, seed=108)
-    got = out_to_f64(out)[rows]
-    check_close(got, p.ref(rows=rows), what=f"prefill {case}")
+    check_close(out_to_f64(out), p.ref(), what=f"prefill {case}")
 
 
 def _bf16_cast_copy(p):
@@ -119,9 +118,13 @@ def _bf16_cast_copy(p):
 
 @pytest.mark.parametrize("M,N,K", [(7, 4096, 4096), (1024, 1024, 2048)])
 def test_bf16_activations_match_cast_copy(M, N, K):
-    # with bf16 activations the MMA operand is RN_bf((q - 8) * s): bf16's 8-bit
-    # significand costs ~1e-3 relative per weight, so the bar is the same rounding
-    # done by materialising the bf16 weight and calling a dense GEMM
+    # with bf16 activations the tile kernels' MMA operand is RN_bf((q - 8) * s): bf16's
+    # 8-bit significand costs ~1e-3 relative per weight, so the bar is the same rounding
+    # done by materialising the bf16 weight and calling a dense GEMM.  The two make the
+    # same operand rounding and differ only in their fp32 summation order, which moves
+    # the mean error by a few 1e-5 relative either way (measured on GB300 over five
+    # shapes: ratios 0.99999-1.00003); the gate treats a ratio within 1e-3 as a tie.
+    # (M = 7 runs on the decode kernel, whose operand is exact: ratio ~0.62.)
     p = Int4Problem(M, N, K, 128, a_dtype="bf16", seed=109 + M).pack()
     out = p.run()
     cast = _bf16_cast_copy(p)
@@ -131,7 +134,7 @@ def test_bf16_activations_match_cast_copy(M, N, K):
     k_max, k_mean = oracle.rel_errors(out_to_f64(out)[rows], ref)
     c_max, c_mean = oracle.rel_errors(out_to_f64(cast)[rows], ref)
     assert k_max <= 5e-3
-    assert k_mean <= 1.02 * c_mean, f"kernel {k_mean:.3e} vs cast-copy {c_mean:.3e}"
+    assert k_mean <= (1.0 + 1e-3) * c_mean, f"kernel {k_mean:.3e} vs cast-copy {c_mean:.3e}"
 
 
 def test_split_k_is_deterministic():
