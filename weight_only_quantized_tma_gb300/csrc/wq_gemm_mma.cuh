@@ -23,15 +23,14 @@
 // same for every weight row: one warp of the CTA computes it per stage (an MMA with
 // an all-ones operand) and shares it through shared memory.
 //
-// Work split: one CTA per (128-row tile, K slice).  Warps: 0-7 compute (warp w owns
-// rows 16w .. 16w + 15 of the tile, so each row's sum lives in one warp), 8 computes
-// S, 9 is the producer.  When K is split, the S slices of a tile are the CTAs of one
-// thread-block cluster: each sends the fp32 partial sums of the rows it does not own
-// to the owning CTA's shared memory (CTA r owns rows [r R, r R + R), R = ceil(128 /
-// S)), and after one cluster barrier each adds its own rows over the ranks in rank
-// order, reading only its own
-// shared memory -- deterministic, no workspace, and the reduction is spread over all
-// S CTAs.  The producer streams the weights and scales
+// Work split: one CTA per (128-row tile, K slice).  Warps: 0-3 compute (warp w owns
+// rows 32w .. 32w + 31 of the tile, so each row's sum lives in one warp), 4 computes
+// S, 5 is the producer.  When K is split, the S slices of a tile are the CTAs of one
+// thread-block cluster: each sends the fp32 partial sums of every row to the row's
+// owner (CTA r owns rows [r R, r R + R), R = ceil(128 / S)) with st.async, which
+// completes on the owner's inbox barrier, and each adds its own rows over the ranks in
+// rank order, reading only its own shared memory -- deterministic, no workspace, and
+// the reduction is spread over all S CTAs.  The producer streams the weights and scales
 // of its first stages before waiting for the preceding kernel on the stream
 // (programmatic dependent launch): they are constant inputs; activations and outputs
 // are touched only after that wait.
@@ -43,10 +42,11 @@ namespace wq {
 
 template <int BK, int STAGES, bool ZP = false>
 struct MmaDecodeCfg {
-    // compute warps: eight of 16 weight rows each (two CTAs per SM then give four
-    // compute warps per scheduler to hide the unpack / mma.sync latencies; measured
-    // ~2-5 % faster per GEMM than four warps of 32 rows)
-    static constexpr int NCW = 8;
+    // compute warps: four of 32 weight rows each -- the two 16-row groups of a warp
+    // share each activation fragment, which halves the activation reads from shared
+    // memory (measured on GB300, in-graph decode step: ~5 % faster than eight warps of
+    // 16 rows; two warps of 64 rows ~35 % slower)
+    static constexpr int NCW = 4;
     static constexpr int RGW = TILE_N / 16 / NCW;             // 16-row groups per compute warp
     static constexpr int S_WARP = NCW;                        // activation-sum warp
     static constexpr int P_WARP = NCW + 1;                    // producer warp
@@ -74,6 +74,9 @@ struct MmaDecodeCfg {
     static constexpr int INBOX = A_BASE + STAGES * A_STAGE;
     static constexpr int INBOX_BYTES = 16 * (TILE_N + 16) * 4;
     static constexpr int OFF_BAR = INBOX + INBOX_BYTES;
+    // barriers: full, sready, empty per stage; then the abort flag (4 B) and the inbox
+    // barrier (8 B, split-K)
+    static constexpr int OFF_INBOX_BAR = OFF_BAR + 3 * STAGES * 8 + 8;
     static constexpr int SMEM_USED = OFF_BAR + 3 * STAGES * 8 + 16;
     static constexpr int SMEM_BYTES = SMEM_USED + 1024;
     static_assert(BK == 128, "BK");
@@ -132,7 +135,8 @@ __device__ __forceinline__ void int4_word_to_frag(uint32_t w, uint32_t (&a)[4]) 
 // stage).  One CTA per item (tile, K slice): gridDim.x == n_items, and the slices of
 // a tile form one cluster of p.splits CTAs.
 template <bool BF16, int NT, int GSTEPS, int BK, int STAGES, bool ZP = false>
-__global__ void __launch_bounds__(320, 2) wq_decode_mma_kernel(const __grid_constant__ GemmParams p) {
+__global__ void __launch_bounds__(MmaDecodeCfg<BK, STAGES, ZP>::NTHREADS, 2)
+    wq_decode_mma_kernel(const __grid_constant__ GemmParams p) {
     using C = MmaDecodeCfg<BK, STAGES, ZP>;
     constexpr int NZ = C::NZ;
     constexpr int NCW = C::NCW;
@@ -151,26 +155,38 @@ __global__ void __launch_bounds__(320, 2) wq_decode_mma_kernel(const __grid_cons
     auto sready_bar = [&](int s) { return bar0 + 8u * (STAGES + s); };
     auto empty_bar = [&](int s) { return bar0 + 8u * (2 * STAGES + s); };
     volatile uint32_t* abort_flag = reinterpret_cast<volatile uint32_t*>(smem + C::OFF_BAR + 3 * STAGES * 8);
+    const uint32_t inbox_bar = sbase + C::OFF_INBOX_BAR;
 
     const int warp = threadIdx.x >> 5;
     const int lane = threadIdx.x & 31;
+    const Item it = decode_item(p, (int)blockIdx.x);
+    const int nunits = it.kb_end - it.kb_begin;
+    const int tile = it.n_tile;
+    // split-K: CTA `rank` of the tile's cluster owns rows [rank R, rank R + R) of the tile
+    const int S = p.splits;
+    const int R = (TILE_N + S - 1) / S;
+    const int rank = S > 1 ? (int)ptx::cluster_ctarank() : 0;
+    const int rows_own = min(TILE_N, (rank + 1) * R) - rank * R;
     if (threadIdx.x == 0) {
         for (int s = 0; s < STAGES; ++s) {
             ptx::mbar_init(full_bar(s), 1);
             ptx::mbar_init(sready_bar(s), 1);
             ptx::mbar_init(empty_bar(s), NCW + 1);   // compute warps and the S warp
         }
+        ptx::mbar_init(inbox_bar, 1);
         *abort_flag = 0u;
         ptx::fence_barrier_init();
+        // the inbox phase completes once the S slices' partial rows of this CTA's rows
+        // (NT x 32 bytes per row and slice) have landed
+        if (S > 1) ptx::mbar_arrive_expect_tx(inbox_bar, (uint32_t)(S * rows_own * NT * 32));
         ptx::fence_proxy_async_smem();
     }
     if (warp == C::P_WARP && lane == 0) ptx::prefetch_tmap(&p.tmap_a);
     __syncthreads();
+    // every CTA of the cluster arrives once its barriers exist; the matching wait,
+    // before the first remote store, is long satisfied by then
+    if (S > 1) ptx::cluster_arrive_relaxed();
     if (threadIdx.x == 0) ptx::grid_launch_dependents();
-
-    const Item it = decode_item(p, (int)blockIdx.x);
-    const int nunits = it.kb_end - it.kb_begin;
-    const int tile = it.n_tile;
 
     // activation fragment addresses inside a stage's boxes (box z = t / 4 holds k
     // 64z .. 64z + 63 as 128-byte token rows, row z * M + m, 128-byte swizzle);
@@ -446,13 +462,13 @@ __global__ void __launch_bounds__(320, 2) wq_decode_mma_kernel(const __grid_cons
                     }
         }
     } else {
-        // Each CTA sends the rows it does not own to their owners' inboxes (remote
-        // shared-memory stores), one cluster barrier makes them visible, and each CTA
-        // adds its own rows over the ranks in rank order: deterministic, and no CTA
-        // reads another's shared memory, so none waits for its peers after the barrier.
-        const int S = p.splits;
-        const int rank = (int)ptx::cluster_ctarank();
-        const int R = (TILE_N + S - 1) / S;
+        // Each CTA sends every row's partial sums to the row's owner (its own rows to
+        // itself) with st.async, which completes on the owner's inbox barrier; the
+        // owner then adds the S slices of its rows in rank order (deterministic) and
+        // reads only its own shared memory.  No cluster-wide barrier has to wait for
+        // the remote stores to complete (measured on GB300: a barrier.cluster with
+        // release semantics after remote stores cost ~1 us per launch).
+        ptx::cluster_wait();   // every CTA of the cluster has initialised its barriers
         const uint32_t inbox = sbase + C::INBOX;
         if (warp < NCW) {
 #pragma unroll
@@ -463,29 +479,25 @@ __global__ void __launch_bounds__(320, 2) wq_decode_mma_kernel(const __grid_cons
                     const int owner = r / R;
                     const uint32_t off = inbox + (uint32_t)((rank * R + (r - owner * R)) * 16 + 4 * c) * 4u;
                     const uint32_t dst = ptx::mapa_shared(off, (uint32_t)owner);
+                    const uint32_t rbar = ptx::mapa_shared(inbox_bar, (uint32_t)owner);
                     if constexpr (NT == 2)
-                        ptx::st_shared_cluster_v4f32(dst, acc[j][0][2 * h], acc[j][0][2 * h + 1], acc[j][1][2 * h],
-                                                     acc[j][1][2 * h + 1]);
+                        ptx::st_async_v4f32(dst, acc[j][0][2 * h], acc[j][0][2 * h + 1], acc[j][1][2 * h],
+                                            acc[j][1][2 * h + 1], rbar);
                     else
-                        ptx::st_shared_cluster_v2f32(dst, acc[j][0][2 * h], acc[j][0][2 * h + 1]);
+                        ptx::st_async_v2f32(dst, acc[j][0][2 * h], acc[j][0][2 * h + 1], rbar);
                 }
         }
-        ptx::cluster_sync();
+        // (bounded like every wait: a timeout sets the status word; nothing is read then)
+        if (!bounded_wait<true>(inbox_bar, 0u, abort_flag, p.status, DEVICE_TIMEOUT_EPILOGUE, p.timeout_ns)) return;
         const int row0 = rank * R;
-        const int rows = min(TILE_N, row0 + R) - row0;
         const float* box = reinterpret_cast<const float*>(smem + C::INBOX);
-        // token fastest: a warp reads whole 16-slot rows of the inbox (no bank conflicts)
-        for (int e = threadIdx.x; e < p.M * rows; e += blockDim.x) {
-            const int r = e / p.M;
-            const int m = e - r * p.M;
+        // weight row fastest: a warp stores consecutive output columns of one token
+        for (int e = threadIdx.x; e < p.M * rows_own; e += blockDim.x) {
+            const int m = e / rows_own;
+            const int r = e - m * rows_own;
             const int slot = 4 * ((m & 7) >> 1) + (m & 1) + 2 * (m >> 3);
-            float v[kMaxDecodeCluster];
-#pragma unroll
-            for (int q = 0; q < kMaxDecodeCluster; ++q) v[q] = q < S ? box[(q * R + r) * 16 + slot] : 0.0f;
             float tot = 0.0f;
-#pragma unroll
-            for (int q = 0; q < kMaxDecodeCluster; ++q)
-                if (q < S) tot += v[q];
+            for (int q = 0; q < S; ++q) tot += box[(q * R + r) * 16 + slot];
             const int n = tile * TILE_N + row0 + r;
             if (n < p.N) store_out<BF16>(p.out, (size_t)m * p.N + n, tot);
         }
