@@ -347,9 +347,14 @@ __global__ void __launch_bounds__(MmaDecodeCfg<BK, STAGES, ZP>::NTHREADS, 2)
         int s = 0;
         uint32_t ph = 0;
         for (int i = 0; i < nunits; ++i) {
-            const bool w1 = bounded_wait(full_bar(s), ph, abort_flag, p.status, DEVICE_TIMEOUT_TRANSFORM,
+            // One wait per stage: the S warp arrives on sready(s) only after it waited for
+            // the stage's copies (full(s)) and wrote the stage's offset terms, so its
+            // phase completing covers both.  (A wait on an mbarrier phase costs a few
+            // hundred cycles even when the phase completed long before -- measured on
+            // GB300 -- which is why the compute warps do not wait on full(s) as well.)
+            const bool w2 = bounded_wait(sready_bar(s), ph, abort_flag, p.status, DEVICE_TIMEOUT_TRANSFORM,
                                          p.timeout_ns);
-            if (!__all_sync(0xffffffffu, w1)) break;
+            if (!__all_sync(0xffffffffu, w2)) break;
             const uint8_t* stp = smem + s * C::WS_STAGE;
             const uint32_t st = sbase + C::A_BASE + s * C::A_STAGE;   // this stage's activation boxes
             const uint16_t* sc = reinterpret_cast<const uint16_t*>(stp + C::SC_OFF);
@@ -360,10 +365,6 @@ __global__ void __launch_bounds__(MmaDecodeCfg<BK, STAGES, ZP>::NTHREADS, 2)
 #pragma unroll
                 for (int j = 0; j < RGW; ++j)
                     wv[tq][j] = *reinterpret_cast<const uint4*>(stp + tq * 4096 + w_off + j * 512);
-            // the offset terms of this stage's groups (written by the S warp)
-            const bool w2 = bounded_wait(sready_bar(s), ph, abort_flag, p.status, DEVICE_TIMEOUT_TRANSFORM,
-                                         p.timeout_ns);
-            if (!__all_sync(0xffffffffu, w2)) break;
             float tmp[RGW][SETS][NT][4];
 #pragma unroll
             for (int t = 0; t < KSTEPS; ++t) {
