@@ -316,41 +316,50 @@ def run_ours(args, rank, world, local_rank):
     # whole job: every rank (an independent replica) streams step_bytes per step
     value = step_bytes * world / (step_ms * 1e-3) / 1e9
 
-    # ---------------- per-launch durations (CUDA events on the launching stream)
-    per_steps = max(3, min(args.steps, 30))
-    evs = []
-    with torch.cuda.stream(stream):
-        torch.cuda._sleep(int(2e8))          # keep the GPU busy while the launches queue up
-        for i in range(per_steps):
-            for (M, N, K, A, wk, sk, out) in gemms[i % ROTATING_SETS]:
-                a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-                a.record(stream)
-                wq.wq_gemm_w4a16(A, wk, sk, N, K, G, out=out, ws=ws)
-                b.record(stream)
-                evs.append(((M, N, K), a, b))
-    torch.cuda.synchronize(dev)
-    per = {}
-    for key, a, b in evs:
-        per.setdefault(key, []).append(a.elapsed_time(b) * 1e3)   # microseconds
+    # ---------------- per-GEMM times inside a CUDA graph: for each decode shape, one graph of
+    # back-to-back launches over rotating weight sets larger than L2 (the step's own
+    # conditions: programmatic dependent launch, no host gaps), replayed 100 times
+    L2_BYTES = 129e6
     per_gemm = []
     tot_bytes, tot_us = 0.0, 0.0
-    for (M, N, K), us in per.items():
-        mean_us = statistics.mean(us)
+    for (M, N, K, A0, wk0, sk0, out0) in gemms[0]:
+        nsets = max(ROTATING_SETS, int(np.ceil(2.2 * L2_BYTES / (N * K / 2))))
+        with torch.cuda.stream(stream):
+            sets = [(A0, wk0, sk0, out0)] + [
+                (torch.randn((M, K), device=dev).to(torch.float16),
+                 torch.randint(0, 256, wk0.shape, dtype=torch.uint8, device=dev), sk0,
+                 torch.empty((M, N), dtype=torch.float16, device=dev)) for _ in range(nsets - 1)]
+            for (A, wk, sk, out) in sets:
+                wq.wq_gemm_w4a16(A, wk, sk, N, K, G, out=out, ws=ws)
+            torch.cuda.synchronize(dev)
+            g = torch.cuda.CUDAGraph()
+            with torch.cuda.graph(g, stream=stream):
+                for (A, wk, sk, out) in sets:
+                    wq.wq_gemm_w4a16(A, wk, sk, N, K, G, out=out, ws=ws)
+            for _ in range(3):
+                g.replay()
+            a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            a.record(stream)
+            for _ in range(100):
+                g.replay()
+            b.record(stream)
+        torch.cuda.synchronize(dev)
+        us = a.elapsed_time(b) * 1e3 / (100 * nsets)
         byts = algo_bytes(M, N, K, G)
         tot_bytes += byts
-        tot_us += mean_us
+        tot_us += us
         plan = wq.get_plan(wq.WQ_OP_W4A16, wq.WQ_F16, M, N, K, G)
-        per_gemm.append({"M": M, "N": N, "K": K, "us": round(mean_us, 3), "bytes": byts,
-                         "GB/s": round(byts / (mean_us * 1e-6) / 1e9, 1),
-                         "frac_hbm": round(byts / (mean_us * 1e-6) / 1e9 / peaks["hbm_gbs"], 4),
-                         "splits": plan["splits"], "grid": plan["grid"]})
+        per_gemm.append({"M": M, "N": N, "K": K, "us": round(us, 3), "bytes": byts,
+                         "GB/s": round(byts / (us * 1e-6) / 1e9, 1),
+                         "frac_hbm": round(byts / (us * 1e-6) / 1e9 / peaks["hbm_gbs"], 4),
+                         "splits": plan["splits"], "grid": plan["grid"], "weight_sets": nsets})
+        del sets, g
     # the roofline's achieved rate: algorithmic bytes of an average launch over the
     # decode kernel's average launch duration in the timed region, where it is the
     # only kernel (8 launches per step): the step's bytes over the step time on one
-    # rank.  The isolated per-launch pass above (events between launches, so each
-    # launch also pays the device-side launch gap) reports the per-GEMM times.
+    # rank.  The per-shape graphs above give each GEMM's own in-graph time.
     achieved = step_bytes / (step_ms * 1e-3) / 1e9
-    isolated = tot_bytes / (tot_us * 1e-6) / 1e9
+    per_shape_rate = tot_bytes / (tot_us * 1e-6) / 1e9
     traffic = profiled_traffic(lambda M, N, K, Gc: wq.get_plan(wq.WQ_OP_W4A16, wq.WQ_F16, M, N, K, Gc))
 
     # ---------------- prefill extras (M = 4096), L2 flushed between runs
@@ -568,7 +577,7 @@ def run_ours(args, rank, world, local_rank):
                      "kernel": "wq_decode_mma_kernel<f16, NT=1|2, BK=128> (register-resident mma.sync, split-K)",
                      "achieved_from": "CUDA events on the launching stream over the timed region (graph "
                                       "replays; the decode kernel is the only kernel there): step bytes / step time",
-                     "isolated_launches_GB/s": round(isolated, 1)},
+                     "per_shape_graphs_GB/s": round(per_shape_rate, 1)},
         "per_gemm": sorted(per_gemm, key=lambda d: (d["M"], d["N"], d["K"])),
         "prefill": prefill,
         "quantiser": quantiser,

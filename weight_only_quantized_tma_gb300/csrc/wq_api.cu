@@ -186,7 +186,14 @@ wq_status make_plan(int fmt, bool bf16, int64_t M, int64_t N, int64_t K, int sms
     // as 64-wide boxes, so it needs K % 64 == 0
     // decode_kind: 0 symmetric, 1 zero points, -1 no decode kernel
     const bool decode = decode_kind >= 0 && fmt == FMT_INT4 && M <= 16 && K % 64 == 0;
-    if (decode) found = get_config(FMT_INT4 + 16 + decode_kind, bf16, 16, sms > 0, &cfg);
+    if (decode) {
+        found = get_config(FMT_INT4 + 16 + decode_kind, bf16, 16, sms > 0, &cfg);
+        // stages of 256 values when K allows (the launch picks the same instantiation)
+        if (found && K % 256 == 0) {
+            cfg.bk = 256;
+            cfg.stages = 3;
+        }
+    }
     for (int i = 0; i < 4 && !found; ++i) {
         if (M <= kTiles[i] || i == 3) found = get_config(fmt, bf16, kTiles[i], sms > 0, &cfg);
     }

@@ -79,7 +79,7 @@ struct MmaDecodeCfg {
     static constexpr int OFF_INBOX_BAR = OFF_BAR + 3 * STAGES * 8 + 8;
     static constexpr int SMEM_USED = OFF_BAR + 3 * STAGES * 8 + 16;
     static constexpr int SMEM_BYTES = SMEM_USED + 1024;
-    static_assert(BK == 128, "BK");
+    static_assert(BK == 128 || BK == 256, "BK");
     static_assert(WS_STAGE % 16 == 0 && A_STAGE % 1024 == 0, "bulk-copy and swizzle alignment");
 };
 
@@ -146,7 +146,7 @@ __global__ void __launch_bounds__(MmaDecodeCfg<BK, STAGES, ZP>::NTHREADS, 2)
     constexpr float CORR_LO = BF16 ? 136.0f : 1032.0f;  // b + 8, rows g
     constexpr float CORR_HI = BF16 ? 136.0f : 72.0f;    // b + 8, rows g + 8
     constexpr uint32_t ONES = BF16 ? 0x3F803F80u : 0x3C003C00u;
-    static_assert(GSTEPS == 2 || GSTEPS == 4 || GSTEPS == 8, "GSTEPS");
+    static_assert((GSTEPS == 2 || GSTEPS == 4 || GSTEPS == 8 || GSTEPS == 16) && GSTEPS <= KSTEPS, "GSTEPS");
     extern __shared__ uint8_t smem_raw[];
     uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
     const uint32_t sbase = ptx::smem_u32(smem);
