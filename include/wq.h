@@ -258,7 +258,10 @@ wq_status wq_debug_dequant_fp8(const uint8_t* w_e4m3, int64_t N, int64_t K, wq_d
  * A: a_dtype [M][K], 16-byte aligned, K % 16 == 0.  w_e4m3: uint8 [N][K],
  * 16-byte aligned.  alpha: device pointer to one float (element aligned; read
  * by the kernel, so a CUDA graph can capture the call).  bias: NULL or [N] of
- * the type of A.  out, ws: as for wq_gemm_w4a16 (op WQ_OP_FP8). */
+ * the type of A.  out, ws: as for wq_gemm_w4a16 (op WQ_OP_FP8).  M <= 16 with
+ * K % 64 == 0 runs on the decode kernel (WQ_KERNEL_DECODE: the codes read straight
+ * from W, converted in registers, no workspace); other shapes on the tile kernels.
+ * The e4m3 codes S.1111.111 decode as NaN on every path. */
 wq_status wq_gemm_w8a16_fp8(const void* A, wq_dtype a_dtype, const uint8_t* w_e4m3, const float* alpha,
                             const void* bias, int64_t M, int64_t N, int64_t K, void* out, void* ws,
                             size_t ws_bytes, wq_stream_t stream);
@@ -314,8 +317,9 @@ typedef struct {
 } wq_plan;
 
 /* Kernels a plan can pick.  TILE: the tcgen05 kernel (weights dequantized into
- * tensor memory, any M).  DECODE: W4A16 with M <= 16 and K % 64 == 0, operands
- * built in registers from the fragment-order layout, group scale applied in fp32. */
+ * tensor memory, any M).  DECODE: W4A16 or FP8 with M <= 16 and K % 64 == 0, MMA
+ * operands built in registers (W4A16: from the fragment-order layout, group scale
+ * applied in fp32; FP8: from the plain e4m3 codes, alpha applied in fp32). */
 #define WQ_KERNEL_TILE 0
 #define WQ_KERNEL_DECODE 1
 /* TILE_PAIR: W4A16 with large M.  The tile kernel on two-CTA clusters: 256 weight

@@ -57,6 +57,28 @@ class Int4Problem:
                                  self.G, rows=rows)
 
 
+class Fp8Problem:
+    """Seeded FP8 (W8A16) problem: e4m3 codes, per-tensor scale, optional bias."""
+
+    def __init__(self, M, N, K, a_dtype="bf16", seed=0, with_bias=False):
+        self.M, self.N, self.K, self.a_dtype = M, N, K, a_dtype
+        self.A = synth.activations(M, K, a_dtype, seed)
+        self.wts = synth.fp8_weights(N, K, seed + 1)
+        self.bias = synth.bias(N, a_dtype, seed + 2) if with_bias else None
+        self.A_d = to_dev_f16bits(self.A, a_dtype)
+        self.w_d = torch.from_numpy(self.wts.w).to(DEV)
+        self.alpha = torch.tensor([self.wts.scale], dtype=torch.float32, device=DEV)
+        self.bias_d = to_dev_f16bits(self.bias, a_dtype) if with_bias else None
+
+    def run(self, alpha=None):
+        import weight_only_quantized_tma_gb300 as wq
+        return wq.wq_gemm_w8a16_fp8(self.A_d, self.w_d, self.alpha if alpha is None else alpha, bias=self.bias_d)
+
+    def ref(self, rows=None):
+        return oracle.gemm_w8a16_fp8(self.A, self.a_dtype == "bf16", self.wts.w, float(self.wts.scale), self.M,
+                                     self.N, self.K, bias_bits=self.bias, rows=rows)
+
+
 def rounded_ref(ref, out_dtype):
     """The float64 reference correctly rounded (RNE) to the output type."""
     if out_dtype == "bf16":

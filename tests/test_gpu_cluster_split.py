@@ -83,7 +83,9 @@ CASES = {
 def test_cluster_and_workspace_split_vs_oracle(name, monkeypatch):
     # the default plan (cluster split-K for token tiles >= 64 when the clusters fit in
     # one wave) and the workspace reduction both match the oracle; with the same slice
-    # count they add the same partial sums in the same order, so the bits agree
+    # count they add the same partial sums in the same order, so the bits agree.  FP8
+    # at M <= 16 runs on the tile kernel here (WQ_DISABLE_DECODE=1), not the decode one
+    monkeypatch.setenv("WQ_DISABLE_DECODE", "1")
     (op, adt, G), run, ref = CASES[name]()
     shape = run_shape(name)
     want = ref()
@@ -114,8 +116,10 @@ def test_cluster_and_workspace_split_vs_oracle(name, monkeypatch):
 @pytest.mark.parametrize("name", ["int4_M300_N520", "fp8_M1", "fp4_M128", "int2_M7", "lut_M16"])
 def test_forced_cluster_split_vs_oracle(name, monkeypatch):
     # WQ_SPLITK_CLUSTER=1: the cluster reduction at any token tile (16 and 256 too)
-    # whenever the clusters fit in one wave; checked against the oracle
+    # whenever the clusters fit in one wave; checked against the oracle (tile kernel
+    # for FP8 at M <= 16 too)
     monkeypatch.setenv("WQ_SPLITK_CLUSTER", "1")
+    monkeypatch.setenv("WQ_DISABLE_DECODE", "1")
     (op, adt, G), run, ref = CASES[name]()
     plan = wq.get_plan(op, adt, *run_shape(name), G)
     if plan["cluster_split"]:

@@ -13,7 +13,7 @@ import oracle
 import weight_only_quantized_tma_gb300 as wq
 from weight_only_quantized_tma_gb300 import synth
 
-from gpu_helpers import DEV, REL_MAX, REL_MEAN, check_close, out_bits, out_to_f64, rounded_ref, to_dev_f16bits
+from gpu_helpers import DEV, Fp8Problem, check_close, out_bits, out_to_f64, to_dev_f16bits
 
 pytestmark = pytest.mark.gpu
 
@@ -49,25 +49,6 @@ def _gate_vs_cast_copy(got, cast, ref, what):
     assert k_mean <= c_mean, f"{what}: kernel rel_mean {k_mean:.3e} > cast-copy {c_mean:.3e}"
     assert k_max <= c_max + BF16_ULP_REL * 0.5, f"{what}: kernel rel_max {k_max:.3e} > cast-copy {c_max:.3e}"
     return (k_max, k_mean), (c_max, c_mean)
-
-
-class Fp8Problem:
-    def __init__(self, M, N, K, a_dtype="bf16", seed=0, with_bias=False):
-        self.M, self.N, self.K, self.a_dtype = M, N, K, a_dtype
-        self.A = synth.activations(M, K, a_dtype, seed)
-        self.wts = synth.fp8_weights(N, K, seed + 1)
-        self.bias = synth.bias(N, a_dtype, seed + 2) if with_bias else None
-        self.A_d = to_dev_f16bits(self.A, a_dtype)
-        self.w_d = torch.from_numpy(self.wts.w).to(DEV)
-        self.alpha = torch.tensor([self.wts.scale], dtype=torch.float32, device=DEV)
-        self.bias_d = to_dev_f16bits(self.bias, a_dtype) if with_bias else None
-
-    def run(self, alpha=None):
-        return wq.wq_gemm_w8a16_fp8(self.A_d, self.w_d, self.alpha if alpha is None else alpha, bias=self.bias_d)
-
-    def ref(self, rows=None):
-        return oracle.gemm_w8a16_fp8(self.A, self.a_dtype == "bf16", self.wts.w, float(self.wts.scale), self.M,
-                                     self.N, self.K, bias_bits=self.bias, rows=rows)
 
 
 class Fp4Problem:

@@ -105,19 +105,26 @@ struct Plan {
     int tiles_n, tiles_m, nkb, splits, n_items, grid, walk_n_fast;
     int n_full;    // tile kernel: whole-tile items; the rest are half tiles
     size_t ws_bytes;
-    bool decode;   // W4A16 decode kernel (register-resident mma.sync, M <= 16)
+    bool decode;   // W4A16 / FP8 decode kernel (register-resident mma.sync, M <= 16)
     bool pair;     // tile kernel on two-CTA clusters (256 weight rows per tile)
     bool csplit;   // tile kernel split-K reduced inside thread-block clusters (no workspace)
 };
 
+// Configuration codes past the tile formats: the decode kernels, then the pair kernels.
+constexpr int kCfgDecodeInt4 = 16;     // + decode_kind (0 symmetric, 1 zero points)
+constexpr int kCfgDecodeFp8 = 18;
+constexpr int kNumDecodeCfgs = 3;
+constexpr int kCfgPair = 32;           // + format
+
 bool get_config_uncached(int fmt, bool bf16, int bn, bool query, KernelConfig* cfg) {
-    if (fmt == FMT_INT4 + 16) return config_int4_decode(bf16, query, cfg);
-    if (fmt == FMT_INT4 + 17) return config_int4_decode_zp(bf16, query, cfg);
-    if (fmt == FMT_INT4 + 32) return config_int4_pair(bf16, query, cfg);
-    if (fmt == FMT_FP8 + 32) return config_fp8_pair(bf16, query, cfg);
-    if (fmt == FMT_FP4 + 32) return bf16 && config_fp4_pair(query, cfg);
-    if (fmt == FMT_LUT4 + 32) return config_lut4_pair(bf16, query, cfg);
-    if (fmt == FMT_INT2 + 32) return config_int2_pair(bf16, query, cfg);
+    if (fmt == kCfgDecodeInt4) return config_int4_decode(bf16, query, cfg);
+    if (fmt == kCfgDecodeInt4 + 1) return config_int4_decode_zp(bf16, query, cfg);
+    if (fmt == kCfgDecodeFp8) return config_fp8_decode(bf16, query, cfg);
+    if (fmt == kCfgPair + FMT_INT4) return config_int4_pair(bf16, query, cfg);
+    if (fmt == kCfgPair + FMT_FP8) return config_fp8_pair(bf16, query, cfg);
+    if (fmt == kCfgPair + FMT_FP4) return bf16 && config_fp4_pair(query, cfg);
+    if (fmt == kCfgPair + FMT_LUT4) return config_lut4_pair(bf16, query, cfg);
+    if (fmt == kCfgPair + FMT_INT2) return config_int2_pair(bf16, query, cfg);
     switch (fmt) {
         case FMT_INT4: return config_int4(bf16, bn, query, cfg);
         case FMT_FP8: return config_fp8(bf16, bn, query, cfg);
@@ -130,9 +137,9 @@ bool get_config_uncached(int fmt, bool bf16, int bn, bool query, KernelConfig* c
 
 // The device query behind a configuration (attributes, residency) is done once per
 // device and instantiation; later calls read the cached answer.
-// Slots: the tile formats 0 .. kNumFmts - 1, the W4A16 decode kernels (symmetric, zero
-// point), the pair kernels.
-constexpr int kCfgSlots = 2 * kNumFmts + 2;
+// Slots: the tile formats 0 .. kNumFmts - 1, the decode kernels (W4A16 symmetric, W4A16
+// zero point, FP8), the pair kernels.
+constexpr int kCfgSlots = 2 * kNumFmts + kNumDecodeCfgs;
 struct ConfigCache {
     std::mutex mu;
     bool have[kMaxDevices][kCfgSlots][2][4] = {};
@@ -143,7 +150,9 @@ ConfigCache g_cfg_cache;
 
 bool get_config(int fmt, bool bf16, int bn, bool query, KernelConfig* cfg) {
     const int bi = bn == 16 ? 0 : bn == 64 ? 1 : bn == 128 ? 2 : bn == 256 ? 3 : -1;
-    const int fi = (fmt >= 16 && fmt < 32) ? kNumFmts + (fmt - 16) : fmt >= 32 ? kNumFmts + 2 + (fmt - 32) : fmt;
+    const int fi = (fmt >= kCfgDecodeInt4 && fmt < kCfgPair) ? kNumFmts + (fmt - kCfgDecodeInt4)
+                   : fmt >= kCfgPair                          ? kNumFmts + kNumDecodeCfgs + (fmt - kCfgPair)
+                                                              : fmt;
     int dev = 0;
     if (!query || bi < 0 || fi < 0 || fi >= kCfgSlots || cudaGetDevice(&dev) != cudaSuccess || dev < 0 ||
         dev >= kMaxDevices)
@@ -166,6 +175,13 @@ size_t split_ws_bytes(int tiles, int splits, int bn) {
     return kSplitCounterBytes + (size_t)tiles * splits * bn * TILE_N * sizeof(float);
 }
 
+// WQ_DISABLE_DECODE=1 in the environment keeps M <= 16 on the tile kernel, e.g. to
+// compare the two.
+bool decode_disabled() {
+    const char* e = std::getenv("WQ_DISABLE_DECODE");
+    return e && e[0] == '1';
+}
+
 // Deterministic in (fmt, dtype, M, N, K) and the device's SM count.
 //  * token tile BN: the smallest compiled tile that covers M (16, 64, 128), 256
 //    for larger M;
@@ -182,12 +198,15 @@ wq_status make_plan(int fmt, bool bf16, int64_t M, int64_t N, int64_t K, int sms
     static const int kTiles[4] = {16, 64, 128, 256};
     KernelConfig cfg{};
     bool found = false;
-    // decode (M <= 16): the register-resident kernel; its activation copy views A
-    // as 64-wide boxes, so it needs K % 64 == 0
-    // decode_kind: 0 symmetric, 1 zero points, -1 no decode kernel
-    const bool decode = decode_kind >= 0 && fmt == FMT_INT4 && M <= 16 && K % 64 == 0;
-    if (decode) {
-        found = get_config(FMT_INT4 + 16 + decode_kind, bf16, 16, sms > 0, &cfg);
+    // decode (M <= 16): the register-resident kernels (W4A16, FP8); their activation
+    // copy views A as 64-wide boxes, so they need K % 64 == 0
+    // decode_kind (W4A16): 0 symmetric, 1 zero points, -1 no decode kernel
+    const bool decode =
+        decode_kind >= 0 && (fmt == FMT_INT4 || fmt == FMT_FP8) && M <= 16 && K % 64 == 0 && !decode_disabled();
+    if (decode && fmt == FMT_FP8) {
+        found = get_config(kCfgDecodeFp8, bf16, 16, sms > 0, &cfg);
+    } else if (decode) {
+        found = get_config(kCfgDecodeInt4 + decode_kind, bf16, 16, sms > 0, &cfg);
         // stages of 256 values when K allows (the launch picks the same instantiation)
         if (found && K % 256 == 0) {
             cfg.bk = 256;
@@ -255,7 +274,7 @@ wq_status make_plan(int fmt, bool bf16, int64_t M, int64_t N, int64_t K, int sms
     const bool pair_allowed = !(no_pair && no_pair[0] == '1');
     if (pair_allowed && !decode && cfg.bn == 256 && p.splits == 1 && sms > 0 && N % 8 == 0) {
         KernelConfig pc{};
-        if (get_config(fmt + 32, bf16, 256, true, &pc) && pc.max_clusters[2] > 0) {
+        if (get_config(kCfgPair + fmt, bf16, 256, true, &pc) && pc.max_clusters[2] > 0) {
             const long long tn2 = (p.tiles_n + 1) / 2;
             const long long items2 = tn2 * p.tiles_m;
             const long long pslots = pc.max_clusters[2];
@@ -588,8 +607,9 @@ wq_status wq_get_plan(wq_op op, wq_dtype a_dtype, int64_t M, int64_t N, int64_t 
     if (a_dtype != WQ_F16 && a_dtype != WQ_BF16) return WQ_ERR_DTYPE;
     const bool bf16 = (op == WQ_OP_FP4) ? true : (a_dtype == WQ_BF16);
     Plan pl{};
-    wq_status st = plan_for(fmt, bf16, M > 0 ? M : 1, N, K, &pl, grouped ? G : 0,
-                            op == WQ_OP_W4A16 ? 0 : op == WQ_OP_W4A16_ZP ? 1 : -1);
+    // the decode kind the GEMM entry points pass (make_plan takes the decode kernels
+    // for W4A16 and FP8 only)
+    wq_status st = plan_for(fmt, bf16, M > 0 ? M : 1, N, K, &pl, grouped ? G : 0, op == WQ_OP_W4A16_ZP ? 1 : 0);
     if (st != WQ_OK) return st;
     if (plan) {
         plan->bn = pl.cfg.bn;
@@ -783,7 +803,9 @@ wq_status wq_gemm_w8a16_fp8(const void* A, wq_dtype a_dtype, const uint8_t* w_e4
     if ((st = check_ws(pl, ws, ws_bytes)) != WQ_OK) return st;
     GemmParams gp;
     std::memset(&gp, 0, sizeof(gp));
-    if (!encode_a(gp, A, bf16, M, K, pl.pair ? pl.cfg.bn / 2 : pl.cfg.bn)) return WQ_ERR_CUDA;
+    if (pl.decode ? !encode_a_boxes(gp, A, bf16, M, K, pl.cfg.bk)
+                  : !encode_a(gp, A, bf16, M, K, pl.pair ? pl.cfg.bn / 2 : pl.cfg.bn))
+        return WQ_ERR_CUDA;
     if (pl.pair && !encode_out(gp, out, bf16, M, N)) return WQ_ERR_CUDA;
     const int bk = pl.cfg.bk;
     if (!encode_2d(&gp.tmap_w, CU_TENSOR_MAP_DATA_TYPE_UINT8, w_e4m3, (uint64_t)K, (uint64_t)N, (uint64_t)K,
@@ -792,6 +814,7 @@ wq_status wq_gemm_w8a16_fp8(const void* A, wq_dtype a_dtype, const uint8_t* w_e4
     gp.alpha = alpha;
     gp.bias = bias;
     fill_common(gp, pl, M, N, K, out, ws, d->status);
+    if (pl.decode) return finish_launch(launch_gemm_fp8_decode(gp, bf16, pl.grid, (cudaStream_t)stream));
     if (pl.pair) return finish_launch(launch_gemm_fp8_pair(gp, bf16, pl.grid, (cudaStream_t)stream));
     return finish_launch(launch_gemm_fp8(gp, bf16, pl.cfg.bn, pl.grid, (cudaStream_t)stream));
 }

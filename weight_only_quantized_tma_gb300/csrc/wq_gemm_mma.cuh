@@ -112,6 +112,56 @@ __device__ __forceinline__ void ldmatrix_x4(uint32_t addr, uint32_t& r0, uint32_
                  : "memory");
 }
 
+// ---------------------------------------------------------------- split-K exchange
+// Shared by the decode kernels.  The S slices of a 128-row tile are the CTAs of one
+// cluster; CTA `rank` owns rows [rank R, rank R + R) of the tile, R = ceil(128 / S).
+// Each CTA sends every row's fp32 partial sums to the row's owner (its own rows to
+// itself) with st.async, which completes on the owner's inbox barrier; the owner then
+// adds the S slices of its rows in rank order (deterministic) and reads only its own
+// shared memory.  No cluster-wide barrier has to wait for the remote stores to
+// complete (measured on GB300: a barrier.cluster with release semantics after remote
+// stores cost ~1 us per launch).  Inbox: fp32 [S][R][16 token slots]; token slot
+// 4c + i holds token 2c + (i & 1) + 8 (i >> 1), the order of a lane's accumulator
+// values, so a lane sends a row's values with one vector store.
+
+// Compute warp `warp` holds rows 16 RGW warp + 16 j + g (+ 8) of the tile in
+// acc[j][nt][e] (e = 0, 1: row g, tokens 8 nt + 2c + e; e = 2, 3: row g + 8).
+template <int NT, int RGW>
+__device__ __forceinline__ void decode_send_partials(const float (&acc)[RGW][NT][4], int warp, int lane, int rank,
+                                                     int R, uint32_t inbox, uint32_t inbox_bar) {
+    const int g = lane >> 2, c = lane & 3;
+#pragma unroll
+    for (int j = 0; j < RGW; ++j)
+#pragma unroll
+        for (int h = 0; h < 2; ++h) {
+            const int r = (warp * RGW + j) * 16 + g + 8 * h;   // e = 2h, 2h + 1
+            const int owner = r / R;
+            const uint32_t off = inbox + (uint32_t)((rank * R + (r - owner * R)) * 16 + 4 * c) * 4u;
+            const uint32_t dst = ptx::mapa_shared(off, (uint32_t)owner);
+            const uint32_t rbar = ptx::mapa_shared(inbox_bar, (uint32_t)owner);
+            if constexpr (NT == 2)
+                ptx::st_async_v4f32(dst, acc[j][0][2 * h], acc[j][0][2 * h + 1], acc[j][1][2 * h],
+                                    acc[j][1][2 * h + 1], rbar);
+            else
+                ptx::st_async_v2f32(dst, acc[j][0][2 * h], acc[j][0][2 * h + 1], rbar);
+        }
+}
+
+// After the inbox phase completed: store(m, r, v) for token m < M and owned row r,
+// with v the sum of the S slices in rank order.  Weight row fastest: a warp stores
+// consecutive output columns of one token.
+template <typename Store>
+__device__ __forceinline__ void decode_reduce_rows(const float* box, int S, int R, int rows_own, int M, Store store) {
+    for (int e = threadIdx.x; e < M * rows_own; e += blockDim.x) {
+        const int m = e / rows_own;
+        const int r = e - m * rows_own;
+        const int slot = 4 * ((m & 7) >> 1) + (m & 1) + 2 * (m >> 3);
+        float tot = 0.0f;
+        for (int q = 0; q < S; ++q) tot += box[(q * R + r) * 16 + slot];
+        store(m, r, tot);
+    }
+}
+
 // One 32-bit word of the fragment-order layout -> the four A-fragment registers of
 // one k step, each holding two values b + q, exact.
 template <bool BF16>
@@ -463,46 +513,81 @@ __global__ void __launch_bounds__(MmaDecodeCfg<BK, STAGES, ZP>::NTHREADS, 2)
                     }
         }
     } else {
-        // Each CTA sends every row's partial sums to the row's owner (its own rows to
-        // itself) with st.async, which completes on the owner's inbox barrier; the
-        // owner then adds the S slices of its rows in rank order (deterministic) and
-        // reads only its own shared memory.  No cluster-wide barrier has to wait for
-        // the remote stores to complete (measured on GB300: a barrier.cluster with
-        // release semantics after remote stores cost ~1 us per launch).
+        // split-K: partial rows to their owners, the owners add them in rank order
         ptx::cluster_wait();   // every CTA of the cluster has initialised its barriers
-        const uint32_t inbox = sbase + C::INBOX;
-        if (warp < NCW) {
-#pragma unroll
-            for (int j = 0; j < RGW; ++j)
-#pragma unroll
-                for (int h = 0; h < 2; ++h) {
-                    const int r = (warp * RGW + j) * 16 + g + 8 * h;   // e = 2h, 2h + 1
-                    const int owner = r / R;
-                    const uint32_t off = inbox + (uint32_t)((rank * R + (r - owner * R)) * 16 + 4 * c) * 4u;
-                    const uint32_t dst = ptx::mapa_shared(off, (uint32_t)owner);
-                    const uint32_t rbar = ptx::mapa_shared(inbox_bar, (uint32_t)owner);
-                    if constexpr (NT == 2)
-                        ptx::st_async_v4f32(dst, acc[j][0][2 * h], acc[j][0][2 * h + 1], acc[j][1][2 * h],
-                                            acc[j][1][2 * h + 1], rbar);
-                    else
-                        ptx::st_async_v2f32(dst, acc[j][0][2 * h], acc[j][0][2 * h + 1], rbar);
-                }
-        }
+        if (warp < NCW) decode_send_partials<NT, RGW>(acc, warp, lane, rank, R, sbase + C::INBOX, inbox_bar);
         // (bounded like every wait: a timeout sets the status word; nothing is read then)
         if (!bounded_wait<true>(inbox_bar, 0u, abort_flag, p.status, DEVICE_TIMEOUT_EPILOGUE, p.timeout_ns)) return;
-        const int row0 = rank * R;
-        const float* box = reinterpret_cast<const float*>(smem + C::INBOX);
-        // weight row fastest: a warp stores consecutive output columns of one token
-        for (int e = threadIdx.x; e < p.M * rows_own; e += blockDim.x) {
-            const int m = e / rows_own;
-            const int r = e - m * rows_own;
-            const int slot = 4 * ((m & 7) >> 1) + (m & 1) + 2 * (m >> 3);
-            float tot = 0.0f;
-            for (int q = 0; q < S; ++q) tot += box[(q * R + r) * 16 + slot];
-            const int n = tile * TILE_N + row0 + r;
-            if (n < p.N) store_out<BF16>(p.out, (size_t)m * p.N + n, tot);
-        }
+        decode_reduce_rows(reinterpret_cast<const float*>(smem + C::INBOX), S, R, rows_own, p.M,
+                           [&](int m, int r, float v) {
+                               const int n = tile * TILE_N + rank * R + r;
+                               if (n < p.N) store_out<BF16>(p.out, (size_t)m * p.N + n, v);
+                           });
     }
+}
+
+// Resident CTAs per SM of a decode kernel from registers, shared memory, threads and
+// the block limit; and, per cluster size S = 2..16, how many S-CTA clusters the device
+// can hold at once (the plan keeps a split-K grid within one such wave).
+template <typename Kernel>
+void decode_residency(Kernel kernel, int threads, int smem_bytes, KernelConfig* k) {
+    int dev = 0, smem_sm = 0, smem_rsv = 0, regs_sm = 0, thr_sm = 0, blk_sm = 0;
+    cudaFuncAttributes fa;
+    if (cudaGetDevice(&dev) != cudaSuccess || cudaFuncGetAttributes(&fa, kernel) != cudaSuccess ||
+        cudaDeviceGetAttribute(&smem_sm, cudaDevAttrMaxSharedMemoryPerMultiprocessor, dev) != cudaSuccess ||
+        cudaDeviceGetAttribute(&smem_rsv, cudaDevAttrReservedSharedMemoryPerBlock, dev) != cudaSuccess ||
+        cudaDeviceGetAttribute(&regs_sm, cudaDevAttrMaxRegistersPerMultiprocessor, dev) != cudaSuccess ||
+        cudaDeviceGetAttribute(&thr_sm, cudaDevAttrMaxThreadsPerMultiProcessor, dev) != cudaSuccess ||
+        cudaDeviceGetAttribute(&blk_sm, cudaDevAttrMaxBlocksPerMultiprocessor, dev) != cudaSuccess)
+        return;
+    const int regs_warp = ((fa.numRegs * 32 + 255) / 256) * 256;
+    int n = regs_sm / (regs_warp * (threads / 32));
+    const int by_smem = smem_sm / (smem_bytes + (int)fa.sharedSizeBytes + smem_rsv);
+    if (by_smem < n) n = by_smem;
+    if (thr_sm / threads < n) n = thr_sm / threads;
+    if (blk_sm < n) n = blk_sm;
+    if (n >= 1) k->ctas_per_sm = n;
+    for (int S = 2; S <= kMaxDecodeCluster; ++S) {
+        cudaLaunchConfig_t cfg = {};
+        cfg.gridDim = dim3((unsigned)S, 1, 1);
+        cfg.blockDim = dim3((unsigned)threads, 1, 1);
+        cfg.dynamicSmemBytes = (size_t)smem_bytes;
+        cudaLaunchAttribute attr[1];
+        attr[0].id = cudaLaunchAttributeClusterDimension;
+        attr[0].val.clusterDim.x = (unsigned)S;
+        attr[0].val.clusterDim.y = 1;
+        attr[0].val.clusterDim.z = 1;
+        cfg.attrs = attr;
+        cfg.numAttrs = 1;
+        int nc = 0;
+        if (cudaOccupancyMaxActiveClusters(&nc, kernel, &cfg) != cudaSuccess) {
+            (void)cudaGetLastError();
+            nc = 0;
+        }
+        k->max_clusters[S] = nc;
+    }
+}
+
+// One CTA per (tile, slice); the slices of a tile form one cluster.  Programmatic
+// dependent launch: the kernel waits for its predecessor only where it must.
+template <typename Kernel>
+cudaError_t launch_decode_grid(Kernel kernel, const GemmParams& p, int grid, int threads, int smem_bytes,
+                               cudaStream_t st) {
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3((unsigned)grid, 1, 1);
+    cfg.blockDim = dim3((unsigned)threads, 1, 1);
+    cfg.dynamicSmemBytes = (size_t)smem_bytes;
+    cfg.stream = st;
+    cudaLaunchAttribute attr[2];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    attr[1].id = cudaLaunchAttributeClusterDimension;
+    attr[1].val.clusterDim.x = (unsigned)(p.splits > 1 ? p.splits : 1);
+    attr[1].val.clusterDim.y = 1;
+    attr[1].val.clusterDim.z = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = p.splits > 1 ? 2 : 1;
+    return cudaLaunchKernelEx(&cfg, kernel, p);
 }
 
 template <bool BF16, int NT, int GSTEPS, int BK, int STAGES, bool ZP = false>
@@ -522,69 +607,17 @@ struct MmaDecodeLauncher {
         if (e == cudaSuccess && dev < 64) attr_set[dev] = 1;
         return e;
     }
-    // Resident CTAs per SM from registers, shared memory, threads and the block
-    // limit; and, per cluster size S = 2..16, how many S-CTA clusters the device can
-    // hold at once (the plan keeps a split-K grid within one such wave).
     static KernelConfig config(bool query_device) {
         KernelConfig k{FMT_INT4, BF16 ? 1 : 0, 16, BK, STAGES, 0, C::NTHREADS, C::SMEM_BYTES, 0, 1};
         if (!query_device || prepare() != cudaSuccess) return k;
-        int dev = 0, smem_sm = 0, smem_rsv = 0, regs_sm = 0, thr_sm = 0, blk_sm = 0;
-        cudaFuncAttributes fa;
-        if (cudaGetDevice(&dev) != cudaSuccess || cudaFuncGetAttributes(&fa, kernel) != cudaSuccess ||
-            cudaDeviceGetAttribute(&smem_sm, cudaDevAttrMaxSharedMemoryPerMultiprocessor, dev) != cudaSuccess ||
-            cudaDeviceGetAttribute(&smem_rsv, cudaDevAttrReservedSharedMemoryPerBlock, dev) != cudaSuccess ||
-            cudaDeviceGetAttribute(&regs_sm, cudaDevAttrMaxRegistersPerMultiprocessor, dev) != cudaSuccess ||
-            cudaDeviceGetAttribute(&thr_sm, cudaDevAttrMaxThreadsPerMultiProcessor, dev) != cudaSuccess ||
-            cudaDeviceGetAttribute(&blk_sm, cudaDevAttrMaxBlocksPerMultiprocessor, dev) != cudaSuccess)
-            return k;
-        const int regs_warp = ((fa.numRegs * 32 + 255) / 256) * 256;
-        int n = regs_sm / (regs_warp * (C::NTHREADS / 32));
-        const int by_smem = smem_sm / (C::SMEM_BYTES + (int)fa.sharedSizeBytes + smem_rsv);
-        if (by_smem < n) n = by_smem;
-        if (thr_sm / C::NTHREADS < n) n = thr_sm / C::NTHREADS;
-        if (blk_sm < n) n = blk_sm;
-        if (n >= 1) k.ctas_per_sm = n;
-        for (int S = 2; S <= kMaxDecodeCluster; ++S) {
-            cudaLaunchConfig_t cfg = {};
-            cfg.gridDim = dim3((unsigned)S, 1, 1);
-            cfg.blockDim = dim3(C::NTHREADS, 1, 1);
-            cfg.dynamicSmemBytes = C::SMEM_BYTES;
-            cudaLaunchAttribute attr[1];
-            attr[0].id = cudaLaunchAttributeClusterDimension;
-            attr[0].val.clusterDim.x = (unsigned)S;
-            attr[0].val.clusterDim.y = 1;
-            attr[0].val.clusterDim.z = 1;
-            cfg.attrs = attr;
-            cfg.numAttrs = 1;
-            int nc = 0;
-            if (cudaOccupancyMaxActiveClusters(&nc, kernel, &cfg) != cudaSuccess) {
-                (void)cudaGetLastError();
-                nc = 0;
-            }
-            k.max_clusters[S] = nc;
-        }
+        decode_residency(kernel, C::NTHREADS, C::SMEM_BYTES, &k);
         return k;
     }
-    // One CTA per (tile, slice); the slices of a tile form one cluster.
     static cudaError_t launch(const GemmParams& p, int grid, cudaStream_t st) {
         cudaError_t e = prepare();
         if (e != cudaSuccess) return e;
         if (p.splits > kMaxDecodeCluster || grid != p.n_items || p.M > 16 || p.M < 1) return cudaErrorInvalidValue;
-        cudaLaunchConfig_t cfg = {};
-        cfg.gridDim = dim3((unsigned)grid, 1, 1);
-        cfg.blockDim = dim3(C::NTHREADS, 1, 1);
-        cfg.dynamicSmemBytes = C::SMEM_BYTES;
-        cfg.stream = st;
-        cudaLaunchAttribute attr[2];
-        attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
-        attr[0].val.programmaticStreamSerializationAllowed = 1;
-        attr[1].id = cudaLaunchAttributeClusterDimension;
-        attr[1].val.clusterDim.x = (unsigned)(p.splits > 1 ? p.splits : 1);
-        attr[1].val.clusterDim.y = 1;
-        attr[1].val.clusterDim.z = 1;
-        cfg.attrs = attr;
-        cfg.numAttrs = p.splits > 1 ? 2 : 1;
-        return cudaLaunchKernelEx(&cfg, kernel, p);
+        return launch_decode_grid(kernel, p, grid, C::NTHREADS, C::SMEM_BYTES, st);
     }
 };
 
