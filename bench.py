@@ -411,6 +411,34 @@ def run_ours(args, rank, world, local_rank):
             torch.cuda.synchronize(dev)
             return statistics.median([a.elapsed_time(b) * 1e3 for a, b in times[3:]])
 
+        def graph_us(calls, reps=50):
+            # back-to-back calls on distinct weight copies (together larger than L2) in
+            # one CUDA graph: the per-call time without host gaps or launch ramp
+            with torch.cuda.stream(stream):
+                for c in calls:
+                    c()
+                torch.cuda.synchronize(dev)
+                g = torch.cuda.CUDAGraph()
+                with torch.cuda.graph(g, stream=stream):
+                    for c in calls:
+                        c()
+                for _ in range(3):
+                    g.replay()
+                a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+                a.record(stream)
+                for _ in range(reps):
+                    g.replay()
+                b.record(stream)
+            torch.cuda.synchronize(dev)
+            return a.elapsed_time(b) * 1e3 / (reps * len(calls))
+
+        def graph_fields(us, byts):
+            return {"us_graph": round(us, 2), "GB/s_graph": round(byts / (us * 1e-6) / 1e9, 1),
+                    "frac_hbm_graph": round(byts / (us * 1e-6) / 1e9 / peaks["hbm_gbs"], 4)}
+
+        def n_copies(wbytes):
+            return max(ROTATING_SETS, int(np.ceil(2.2 * L2_BYTES / wbytes)))
+
         def entry(op, M, N, K, adt, us, byts, extra=None, into=None):
             d = {"op": op, "M": M, "N": N, "K": K, "A": adt, "us": round(us, 2),
                  "TFLOP/s": round(2.0 * M * N * K / (us * 1e-6) / 1e12, 1),
@@ -438,7 +466,17 @@ def run_ours(args, rank, world, local_rank):
             wsx = torch.zeros(wq.get_plan(wq.WQ_OP_FP8, wq.WQ_F16 if adt == "f16" else wq.WQ_BF16, M, N, K, 0)
                              ["ws_bytes"] + 16, dtype=torch.uint8, device=dev)
             us = time_call(lambda: wq.wq_gemm_w8a16_fp8(Ax, wd, alpha, bias=bias, out=outx, ws=wsx))
-            entry("fp8", M, N, K, adt, us, N * K + M * K * 2 + M * N * 2, {"bias": with_bias})
+            byts = N * K + M * K * 2 + M * N * 2
+            extra = {"bias": with_bias}
+            if M <= 128:
+                copies = [wd] + [wd.clone() for _ in range(n_copies(N * K) - 1)]
+                extra.update(graph_fields(graph_us([
+                    (lambda w=w: wq.wq_gemm_w8a16_fp8(Ax, w, alpha, bias=bias, out=outx, ws=wsx)) for w in copies]),
+                    byts))
+                del copies
+            extra["kernel"] = ["tile", "decode", "tile_pair"][wq.get_plan(
+                wq.WQ_OP_FP8, wq.WQ_F16 if adt == "f16" else wq.WQ_BF16, M, N, K, 0)["kernel"]]
+            entry("fp8", M, N, K, adt, us, byts, extra)
             del Ax, wd, outx, wsx
         fp4_cases = [(1, 12800, 5120, None), (128, 12800, 5120, None), (8192, 12800, 5120, None),
                      (128, 6656, 19968, "FP4 page (#4466) quotes 43.90 us for its cute-dsl kernel at this shape, "
@@ -454,8 +492,15 @@ def run_ours(args, rank, world, local_rank):
             wsx = torch.zeros(wq.get_plan(wq.WQ_OP_FP4, wq.WQ_BF16, M, N, K, 0)["ws_bytes"] + 16,
                              dtype=torch.uint8, device=dev)
             us = time_call(lambda: wq.wq_gemm_bf16_fp4(Ax, wd, sfk, alpha, out=outx, ws=wsx))
-            entry("fp4", M, N, K, "bf16", us, N * K // 2 + N * K // 16 + M * K * 2 + M * N * 2,
-                  {"context": note} if note else None)
+            byts = N * K // 2 + N * K // 16 + M * K * 2 + M * N * 2
+            extra = {"context": note} if note else {}
+            if M <= 128:
+                copies = [(wd, sfk)] + [(wd.clone(), sfk.clone()) for _ in range(n_copies(N * K // 2) - 1)]
+                extra.update(graph_fields(graph_us([
+                    (lambda w=w, f=f: wq.wq_gemm_bf16_fp4(Ax, w, f, alpha, out=outx, ws=wsx)) for (w, f) in copies]),
+                    byts))
+                del copies
+            entry("fp4", M, N, K, "bf16", us, byts, extra)
             del Ax, wd, outx, wsx
         # zero-point INT4 beside the symmetric format at the same shapes (the zero-point
         # path runs on the tile kernels at every M)
@@ -574,7 +619,7 @@ def run_ours(args, rank, world, local_rank):
                      "frac": round(achieved / peaks["hbm_gbs"], 4), "traffic": traffic,
                      "peak_source": f"{peaks_src} (MEASURED_PEAKS.json hbm_gbs)" if peaks_src == "measured"
                      else "fallback 6.8 TB/s",
-                     "kernel": "wq_decode_mma_kernel<f16, NT=1|2, BK=128> (register-resident mma.sync, split-K)",
+                     "kernel": "wq_decode_mma_kernel<f16, NT=1|2, BK=256> (register-resident mma.sync, split-K)",
                      "achieved_from": "CUDA events on the launching stream over the timed region (graph "
                                       "replays; the decode kernel is the only kernel there): step bytes / step time",
                      "per_shape_graphs_GB/s": round(per_shape_rate, 1)},

@@ -241,11 +241,17 @@ wq_status make_plan(int fmt, bool bf16, int64_t M, int64_t N, int64_t K, int sms
         // k-blocks per slice, tiles x S within the CTAs the GPU holds at once (the
         // kernel's shared memory is sized so that this is two per SM: the decode
         // consumer is compute-bound, and a third CTA on some SMs would make them the
-        // tail), and all clusters in one wave; the largest such S
+        // tail), and all clusters in one wave with a margin of 1/16 below the cluster
+        // count the occupancy query reports: the hardware does not place that many at
+        // once (measured on GB300, 3-CTA clusters, capacity reported 97: W4A16 M = 1,
+        // K = 4096 takes 8.7 us at 90 tiles, 9.7 at 93, 11.7 at 95 and 13.0 at 96,
+        // against 10.5 us with 2 slices at 96 tiles); the largest such S
         const long long budget = (long long)(sms > 0 ? sms : 148) * (cfg.ctas_per_sm > 0 ? cfg.ctas_per_sm : 1);
         int best = 1;
-        for (int S = 2; S <= kMaxDecodeCluster; ++S)
-            if (p.nkb >= 2 * S && tiles * S <= budget && tiles <= cfg.max_clusters[S]) best = S;
+        for (int S = 2; S <= kMaxDecodeCluster; ++S) {
+            const int cap = cfg.max_clusters[S];
+            if (p.nkb >= 2 * S && tiles * S <= budget && tiles <= cap - (cap + 15) / 16) best = S;
+        }
         p.splits = best;
         items = tiles * best;
     }
