@@ -15,7 +15,9 @@
 // fragment positions 2c, 2c + 1, 2c + 8, 2c + 9 stand for k = 4c, 4c + 1, 4c + 2,
 // 4c + 3 of the step, and the lane's activation operand is the four consecutive values
 // k = 4c .. 4c + 3 of its token: one 8-byte shared-memory load.  No layout transform
-// of the weights is needed, offline or in the kernel.
+// of the weights is needed, offline or in the kernel.  MMA column n of an 8-token
+// tile holds token 2 (n % 4) + n / 4, so that the 8-byte loads of a half-warp read
+// even (or odd) token rows, which the 128-byte swizzle puts on distinct banks.
 //
 // Work split, pipeline and split-K are those of the W4A16 decode kernel: one CTA per
 // (128-row tile, K slice), warps 0-3 compute 32 rows each, warp 4 is the producer, the
@@ -181,14 +183,15 @@ __global__ void __launch_bounds__(Fp8DecodeCfg<STAGES>::NTHREADS, 2)
         uint32_t w_chunk[KSTEPS / 2];
 #pragma unroll
         for (int h = 0; h < KSTEPS / 2; ++h) w_chunk[h] = (uint32_t)(((2 * h + (lane >> 4)) ^ (lane & 7)) << 4);
-        // activation operand of step t, token 8 nt + g: k = 16 t + 4c .. + 3, i.e. box
-        // t / 4, byte 32 (t % 4) + 8c of the token's 128-byte row
+        // activation operand of step t, MMA column g of tile nt (token 8 nt + 2 (g % 4) +
+        // g / 4, spread over the banks): k = 16 t + 4c .. + 3, i.e. box t / 4, byte
+        // 32 (t % 4) + 8c of the token's 128-byte row
         uint32_t a_off[KSTEPS][NT];
 #pragma unroll
         for (int t = 0; t < KSTEPS; ++t)
 #pragma unroll
             for (int nt = 0; nt < NT; ++nt) {
-                const int row = (t >> 2) * p.a_box_rows + nt * 8 + g;
+                const int row = (t >> 2) * p.a_box_rows + nt * 8 + token_of_column<true>(g);
                 const int chunk = 2 * (t & 3) + (c >> 1);
                 a_off[t][nt] = (uint32_t)(row * 128 + ((chunk ^ (row & 7)) << 4) + 8 * (c & 1));
             }
@@ -256,7 +259,7 @@ __global__ void __launch_bounds__(Fp8DecodeCfg<STAGES>::NTHREADS, 2)
 #pragma unroll
                     for (int e = 0; e < 4; ++e) {
                         const int n = tile * TILE_N + (warp * RGW + j) * 16 + g + 8 * (e >> 1);
-                        const int m = nt * 8 + 2 * c + (e & 1);
+                        const int m = nt * 8 + token_of_column<true>(2 * c + (e & 1));
                         if (n < p.N && m < p.M) finish(m, n, sum[j][nt][e]);
                     }
         }
@@ -264,7 +267,7 @@ __global__ void __launch_bounds__(Fp8DecodeCfg<STAGES>::NTHREADS, 2)
         ptx::cluster_wait();   // every CTA of the cluster has initialised its barriers
         if (warp < NCW) decode_send_partials<NT, RGW>(sum, warp, lane, rank, R, sbase + C::INBOX, inbox_bar);
         if (!bounded_wait<true>(inbox_bar, 0u, abort_flag, p.status, DEVICE_TIMEOUT_EPILOGUE, p.timeout_ns)) return;
-        decode_reduce_rows(reinterpret_cast<const float*>(smem + C::INBOX), S, R, rows_own, p.M,
+        decode_reduce_rows<true>(reinterpret_cast<const float*>(smem + C::INBOX), S, R, rows_own, p.M,
                            [&](int m, int r, float v) {
                                const int n = tile * TILE_N + rank * R + r;
                                if (n < p.N) finish(m, n, v);

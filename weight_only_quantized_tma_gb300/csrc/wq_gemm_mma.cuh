@@ -147,15 +147,26 @@ __device__ __forceinline__ void decode_send_partials(const float (&acc)[RGW][NT]
         }
 }
 
+// MMA column n (0..7) of an 8-token tile holds token n, or with SPREAD token
+// 2 (n % 4) + n / 4: the half-warp that loads columns 0-3 then reads tokens 0, 2, 4, 6
+// (and the other half 1, 3, 5, 7), whose rows of a 128-byte-swizzled activation box
+// fall on distinct banks for 8-byte loads.  Inverse: token t sits in column
+// t / 2 + 4 (t % 2).
+template <bool SPREAD>
+__device__ __forceinline__ int token_of_column(int n) { return SPREAD ? 2 * (n & 3) + (n >> 2) : n; }
+template <bool SPREAD>
+__device__ __forceinline__ int column_of_token(int t) { return SPREAD ? (t >> 1) + 4 * (t & 1) : t; }
+
 // After the inbox phase completed: store(m, r, v) for token m < M and owned row r,
 // with v the sum of the S slices in rank order.  Weight row fastest: a warp stores
 // consecutive output columns of one token.
-template <typename Store>
+template <bool SPREAD = false, typename Store>
 __device__ __forceinline__ void decode_reduce_rows(const float* box, int S, int R, int rows_own, int M, Store store) {
     for (int e = threadIdx.x; e < M * rows_own; e += blockDim.x) {
         const int m = e / rows_own;
         const int r = e - m * rows_own;
-        const int slot = 4 * ((m & 7) >> 1) + (m & 1) + 2 * (m >> 3);
+        const int n = column_of_token<SPREAD>(m & 7);   // lane 4 g + n / 2 holds it as value n % 2
+        const int slot = 4 * (n >> 1) + (n & 1) + 2 * (m >> 3);
         float tot = 0.0f;
         for (int q = 0; q < S; ++q) tot += box[(q * R + r) * 16 + slot];
         store(m, r, tot);
