@@ -21,8 +21,7 @@
 //
 // Work split, pipeline and split-K are those of the W4A16 decode kernel: one CTA per
 // (128-row tile, K slice), warps 0-3 compute 32 rows each, warp 4 is the producer, the
-// K slices of a tile are one thread-block cluster reducing through st.async.  There is
-// no activation-sum warp: the codes need no offset correction.
+// K slices of a tile are one thread-block cluster reducing through st.async.
 #pragma once
 
 #include "wq_gemm_mma.cuh"

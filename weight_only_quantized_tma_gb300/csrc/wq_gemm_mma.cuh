@@ -8,24 +8,25 @@
 // bulk-copy ring into shared memory, each lane turns its 32-bit word straight into an
 // m16n8k16 A fragment, and mma.sync accumulates in fp32.  At full HBM rate an SM has
 // ~360 cycles per 8 KB of weights, so the instruction count per word decides the
-// speed: one shift and four AND-ORs per word (8 weights), no per-weight arithmetic.
+// speed: one shift, four AND-ORs and four subtractions per word (8 weights).
 //
 // Operand: the fragment-order layout puts the codes of a fragment register at bits
 // 0-3/16-19 (rows g) or 4-7/20-23 (rows g + 8) of a word.  One AND-OR with an fp16
 // "magic number" gives b + q with b = 1024 (exponent 2^10) or b = 64 (exponent 2^6,
-// whose mantissa unit is 1/16); bf16 operands give 128 + q.  The MMA sums A (b + q)
-// exactly in fp32, and the group scale and the offset are applied once per group:
+// whose mantissa unit is 1/16); bf16 operands give 128 + q.  Subtracting b + 8 (or
+// b + z with a zero point z) leaves q - 8 exactly (small integers), so the MMA sums
+// A (q - 8) in fp32 and the group scale is applied once per group on those sums:
 //
-//   sum_{k in g} A[m,k] (q - 8) s  =  s * ( D[n,m] - (b_n + 8) * S_g[m] )
-//   D[n,m] = sum_{k in g} A[m,k] (b_n + q[n,k]),   S_g[m] = sum_{k in g} A[m,k]
+//   sum_{k in g} A[m,k] (q - 8) s  =  s * sum_{k in g} A[m,k] (q[n,k] - 8)
 //
-// ("Low Bit Triton Kernels", §03: the dequantized value is (q - 8) * s).  S_g is the
-// same for every weight row: one warp of the CTA computes it per stage (an MMA with
-// an all-ones operand) and shares it through shared memory.
+// ("Low Bit Triton Kernels", §03: the dequantized value is (q - 8) * s).  (Measured on
+// GB300: one subtraction per register costs less than forming the sums of b + q and
+// correcting them per group with activation sums computed by a separate warp, which
+// the compute warps had to wait for on every stage: decode step 75.2 -> 73.7 us.)
 //
 // Work split: one CTA per (128-row tile, K slice).  Warps: 0-3 compute (warp w owns
-// rows 32w .. 32w + 31 of the tile, so each row's sum lives in one warp), 4 computes
-// S, 5 is the producer.  When K is split, the S slices of a tile are the CTAs of one
+// rows 32w .. 32w + 31 of the tile, so each row's sum lives in one warp), 4 is the
+// producer.  When K is split, the S slices of a tile are the CTAs of one
 // thread-block cluster: each sends the fp32 partial sums of every row to the row's
 // owner (CTA r owns rows [r R, r R + R), R = ceil(128 / S)) with st.async, which
 // completes on the owner's inbox barrier, and each adds its own rows over the ranks in
@@ -48,21 +49,16 @@ struct MmaDecodeCfg {
     // 16 rows; two warps of 64 rows ~35 % slower)
     static constexpr int NCW = 4;
     static constexpr int RGW = TILE_N / 16 / NCW;             // 16-row groups per compute warp
-    static constexpr int S_WARP = NCW;                        // activation-sum warp
-    static constexpr int P_WARP = NCW + 1;                    // producer warp
-    static constexpr int NTHREADS = 32 * (NCW + 2);
+    static constexpr int P_WARP = NCW;                        // producer warp
+    static constexpr int NTHREADS = 32 * (NCW + 1);
     static constexpr int NZ = BK / 64;                        // 64-wide activation boxes per stage
-    // per stage: packed weights, scales (up to BK / 32 groups, G = 32) and the offset
-    // terms -(b + 8) S_g[m] for both row halves in one region; the 128-byte-swizzled
-    // activation boxes in a second, 1024-byte aligned region
+    // per stage: packed weights, scales (up to BK / 32 groups, G = 32) and, with zero
+    // points, the stage's zero points (uint8 [BK / 32][128]) in one region; the
+    // 128-byte-swizzled activation boxes in a second, 1024-byte aligned region
     static constexpr int W_STAGE = TILE_N * BK / 2;
     static constexpr int SC_OFF = W_STAGE;
-    static constexpr int S_OFF = SC_OFF + (BK / 32) * TILE_N * 2;
-    // zero-point variant: the stage's zero points (uint8 [BK / 32][128]) and the plain
-    // activation sums S_g[m] (fp32 [BK / 32][16])
-    static constexpr int Z_OFF = S_OFF + (BK / 32) * 2 * 16 * 4;   // after -(b + 8) S_g[m], fp32 [BK / 32][2][16]
-    static constexpr int SR_OFF = Z_OFF + (ZP ? (BK / 32) * TILE_N : 0);
-    static constexpr int WS_STAGE = SR_OFF + (ZP ? (BK / 32) * 16 * 4 : 0);
+    static constexpr int Z_OFF = SC_OFF + (BK / 32) * TILE_N * 2;
+    static constexpr int WS_STAGE = Z_OFF + (ZP ? (BK / 32) * TILE_N : 0);
     static constexpr int A_STAGE = 16 * 128 * NZ;             // up to 16 token rows of 128 bytes per box
     static constexpr int A_BASE = (STAGES * WS_STAGE + 1023) / 1024 * 1024;
     // split-K inbox: the partial sums the S CTAs of a cluster send to the CTA that
@@ -74,10 +70,10 @@ struct MmaDecodeCfg {
     static constexpr int INBOX = A_BASE + STAGES * A_STAGE;
     static constexpr int INBOX_BYTES = 16 * (TILE_N + 16) * 4;
     static constexpr int OFF_BAR = INBOX + INBOX_BYTES;
-    // barriers: full, sready, empty per stage; then the abort flag (4 B) and the inbox
-    // barrier (8 B, split-K)
-    static constexpr int OFF_INBOX_BAR = OFF_BAR + 3 * STAGES * 8 + 8;
-    static constexpr int SMEM_USED = OFF_BAR + 3 * STAGES * 8 + 16;
+    // barriers: full and empty per stage; then the abort flag (4 B, padded to 8) and the
+    // inbox barrier (8 B, split-K)
+    static constexpr int OFF_INBOX_BAR = OFF_BAR + 2 * STAGES * 8 + 8;
+    static constexpr int SMEM_USED = OFF_INBOX_BAR + 8;
     static constexpr int SMEM_BYTES = SMEM_USED + 1024;
     static_assert(BK == 128 || BK == 256, "BK");
     static_assert(WS_STAGE % 16 == 0 && A_STAGE % 1024 == 0, "bulk-copy and swizzle alignment");
@@ -173,21 +169,39 @@ __device__ __forceinline__ void decode_reduce_rows(const float* box, int S, int 
     }
 }
 
-// One 32-bit word of the fragment-order layout -> the four A-fragment registers of
-// one k step, each holding two values b + q, exact.
+// b + z of rows g (upper = false) or g + 8 (upper = true) as a pair of 16-bit values:
+// fp16 1024 + z and 64 + z (mantissa unit 1/16), bf16 128 + z; z = 8 without zero points.
 template <bool BF16>
-__device__ __forceinline__ void int4_word_to_frag(uint32_t w, uint32_t (&a)[4]) {
+__device__ __forceinline__ uint32_t int4_offset(bool upper, uint32_t z) {
+    const uint32_t v = BF16 ? 0x4300u + z : upper ? 0x5400u + (z << 4) : 0x6400u + z;
+    return v | (v << 16);
+}
+
+__device__ __forceinline__ uint32_t sub_16x2(uint32_t a, uint32_t b, bool bf16) {
+    uint32_t r;
+    if (bf16)
+        asm("sub.rn.bf16x2 %0, %1, %2;" : "=r"(r) : "r"(a), "r"(b));
+    else
+        asm("sub.rn.f16x2 %0, %1, %2;" : "=r"(r) : "r"(a), "r"(b));
+    return r;
+}
+
+// One 32-bit word of the fragment-order layout -> the four A-fragment registers of
+// one k step, each holding two values q - z, exact: b + q from an AND-OR with the
+// magic number, minus b + z (off_lo for rows g, off_hi for rows g + 8).
+template <bool BF16>
+__device__ __forceinline__ void int4_word_to_frag(uint32_t w, uint32_t off_lo, uint32_t off_hi, uint32_t (&a)[4]) {
     if (BF16) {
-        a[0] = (w & 0x000F000Fu) | 0x43004300u;           // rows g,     k       (128 + q)
-        a[1] = ((w >> 4) & 0x000F000Fu) | 0x43004300u;    // rows g + 8, k
-        a[2] = ((w >> 8) & 0x000F000Fu) | 0x43004300u;    // rows g,     k + 8
-        a[3] = ((w >> 12) & 0x000F000Fu) | 0x43004300u;   // rows g + 8, k + 8
+        a[0] = sub_16x2((w & 0x000F000Fu) | 0x43004300u, off_lo, true);           // rows g,     k
+        a[1] = sub_16x2(((w >> 4) & 0x000F000Fu) | 0x43004300u, off_hi, true);    // rows g + 8, k
+        a[2] = sub_16x2(((w >> 8) & 0x000F000Fu) | 0x43004300u, off_lo, true);    // rows g,     k + 8
+        a[3] = sub_16x2(((w >> 12) & 0x000F000Fu) | 0x43004300u, off_hi, true);   // rows g + 8, k + 8
     } else {
         const uint32_t w8 = w >> 8;
-        a[0] = (w & 0x000F000Fu) | 0x64006400u;           // 1024 + q
-        a[1] = (w & 0x00F000F0u) | 0x54005400u;           // 64 + q
-        a[2] = (w8 & 0x000F000Fu) | 0x64006400u;
-        a[3] = (w8 & 0x00F000F0u) | 0x54005400u;
+        a[0] = sub_16x2((w & 0x000F000Fu) | 0x64006400u, off_lo, false);          // 1024 + q
+        a[1] = sub_16x2((w & 0x00F000F0u) | 0x54005400u, off_hi, false);          // 64 + q
+        a[2] = sub_16x2((w8 & 0x000F000Fu) | 0x64006400u, off_lo, false);
+        a[3] = sub_16x2((w8 & 0x00F000F0u) | 0x54005400u, off_hi, false);
     }
 }
 
@@ -204,18 +218,14 @@ __global__ void __launch_bounds__(MmaDecodeCfg<BK, STAGES, ZP>::NTHREADS, 2)
     constexpr int RGW = C::RGW;
     constexpr int KSTEPS = BK / 16;
     constexpr int SETS = NT == 1 ? 2 : 1;               // accumulator sets per chain (even / odd k steps)
-    constexpr float CORR_LO = BF16 ? 136.0f : 1032.0f;  // b + 8, rows g
-    constexpr float CORR_HI = BF16 ? 136.0f : 72.0f;    // b + 8, rows g + 8
-    constexpr uint32_t ONES = BF16 ? 0x3F803F80u : 0x3C003C00u;
     static_assert((GSTEPS == 2 || GSTEPS == 4 || GSTEPS == 8 || GSTEPS == 16) && GSTEPS <= KSTEPS, "GSTEPS");
     extern __shared__ uint8_t smem_raw[];
     uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
     const uint32_t sbase = ptx::smem_u32(smem);
     const uint32_t bar0 = sbase + C::OFF_BAR;
     auto full_bar = [&](int s) { return bar0 + 8u * s; };
-    auto sready_bar = [&](int s) { return bar0 + 8u * (STAGES + s); };
-    auto empty_bar = [&](int s) { return bar0 + 8u * (2 * STAGES + s); };
-    volatile uint32_t* abort_flag = reinterpret_cast<volatile uint32_t*>(smem + C::OFF_BAR + 3 * STAGES * 8);
+    auto empty_bar = [&](int s) { return bar0 + 8u * (STAGES + s); };
+    volatile uint32_t* abort_flag = reinterpret_cast<volatile uint32_t*>(smem + C::OFF_BAR + 2 * STAGES * 8);
     const uint32_t inbox_bar = sbase + C::OFF_INBOX_BAR;
 
     const int warp = threadIdx.x >> 5;
@@ -231,8 +241,7 @@ __global__ void __launch_bounds__(MmaDecodeCfg<BK, STAGES, ZP>::NTHREADS, 2)
     if (threadIdx.x == 0) {
         for (int s = 0; s < STAGES; ++s) {
             ptx::mbar_init(full_bar(s), 1);
-            ptx::mbar_init(sready_bar(s), 1);
-            ptx::mbar_init(empty_bar(s), NCW + 1);   // compute warps and the S warp
+            ptx::mbar_init(empty_bar(s), NCW);
         }
         ptx::mbar_init(inbox_bar, 1);
         *abort_flag = 0u;
@@ -277,13 +286,11 @@ __global__ void __launch_bounds__(MmaDecodeCfg<BK, STAGES, ZP>::NTHREADS, 2)
     if (warp == C::P_WARP) {
         // ------------------------------------------------------------ producer
         // Lane 0 streams weights and scales; the first STAGES k-blocks' go out at once,
-        // before the grid dependency wait (constant inputs).  Their activation copies
-        // are issued by the S warp (below) as soon as the preceding kernel is done, so
-        // the first stage is not held behind the other stages' weight copies.  The
-        // order in which a stage's bytes land does not matter: its phase cannot
-        // complete before this lane's arrive-expect-tx.  The loop after that can stop
-        // early only at a wait, and it waits only after passing those stages, so every
-        // barrier armed here gets all of its bytes.
+        // before the grid dependency wait (constant inputs), their activation copies
+        // right after it.  The order in which a stage's bytes land does not matter: its
+        // phase cannot complete before this lane's arrive-expect-tx.  The loop after
+        // that can stop early only at a wait, and it waits only after passing those
+        // stages, so every barrier armed here gets all of its bytes.
         const int pre = nunits < STAGES ? nunits : STAGES;
         const uint32_t a_bytes = (uint32_t)NZ * (uint32_t)p.a_box_rows * 128u;
         if (lane == 0) {
@@ -306,8 +313,13 @@ __global__ void __launch_bounds__(MmaDecodeCfg<BK, STAGES, ZP>::NTHREADS, 2)
                     ptx::bulk_load(st + C::Z_OFF, p.zp + ((size_t)tile * p.ngroups_pad + g0) * TILE_N, zp_bytes, fb,
                                    pol_w);
             };
+            // activation box {64 k, M tokens, NZ}: k-block kb starts at z = kb * NZ
+            auto load_a = [&](int s, int kb) {
+                ptx::tma_load_3d(sbase + C::A_BASE + s * C::A_STAGE, &p.tmap_a, 0, 0, kb * NZ, full_bar(s), pol_a);
+            };
             for (int i = 0; i < pre; ++i) load_w(i, it.kb_begin + i);
             ptx::grid_dependency_wait();
+            for (int i = 0; i < pre; ++i) load_a(i, it.kb_begin + i);
             int s = pre % STAGES;
             uint32_t ph = pre == STAGES ? 1u : 0u;
             int issued = pre;
@@ -317,8 +329,7 @@ __global__ void __launch_bounds__(MmaDecodeCfg<BK, STAGES, ZP>::NTHREADS, 2)
                                   p.timeout_ns))
                     break;
                 load_w(s, kb);
-                // activation box {64 k, M tokens, NZ}: k-block kb starts at z = kb * NZ
-                ptx::tma_load_3d(sbase + C::A_BASE + s * C::A_STAGE, &p.tmap_a, 0, 0, kb * NZ, full_bar(s), pol_a);
+                load_a(s, kb);
                 ++issued;
                 if (++s == STAGES) {
                     s = 0;
@@ -333,73 +344,6 @@ __global__ void __launch_bounds__(MmaDecodeCfg<BK, STAGES, ZP>::NTHREADS, 2)
             }
         }
         __syncwarp();
-    } else if (warp == C::S_WARP) {
-        // ------------------------------------------------------------ activation sums
-        // S_g[m] per scale group of the stage, from an MMA with an all-ones operand;
-        // row g = 0 of the accumulator (lanes 0-3) holds tokens 2c, 2c + 1 (+ 8 nt).
-        // Stored as the starting values of the compute warps' group sums:
-        // -(b + 8) S_g[m] for rows g (b = 1024, bf16 128) and rows g + 8 (b = 64).
-        // This warp runs up to STAGES stages ahead of the compute warps.  First, its
-        // lane 0 issues the activation copies of the producer's first STAGES stages.
-        if (lane == 0) {
-            const uint64_t pol_a = ptx::policy_evict_last();
-            const int pre = nunits < STAGES ? nunits : STAGES;
-            ptx::grid_dependency_wait();
-            for (int i = 0; i < pre; ++i)
-                ptx::tma_load_3d(sbase + C::A_BASE + i * C::A_STAGE, &p.tmap_a, 0, 0, (it.kb_begin + i) * NZ,
-                                 full_bar(i), pol_a);
-        }
-        __syncwarp();
-        const uint32_t ones[4] = {ONES, ONES, ONES, ONES};
-        int s = 0;
-        uint32_t ph = 0;
-        for (int i = 0; i < nunits; ++i) {
-            const bool w1 = bounded_wait(full_bar(s), ph, abort_flag, p.status, DEVICE_TIMEOUT_TRANSFORM,
-                                         p.timeout_ns);
-            if (!__all_sync(0xffffffffu, w1)) break;
-            const uint32_t st = sbase + C::A_BASE + s * C::A_STAGE;   // this stage's activation boxes
-            float* sg = reinterpret_cast<float*>(smem + s * C::WS_STAGE + C::S_OFF);
-            float sacc[NT][4];
-#pragma unroll
-            for (int t = 0; t < KSTEPS; ++t) {
-                if (t % GSTEPS == 0) {
-#pragma unroll
-                    for (int nt = 0; nt < NT; ++nt)
-#pragma unroll
-                        for (int e = 0; e < 4; ++e) sacc[nt][e] = 0.0f;
-                }
-                uint32_t b[NT][2];
-                if constexpr (NT == 2)
-                    ldmatrix_x4(st + a_off[t], b[0][0], b[0][1], b[NT - 1][0], b[NT - 1][1]);
-                else
-                    ldmatrix_x2(st + a_off[t], b[0][0], b[0][1]);
-#pragma unroll
-                for (int nt = 0; nt < NT; ++nt) mma_16816(sacc[nt], ones, b[nt][0], b[nt][1], BF16);
-                if ((t + 1) % GSTEPS == 0 && lane < 4) {
-                    float* dst = sg + (t / GSTEPS) * 32;
-#pragma unroll
-                    for (int nt = 0; nt < NT; ++nt) {
-                        const int m = nt * 8 + 2 * lane;
-                        *reinterpret_cast<float2*>(dst + m) = make_float2(-CORR_LO * sacc[nt][0], -CORR_LO * sacc[nt][1]);
-                        *reinterpret_cast<float2*>(dst + 16 + m) =
-                            make_float2(-CORR_HI * sacc[nt][0], -CORR_HI * sacc[nt][1]);
-                        if (ZP) {
-                            float* raw = reinterpret_cast<float*>(smem + s * C::WS_STAGE + C::SR_OFF) + (t / GSTEPS) * 16;
-                            *reinterpret_cast<float2*>(raw + m) = make_float2(sacc[nt][0], sacc[nt][1]);
-                        }
-                    }
-                }
-            }
-            __syncwarp();
-            if (lane == 0) {
-                ptx::mbar_arrive(sready_bar(s));
-                ptx::mbar_arrive(empty_bar(s));
-            }
-            if (++s == STAGES) {
-                s = 0;
-                ph ^= 1u;
-            }
-        }
     } else {
         // ------------------------------------------------------------ compute warps
         const int g = lane >> 2, c = lane & 3;
@@ -408,18 +352,12 @@ __global__ void __launch_bounds__(MmaDecodeCfg<BK, STAGES, ZP>::NTHREADS, 2)
         int s = 0;
         uint32_t ph = 0;
         for (int i = 0; i < nunits; ++i) {
-            // One wait per stage: the S warp arrives on sready(s) only after it waited for
-            // the stage's copies (full(s)) and wrote the stage's offset terms, so its
-            // phase completing covers both.  (A wait on an mbarrier phase costs a few
-            // hundred cycles even when the phase completed long before -- measured on
-            // GB300 -- which is why the compute warps do not wait on full(s) as well.)
-            const bool w2 = bounded_wait(sready_bar(s), ph, abort_flag, p.status, DEVICE_TIMEOUT_TRANSFORM,
+            const bool ok = bounded_wait(full_bar(s), ph, abort_flag, p.status, DEVICE_TIMEOUT_TRANSFORM,
                                          p.timeout_ns);
-            if (!__all_sync(0xffffffffu, w2)) break;
+            if (!__all_sync(0xffffffffu, ok)) break;
             const uint8_t* stp = smem + s * C::WS_STAGE;
             const uint32_t st = sbase + C::A_BASE + s * C::A_STAGE;   // this stage's activation boxes
             const uint16_t* sc = reinterpret_cast<const uint16_t*>(stp + C::SC_OFF);
-            const float* sg = reinterpret_cast<const float*>(stp + C::S_OFF);
             uint4 wv[KSTEPS / 4][RGW];
 #pragma unroll
             for (int tq = 0; tq < KSTEPS / 4; ++tq)
@@ -427,26 +365,27 @@ __global__ void __launch_bounds__(MmaDecodeCfg<BK, STAGES, ZP>::NTHREADS, 2)
                 for (int j = 0; j < RGW; ++j)
                     wv[tq][j] = *reinterpret_cast<const uint4*>(stp + tq * 4096 + w_off + j * 512);
             float tmp[RGW][SETS][NT][4];
+            uint32_t off_lo[RGW], off_hi[RGW];   // b + z of the group, rows g and g + 8
 #pragma unroll
             for (int t = 0; t < KSTEPS; ++t) {
                 if (t % GSTEPS == 0) {
-                    // group start: D begins at -(b + 8) S_g, so that it ends as D - (b + 8) S_g
-                    const float* so = sg + (t / GSTEPS) * 32;
+                    // group start: sums from zero; the zero points of the group's rows
 #pragma unroll
-                    for (int nt = 0; nt < NT; ++nt) {
-                        const float2 lo = *reinterpret_cast<const float2*>(so + nt * 8 + 2 * c);
-                        const float2 hi = *reinterpret_cast<const float2*>(so + 16 + nt * 8 + 2 * c);
+                    for (int j = 0; j < RGW; ++j) {
 #pragma unroll
-                        for (int j = 0; j < RGW; ++j) {
-                            tmp[j][0][nt][0] = lo.x;
-                            tmp[j][0][nt][1] = lo.y;
-                            tmp[j][0][nt][2] = hi.x;
-                            tmp[j][0][nt][3] = hi.y;
+                        for (int h = 0; h < SETS; ++h)
 #pragma unroll
-                            for (int h = 1; h < SETS; ++h)
+                            for (int nt = 0; nt < NT; ++nt)
 #pragma unroll
                                 for (int e = 0; e < 4; ++e) tmp[j][h][nt][e] = 0.0f;
+                        uint32_t z_lo = 8u, z_hi = 8u;
+                        if constexpr (ZP) {
+                            const uint8_t* zp = stp + C::Z_OFF + (t / GSTEPS) * TILE_N + (warp * RGW + j) * 16 + g;
+                            z_lo = zp[0];
+                            z_hi = zp[8];
                         }
+                        off_lo[j] = int4_offset<BF16>(false, z_lo);
+                        off_hi[j] = int4_offset<BF16>(true, z_hi);
                     }
                 }
                 uint32_t b[NT][2];
@@ -459,37 +398,24 @@ __global__ void __launch_bounds__(MmaDecodeCfg<BK, STAGES, ZP>::NTHREADS, 2)
                     const uint4& q4 = wv[t >> 2][j];
                     const uint32_t word = (t & 3) == 0 ? q4.x : (t & 3) == 1 ? q4.y : (t & 3) == 2 ? q4.z : q4.w;
                     uint32_t a[4];
-                    int4_word_to_frag<BF16>(word, a);
+                    int4_word_to_frag<BF16>(word, off_lo[j], off_hi[j], a);
 #pragma unroll
                     for (int nt = 0; nt < NT; ++nt) mma_16816(tmp[j][t % SETS][nt], a, b[nt][0], b[nt][1], BF16);
                 }
                 if ((t + 1) % GSTEPS == 0) {
-                    // acc += s * (D - (b + 8) S_g); with zero points z per row,
-                    // D - (b + z) S_g = (D - (b + 8) S_g) + (8 - z) S_g
+                    // acc += s * sum_{k in group} A (q - z)
                     const int gi = t / GSTEPS;
 #pragma unroll
                     for (int j = 0; j < RGW; ++j) {
                         const uint16_t* sp = sc + gi * TILE_N + (warp * RGW + j) * 16 + g;
                         const float s_lo = __half2float(__ushort_as_half(sp[0]));
                         const float s_hi = __half2float(__ushort_as_half(sp[8]));
-                        float dz_lo = 0.0f, dz_hi = 0.0f;
-                        float2 sraw[NT];
-                        if constexpr (ZP) {
-                            const uint8_t* zp = stp + C::Z_OFF + gi * TILE_N + (warp * RGW + j) * 16 + g;
-                            dz_lo = (float)(8 - (int)zp[0]);
-                            dz_hi = (float)(8 - (int)zp[8]);
-                            const float* raw = reinterpret_cast<const float*>(stp + C::SR_OFF) + gi * 16;
-#pragma unroll
-                            for (int nt = 0; nt < NT; ++nt)
-                                sraw[nt] = *reinterpret_cast<const float2*>(raw + nt * 8 + 2 * c);
-                        }
 #pragma unroll
                         for (int nt = 0; nt < NT; ++nt)
 #pragma unroll
                             for (int e = 0; e < 4; ++e) {
                                 float d = tmp[j][0][nt][e];
                                 if constexpr (SETS == 2) d += tmp[j][1][nt][e];
-                                if constexpr (ZP) d = fmaf((e < 2) ? dz_lo : dz_hi, (e & 1) ? sraw[nt].y : sraw[nt].x, d);
                                 acc[j][nt][e] = fmaf((e < 2) ? s_lo : s_hi, d, acc[j][nt][e]);
                             }
                     }

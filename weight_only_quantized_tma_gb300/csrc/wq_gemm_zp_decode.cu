@@ -1,5 +1,5 @@
 // wq_gemm_zp_decode.cu -- the register-resident decode kernel (M <= 16) for zero-point
-// INT4: each group's fold adds (8 - z) S_g[m] per row, with the zero points streamed
+// INT4: the operands are q - z, with the zero points of each group and row streamed
 // beside the scales.  Same shapes and instantiation grid as the symmetric decode
 // kernel in wq_gemm_int4.cu.
 #include "wq_gemm_mma.cuh"
