@@ -92,9 +92,10 @@ __global__ void __launch_bounds__(Fp8DecodeCfg<STAGES>::NTHREADS, 2)
     const int nunits = it.kb_end - it.kb_begin;
     const int tile = it.n_tile;
     const int S = p.splits;
-    const int R = (TILE_N + S - 1) / S;
+    const int R = (TILE_N + S - 1) / S;   // inbox rows per slice: an owner's rows, at most
     const int rank = S > 1 ? (int)ptx::cluster_ctarank() : 0;
-    const int rows_own = min(TILE_N, (rank + 1) * R) - rank * R;
+    const int row0 = rank * TILE_N / S;     // this CTA's rows of the tile: [row0, row0 + rows_own)
+    const int rows_own = (rank + 1) * TILE_N / S - row0;
     if (threadIdx.x == 0) {
         for (int s = 0; s < STAGES; ++s) {
             ptx::mbar_init(full_bar(s), 1);
@@ -264,11 +265,11 @@ __global__ void __launch_bounds__(Fp8DecodeCfg<STAGES>::NTHREADS, 2)
         }
     } else {
         ptx::cluster_wait();   // every CTA of the cluster has initialised its barriers
-        if (warp < NCW) decode_send_partials<NT, RGW>(sum, warp, lane, rank, R, sbase + C::INBOX, inbox_bar);
+        if (warp < NCW) decode_send_partials<NT, RGW>(sum, warp, lane, rank, S, R, sbase + C::INBOX, inbox_bar);
         if (!bounded_wait<true>(inbox_bar, 0u, abort_flag, p.status, DEVICE_TIMEOUT_EPILOGUE, p.timeout_ns)) return;
         decode_reduce_rows<true>(reinterpret_cast<const float*>(smem + C::INBOX), S, R, rows_own, p.M,
                            [&](int m, int r, float v) {
-                               const int n = tile * TILE_N + rank * R + r;
+                               const int n = tile * TILE_N + row0 + r;
                                if (n < p.N) finish(m, n, v);
                            });
     }

@@ -62,8 +62,8 @@ struct MmaDecodeCfg {
     static constexpr int A_STAGE = 16 * 128 * NZ;             // up to 16 token rows of 128 bytes per box
     static constexpr int A_BASE = (STAGES * WS_STAGE + 1023) / 1024 * 1024;
     // split-K inbox: the partial sums the S CTAs of a cluster send to the CTA that
-    // owns R = ceil(128 / S) of the tile's rows, fp32 [S][R][16 token slots] -- at
-    // most 16 * (128 + 15) values; never used by the main loop, so a peer may write
+    // owns at most R = ceil(128 / S) of the tile's rows, fp32 [S][R][16 token slots] --
+    // at most 16 * (128 + 15) values; never used by the main loop, so a peer may write
     // into it while this CTA is still streaming.  Token slot 4c + i holds token
     // 2c + (i & 1) + 8 (i >> 1): the order of a lane's accumulator values, so each
     // lane sends a row's values with one vector store.
@@ -110,13 +110,14 @@ __device__ __forceinline__ void ldmatrix_x4(uint32_t addr, uint32_t& r0, uint32_
 
 // ---------------------------------------------------------------- split-K exchange
 // Shared by the decode kernels.  The S slices of a 128-row tile are the CTAs of one
-// cluster; CTA `rank` owns rows [rank R, rank R + R) of the tile, R = ceil(128 / S).
+// cluster; CTA `rank` owns rows [128 rank / S, 128 (rank + 1) / S) of the tile (an even
+// split: 8 to 64 rows each, none empty for any S <= 16).
 // Each CTA sends every row's fp32 partial sums to the row's owner (its own rows to
 // itself) with st.async, which completes on the owner's inbox barrier; the owner then
 // adds the S slices of its rows in rank order (deterministic) and reads only its own
 // shared memory.  No cluster-wide barrier has to wait for the remote stores to
 // complete (measured on GB300: a barrier.cluster with release semantics after remote
-// stores cost ~1 us per launch).  Inbox: fp32 [S][R][16 token slots]; token slot
+// stores cost ~1 us per launch).  Inbox: fp32 [S][R = ceil(128 / S)][16 token slots]; token slot
 // 4c + i holds token 2c + (i & 1) + 8 (i >> 1), the order of a lane's accumulator
 // values, so a lane sends a row's values with one vector store.
 
@@ -124,15 +125,15 @@ __device__ __forceinline__ void ldmatrix_x4(uint32_t addr, uint32_t& r0, uint32_
 // acc[j][nt][e] (e = 0, 1: row g, tokens 8 nt + 2c + e; e = 2, 3: row g + 8).
 template <int NT, int RGW>
 __device__ __forceinline__ void decode_send_partials(const float (&acc)[RGW][NT][4], int warp, int lane, int rank,
-                                                     int R, uint32_t inbox, uint32_t inbox_bar) {
+                                                     int S, int R, uint32_t inbox, uint32_t inbox_bar) {
     const int g = lane >> 2, c = lane & 3;
 #pragma unroll
     for (int j = 0; j < RGW; ++j)
 #pragma unroll
         for (int h = 0; h < 2; ++h) {
             const int r = (warp * RGW + j) * 16 + g + 8 * h;   // e = 2h, 2h + 1
-            const int owner = r / R;
-            const uint32_t off = inbox + (uint32_t)((rank * R + (r - owner * R)) * 16 + 4 * c) * 4u;
+            const int owner = ((r + 1) * S - 1) / TILE_N;       // 128 owner / S <= r < 128 (owner + 1) / S
+            const uint32_t off = inbox + (uint32_t)((rank * R + (r - owner * TILE_N / S)) * 16 + 4 * c) * 4u;
             const uint32_t dst = ptx::mapa_shared(off, (uint32_t)owner);
             const uint32_t rbar = ptx::mapa_shared(inbox_bar, (uint32_t)owner);
             if constexpr (NT == 2)
@@ -153,8 +154,8 @@ __device__ __forceinline__ int token_of_column(int n) { return SPREAD ? 2 * (n &
 template <bool SPREAD>
 __device__ __forceinline__ int column_of_token(int t) { return SPREAD ? (t >> 1) + 4 * (t & 1) : t; }
 
-// After the inbox phase completed: store(m, r, v) for token m < M and owned row r,
-// with v the sum of the S slices in rank order.  Weight row fastest: a warp stores
+// After the inbox phase completed: store(m, r, v) for token m < M and the r-th owned
+// row, with v the sum of the S slices in rank order.  Weight row fastest: a warp stores
 // consecutive output columns of one token.
 template <bool SPREAD = false, typename Store>
 __device__ __forceinline__ void decode_reduce_rows(const float* box, int S, int R, int rows_own, int M, Store store) {
@@ -233,11 +234,12 @@ __global__ void __launch_bounds__(MmaDecodeCfg<BK, STAGES, ZP>::NTHREADS, 2)
     const Item it = decode_item(p, (int)blockIdx.x);
     const int nunits = it.kb_end - it.kb_begin;
     const int tile = it.n_tile;
-    // split-K: CTA `rank` of the tile's cluster owns rows [rank R, rank R + R) of the tile
+    // split-K: CTA `rank` of the tile's cluster owns rows [128 rank / S, 128 (rank + 1) / S)
     const int S = p.splits;
-    const int R = (TILE_N + S - 1) / S;
+    const int R = (TILE_N + S - 1) / S;   // inbox rows per slice: an owner's rows, at most
     const int rank = S > 1 ? (int)ptx::cluster_ctarank() : 0;
-    const int rows_own = min(TILE_N, (rank + 1) * R) - rank * R;
+    const int row0 = rank * TILE_N / S;
+    const int rows_own = (rank + 1) * TILE_N / S - row0;
     if (threadIdx.x == 0) {
         for (int s = 0; s < STAGES; ++s) {
             ptx::mbar_init(full_bar(s), 1);
@@ -452,12 +454,12 @@ __global__ void __launch_bounds__(MmaDecodeCfg<BK, STAGES, ZP>::NTHREADS, 2)
     } else {
         // split-K: partial rows to their owners, the owners add them in rank order
         ptx::cluster_wait();   // every CTA of the cluster has initialised its barriers
-        if (warp < NCW) decode_send_partials<NT, RGW>(acc, warp, lane, rank, R, sbase + C::INBOX, inbox_bar);
+        if (warp < NCW) decode_send_partials<NT, RGW>(acc, warp, lane, rank, S, R, sbase + C::INBOX, inbox_bar);
         // (bounded like every wait: a timeout sets the status word; nothing is read then)
         if (!bounded_wait<true>(inbox_bar, 0u, abort_flag, p.status, DEVICE_TIMEOUT_EPILOGUE, p.timeout_ns)) return;
         decode_reduce_rows(reinterpret_cast<const float*>(smem + C::INBOX), S, R, rows_own, p.M,
                            [&](int m, int r, float v) {
-                               const int n = tile * TILE_N + rank * R + r;
+                               const int n = tile * TILE_N + row0 + r;
                                if (n < p.N) store_out<BF16>(p.out, (size_t)m * p.N + n, v);
                            });
     }
