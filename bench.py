@@ -494,6 +494,7 @@ def run_ours(args, rank, world, local_rank):
             us = time_call(lambda: wq.wq_gemm_bf16_fp4(Ax, wd, sfk, alpha, out=outx, ws=wsx))
             byts = N * K // 2 + N * K // 16 + M * K * 2 + M * N * 2
             extra = {"context": note} if note else {}
+            extra["kernel"] = ["tile", "decode", "tile_pair"][wq.get_plan(wq.WQ_OP_FP4, wq.WQ_BF16, M, N, K, 0)["kernel"]]
             if M <= 128:
                 copies = [(wd, sfk)] + [(wd.clone(), sfk.clone()) for _ in range(n_copies(N * K // 2) - 1)]
                 extra.update(graph_fields(graph_us([
