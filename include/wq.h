@@ -285,7 +285,9 @@ wq_status wq_debug_dequant_fp4(const uint8_t* w_e2m1, const uint8_t* sf_kernel, 
 /* BF16 x FP4 GEMM: out[M][N] bf16 = alpha * (A . (e2m1(W) * e4m3(SF))^T).
  * A: bf16 [M][K], 16-byte aligned, K % 32 == 0.  w_e2m1: uint8 [N][K/2], 16-byte
  * aligned.  sf_kernel: output of wq_pack_fp4_sf.  alpha: device pointer to one
- * float.  out, ws: as for wq_gemm_w4a16 (op WQ_OP_FP4). */
+ * float.  out, ws: as for wq_gemm_w4a16 (op WQ_OP_FP4).  M <= 16 with K % 256 == 0
+ * runs on the decode kernel (WQ_KERNEL_DECODE: codes and block scales turned into
+ * exact bf16 operands in registers, no workspace); other shapes on the tile kernels. */
 wq_status wq_gemm_bf16_fp4(const void* A, const uint8_t* w_e2m1, const uint8_t* sf_kernel, const float* alpha,
                            int64_t M, int64_t N, int64_t K, void* out, void* ws, size_t ws_bytes,
                            wq_stream_t stream);
@@ -317,9 +319,10 @@ typedef struct {
 } wq_plan;
 
 /* Kernels a plan can pick.  TILE: the tcgen05 kernel (weights dequantized into
- * tensor memory, any M).  DECODE: W4A16 or FP8 with M <= 16 and K % 64 == 0, MMA
- * operands built in registers (W4A16: from the fragment-order layout, group scale
- * applied in fp32; FP8: from the plain e4m3 codes, alpha applied in fp32). */
+ * tensor memory, any M).  DECODE: W4A16 or FP8 with M <= 16 and K % 64 == 0, or FP4
+ * with M <= 16 and K % 256 == 0; MMA operands built in registers (W4A16: from the
+ * fragment-order layout, group scale applied in fp32; FP8 / FP4: from the plain codes
+ * (and the prepacked block scales), alpha applied in fp32). */
 #define WQ_KERNEL_TILE 0
 #define WQ_KERNEL_DECODE 1
 /* TILE_PAIR: W4A16 with large M.  The tile kernel on two-CTA clusters: 256 weight

@@ -79,6 +79,29 @@ class Fp8Problem:
                                      self.N, self.K, bias_bits=self.bias, rows=rows)
 
 
+class Fp4Problem:
+    """Seeded BF16 x FP4 problem: e2m1 codes, e4m3 block scales (prepacked), global alpha."""
+
+    def __init__(self, M, N, K, seed=0):
+        self.M, self.N, self.K = M, N, K
+        self.A = synth.activations(M, K, "bf16", seed)
+        self.wts = synth.fp4_weights(N, K, seed + 1)
+        self.A_d = to_dev_f16bits(self.A, "bf16")
+        self.w_d = torch.from_numpy(self.wts.w).to(DEV)
+        self.sf_d = torch.from_numpy(self.wts.sf).to(DEV)
+        import weight_only_quantized_tma_gb300 as wq
+        self.sfk = wq.wq_pack_fp4_sf(self.sf_d, N, K)
+        self.alpha = torch.tensor([self.wts.alpha], dtype=torch.float32, device=DEV)
+
+    def run(self):
+        import weight_only_quantized_tma_gb300 as wq
+        return wq.wq_gemm_bf16_fp4(self.A_d, self.w_d, self.sfk, self.alpha)
+
+    def ref(self, rows=None):
+        return oracle.gemm_bf16_fp4(self.A, self.wts.w, self.wts.sf, float(self.wts.alpha), self.M, self.N, self.K,
+                                    rows=rows)
+
+
 def rounded_ref(ref, out_dtype):
     """The float64 reference correctly rounded (RNE) to the output type."""
     if out_dtype == "bf16":

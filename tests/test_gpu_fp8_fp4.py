@@ -13,7 +13,7 @@ import oracle
 import weight_only_quantized_tma_gb300 as wq
 from weight_only_quantized_tma_gb300 import synth
 
-from gpu_helpers import DEV, Fp8Problem, check_close, out_bits, out_to_f64, to_dev_f16bits
+from gpu_helpers import DEV, Fp4Problem, Fp8Problem, check_close, out_bits, out_to_f64, to_dev_f16bits
 
 pytestmark = pytest.mark.gpu
 
@@ -49,25 +49,6 @@ def _gate_vs_cast_copy(got, cast, ref, what):
     assert k_mean <= c_mean, f"{what}: kernel rel_mean {k_mean:.3e} > cast-copy {c_mean:.3e}"
     assert k_max <= c_max + BF16_ULP_REL * 0.5, f"{what}: kernel rel_max {k_max:.3e} > cast-copy {c_max:.3e}"
     return (k_max, k_mean), (c_max, c_mean)
-
-
-class Fp4Problem:
-    def __init__(self, M, N, K, seed=0):
-        self.M, self.N, self.K = M, N, K
-        self.A = synth.activations(M, K, "bf16", seed)
-        self.wts = synth.fp4_weights(N, K, seed + 1)
-        self.A_d = to_dev_f16bits(self.A, "bf16")
-        self.w_d = torch.from_numpy(self.wts.w).to(DEV)
-        self.sf_d = torch.from_numpy(self.wts.sf).to(DEV)
-        self.sfk = wq.wq_pack_fp4_sf(self.sf_d, N, K)
-        self.alpha = torch.tensor([self.wts.alpha], dtype=torch.float32, device=DEV)
-
-    def run(self):
-        return wq.wq_gemm_bf16_fp4(self.A_d, self.w_d, self.sfk, self.alpha)
-
-    def ref(self, rows=None):
-        return oracle.gemm_bf16_fp4(self.A, self.wts.w, self.wts.sf, float(self.wts.alpha), self.M, self.N, self.K,
-                                    rows=rows)
 
 
 # ------------------------------------------------------------------ FP8

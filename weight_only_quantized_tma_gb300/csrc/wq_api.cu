@@ -113,13 +113,15 @@ struct Plan {
 // Configuration codes past the tile formats: the decode kernels, then the pair kernels.
 constexpr int kCfgDecodeInt4 = 16;     // + decode_kind (0 symmetric, 1 zero points)
 constexpr int kCfgDecodeFp8 = 18;
-constexpr int kNumDecodeCfgs = 3;
+constexpr int kCfgDecodeFp4 = 19;
+constexpr int kNumDecodeCfgs = 4;
 constexpr int kCfgPair = 32;           // + format
 
 bool get_config_uncached(int fmt, bool bf16, int bn, bool query, KernelConfig* cfg) {
     if (fmt == kCfgDecodeInt4) return config_int4_decode(bf16, query, cfg);
     if (fmt == kCfgDecodeInt4 + 1) return config_int4_decode_zp(bf16, query, cfg);
     if (fmt == kCfgDecodeFp8) return config_fp8_decode(bf16, query, cfg);
+    if (fmt == kCfgDecodeFp4) return bf16 && config_fp4_decode(query, cfg);
     if (fmt == kCfgPair + FMT_INT4) return config_int4_pair(bf16, query, cfg);
     if (fmt == kCfgPair + FMT_FP8) return config_fp8_pair(bf16, query, cfg);
     if (fmt == kCfgPair + FMT_FP4) return bf16 && config_fp4_pair(query, cfg);
@@ -138,7 +140,7 @@ bool get_config_uncached(int fmt, bool bf16, int bn, bool query, KernelConfig* c
 // The device query behind a configuration (attributes, residency) is done once per
 // device and instantiation; later calls read the cached answer.
 // Slots: the tile formats 0 .. kNumFmts - 1, the decode kernels (W4A16 symmetric, W4A16
-// zero point, FP8), the pair kernels.
+// zero point, FP8, FP4), the pair kernels.
 constexpr int kCfgSlots = 2 * kNumFmts + kNumDecodeCfgs;
 struct ConfigCache {
     std::mutex mu;
@@ -198,12 +200,15 @@ wq_status make_plan(int fmt, bool bf16, int64_t M, int64_t N, int64_t K, int sms
     static const int kTiles[4] = {16, 64, 128, 256};
     KernelConfig cfg{};
     bool found = false;
-    // decode (M <= 16): the register-resident kernels (W4A16, FP8); their activation
-    // copy views A as 64-wide boxes, so they need K % 64 == 0
+    // decode (M <= 16): the register-resident kernels (W4A16, FP8, FP4); their
+    // activation copy views A as 64-wide boxes, so they need K % 64 == 0 (FP4: whole
+    // 256-code stages, K % 256 == 0, so that no stage reads block scales past K)
     // decode_kind (W4A16): 0 symmetric, 1 zero points, -1 no decode kernel
-    const bool decode =
-        decode_kind >= 0 && (fmt == FMT_INT4 || fmt == FMT_FP8) && M <= 16 && K % 64 == 0 && !decode_disabled();
-    if (decode && fmt == FMT_FP8) {
+    const bool decode = decode_kind >= 0 && (fmt == FMT_INT4 || fmt == FMT_FP8 || fmt == FMT_FP4) && M <= 16 &&
+                        K % (fmt == FMT_FP4 ? 256 : 64) == 0 && !decode_disabled();
+    if (decode && fmt == FMT_FP4) {
+        found = get_config(kCfgDecodeFp4, bf16, 16, sms > 0, &cfg);
+    } else if (decode && fmt == FMT_FP8) {
         found = get_config(kCfgDecodeFp8, bf16, 16, sms > 0, &cfg);
     } else if (decode) {
         found = get_config(kCfgDecodeInt4 + decode_kind, bf16, 16, sms > 0, &cfg);
@@ -844,7 +849,9 @@ wq_status wq_gemm_bf16_fp4(const void* A, const uint8_t* w_e2m1, const uint8_t* 
     if ((st = check_ws(pl, ws, ws_bytes)) != WQ_OK) return st;
     GemmParams gp;
     std::memset(&gp, 0, sizeof(gp));
-    if (!encode_a(gp, A, true, M, K, pl.pair ? pl.cfg.bn / 2 : pl.cfg.bn)) return WQ_ERR_CUDA;
+    if (pl.decode ? !encode_a_boxes(gp, A, true, M, K, pl.cfg.bk)
+                  : !encode_a(gp, A, true, M, K, pl.pair ? pl.cfg.bn / 2 : pl.cfg.bn))
+        return WQ_ERR_CUDA;
     if (pl.pair && !encode_out(gp, out, true, M, N)) return WQ_ERR_CUDA;
     const int pitch = pl.cfg.bk / 2;
     if (!encode_2d(&gp.tmap_w, CU_TENSOR_MAP_DATA_TYPE_UINT8, w_e2m1, (uint64_t)(K / 2), (uint64_t)N,
@@ -854,6 +861,7 @@ wq_status wq_gemm_bf16_fp4(const void* A, const uint8_t* w_e2m1, const uint8_t* 
     gp.alpha = alpha;
     gp.nchunks_pad = (int)(round_up(K, KPAD_FP4SF) / 64);
     fill_common(gp, pl, M, N, K, out, ws, d->status);
+    if (pl.decode) return finish_launch(launch_gemm_fp4_decode(gp, pl.grid, (cudaStream_t)stream));
     if (pl.pair) return finish_launch(launch_gemm_fp4_pair(gp, pl.grid, (cudaStream_t)stream));
     return finish_launch(launch_gemm_fp4(gp, true, pl.cfg.bn, pl.grid, (cudaStream_t)stream));
 }
