@@ -212,10 +212,11 @@ wq_status make_plan(int fmt, bool bf16, int64_t M, int64_t N, int64_t K, int sms
         found = get_config(kCfgDecodeFp8, bf16, 16, sms > 0, &cfg);
     } else if (decode) {
         found = get_config(kCfgDecodeInt4 + decode_kind, bf16, 16, sms > 0, &cfg);
-        // stages of 256 values when K allows (the launch picks the same instantiation)
+        // stages of 256 values when K allows (the launch picks the same instantiation,
+        // half as many stages)
         if (found && K % 256 == 0) {
             cfg.bk = 256;
-            cfg.stages = 3;
+            cfg.stages /= 2;
         }
     }
     for (int i = 0; i < 4 && !found; ++i) {
@@ -243,10 +244,9 @@ wq_status make_plan(int fmt, bool bf16, int64_t M, int64_t N, int64_t K, int sms
     long long items = tiles * splits;
     if (decode) {
         // split-K across a cluster of S CTAs (one slice each): S <= 16, at least two
-        // k-blocks per slice, tiles x S within the CTAs the GPU holds at once (the
-        // kernel's shared memory is sized so that this is two per SM: the decode
-        // consumer is compute-bound, and a third CTA on some SMs would make them the
-        // tail), and all clusters in one wave with a margin of 1/16 below the cluster
+        // k-blocks per slice, tiles x S within the CTAs the GPU holds at once (two or
+        // three per SM by the kernel's shared memory), and all clusters in one wave
+        // with a margin of 1/16 below the cluster
         // count the occupancy query reports: the hardware does not place that many at
         // once (measured on GB300, 3-CTA clusters, capacity reported 97: W4A16 M = 1,
         // K = 4096 takes 8.7 us at 90 tiles, 9.7 at 93, 11.7 at 95 and 13.0 at 96,

@@ -30,12 +30,16 @@ cudaError_t launch_gemm_int4_pair(const GemmParams& p, bool bf16, int grid, cuda
 }
 // Decode (M <= 16): register-resident mma.sync kernel, one 8-token column tile for
 // M <= 8, two for M <= 16, and the fold position (k steps per group) fixed at compile
-// time.  Stages of 256 values (three of them) when K % 256 == 0, else of 128 (six):
-// the same bytes in flight, half the per-stage barrier waits and hand-offs per byte.
-// All instantiations share threads, the two-CTAs-per-SM shared memory and the
-// cluster limits.
+// time.  Stages of 256 values (two of them) when K % 256 == 0, else of 128 (four): the
+// same bytes in flight, half the per-stage barrier waits and hand-offs per byte.  The
+// ring leaves room for three CTAs per SM, which then split K further: measured on
+// GB300, in-graph decode step 74.6 us with three stages of 256 (two CTAs per SM) and
+// 70.3 us with two (the 12288 x 4096 shapes 10.6 -> 8.7 us at M = 1, the 4096 x 4096
+// ones 4.9 -> 5.5 us; choosing per shape measured 72.1 us: kernels with different
+// footprints overlap worse across launches).  All instantiations share threads, shared
+// memory and the cluster limits.
 template <bool BF16, int NT, int GSTEPS, int BK>
-using I4Dec = MmaDecodeLauncher<BF16, NT, GSTEPS, BK, BK == 256 ? 3 : 6>;
+using I4Dec = MmaDecodeLauncher<BF16, NT, GSTEPS, BK, BK == 256 ? 2 : 4>;
 
 bool config_int4_decode(bool bf16, bool query, KernelConfig* cfg) {
     *cfg = bf16 ? I4Dec<true, 2, 8, 128>::config(query) : I4Dec<false, 2, 8, 128>::config(query);
