@@ -451,7 +451,8 @@ def run_ours(args, rank, world, local_rank):
         fp8_cases = [(32768, 3200, 5120, "bf16", False), (16384, 12800, 5120, "bf16", False),
                      (8192, 10240, 5120, "bf16", False), (8192, 10240, 5120, "f16", False),
                      (8192, 10240, 5120, "f16", True), (1, 10240, 5120, "bf16", False),
-                     (16, 10240, 5120, "bf16", False), (64, 10240, 5120, "bf16", False),
+                     (16, 10240, 5120, "bf16", False), (32, 10240, 5120, "bf16", False),
+                     (64, 10240, 5120, "bf16", False),
                      (16, 10240, 5120, "f16", True)]
         for (M, N, K, adt, with_bias) in fp8_cases:
             seed = 4000 + M

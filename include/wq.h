@@ -258,7 +258,7 @@ wq_status wq_debug_dequant_fp8(const uint8_t* w_e4m3, int64_t N, int64_t K, wq_d
  * A: a_dtype [M][K], 16-byte aligned, K % 16 == 0.  w_e4m3: uint8 [N][K],
  * 16-byte aligned.  alpha: device pointer to one float (element aligned; read
  * by the kernel, so a CUDA graph can capture the call).  bias: NULL or [N] of
- * the type of A.  out, ws: as for wq_gemm_w4a16 (op WQ_OP_FP8).  M <= 16 with
+ * the type of A.  out, ws: as for wq_gemm_w4a16 (op WQ_OP_FP8).  M <= 32 with
  * K % 64 == 0 runs on the decode kernel (WQ_KERNEL_DECODE: the codes read straight
  * from W, converted in registers, no workspace); other shapes on the tile kernels.
  * The e4m3 codes S.1111.111 decode as NaN on every path. */
@@ -319,8 +319,8 @@ typedef struct {
 } wq_plan;
 
 /* Kernels a plan can pick.  TILE: the tcgen05 kernel (weights dequantized into
- * tensor memory, any M).  DECODE: W4A16 or FP8 with M <= 16 and K % 64 == 0, or FP4
- * with M <= 16 and K % 256 == 0; MMA operands built in registers (W4A16: from the
+ * tensor memory, any M).  DECODE: W4A16 with M <= 16 and K % 64 == 0, FP8 with
+ * M <= 32 and K % 64 == 0, or FP4 with M <= 16 and K % 256 == 0; MMA operands built in registers (W4A16: from the
  * fragment-order layout, group scale applied in fp32; FP8 / FP4: from the plain codes
  * (and the prepacked block scales), alpha applied in fp32). */
 #define WQ_KERNEL_TILE 0

@@ -1,4 +1,4 @@
-"""GPU parity of the FP8 decode kernel (M <= 16, K % 64 == 0) against the oracle.
+"""GPU parity of the FP8 decode kernel (M <= 32, K % 64 == 0) against the oracle.
 
 The decode kernel reads the plain e4m3 codes, converts them to the activation type
 in registers (exact) and sums in fp32, with alpha and the bias applied once in the
@@ -31,11 +31,11 @@ def _one_hot(ks, K, a_dtype):
 
 
 def test_fp8_decode_plan():
-    for M in (1, 16):
+    for M in (1, 16, 17, 32):
         plan = wq.get_plan(wq.WQ_OP_FP8, wq.WQ_BF16, M, 10240, 5120, 0)
         assert plan["kernel"] == wq.WQ_KERNEL_DECODE
-        assert plan["ws_bytes"] == 0
-    assert wq.get_plan(wq.WQ_OP_FP8, wq.WQ_BF16, 17, 10240, 5120, 0)["kernel"] == wq.WQ_KERNEL_TILE
+        assert plan["ws_bytes"] == 0 and plan["tiles_m"] == 1
+    assert wq.get_plan(wq.WQ_OP_FP8, wq.WQ_BF16, 33, 10240, 5120, 0)["kernel"] == wq.WQ_KERNEL_TILE
     assert wq.get_plan(wq.WQ_OP_FP8, wq.WQ_F16, 4, 1024, 1040, 0)["kernel"] == wq.WQ_KERNEL_TILE
 
 
@@ -60,10 +60,10 @@ def test_fp8_decode_one_hot_bit_exact(a_dtype, shift):
     assert np.array_equal(out_to_f64(out), w[:, ks].T)
 
 
-@pytest.mark.parametrize("M", [1, 4, 40])
+@pytest.mark.parametrize("M", [1, 4, 24, 40])
 def test_fp8_nan_codes_propagate(M):
     # e4m3 S.1111.111 is NaN: a NaN code in weight row n makes column n of the output
-    # NaN for every token (0 * NaN = NaN), on the decode kernel (M <= 16) and the tile
+    # NaN for every token (0 * NaN = NaN), on the decode kernel (M <= 32) and the tile
     # kernel alike; the other columns are unaffected
     N, K = 256, 1024
     p = Fp8Problem(M, N, K, seed=410)
@@ -73,7 +73,7 @@ def test_fp8_nan_codes_propagate(M):
             p.wts.w[n, k] = 0x7F if i % 2 == 0 else 0xFF
     p.w_d = torch.from_numpy(p.wts.w).to(DEV)
     kernel = wq.get_plan(wq.WQ_OP_FP8, wq.WQ_BF16, M, N, K, 0)["kernel"]
-    assert kernel == (wq.WQ_KERNEL_DECODE if M <= 16 else wq.WQ_KERNEL_TILE)
+    assert kernel == (wq.WQ_KERNEL_DECODE if M <= 32 else wq.WQ_KERNEL_TILE)
     out = out_to_f64(p.run())
     torch.cuda.synchronize()
     ref = p.ref()
@@ -96,6 +96,47 @@ def test_fp8_decode_ragged(M, N, K):
     out = p.run()
     torch.cuda.synchronize()
     check_close(out_to_f64(out), p.ref(), out_dtype=a_dtype, what=f"fp8 decode M={M} N={N} K={K}")
+
+
+@pytest.mark.parametrize("a_dtype", ["bf16", "f16"])
+@pytest.mark.parametrize("shift", [0, 1])
+@pytest.mark.parametrize("M", [24, 32])
+def test_fp8_decode_one_hot_wide(M, shift, a_dtype):
+    # 4 token tiles: every token selects its own k, so a wrong token <-> column or
+    # inbox-slot mapping for tiles 2 and 3 moves outputs between rows of the result
+    N, K = 392, 2048
+    ks = [16 * ((11 * m + 5 * shift) % (K // 16)) + (m + 3 * shift) % 16 for m in range(M)]
+    p = Fp8Problem(M, N, K, a_dtype=a_dtype, seed=470 + M + shift)
+    plan = wq.get_plan(wq.WQ_OP_FP8, _dt(a_dtype), M, N, K, 0)
+    assert plan["kernel"] == wq.WQ_KERNEL_DECODE and plan["splits"] > 1
+    p.A = _one_hot(ks, K, a_dtype)
+    p.A_d = to_dev_f16bits(p.A, a_dtype)
+    out = p.run(alpha=torch.ones(1, dtype=torch.float32, device=DEV))
+    torch.cuda.synchronize()
+    w = oracle.dequant_fp8(p.wts.w).astype(np.float64)
+    assert np.array_equal(out_to_f64(out), w[:, ks].T)
+
+
+@pytest.mark.parametrize("M", list(range(17, 33)))
+def test_fp8_decode_wide_ragged(M):
+    # 17-32 tokens: 4 token tiles; tail rows (N = 1000) and a half-stage K tail
+    a_dtype = "f16" if M % 2 else "bf16"
+    N, K = 1000, 4160
+    p = Fp8Problem(M, N, K, a_dtype=a_dtype, seed=480 + M, with_bias=M % 3 == 0)
+    assert wq.get_plan(wq.WQ_OP_FP8, _dt(a_dtype), M, N, K, 0)["kernel"] == wq.WQ_KERNEL_DECODE
+    out = p.run()
+    torch.cuda.synchronize()
+    check_close(out_to_f64(out), p.ref(), out_dtype=a_dtype, what=f"fp8 decode M={M}")
+
+
+@pytest.mark.parametrize("M", [20, 32])
+def test_fp8_decode_wide_deterministic(M):
+    p = Fp8Problem(M, 2048, 8192, seed=490 + M)
+    first = p.run()
+    torch.cuda.synchronize()
+    check_close(out_to_f64(first), p.ref(), out_dtype="bf16", what=f"fp8 decode M={M}")
+    for _ in range(3):
+        assert torch.equal(p.run(), first)
 
 
 @pytest.mark.parametrize("M", list(range(1, 17)))

@@ -105,7 +105,7 @@ struct Plan {
     int tiles_n, tiles_m, nkb, splits, n_items, grid, walk_n_fast;
     int n_full;    // tile kernel: whole-tile items; the rest are half tiles
     size_t ws_bytes;
-    bool decode;   // W4A16 / FP8 decode kernel (register-resident mma.sync, M <= 16)
+    bool decode;   // register-resident mma.sync decode kernel (M <= 16; FP8 M <= 32)
     bool pair;     // tile kernel on two-CTA clusters (256 weight rows per tile)
     bool csplit;   // tile kernel split-K reduced inside thread-block clusters (no workspace)
 };
@@ -114,13 +114,15 @@ struct Plan {
 constexpr int kCfgDecodeInt4 = 16;     // + decode_kind (0 symmetric, 1 zero points)
 constexpr int kCfgDecodeFp8 = 18;
 constexpr int kCfgDecodeFp4 = 19;
-constexpr int kNumDecodeCfgs = 4;
+constexpr int kCfgDecodeFp8N4 = 20;   // FP8 decode with 4 token tiles (M <= 32)
+constexpr int kNumDecodeCfgs = 5;
 constexpr int kCfgPair = 32;           // + format
 
 bool get_config_uncached(int fmt, bool bf16, int bn, bool query, KernelConfig* cfg) {
     if (fmt == kCfgDecodeInt4) return config_int4_decode(bf16, query, cfg);
     if (fmt == kCfgDecodeInt4 + 1) return config_int4_decode_zp(bf16, query, cfg);
-    if (fmt == kCfgDecodeFp8) return config_fp8_decode(bf16, query, cfg);
+    if (fmt == kCfgDecodeFp8) return config_fp8_decode(bf16, 2, query, cfg);
+    if (fmt == kCfgDecodeFp8N4) return config_fp8_decode(bf16, 4, query, cfg);
     if (fmt == kCfgDecodeFp4) return bf16 && config_fp4_decode(query, cfg);
     if (fmt == kCfgPair + FMT_INT4) return config_int4_pair(bf16, query, cfg);
     if (fmt == kCfgPair + FMT_FP8) return config_fp8_pair(bf16, query, cfg);
@@ -140,7 +142,7 @@ bool get_config_uncached(int fmt, bool bf16, int bn, bool query, KernelConfig* c
 // The device query behind a configuration (attributes, residency) is done once per
 // device and instantiation; later calls read the cached answer.
 // Slots: the tile formats 0 .. kNumFmts - 1, the decode kernels (W4A16 symmetric, W4A16
-// zero point, FP8, FP4), the pair kernels.
+// zero point, FP8, FP4, FP8 with 4 and 8 token tiles), the pair kernels.
 constexpr int kCfgSlots = 2 * kNumFmts + kNumDecodeCfgs;
 struct ConfigCache {
     std::mutex mu;
@@ -177,7 +179,7 @@ size_t split_ws_bytes(int tiles, int splits, int bn) {
     return kSplitCounterBytes + (size_t)tiles * splits * bn * TILE_N * sizeof(float);
 }
 
-// WQ_DISABLE_DECODE=1 in the environment keeps M <= 16 on the tile kernel, e.g. to
+// WQ_DISABLE_DECODE=1 in the environment keeps decode shapes on the tile kernel, e.g. to
 // compare the two.
 bool decode_disabled() {
     const char* e = std::getenv("WQ_DISABLE_DECODE");
@@ -200,16 +202,17 @@ wq_status make_plan(int fmt, bool bf16, int64_t M, int64_t N, int64_t K, int sms
     static const int kTiles[4] = {16, 64, 128, 256};
     KernelConfig cfg{};
     bool found = false;
-    // decode (M <= 16): the register-resident kernels (W4A16, FP8, FP4); their
-    // activation copy views A as 64-wide boxes, so they need K % 64 == 0 (FP4: whole
-    // 256-code stages, K % 256 == 0, so that no stage reads block scales past K)
+    // decode (M <= 16; FP8 M <= 32): the register-resident kernels (W4A16, FP8, FP4);
+    // their activation copy views A as 64-wide boxes, so they need K % 64 == 0 (FP4:
+    // whole 256-code stages, K % 256 == 0, so that no stage reads block scales past K)
     // decode_kind (W4A16): 0 symmetric, 1 zero points, -1 no decode kernel
-    const bool decode = decode_kind >= 0 && (fmt == FMT_INT4 || fmt == FMT_FP8 || fmt == FMT_FP4) && M <= 16 &&
-                        K % (fmt == FMT_FP4 ? 256 : 64) == 0 && !decode_disabled();
+    const bool decode = decode_kind >= 0 && (fmt == FMT_INT4 || fmt == FMT_FP8 || fmt == FMT_FP4) &&
+                        M <= (fmt == FMT_FP8 ? 32 : 16) && K % (fmt == FMT_FP4 ? 256 : 64) == 0 &&
+                        !decode_disabled();
     if (decode && fmt == FMT_FP4) {
         found = get_config(kCfgDecodeFp4, bf16, 16, sms > 0, &cfg);
     } else if (decode && fmt == FMT_FP8) {
-        found = get_config(kCfgDecodeFp8, bf16, 16, sms > 0, &cfg);
+        found = get_config(M <= 16 ? kCfgDecodeFp8 : kCfgDecodeFp8N4, bf16, 16, sms > 0, &cfg);
     } else if (decode) {
         found = get_config(kCfgDecodeInt4 + decode_kind, bf16, 16, sms > 0, &cfg);
         // stages of 256 values when K allows (the launch picks the same instantiation,
@@ -431,7 +434,7 @@ bool encode_out(GemmParams& gp, void* out, bool bf16, int64_t M, int64_t N) {
 // z * M + m), each row 128 bytes with the 128-byte swizzle.  Needs K % 64 == 0.
 bool encode_a_boxes(GemmParams& gp, const void* A, bool bf16, int64_t M, int64_t K, int bk) {
     auto fn = encode_fn();
-    if (!fn || K % 64 != 0 || M > 16) return false;
+    if (!fn || K % 64 != 0 || M > 32) return false;
     gp.a_box_rows = (int)M;
     cuuint64_t dims[3] = {64, (cuuint64_t)M, (cuuint64_t)(K / 64)};
     cuuint64_t strides[2] = {(cuuint64_t)K * 2, 128};

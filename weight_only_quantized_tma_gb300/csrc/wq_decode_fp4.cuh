@@ -274,7 +274,7 @@ __global__ void __launch_bounds__(Fp4DecodeCfg<STAGES>::NTHREADS, 2)
         ptx::cluster_wait();   // every CTA of the cluster has initialised its barriers
         if (warp < NCW) decode_send_partials<NT, RGW>(sum, warp, lane, rank, S, R, sbase + C::INBOX, inbox_bar);
         if (!bounded_wait<true>(inbox_bar, 0u, abort_flag, p.status, DEVICE_TIMEOUT_EPILOGUE, p.timeout_ns)) return;
-        decode_reduce_rows(reinterpret_cast<const float*>(smem + C::INBOX), S, R, rows_own, p.M,
+        decode_reduce_rows<NT>(reinterpret_cast<const float*>(smem + C::INBOX), S, R, rows_own, p.M,
                            [&](int m, int r, float v) {
                                const int n = tile * TILE_N + row0 + r;
                                if (n < p.N) store_out<true>(p.out, (size_t)m * p.N + n, alpha * v);

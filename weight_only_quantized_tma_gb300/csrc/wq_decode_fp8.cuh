@@ -1,4 +1,4 @@
-// wq_decode_fp8.cuh -- FP8 (e4m3) decode kernel (M <= 16 tokens).
+// wq_decode_fp8.cuh -- FP8 (e4m3) decode kernel (M <= 32 tokens).
 //
 // The register-resident scheme of the W4A16 decode kernel (wq_gemm_mma.cuh) on plain
 // e4m3 weights W[N][K]: TMA copies 128-row x 128-byte weight boxes (128-byte swizzle)
@@ -28,7 +28,8 @@
 
 namespace wq {
 
-template <int STAGES>
+// NT: 8-token MMA column tiles per row group (1, 2 or 4: M up to 32).
+template <int STAGES, int NT = 2>
 struct Fp8DecodeCfg {
     static constexpr int BK = 128;                       // k values (= weight bytes per row) per stage
     static constexpr int NCW = 4;                        // compute warps, 32 rows each
@@ -37,10 +38,11 @@ struct Fp8DecodeCfg {
     static constexpr int NTHREADS = 32 * (NCW + 1);
     static constexpr int NZ = BK / 64;                   // 64-wide activation boxes per stage
     static constexpr int W_STAGE = TILE_N * BK;          // one 128 x 128-byte box, 1024-byte aligned
-    static constexpr int A_STAGE = 16 * 128 * NZ;        // up to 16 token rows of 128 bytes per box
+    static constexpr int NTA = NT < 2 ? 2 : NT;
+    static constexpr int A_STAGE = 8 * NTA * 128 * NZ;   // up to 8 NTA token rows of 128 bytes per box
     static constexpr int A_BASE = STAGES * W_STAGE;
     static constexpr int INBOX = A_BASE + STAGES * A_STAGE;
-    static constexpr int INBOX_BYTES = 16 * (TILE_N + 16) * 4;   // fp32 [S][R][16], S * R <= 128 + 15
+    static constexpr int INBOX_BYTES = inbox_row_floats(NT) * (TILE_N + 16) * 4;   // fp32 [S][R][row], S * R <= 143
     static constexpr int OFF_BAR = INBOX + INBOX_BYTES;
     // barriers: full and empty per stage; then the abort flag (4 B, padded to 8) and the
     // inbox barrier (split-K)
@@ -66,12 +68,12 @@ __device__ __forceinline__ void ld_shared_v2(uint32_t addr, uint32_t& r0, uint32
     asm volatile("ld.shared.v2.b32 {%0, %1}, [%2];" : "=r"(r0), "=r"(r1) : "r"(addr) : "memory");
 }
 
-// NT: 8-token MMA column tiles (1 for M <= 8, 2 for M <= 16).  One CTA per item
-// (tile, K slice): gridDim.x == n_items, the slices of a tile form one cluster.
+// NT: 8-token MMA column tiles (1 for M <= 8, 2 for M <= 16, 4 for M <= 32).  One CTA per item (tile, K slice): gridDim.x == n_items, the slices of a
+// tile form one cluster.
 template <bool BF16, int NT, int STAGES>
-__global__ void __launch_bounds__(Fp8DecodeCfg<STAGES>::NTHREADS, 2)
+__global__ void __launch_bounds__(Fp8DecodeCfg<STAGES, NT>::NTHREADS, 2)
     wq_decode_fp8_kernel(const __grid_constant__ GemmParams p) {
-    using C = Fp8DecodeCfg<STAGES>;
+    using C = Fp8DecodeCfg<STAGES, NT>;
     constexpr int NCW = C::NCW;
     constexpr int RGW = C::RGW;
     constexpr int NZ = C::NZ;
@@ -267,7 +269,7 @@ __global__ void __launch_bounds__(Fp8DecodeCfg<STAGES>::NTHREADS, 2)
         ptx::cluster_wait();   // every CTA of the cluster has initialised its barriers
         if (warp < NCW) decode_send_partials<NT, RGW>(sum, warp, lane, rank, S, R, sbase + C::INBOX, inbox_bar);
         if (!bounded_wait<true>(inbox_bar, 0u, abort_flag, p.status, DEVICE_TIMEOUT_EPILOGUE, p.timeout_ns)) return;
-        decode_reduce_rows<true>(reinterpret_cast<const float*>(smem + C::INBOX), S, R, rows_own, p.M,
+        decode_reduce_rows<NT, true>(reinterpret_cast<const float*>(smem + C::INBOX), S, R, rows_own, p.M,
                            [&](int m, int r, float v) {
                                const int n = tile * TILE_N + row0 + r;
                                if (n < p.N) finish(m, n, v);
@@ -277,7 +279,7 @@ __global__ void __launch_bounds__(Fp8DecodeCfg<STAGES>::NTHREADS, 2)
 
 template <bool BF16, int NT, int STAGES>
 struct Fp8DecodeLauncher {
-    using C = Fp8DecodeCfg<STAGES>;
+    using C = Fp8DecodeCfg<STAGES, NT>;
     static constexpr auto kernel = wq_decode_fp8_kernel<BF16, NT, STAGES>;
     static cudaError_t prepare() {
         static int attr_set[64] = {0};
@@ -292,7 +294,7 @@ struct Fp8DecodeLauncher {
         return e;
     }
     static KernelConfig config(bool query_device) {
-        KernelConfig k{FMT_FP8, BF16 ? 1 : 0, 16, C::BK, STAGES, 0, C::NTHREADS, C::SMEM_BYTES, 0, 1};
+        KernelConfig k{FMT_FP8, BF16 ? 1 : 0, 8 * C::NTA, C::BK, STAGES, 0, C::NTHREADS, C::SMEM_BYTES, 0, 1};
         if (!query_device || prepare() != cudaSuccess) return k;
         decode_residency(kernel, C::NTHREADS, C::SMEM_BYTES, &k);
         return k;
@@ -300,7 +302,7 @@ struct Fp8DecodeLauncher {
     static cudaError_t launch(const GemmParams& p, int grid, cudaStream_t st) {
         cudaError_t e = prepare();
         if (e != cudaSuccess) return e;
-        if (p.splits > kMaxDecodeCluster || grid != p.n_items || p.M > 16 || p.M < 1) return cudaErrorInvalidValue;
+        if (p.splits > kMaxDecodeCluster || grid != p.n_items || p.M > 8 * NT || p.M < 1) return cudaErrorInvalidValue;
         return launch_decode_grid(kernel, p, grid, C::NTHREADS, C::SMEM_BYTES, st);
     }
 };

@@ -117,15 +117,19 @@ __device__ __forceinline__ void ldmatrix_x4(uint32_t addr, uint32_t& r0, uint32_
 // adds the S slices of its rows in rank order (deterministic) and reads only its own
 // shared memory.  No cluster-wide barrier has to wait for the remote stores to
 // complete (measured on GB300: a barrier.cluster with release semantics after remote
-// stores cost ~1 us per launch).  Inbox: fp32 [S][R = ceil(128 / S)][16 token slots]; token slot
-// 4c + i holds token 2c + (i & 1) + 8 (i >> 1), the order of a lane's accumulator
-// values, so a lane sends a row's values with one vector store.
+// stores cost ~1 us per launch).  Inbox: fp32 [S][R = ceil(128 / S)][inbox_row_floats(NT)]
+// per row and slice, the token slots in the order of a lane's accumulator values:
+// lane c's values for MMA columns 2c, 2c + 1 of the 8-token tiles nt = 0 .. NT - 1 at
+// slots (16 / 4 or 8 NT / 4) c + 2 nt + {0, 1}, so a lane sends a row's values with
+// one to four vector stores.
+__host__ __device__ constexpr int inbox_row_floats(int NT) { return NT <= 2 ? 16 : 8 * NT; }
 
 // Compute warp `warp` holds rows 16 RGW warp + 16 j + g (+ 8) of the tile in
-// acc[j][nt][e] (e = 0, 1: row g, tokens 8 nt + 2c + e; e = 2, 3: row g + 8).
+// acc[j][nt][e] (e = 0, 1: row g, MMA columns 8 nt + 2c + e; e = 2, 3: row g + 8).
 template <int NT, int RGW>
 __device__ __forceinline__ void decode_send_partials(const float (&acc)[RGW][NT][4], int warp, int lane, int rank,
                                                      int S, int R, uint32_t inbox, uint32_t inbox_bar) {
+    constexpr int ROWF = inbox_row_floats(NT);
     const int g = lane >> 2, c = lane & 3;
 #pragma unroll
     for (int j = 0; j < RGW; ++j)
@@ -133,14 +137,18 @@ __device__ __forceinline__ void decode_send_partials(const float (&acc)[RGW][NT]
         for (int h = 0; h < 2; ++h) {
             const int r = (warp * RGW + j) * 16 + g + 8 * h;   // e = 2h, 2h + 1
             const int owner = ((r + 1) * S - 1) / TILE_N;       // 128 owner / S <= r < 128 (owner + 1) / S
-            const uint32_t off = inbox + (uint32_t)((rank * R + (r - owner * TILE_N / S)) * 16 + 4 * c) * 4u;
+            const uint32_t off =
+                inbox + (uint32_t)((rank * R + (r - owner * TILE_N / S)) * ROWF + (ROWF / 4) * c) * 4u;
             const uint32_t dst = ptx::mapa_shared(off, (uint32_t)owner);
             const uint32_t rbar = ptx::mapa_shared(inbox_bar, (uint32_t)owner);
-            if constexpr (NT == 2)
-                ptx::st_async_v4f32(dst, acc[j][0][2 * h], acc[j][0][2 * h + 1], acc[j][1][2 * h],
-                                    acc[j][1][2 * h + 1], rbar);
-            else
+            if constexpr (NT == 1) {
                 ptx::st_async_v2f32(dst, acc[j][0][2 * h], acc[j][0][2 * h + 1], rbar);
+            } else {
+#pragma unroll
+                for (int nt = 0; nt < NT; nt += 2)
+                    ptx::st_async_v4f32(dst + 8u * nt, acc[j][nt][2 * h], acc[j][nt][2 * h + 1], acc[j][nt + 1][2 * h],
+                                        acc[j][nt + 1][2 * h + 1], rbar);
+            }
         }
 }
 
@@ -157,15 +165,16 @@ __device__ __forceinline__ int column_of_token(int t) { return SPREAD ? (t >> 1)
 // After the inbox phase completed: store(m, r, v) for token m < M and the r-th owned
 // row, with v the sum of the S slices in rank order.  Weight row fastest: a warp stores
 // consecutive output columns of one token.
-template <bool SPREAD = false, typename Store>
+template <int NT, bool SPREAD = false, typename Store>
 __device__ __forceinline__ void decode_reduce_rows(const float* box, int S, int R, int rows_own, int M, Store store) {
+    constexpr int ROWF = inbox_row_floats(NT);
     for (int e = threadIdx.x; e < M * rows_own; e += blockDim.x) {
         const int m = e / rows_own;
         const int r = e - m * rows_own;
         const int n = column_of_token<SPREAD>(m & 7);   // lane 4 g + n / 2 holds it as value n % 2
-        const int slot = 4 * (n >> 1) + (n & 1) + 2 * (m >> 3);
+        const int slot = (ROWF / 4) * (n >> 1) + (n & 1) + 2 * (m >> 3);
         float tot = 0.0f;
-        for (int q = 0; q < S; ++q) tot += box[(q * R + r) * 16 + slot];
+        for (int q = 0; q < S; ++q) tot += box[(q * R + r) * ROWF + slot];
         store(m, r, tot);
     }
 }
@@ -457,7 +466,7 @@ __global__ void __launch_bounds__(MmaDecodeCfg<BK, STAGES, ZP>::NTHREADS, 2)
         if (warp < NCW) decode_send_partials<NT, RGW>(acc, warp, lane, rank, S, R, sbase + C::INBOX, inbox_bar);
         // (bounded like every wait: a timeout sets the status word; nothing is read then)
         if (!bounded_wait<true>(inbox_bar, 0u, abort_flag, p.status, DEVICE_TIMEOUT_EPILOGUE, p.timeout_ns)) return;
-        decode_reduce_rows(reinterpret_cast<const float*>(smem + C::INBOX), S, R, rows_own, p.M,
+        decode_reduce_rows<NT>(reinterpret_cast<const float*>(smem + C::INBOX), S, R, rows_own, p.M,
                            [&](int m, int r, float v) {
                                const int n = tile * TILE_N + row0 + r;
                                if (n < p.N) store_out<BF16>(p.out, (size_t)m * p.N + n, v);

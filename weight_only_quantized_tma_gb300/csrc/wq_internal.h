@@ -165,9 +165,10 @@ cudaError_t launch_gemm_int4_decode(const GemmParams& p, bool bf16, int grid, cu
 // The same decode kernel with per-(group, row) zero points (wq_gemm_zp_decode.cu).
 bool config_int4_decode_zp(bool bf16, bool query, KernelConfig* cfg);
 cudaError_t launch_gemm_int4_decode_zp(const GemmParams& p, bool bf16, int grid, cudaStream_t st);
-// FP8 decode kernel (M <= 16, K % 64 == 0): the same register-resident scheme on plain
-// e4m3 weights read through TMA (wq_decode_fp8.cuh).
-bool config_fp8_decode(bool bf16, bool query, KernelConfig* cfg);
+// FP8 decode kernel (M <= 32, K % 64 == 0): the same register-resident scheme on plain
+// e4m3 weights read through TMA (wq_decode_fp8.cuh); `nt` 8-token column tiles (1, 2
+// or 4) select the instantiation whose configuration is returned.
+bool config_fp8_decode(bool bf16, int nt, bool query, KernelConfig* cfg);
 cudaError_t launch_gemm_fp8_decode(const GemmParams& p, bool bf16, int grid, cudaStream_t st);
 // BF16 x FP4 decode kernel (M <= 16, K % 256 == 0): e2m1 codes and block scales turned
 // into bf16 operands in registers (wq_decode_fp4.cuh).
