@@ -52,31 +52,40 @@ struct MmaDecodeCfg {
     static constexpr int P_WARP = NCW;                        // producer warp
     static constexpr int NTHREADS = 32 * (NCW + 1);
     static constexpr int NZ = BK / 64;                        // 64-wide activation boxes per stage
-    // per stage: packed weights, scales (up to BK / 32 groups, G = 32) and, with zero
-    // points, the stage's zero points (uint8 [BK / 32][128]) in one region; the
-    // 128-byte-swizzled activation boxes in a second, 1024-byte aligned region
+    // Two rings.  Weights: STAGES slots of packed codes, each released as soon as the
+    // compute warps hold its words in registers (at the start of the stage's MMAs), so
+    // the next copy into it overlaps the stage's arithmetic (measured on GB300, in-graph
+    // decode step: 70.2 -> 68.1 us against one ring released after the MMAs).  Activations, scales (up to
+    // BK / 32 groups, G = 32) and zero points (uint8 [BK / 32][128]): AS_STAGES =
+    // STAGES + 1 slots, released after the stage's MMAs; one more slot than the weights,
+    // so that a weight slot freed for k-block i + STAGES always finds the activation
+    // slot of that k-block free as well (its previous user, k-block i - 1, finished
+    // before k-block i's words were loaded).  The 128-byte-swizzled activation boxes
+    // are 1024-byte aligned.
+    static constexpr int AS_STAGES = STAGES + 1;
     static constexpr int W_STAGE = TILE_N * BK / 2;
-    static constexpr int SC_OFF = W_STAGE;
-    static constexpr int Z_OFF = SC_OFF + (BK / 32) * TILE_N * 2;
-    static constexpr int WS_STAGE = Z_OFF + (ZP ? (BK / 32) * TILE_N : 0);
     static constexpr int A_STAGE = 16 * 128 * NZ;             // up to 16 token rows of 128 bytes per box
-    static constexpr int A_BASE = (STAGES * WS_STAGE + 1023) / 1024 * 1024;
+    static constexpr int SC_BYTES = (BK / 32) * TILE_N * 2;
+    static constexpr int SC_STAGE = SC_BYTES + (ZP ? (BK / 32) * TILE_N : 0);   // zero points at SC_BYTES
+    static constexpr int A_BASE = STAGES * W_STAGE;
+    static constexpr int SC_BASE = A_BASE + AS_STAGES * A_STAGE;
     // split-K inbox: the partial sums the S CTAs of a cluster send to the CTA that
     // owns at most R = ceil(128 / S) of the tile's rows, fp32 [S][R][16 token slots] --
     // at most 16 * (128 + 15) values; never used by the main loop, so a peer may write
     // into it while this CTA is still streaming.  Token slot 4c + i holds token
     // 2c + (i & 1) + 8 (i >> 1): the order of a lane's accumulator values, so each
     // lane sends a row's values with one vector store.
-    static constexpr int INBOX = A_BASE + STAGES * A_STAGE;
+    static constexpr int INBOX = SC_BASE + AS_STAGES * SC_STAGE;
     static constexpr int INBOX_BYTES = 16 * (TILE_N + 16) * 4;
     static constexpr int OFF_BAR = INBOX + INBOX_BYTES;
-    // barriers: full and empty per stage; then the abort flag (4 B, padded to 8) and the
-    // inbox barrier (8 B, split-K)
-    static constexpr int OFF_INBOX_BAR = OFF_BAR + 2 * STAGES * 8 + 8;
+    // barriers: full and empty per weight slot, full and empty per activation slot; then
+    // the abort flag (4 B, padded to 8) and the inbox barrier (8 B, split-K)
+    static constexpr int OFF_INBOX_BAR = OFF_BAR + 2 * (STAGES + AS_STAGES) * 8 + 8;
     static constexpr int SMEM_USED = OFF_INBOX_BAR + 8;
     static constexpr int SMEM_BYTES = SMEM_USED + 1024;
     static_assert(BK == 128 || BK == 256, "BK");
-    static_assert(WS_STAGE % 16 == 0 && A_STAGE % 1024 == 0, "bulk-copy and swizzle alignment");
+    static_assert(W_STAGE % 1024 == 0 && A_STAGE % 1024 == 0 && SC_STAGE % 16 == 0,
+                  "bulk-copy and swizzle alignment");
 };
 
 // Pure register operations: not volatile, so the compiler may interleave them.
@@ -216,8 +225,7 @@ __device__ __forceinline__ void int4_word_to_frag(uint32_t w, uint32_t off_lo, u
 }
 
 // NT: 8-token MMA column tiles (1 for M <= 8, 2 for M <= 16).  GSTEPS: 16-wide k
-// steps per scale group inside a 128-value stage (2, 4 or 8; G >= 128 folds once per
-// stage).  One CTA per item (tile, K slice): gridDim.x == n_items, and the slices of
+// steps per scale group inside a stage (2, 4, 8 or 16; G >= BK folds once per stage).  One CTA per item (tile, K slice): gridDim.x == n_items, and the slices of
 // a tile form one cluster of p.splits CTAs.
 template <bool BF16, int NT, int GSTEPS, int BK, int STAGES, bool ZP = false>
 __global__ void __launch_bounds__(MmaDecodeCfg<BK, STAGES, ZP>::NTHREADS, 2)
@@ -233,9 +241,13 @@ __global__ void __launch_bounds__(MmaDecodeCfg<BK, STAGES, ZP>::NTHREADS, 2)
     uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
     const uint32_t sbase = ptx::smem_u32(smem);
     const uint32_t bar0 = sbase + C::OFF_BAR;
-    auto full_bar = [&](int s) { return bar0 + 8u * s; };
-    auto empty_bar = [&](int s) { return bar0 + 8u * (STAGES + s); };
-    volatile uint32_t* abort_flag = reinterpret_cast<volatile uint32_t*>(smem + C::OFF_BAR + 2 * STAGES * 8);
+    constexpr int AS = C::AS_STAGES;
+    auto full_w = [&](int s) { return bar0 + 8u * s; };
+    auto empty_w = [&](int s) { return bar0 + 8u * (STAGES + s); };
+    auto full_as = [&](int s) { return bar0 + 8u * (2 * STAGES + s); };
+    auto empty_as = [&](int s) { return bar0 + 8u * (2 * STAGES + AS + s); };
+    volatile uint32_t* abort_flag =
+        reinterpret_cast<volatile uint32_t*>(smem + C::OFF_BAR + 2 * (STAGES + AS) * 8);
     const uint32_t inbox_bar = sbase + C::OFF_INBOX_BAR;
 
     const int warp = threadIdx.x >> 5;
@@ -251,8 +263,12 @@ __global__ void __launch_bounds__(MmaDecodeCfg<BK, STAGES, ZP>::NTHREADS, 2)
     const int rows_own = (rank + 1) * TILE_N / S - row0;
     if (threadIdx.x == 0) {
         for (int s = 0; s < STAGES; ++s) {
-            ptx::mbar_init(full_bar(s), 1);
-            ptx::mbar_init(empty_bar(s), NCW);
+            ptx::mbar_init(full_w(s), 1);
+            ptx::mbar_init(empty_w(s), NCW);
+        }
+        for (int s = 0; s < AS; ++s) {
+            ptx::mbar_init(full_as(s), 1);
+            ptx::mbar_init(empty_as(s), NCW);
         }
         ptx::mbar_init(inbox_bar, 1);
         *abort_flag = 0u;
@@ -296,13 +312,15 @@ __global__ void __launch_bounds__(MmaDecodeCfg<BK, STAGES, ZP>::NTHREADS, 2)
 
     if (warp == C::P_WARP) {
         // ------------------------------------------------------------ producer
-        // Lane 0 streams weights and scales; the first STAGES k-blocks' go out at once,
-        // before the grid dependency wait (constant inputs), their activation copies
-        // right after it.  The order in which a stage's bytes land does not matter: its
-        // phase cannot complete before this lane's arrive-expect-tx.  The loop after
-        // that can stop early only at a wait, and it waits only after passing those
-        // stages, so every barrier armed here gets all of its bytes.
-        const int pre = nunits < STAGES ? nunits : STAGES;
+        // Lane 0 streams both rings.  The weights of the first STAGES k-blocks and the
+        // scales (and zero points) of the first AS go out at once, before the grid
+        // dependency wait (constant inputs), the activation copies right after it.  The
+        // order in which a slot's bytes land does not matter: its phase cannot complete
+        // before this lane's arrive-expect-tx.  The loop after that can stop early only
+        // at a wait, and it waits only after passing those slots, so every barrier armed
+        // here gets all of its bytes.
+        const int pre_w = nunits < STAGES ? nunits : STAGES;
+        const int pre_as = nunits < AS ? nunits : AS;
         const uint32_t a_bytes = (uint32_t)NZ * (uint32_t)p.a_box_rows * 128u;
         if (lane == 0) {
             const uint64_t pol_w = ptx::policy_evict_first();
@@ -311,46 +329,63 @@ __global__ void __launch_bounds__(MmaDecodeCfg<BK, STAGES, ZP>::NTHREADS, 2)
             const uint32_t sc_bytes = (uint32_t)gcnt * TILE_N * 2;
             const uint32_t zp_bytes = ZP ? (uint32_t)gcnt * TILE_N : 0u;
             auto load_w = [&](int s, int kb) {
-                const uint32_t fb = full_bar(s);
-                const uint32_t st = sbase + s * C::WS_STAGE;
-                ptx::mbar_arrive_expect_tx(fb, (uint32_t)C::W_STAGE + sc_bytes + zp_bytes + a_bytes);
+                const uint32_t fb = full_w(s);
+                ptx::mbar_arrive_expect_tx(fb, (uint32_t)C::W_STAGE);
                 const uint8_t* wsrc =
                     p.w + ((size_t)tile * p.nchunks_pad + (size_t)kb * (BK / 32)) * (TILE_N * 16);
-                ptx::bulk_load(st, wsrc, C::W_STAGE, fb, pol_w);
+                ptx::bulk_load(sbase + s * C::W_STAGE, wsrc, C::W_STAGE, fb, pol_w);
+            };
+            // scales (+ zero points) of k-block kb; arms the slot for them and its activations
+            auto load_s = [&](int s, int kb) {
+                const uint32_t fb = full_as(s);
+                const uint32_t dst = sbase + C::SC_BASE + s * C::SC_STAGE;
+                ptx::mbar_arrive_expect_tx(fb, sc_bytes + zp_bytes + a_bytes);
                 const int g0 = (kb * BK) >> p.g_shift;
-                const uint8_t* ssrc = p.sc + ((size_t)tile * p.ngroups_pad + g0) * (TILE_N * 2);
-                ptx::bulk_load(st + C::SC_OFF, ssrc, sc_bytes, fb, pol_w);
+                ptx::bulk_load(dst, p.sc + ((size_t)tile * p.ngroups_pad + g0) * (TILE_N * 2), sc_bytes, fb, pol_w);
                 if (ZP)
-                    ptx::bulk_load(st + C::Z_OFF, p.zp + ((size_t)tile * p.ngroups_pad + g0) * TILE_N, zp_bytes, fb,
-                                   pol_w);
+                    ptx::bulk_load(dst + C::SC_BYTES, p.zp + ((size_t)tile * p.ngroups_pad + g0) * TILE_N, zp_bytes,
+                                   fb, pol_w);
             };
             // activation box {64 k, M tokens, NZ}: k-block kb starts at z = kb * NZ
             auto load_a = [&](int s, int kb) {
-                ptx::tma_load_3d(sbase + C::A_BASE + s * C::A_STAGE, &p.tmap_a, 0, 0, kb * NZ, full_bar(s), pol_a);
+                ptx::tma_load_3d(sbase + C::A_BASE + s * C::A_STAGE, &p.tmap_a, 0, 0, kb * NZ, full_as(s), pol_a);
             };
-            for (int i = 0; i < pre; ++i) load_w(i, it.kb_begin + i);
+            for (int i = 0; i < pre_w; ++i) load_w(i, it.kb_begin + i);
+            for (int i = 0; i < pre_as; ++i) load_s(i, it.kb_begin + i);
             ptx::grid_dependency_wait();
-            for (int i = 0; i < pre; ++i) load_a(i, it.kb_begin + i);
-            int s = pre % STAGES;
-            uint32_t ph = pre == STAGES ? 1u : 0u;
-            int issued = pre;
-            for (int i = pre; i < nunits; ++i) {
+            for (int i = 0; i < pre_as; ++i) load_a(i, it.kb_begin + i);
+            int sw = pre_w % STAGES, sa = pre_as % AS;
+            uint32_t phw = pre_w == STAGES ? 1u : 0u, pha = pre_as == AS ? 1u : 0u;
+            int issued_w = pre_w, issued_as = pre_as;
+            for (int i = pre_w; i < nunits; ++i) {
                 const int kb = it.kb_begin + i;
-                if (!bounded_wait(empty_bar(s), ph ^ 1u, abort_flag, p.status, DEVICE_TIMEOUT_PRODUCER,
+                if (!bounded_wait(empty_w(sw), phw ^ 1u, abort_flag, p.status, DEVICE_TIMEOUT_PRODUCER,
                                   p.timeout_ns))
                     break;
-                load_w(s, kb);
-                load_a(s, kb);
-                ++issued;
-                if (++s == STAGES) {
-                    s = 0;
-                    ph ^= 1u;
+                load_w(sw, kb);
+                ++issued_w;
+                if (++sw == STAGES) {
+                    sw = 0;
+                    phw ^= 1u;
+                }
+                if (i < pre_as) continue;
+                if (!bounded_wait(empty_as(sa), pha ^ 1u, abort_flag, p.status, DEVICE_TIMEOUT_PRODUCER,
+                                  p.timeout_ns))
+                    break;
+                load_s(sa, kb);
+                load_a(sa, kb);
+                ++issued_as;
+                if (++sa == AS) {
+                    sa = 0;
+                    pha ^= 1u;
                 }
             }
             if (*abort_flag) {
-                const int first = issued > STAGES ? issued - STAGES : 0;
-                for (int j = first; j < issued; ++j)
-                    if (!drain_wait(full_bar(j % STAGES), (uint32_t)((j / STAGES) & 1), p.timeout_ns))
+                for (int j = issued_w > STAGES ? issued_w - STAGES : 0; j < issued_w; ++j)
+                    if (!drain_wait(full_w(j % STAGES), (uint32_t)((j / STAGES) & 1), p.timeout_ns))
+                        atomicOr(p.status, DEVICE_TIMEOUT_DRAIN);
+                for (int j = issued_as > AS ? issued_as - AS : 0; j < issued_as; ++j)
+                    if (!drain_wait(full_as(j % AS), (uint32_t)((j / AS) & 1), p.timeout_ns))
                         atomicOr(p.status, DEVICE_TIMEOUT_DRAIN);
             }
         }
@@ -360,21 +395,34 @@ __global__ void __launch_bounds__(MmaDecodeCfg<BK, STAGES, ZP>::NTHREADS, 2)
         const int g = lane >> 2, c = lane & 3;
         const int slot = int4_slot(lane);
         const int w_off = warp * RGW * 512 + slot * 16;   // this warp's first 16-row group, this lane's slot
-        int s = 0;
-        uint32_t ph = 0;
+        int sw = 0, sa = 0;
+        uint32_t phw = 0, pha = 0;
         for (int i = 0; i < nunits; ++i) {
-            const bool ok = bounded_wait(full_bar(s), ph, abort_flag, p.status, DEVICE_TIMEOUT_TRANSFORM,
-                                         p.timeout_ns);
-            if (!__all_sync(0xffffffffu, ok)) break;
-            const uint8_t* stp = smem + s * C::WS_STAGE;
-            const uint32_t st = sbase + C::A_BASE + s * C::A_STAGE;   // this stage's activation boxes
-            const uint16_t* sc = reinterpret_cast<const uint16_t*>(stp + C::SC_OFF);
+            // the stage's weight words into registers, then the weight slot is free
+            // (the arrive releases the loads before it, and __syncwarp orders the other
+            // lanes' loads before lane 0's arrive)
+            const bool okw = bounded_wait(full_w(sw), phw, abort_flag, p.status, DEVICE_TIMEOUT_TRANSFORM,
+                                          p.timeout_ns);
+            if (!__all_sync(0xffffffffu, okw)) break;
+            const uint8_t* wst = smem + sw * C::W_STAGE;
             uint4 wv[KSTEPS / 4][RGW];
 #pragma unroll
             for (int tq = 0; tq < KSTEPS / 4; ++tq)
 #pragma unroll
                 for (int j = 0; j < RGW; ++j)
-                    wv[tq][j] = *reinterpret_cast<const uint4*>(stp + tq * 4096 + w_off + j * 512);
+                    wv[tq][j] = *reinterpret_cast<const uint4*>(wst + tq * 4096 + w_off + j * 512);
+            __syncwarp();
+            if (lane == 0) ptx::mbar_arrive(empty_w(sw));
+            if (++sw == STAGES) {
+                sw = 0;
+                phw ^= 1u;
+            }
+            const bool oka = bounded_wait(full_as(sa), pha, abort_flag, p.status, DEVICE_TIMEOUT_TRANSFORM,
+                                          p.timeout_ns);
+            if (!__all_sync(0xffffffffu, oka)) break;
+            const uint8_t* scp = smem + C::SC_BASE + sa * C::SC_STAGE;
+            const uint32_t st = sbase + C::A_BASE + sa * C::A_STAGE;   // this stage's activation boxes
+            const uint16_t* sc = reinterpret_cast<const uint16_t*>(scp);
             float tmp[RGW][SETS][NT][4];
             uint32_t off_lo[RGW], off_hi[RGW];   // b + z of the group, rows g and g + 8
 #pragma unroll
@@ -391,7 +439,7 @@ __global__ void __launch_bounds__(MmaDecodeCfg<BK, STAGES, ZP>::NTHREADS, 2)
                                 for (int e = 0; e < 4; ++e) tmp[j][h][nt][e] = 0.0f;
                         uint32_t z_lo = 8u, z_hi = 8u;
                         if constexpr (ZP) {
-                            const uint8_t* zp = stp + C::Z_OFF + (t / GSTEPS) * TILE_N + (warp * RGW + j) * 16 + g;
+                            const uint8_t* zp = scp + C::SC_BYTES + (t / GSTEPS) * TILE_N + (warp * RGW + j) * 16 + g;
                             z_lo = zp[0];
                             z_hi = zp[8];
                         }
@@ -433,12 +481,11 @@ __global__ void __launch_bounds__(MmaDecodeCfg<BK, STAGES, ZP>::NTHREADS, 2)
                 }
             }
             __syncwarp();
-            if (lane == 0) ptx::mbar_arrive(empty_bar(s));
-            if (++s == STAGES) {
-                s = 0;
-                ph ^= 1u;
+            if (lane == 0) ptx::mbar_arrive(empty_as(sa));
+            if (++sa == AS) {
+                sa = 0;
+                pha ^= 1u;
             }
-
         }
     }
     // Every stage was consumed, or drained after an abort: the stage memory is free.
