@@ -37,7 +37,7 @@ struct Fp4DecodeCfg {
     static constexpr int SF_BASE = STAGES * W_STAGE;
     static constexpr int A_BASE = SF_BASE + STAGES * SF_STAGE;
     static constexpr int INBOX = A_BASE + STAGES * A_STAGE;
-    static constexpr int INBOX_BYTES = 16 * (TILE_N + 16) * 4;   // fp32 [S][R][16], S * R <= 128 + 15
+    static constexpr int INBOX_BYTES = inbox_row_pitch(2) * (TILE_N + 16) * 4;   // fp32 [S][R][pitch], S * R <= 128 + 15
     static constexpr int OFF_BAR = INBOX + INBOX_BYTES;
     // barriers: full and empty per stage; then the abort flag (4 B, padded to 8) and the
     // inbox barrier (split-K)

@@ -42,7 +42,7 @@ struct Fp8DecodeCfg {
     static constexpr int A_STAGE = 8 * NTA * 128 * NZ;   // up to 8 NTA token rows of 128 bytes per box
     static constexpr int A_BASE = STAGES * W_STAGE;
     static constexpr int INBOX = A_BASE + STAGES * A_STAGE;
-    static constexpr int INBOX_BYTES = inbox_row_floats(NT) * (TILE_N + 16) * 4;   // fp32 [S][R][row], S * R <= 143
+    static constexpr int INBOX_BYTES = inbox_row_pitch(NT) * (TILE_N + 16) * 4;   // fp32 [S][R][row], S * R <= 143
     static constexpr int OFF_BAR = INBOX + INBOX_BYTES;
     // barriers: full and empty per stage; then the abort flag (4 B, padded to 8) and the
     // inbox barrier (split-K)

@@ -40,6 +40,10 @@ cudaError_t launch_gemm_int4_pair(const GemmParams& p, bool bf16, int grid, cuda
 // memory and the cluster limits.
 template <bool BF16, int NT, int GSTEPS, int BK>
 using I4Dec = MmaDecodeLauncher<BF16, NT, GSTEPS, BK, BK == 256 ? 2 : 4>;
+// three CTAs per SM: 228 KB of shared memory per SM, 1 KB reserved per CTA
+static_assert(3 * (MmaDecodeCfg<256, 2>::SMEM_BYTES + 1024) <= 228 * 1024 &&
+                  3 * (MmaDecodeCfg<128, 4>::SMEM_BYTES + 1024) <= 228 * 1024,
+              "decode ring no longer fits three CTAs per SM");
 
 bool config_int4_decode(bool bf16, bool query, KernelConfig* cfg) {
     *cfg = bf16 ? I4Dec<true, 2, 8, 128>::config(query) : I4Dec<false, 2, 8, 128>::config(query);

@@ -41,6 +41,11 @@
 
 namespace wq {
 
+// Split-K inbox row: token slots of one weight row (16 for one or two 8-token tiles,
+// 8 NT beyond), and the row pitch in floats (the slots plus 4).
+__host__ __device__ constexpr int inbox_row_floats(int NT) { return NT <= 2 ? 16 : 8 * NT; }
+__host__ __device__ constexpr int inbox_row_pitch(int NT) { return inbox_row_floats(NT) + 4; }
+
 template <int BK, int STAGES, bool ZP = false>
 struct MmaDecodeCfg {
     // compute warps: four of 32 weight rows each -- the two 16-row groups of a warp
@@ -76,7 +81,7 @@ struct MmaDecodeCfg {
     // 2c + (i & 1) + 8 (i >> 1): the order of a lane's accumulator values, so each
     // lane sends a row's values with one vector store.
     static constexpr int INBOX = SC_BASE + AS_STAGES * SC_STAGE;
-    static constexpr int INBOX_BYTES = 16 * (TILE_N + 16) * 4;
+    static constexpr int INBOX_BYTES = inbox_row_pitch(2) * (TILE_N + 16) * 4;
     static constexpr int OFF_BAR = INBOX + INBOX_BYTES;
     // barriers: full and empty per weight slot, full and empty per activation slot; then
     // the abort flag (4 B, padded to 8) and the inbox barrier (8 B, split-K)
@@ -126,12 +131,16 @@ __device__ __forceinline__ void ldmatrix_x4(uint32_t addr, uint32_t& r0, uint32_
 // adds the S slices of its rows in rank order (deterministic) and reads only its own
 // shared memory.  No cluster-wide barrier has to wait for the remote stores to
 // complete (measured on GB300: a barrier.cluster with release semantics after remote
-// stores cost ~1 us per launch).  Inbox: fp32 [S][R = ceil(128 / S)][inbox_row_floats(NT)]
+// stores cost ~1 us per launch).  Inbox: fp32 [S][R = ceil(128 / S)][inbox_row_pitch(NT)]
 // per row and slice, the token slots in the order of a lane's accumulator values:
 // lane c's values for MMA columns 2c, 2c + 1 of the 8-token tiles nt = 0 .. NT - 1 at
 // slots (16 / 4 or 8 NT / 4) c + 2 nt + {0, 1}, so a lane sends a row's values with
-// one to four vector stores.
-__host__ __device__ constexpr int inbox_row_floats(int NT) { return NT <= 2 ? 16 : 8 * NT; }
+// one to four vector stores.  The row pitch is the slot count plus 4: the reduction's
+// warps read one slot of 32 consecutive rows, which a pitch of 16 or 32 floats puts on
+// 2 or 1 banks (16- or 32-way conflicts); the extra 16 bytes spread them over 8 bank
+// quads and keep the rows 16-byte aligned for the vector stores.
+// (inbox_row_floats / inbox_row_pitch: the split-K inbox layout, described with the
+// exchange helpers below)
 
 // Compute warp `warp` holds rows 16 RGW warp + 16 j + g (+ 8) of the tile in
 // acc[j][nt][e] (e = 0, 1: row g, MMA columns 8 nt + 2c + e; e = 2, 3: row g + 8).
@@ -139,6 +148,7 @@ template <int NT, int RGW>
 __device__ __forceinline__ void decode_send_partials(const float (&acc)[RGW][NT][4], int warp, int lane, int rank,
                                                      int S, int R, uint32_t inbox, uint32_t inbox_bar) {
     constexpr int ROWF = inbox_row_floats(NT);
+    constexpr int PITCH = inbox_row_pitch(NT);
     const int g = lane >> 2, c = lane & 3;
 #pragma unroll
     for (int j = 0; j < RGW; ++j)
@@ -147,7 +157,7 @@ __device__ __forceinline__ void decode_send_partials(const float (&acc)[RGW][NT]
             const int r = (warp * RGW + j) * 16 + g + 8 * h;   // e = 2h, 2h + 1
             const int owner = ((r + 1) * S - 1) / TILE_N;       // 128 owner / S <= r < 128 (owner + 1) / S
             const uint32_t off =
-                inbox + (uint32_t)((rank * R + (r - owner * TILE_N / S)) * ROWF + (ROWF / 4) * c) * 4u;
+                inbox + (uint32_t)((rank * R + (r - owner * TILE_N / S)) * PITCH + (ROWF / 4) * c) * 4u;
             const uint32_t dst = ptx::mapa_shared(off, (uint32_t)owner);
             const uint32_t rbar = ptx::mapa_shared(inbox_bar, (uint32_t)owner);
             if constexpr (NT == 1) {
@@ -177,13 +187,14 @@ __device__ __forceinline__ int column_of_token(int t) { return SPREAD ? (t >> 1)
 template <int NT, bool SPREAD = false, typename Store>
 __device__ __forceinline__ void decode_reduce_rows(const float* box, int S, int R, int rows_own, int M, Store store) {
     constexpr int ROWF = inbox_row_floats(NT);
+    constexpr int PITCH = inbox_row_pitch(NT);
     for (int e = threadIdx.x; e < M * rows_own; e += blockDim.x) {
         const int m = e / rows_own;
         const int r = e - m * rows_own;
         const int n = column_of_token<SPREAD>(m & 7);   // lane 4 g + n / 2 holds it as value n % 2
         const int slot = (ROWF / 4) * (n >> 1) + (n & 1) + 2 * (m >> 3);
         float tot = 0.0f;
-        for (int q = 0; q < S; ++q) tot += box[(q * R + r) * ROWF + slot];
+        for (int q = 0; q < S; ++q) tot += box[(q * R + r) * PITCH + slot];
         store(m, r, tot);
     }
 }
