@@ -115,7 +115,8 @@ constexpr int kCfgDecodeInt4 = 16;     // + decode_kind (0 symmetric, 1 zero poi
 constexpr int kCfgDecodeFp8 = 18;
 constexpr int kCfgDecodeFp4 = 19;
 constexpr int kCfgDecodeFp8N4 = 20;   // FP8 decode with 4 token tiles (M <= 32)
-constexpr int kNumDecodeCfgs = 5;
+constexpr int kCfgDecodeFp4N1 = 21;   // FP4 decode with one token tile (M <= 8)
+constexpr int kNumDecodeCfgs = 6;
 constexpr int kCfgPair = 32;           // + format
 
 bool get_config_uncached(int fmt, bool bf16, int bn, bool query, KernelConfig* cfg) {
@@ -123,7 +124,8 @@ bool get_config_uncached(int fmt, bool bf16, int bn, bool query, KernelConfig* c
     if (fmt == kCfgDecodeInt4 + 1) return config_int4_decode_zp(bf16, query, cfg);
     if (fmt == kCfgDecodeFp8) return config_fp8_decode(bf16, 2, query, cfg);
     if (fmt == kCfgDecodeFp8N4) return config_fp8_decode(bf16, 4, query, cfg);
-    if (fmt == kCfgDecodeFp4) return bf16 && config_fp4_decode(query, cfg);
+    if (fmt == kCfgDecodeFp4) return bf16 && config_fp4_decode(2, query, cfg);
+    if (fmt == kCfgDecodeFp4N1) return bf16 && config_fp4_decode(1, query, cfg);
     if (fmt == kCfgPair + FMT_INT4) return config_int4_pair(bf16, query, cfg);
     if (fmt == kCfgPair + FMT_FP8) return config_fp8_pair(bf16, query, cfg);
     if (fmt == kCfgPair + FMT_FP4) return bf16 && config_fp4_pair(query, cfg);
@@ -210,7 +212,7 @@ wq_status make_plan(int fmt, bool bf16, int64_t M, int64_t N, int64_t K, int sms
                         M <= (fmt == FMT_FP8 ? 32 : 16) && K % (fmt == FMT_FP4 ? 256 : 64) == 0 &&
                         !decode_disabled();
     if (decode && fmt == FMT_FP4) {
-        found = get_config(kCfgDecodeFp4, bf16, 16, sms > 0, &cfg);
+        found = get_config(M <= 8 ? kCfgDecodeFp4N1 : kCfgDecodeFp4, bf16, 16, sms > 0, &cfg);
     } else if (decode && fmt == FMT_FP8) {
         found = get_config(M <= 16 ? kCfgDecodeFp8 : kCfgDecodeFp8N4, bf16, 16, sms > 0, &cfg);
     } else if (decode) {

@@ -23,7 +23,9 @@
 
 namespace wq {
 
-template <int STAGES>
+// NT: 8-token MMA column tiles; the activation stages and the split-K inbox hold 8 NT
+// tokens, so the one-tile kernel (M <= 8) fits four CTAs per SM.
+template <int STAGES, int NT = 2>
 struct Fp4DecodeCfg {
     static constexpr int BK = 256;                       // codes per weight row per stage
     static constexpr int NCW = 4;                        // compute warps, 32 rows each
@@ -33,11 +35,11 @@ struct Fp4DecodeCfg {
     static constexpr int NZ = BK / 64;                   // 64-wide activation boxes per stage
     static constexpr int W_STAGE = TILE_N * BK / 2;      // one 128 x 128-byte box
     static constexpr int SF_STAGE = TILE_N * BK / 16;    // [BK / 64 quads][128 rows][4 scales]
-    static constexpr int A_STAGE = 16 * 128 * NZ;        // up to 16 token rows of 128 bytes per box
+    static constexpr int A_STAGE = 8 * NT * 128 * NZ;    // up to 8 NT token rows of 128 bytes per box
     static constexpr int SF_BASE = STAGES * W_STAGE;
     static constexpr int A_BASE = SF_BASE + STAGES * SF_STAGE;
     static constexpr int INBOX = A_BASE + STAGES * A_STAGE;
-    static constexpr int INBOX_BYTES = inbox_row_pitch(2) * (TILE_N + 16) * 4;   // fp32 [S][R][pitch], S * R <= 128 + 15
+    static constexpr int INBOX_BYTES = inbox_row_pitch(NT) * (TILE_N + 16) * 4;   // fp32 [S][R][pitch], S * R <= 128 + 15
     static constexpr int OFF_BAR = INBOX + INBOX_BYTES;
     // barriers: full and empty per stage; then the abort flag (4 B, padded to 8) and the
     // inbox barrier (split-K)
@@ -66,9 +68,9 @@ __device__ __forceinline__ uint4 ld_shared_v4(uint32_t addr) {
 // NT: 8-token MMA column tiles (1 for M <= 8, 2 for M <= 16).  One CTA per item
 // (tile, K slice): gridDim.x == n_items, the slices of a tile form one cluster.
 template <int NT, int STAGES>
-__global__ void __launch_bounds__(Fp4DecodeCfg<STAGES>::NTHREADS, 2)
+__global__ void __launch_bounds__(Fp4DecodeCfg<STAGES, NT>::NTHREADS, NT == 1 ? 4 : 3)
     wq_decode_fp4_kernel(const __grid_constant__ GemmParams p) {
-    using C = Fp4DecodeCfg<STAGES>;
+    using C = Fp4DecodeCfg<STAGES, NT>;
     constexpr int NCW = C::NCW;
     constexpr int RGW = C::RGW;
     constexpr int NZ = C::NZ;
@@ -284,7 +286,7 @@ __global__ void __launch_bounds__(Fp4DecodeCfg<STAGES>::NTHREADS, 2)
 
 template <int NT, int STAGES>
 struct Fp4DecodeLauncher {
-    using C = Fp4DecodeCfg<STAGES>;
+    using C = Fp4DecodeCfg<STAGES, NT>;
     static constexpr auto kernel = wq_decode_fp4_kernel<NT, STAGES>;
     static cudaError_t prepare() {
         static int attr_set[64] = {0};
@@ -307,7 +309,7 @@ struct Fp4DecodeLauncher {
     static cudaError_t launch(const GemmParams& p, int grid, cudaStream_t st) {
         cudaError_t e = prepare();
         if (e != cudaSuccess) return e;
-        if (p.splits > kMaxDecodeCluster || grid != p.n_items || p.M > 16 || p.M < 1) return cudaErrorInvalidValue;
+        if (p.splits > kMaxDecodeCluster || grid != p.n_items || p.M > 8 * NT || p.M < 1) return cudaErrorInvalidValue;
         return launch_decode_grid(kernel, p, grid, C::NTHREADS, C::SMEM_BYTES, st);
     }
 };

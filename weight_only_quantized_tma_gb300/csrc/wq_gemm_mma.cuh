@@ -41,9 +41,9 @@
 
 namespace wq {
 
-// Split-K inbox row: token slots of one weight row (16 for one or two 8-token tiles,
-// 8 NT beyond), and the row pitch in floats (the slots plus 4).
-__host__ __device__ constexpr int inbox_row_floats(int NT) { return NT <= 2 ? 16 : 8 * NT; }
+// Split-K inbox row: token slots of one weight row (8 per 8-token tile), and the row
+// pitch in floats (the slots plus 4).
+__host__ __device__ constexpr int inbox_row_floats(int NT) { return 8 * NT; }
 __host__ __device__ constexpr int inbox_row_pitch(int NT) { return inbox_row_floats(NT) + 4; }
 
 template <int BK, int STAGES, bool ZP = false>
@@ -134,8 +134,8 @@ __device__ __forceinline__ void ldmatrix_x4(uint32_t addr, uint32_t& r0, uint32_
 // stores cost ~1 us per launch).  Inbox: fp32 [S][R = ceil(128 / S)][inbox_row_pitch(NT)]
 // per row and slice, the token slots in the order of a lane's accumulator values:
 // lane c's values for MMA columns 2c, 2c + 1 of the 8-token tiles nt = 0 .. NT - 1 at
-// slots (16 / 4 or 8 NT / 4) c + 2 nt + {0, 1}, so a lane sends a row's values with
-// one to four vector stores.  The row pitch is the slot count plus 4: the reduction's
+// slots 2 NT c + 2 nt + {0, 1}, so a lane sends a row's values with one to four vector
+// stores.  The row pitch is the slot count plus 4: the reduction's
 // warps read one slot of 32 consecutive rows, which a pitch of 16 or 32 floats puts on
 // 2 or 1 banks (16- or 32-way conflicts); the extra 16 bytes spread them over 8 bank
 // quads and keep the rows 16-byte aligned for the vector stores.

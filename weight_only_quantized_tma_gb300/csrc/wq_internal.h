@@ -172,7 +172,7 @@ bool config_fp8_decode(bool bf16, int nt, bool query, KernelConfig* cfg);
 cudaError_t launch_gemm_fp8_decode(const GemmParams& p, bool bf16, int grid, cudaStream_t st);
 // BF16 x FP4 decode kernel (M <= 16, K % 256 == 0): e2m1 codes and block scales turned
 // into bf16 operands in registers (wq_decode_fp4.cuh).
-bool config_fp4_decode(bool query, KernelConfig* cfg);
+bool config_fp4_decode(int nt, bool query, KernelConfig* cfg);
 cudaError_t launch_gemm_fp4_decode(const GemmParams& p, int grid, cudaStream_t st);
 // W4A16 tile kernel on two-CTA clusters (256 weight rows x 256 tokens per tile).
 bool config_int4_pair(bool bf16, bool query, KernelConfig* cfg);
