@@ -504,8 +504,8 @@ def run_ours(args, rank, world, local_rank):
                 del copies
             entry("fp4", M, N, K, "bf16", us, byts, extra)
             del Ax, wd, outx, wsx
-        # zero-point INT4 beside the symmetric format at the same shapes (the zero-point
-        # path runs on the tile kernels at every M)
+        # zero-point INT4 beside the symmetric format at the same shapes (both on the
+        # register decode kernel at M <= 16, the tile kernels above)
         for (M, N, K, Gz) in [(16, 4096, 4096, 128), (128, 4096, 4096, 128), (4096, 4096, 4096, 128),
                               (8192, 8192, 8192, 128)]:
             seed = 6000 + M
@@ -521,14 +521,21 @@ def run_ours(args, rank, world, local_rank):
                 plan = wq.get_plan(opid, wq.WQ_F16, M, N, K, Gz)
                 wsx = torch.zeros(plan["ws_bytes"] + 16, dtype=torch.uint8, device=dev)
                 if op == "w4a16_zp":
-                    us = time_call(lambda: wq.wq_gemm_w4a16_zp(Ax, wkz, skz, zkz, N, K, Gz, out=outx, ws=wsx))
+                    call = lambda w=wkz: wq.wq_gemm_w4a16_zp(Ax, w, skz, zkz, N, K, Gz, out=outx, ws=wsx)
                 else:
-                    us = time_call(lambda: wq.wq_gemm_w4a16(Ax, wkz, skz, N, K, Gz, out=outx, ws=wsx))
-                entry(op, M, N, K, "f16", us, byts if op == "w4a16_zp" else byts - (K // Gz) * N,
-                      {"G": Gz, "kernel": plan["kernel"]}, into=zero_point)
+                    call = lambda w=wkz: wq.wq_gemm_w4a16(Ax, w, skz, N, K, Gz, out=outx, ws=wsx)
+                us = time_call(call)
+                ob = byts if op == "w4a16_zp" else byts - (K // Gz) * N
+                extra = {"G": Gz, "kernel": plan["kernel"]}
+                if M <= 16:
+                    copies = [wkz] + [wkz.clone() for _ in range(n_copies(N * K // 2) - 1)]
+                    extra.update(graph_fields(graph_us([(lambda w=w: call(w)) for w in copies]), ob))
+                    del copies
+                entry(op, M, N, K, "f16", us, ob, extra, into=zero_point)
                 del wsx
             del Ax, wkz, skz, zkz, outx
-        # codebook INT4 (NF4-style table) and INT2 W2A16 on the tile kernels
+        # codebook INT4 (NF4-style table; the register decode kernel at M <= 16) and INT2
+        # W2A16 (the tile kernels at every M)
         for (M, N, K, Gc) in [(16, 4096, 4096, 128), (4096, 4096, 4096, 128), (8192, 8192, 8192, 128)]:
             seed = 7000 + M
             Ax = torch.from_numpy(synth.activations(M, K, "f16", seed).view(np.int16)).to(dev).view(torch.float16)
@@ -540,18 +547,28 @@ def run_ours(args, rank, world, local_rank):
             lut = torch.from_numpy(synth.normal_quantile_codebook().view(np.int16)).to(dev).view(torch.float16)
             plan = wq.get_plan(wq.WQ_OP_W4A16_LUT, wq.WQ_F16, M, N, K, Gc)
             wsx = torch.zeros(plan["ws_bytes"] + 16, dtype=torch.uint8, device=dev)
-            us = time_call(lambda: wq.wq_gemm_w4a16_lut(Ax, wkc, skc, lut, N, K, Gc, out=outx, ws=wsx))
-            entry("w4a16_lut", M, N, K, "f16", us, N * K // 2 + io + 32, {"G": Gc, "kernel": plan["kernel"]},
-                  into=codebook_int2)
+            call = lambda w=wkc: wq.wq_gemm_w4a16_lut(Ax, w, skc, lut, N, K, Gc, out=outx, ws=wsx)
+            us = time_call(call)
+            extra = {"G": Gc, "kernel": plan["kernel"]}
+            if M <= 16:
+                copies = [wkc] + [wkc.clone() for _ in range(n_copies(N * K // 2) - 1)]
+                extra.update(graph_fields(graph_us([(lambda w=w: call(w)) for w in copies]), N * K // 2 + io + 32))
+                del copies
+            entry("w4a16_lut", M, N, K, "f16", us, N * K // 2 + io + 32, extra, into=codebook_int2)
             del wkc, skc, wsx
             w2 = synth.int2_weights(N, K, Gc, seed + 2)
             w2d = torch.from_numpy(w2.w).to(dev)
             sk2 = wq.wq_pack_int2_scales(torch.from_numpy(w2.s.view(np.int16)).to(dev).view(torch.float16), N, K, Gc)
             plan = wq.get_plan(wq.WQ_OP_W2A16, wq.WQ_F16, M, N, K, Gc)
             wsx = torch.zeros(plan["ws_bytes"] + 16, dtype=torch.uint8, device=dev)
-            us = time_call(lambda: wq.wq_gemm_w2a16(Ax, w2d, sk2, N, K, Gc, out=outx, ws=wsx))
-            entry("w2a16", M, N, K, "f16", us, N * K // 4 + io, {"G": Gc, "kernel": plan["kernel"]},
-                  into=codebook_int2)
+            call = lambda w=w2d: wq.wq_gemm_w2a16(Ax, w, sk2, N, K, Gc, out=outx, ws=wsx)
+            us = time_call(call)
+            extra = {"G": Gc, "kernel": plan["kernel"]}
+            if M <= 16:
+                copies = [w2d] + [w2d.clone() for _ in range(n_copies(N * K // 4) - 1)]
+                extra.update(graph_fields(graph_us([(lambda w=w: call(w)) for w in copies]), N * K // 4 + io))
+                del copies
+            entry("w2a16", M, N, K, "f16", us, N * K // 4 + io, extra, into=codebook_int2)
             del Ax, w2d, sk2, wsx, outx, s_dev
         del flush
 

@@ -127,7 +127,8 @@ def test_lut_uniform_grid_matches_int4_bitwise(M, K, G, a_dtype):
                                      (96, 512, 2048, 64), (300, 1024, 1024, 256), (1000, 768, 512, 32)])
 def test_lut_random_vs_oracle(M, N, K, G, a_dtype):
     p = LutProblem(M, N, K, G, a_dtype=a_dtype, seed=707 + M + K)
-    assert wq.get_plan(wq.WQ_OP_W4A16_LUT, _adt(a_dtype), M, N, K, G)["kernel"] != wq.WQ_KERNEL_DECODE
+    decode = a_dtype == "f16" and M <= 16 and K % 64 == 0
+    assert (wq.get_plan(wq.WQ_OP_W4A16_LUT, _adt(a_dtype), M, N, K, G)["kernel"] == wq.WQ_KERNEL_DECODE) == decode
     out = p.run()
     torch.cuda.synchronize()
     _check(p, out, None, f"lut M{M} N{N} K{K} G{G}")
@@ -141,6 +142,97 @@ def test_lut_large_pair_sampled_rows(a_dtype):
     torch.cuda.synchronize()
     rows = synth.sample_rows(M, 24, seed=709)
     _check(p, out, rows, "lut pair sampled")
+
+
+# ------------------------------------------------------------------ codebook decode kernel
+# fp16 activations, M <= 16, K % 64 == 0: the register decode kernel looks up LUT[q]
+# with byte permutes into the MMA fragment registers and applies the group scale to
+# the fp32 sums, so an output is RN16(s * sum_k A LUT[q]) (one rounding of an fp32 value)
+
+def _lut_plan(M, N, K, G, a_dtype="f16"):
+    return wq.get_plan(wq.WQ_OP_W4A16_LUT, _adt(a_dtype), M, N, K, G)
+
+
+def test_lut_decode_plan():
+    assert _lut_plan(1, 4096, 4096, 128)["kernel"] == wq.WQ_KERNEL_DECODE
+    assert _lut_plan(16, 4096, 4096, 128)["kernel"] == wq.WQ_KERNEL_DECODE
+    assert _lut_plan(16, 4096, 4096, 128)["bk"] == 128
+    assert _lut_plan(17, 4096, 4096, 128)["kernel"] == wq.WQ_KERNEL_TILE
+    assert _lut_plan(16, 4096, 4096, 128, "bf16")["kernel"] == wq.WQ_KERNEL_TILE
+    assert _lut_plan(4, 1024, 1056, 32)["kernel"] == wq.WQ_KERNEL_TILE   # K % 64 == 32
+
+
+@pytest.mark.parametrize("G", [32, 64, 128, 256])
+@pytest.mark.parametrize("table", ["nf4", "random"])
+def test_lut_decode_identity_rows_bit_exact(G, table):
+    # A = the first 16 rows of the identity: out[m, n] = RN16(LUT[q[n, m]] * s) exactly
+    # (one non-zero product; s * LUT[q] has at most 22 significant bits, exact in fp32),
+    # so every code position of every row half goes through the lookup and the fragment
+    # order, with K split over several slices
+    M, N, K = 16, 384, 1024
+    lut = synth.normal_quantile_codebook() if table == "nf4" else synth.random_codebook(720 + G)
+    p = LutProblem(M, N, K, G, seed=721, A_bits=_eye_bits(K, "f16")[:M].copy(), lut=lut)
+    plan = _lut_plan(M, N, K, G)
+    assert plan["kernel"] == wq.WQ_KERNEL_DECODE and plan["splits"] > 1
+    out = p.run()
+    torch.cuda.synchronize()
+    assert np.array_equal(out_bits(out), _rn(p.dequant_ref().T[:M], "f16"))
+
+
+@pytest.mark.parametrize("shift", [0, 1])
+def test_lut_decode_one_hot_every_k_step(shift):
+    # token m selects k_m over all 16 positions of a k step and over stages and slices
+    M, N, K, G = 16, 256, 2048, 128
+    ks = [16 * ((7 * m + 5 * shift) % (K // 16)) + (m + 3 * shift) % 16 for m in range(M)]
+    assert sorted(k % 16 for k in ks) == list(range(16))
+    A = np.zeros((M, K), dtype=np.float32)
+    A[np.arange(M), ks] = 1.0
+    p = LutProblem(M, N, K, G, seed=722 + shift, A_bits=A.astype(np.float16).view(np.uint16),
+                   lut=synth.random_codebook(723 + shift))
+    out = p.run()
+    torch.cuda.synchronize()
+    assert np.array_equal(out_bits(out), _rn(p.dequant_ref()[:, ks].T, "f16"))
+
+
+@pytest.mark.parametrize("M", [1, 9, 16])
+def test_lut_decode_uniform_grid_matches_symmetric(M):
+    # LUT[q] = q - 8 is the symmetric format: the operands equal the symmetric decode
+    # kernel's q - 8, and with the same 128-value stages (K % 256 == 64) and K slices
+    # the sums and the outputs are the same bits
+    N, K, G = 512, 4160, 64
+    p = LutProblem(M, N, K, G, seed=724 + M, lut=(np.arange(16) - 8.0).astype(np.float16).view(np.uint16))
+    lp = _lut_plan(M, N, K, G)
+    sp = wq.get_plan(wq.WQ_OP_W4A16, wq.WQ_F16, M, N, K, G)
+    assert lp["kernel"] == sp["kernel"] == wq.WQ_KERNEL_DECODE and lp["bk"] == sp["bk"] == 128
+    got = p.run()
+    sym = wq.wq_gemm_w4a16(p.A_d, p.wk, p.sk, N, K, G)
+    torch.cuda.synchronize()
+    check_close(out_to_f64(got), p.ref(), what=f"lut decode q-8 M={M}")
+    if lp["splits"] == sp["splits"]:
+        assert torch.equal(got.view(torch.int16), sym.view(torch.int16))
+
+
+@pytest.mark.parametrize("M", list(range(1, 17)))
+def test_lut_decode_every_token_count(M):
+    p = LutProblem(M, 256, 1024, 128, seed=730 + M, lut=synth.random_codebook(731))
+    out = p.run()
+    torch.cuda.synchronize()
+    check_close(out_to_f64(out), p.ref(), what=f"lut decode M={M}")
+
+
+@pytest.mark.parametrize("M,N,K,G", [(1, 1000, 4160, 64), (7, 136, 1088, 32), (16, 11008, 4096, 128),
+                                     (3, 264, 192, 64), (16, 256, 16384, 128)])
+def test_lut_decode_ragged_and_deterministic(M, N, K, G):
+    # tail rows, K % 128 == 64 (a half stage of zero fill), one stage, the largest cluster
+    p = LutProblem(M, N, K, G, seed=740 + M + K)
+    assert _lut_plan(M, N, K, G)["kernel"] == wq.WQ_KERNEL_DECODE
+    wq.wq_clear_device_status()
+    first = p.run()
+    torch.cuda.synchronize()
+    assert wq.wq_device_status() == 0
+    check_close(out_to_f64(first), p.ref(), what=f"lut decode M={M} N={N} K={K} G={G}")
+    for _ in range(3):
+        assert torch.equal(p.run(), first)
 
 
 def test_lut_bad_arguments():
@@ -222,10 +314,12 @@ def test_int2_identity_A_pair_kernel_bit_exact(a_dtype):
 
 @pytest.mark.parametrize("a_dtype", ["f16", "bf16"])
 @pytest.mark.parametrize("M", [4, 200, 4096])
-def test_int2_matches_int4_shifted_codes_bitwise(M, a_dtype):
+def test_int2_matches_int4_shifted_codes_bitwise(M, a_dtype, monkeypatch):
     # an INT2 code q has the operand of the INT4 code q + 6; the tile kernels tile both
     # formats alike, so the outputs agree bit for bit (INT4 through the codebook entry
-    # with the uniform-grid table LUT[q] = q - 8, which takes the tile kernels at every M)
+    # with the uniform-grid table LUT[q] = q - 8, kept on the tile kernels: with fp16
+    # activations and M <= 16 the codebook entry would take the register decode kernel)
+    monkeypatch.setenv("WQ_DISABLE_DECODE", "1")
     N, K, G = 512, 1024, 64
     rng = np.random.default_rng(723)
     q = rng.integers(0, 4, size=(N, K), dtype=np.uint8)

@@ -116,7 +116,8 @@ constexpr int kCfgDecodeFp8 = 18;
 constexpr int kCfgDecodeFp4 = 19;
 constexpr int kCfgDecodeFp8N4 = 20;   // FP8 decode with 4 token tiles (M <= 32)
 constexpr int kCfgDecodeFp4N1 = 21;   // FP4 decode with one token tile (M <= 8)
-constexpr int kNumDecodeCfgs = 6;
+constexpr int kCfgDecodeLut = 22;     // codebook INT4 decode (fp16 activations)
+constexpr int kNumDecodeCfgs = 7;
 constexpr int kCfgPair = 32;           // + format
 
 bool get_config_uncached(int fmt, bool bf16, int bn, bool query, KernelConfig* cfg) {
@@ -126,6 +127,7 @@ bool get_config_uncached(int fmt, bool bf16, int bn, bool query, KernelConfig* c
     if (fmt == kCfgDecodeFp8N4) return config_fp8_decode(bf16, 4, query, cfg);
     if (fmt == kCfgDecodeFp4) return bf16 && config_fp4_decode(2, query, cfg);
     if (fmt == kCfgDecodeFp4N1) return bf16 && config_fp4_decode(1, query, cfg);
+    if (fmt == kCfgDecodeLut) return !bf16 && config_int4_decode_lut(query, cfg);
     if (fmt == kCfgPair + FMT_INT4) return config_int4_pair(bf16, query, cfg);
     if (fmt == kCfgPair + FMT_FP8) return config_fp8_pair(bf16, query, cfg);
     if (fmt == kCfgPair + FMT_FP4) return bf16 && config_fp4_pair(query, cfg);
@@ -204,11 +206,13 @@ wq_status make_plan(int fmt, bool bf16, int64_t M, int64_t N, int64_t K, int sms
     static const int kTiles[4] = {16, 64, 128, 256};
     KernelConfig cfg{};
     bool found = false;
-    // decode (M <= 16; FP8 M <= 32): the register-resident kernels (W4A16, FP8, FP4);
+    // decode (M <= 16; FP8 M <= 32): the register-resident kernels (W4A16, codebook INT4
+    // with fp16 activations, FP8, FP4);
     // their activation copy views A as 64-wide boxes, so they need K % 64 == 0 (FP4:
     // whole 256-code stages, K % 256 == 0, so that no stage reads block scales past K)
     // decode_kind (W4A16): 0 symmetric, 1 zero points, -1 no decode kernel
-    const bool decode = decode_kind >= 0 && (fmt == FMT_INT4 || fmt == FMT_FP8 || fmt == FMT_FP4) &&
+    const bool decode = decode_kind >= 0 &&
+                        (fmt == FMT_INT4 || fmt == FMT_FP8 || fmt == FMT_FP4 || (fmt == FMT_LUT4 && !bf16)) &&
                         M <= (fmt == FMT_FP8 ? 32 : 16) && K % (fmt == FMT_FP4 ? 256 : 64) == 0 &&
                         !decode_disabled();
     if (decode && fmt == FMT_FP4) {
@@ -216,10 +220,10 @@ wq_status make_plan(int fmt, bool bf16, int64_t M, int64_t N, int64_t K, int sms
     } else if (decode && fmt == FMT_FP8) {
         found = get_config(M <= 16 ? kCfgDecodeFp8 : kCfgDecodeFp8N4, bf16, 16, sms > 0, &cfg);
     } else if (decode) {
-        found = get_config(kCfgDecodeInt4 + decode_kind, bf16, 16, sms > 0, &cfg);
+        found = get_config(fmt == FMT_LUT4 ? kCfgDecodeLut : kCfgDecodeInt4 + decode_kind, bf16, 16, sms > 0, &cfg);
         // stages of 256 values when K allows (the launch picks the same instantiation,
-        // half as many stages)
-        if (found && K % 256 == 0) {
+        // half as many stages); the codebook kernel keeps stages of 128
+        if (found && K % 256 == 0 && fmt != FMT_LUT4) {
             cfg.bk = 256;
             cfg.stages /= 2;
         }
@@ -623,8 +627,8 @@ wq_status wq_get_plan(wq_op op, wq_dtype a_dtype, int64_t M, int64_t N, int64_t 
     if (a_dtype != WQ_F16 && a_dtype != WQ_BF16) return WQ_ERR_DTYPE;
     const bool bf16 = (op == WQ_OP_FP4) ? true : (a_dtype == WQ_BF16);
     Plan pl{};
-    // the decode kind the GEMM entry points pass (make_plan takes the decode kernels
-    // for W4A16 and FP8 only)
+    // the decode kind the GEMM entry points pass (0 for every format but zero-point
+    // INT4; make_plan picks the decode kernel by format)
     wq_status st = plan_for(fmt, bf16, M > 0 ? M : 1, N, K, &pl, grouped ? G : 0, op == WQ_OP_W4A16_ZP ? 1 : 0);
     if (st != WQ_OK) return st;
     if (plan) {
@@ -655,7 +659,8 @@ wq_status wq_workspace_bytes(wq_op op, wq_dtype a_dtype, int64_t M, int64_t N, i
 }
 
 // W4A16 with the symmetric zero point 8 (z_kernel and lut null), packed zero points,
-// or a 16-entry codebook.  Only the symmetric format has the M <= 16 register kernel.
+// or a 16-entry codebook.  M <= 16 with K % 64 == 0 runs on the register decode kernel
+// (the codebook with fp16 activations only).
 static wq_status gemm_int4(const void* A, wq_dtype a_dtype, const uint8_t* w_kernel, const void* s_kernel,
                            const uint8_t* z_kernel, const uint16_t* lut, int64_t M, int64_t N, int64_t K, int32_t G,
                            void* out, void* ws, size_t ws_bytes, wq_stream_t stream) {
@@ -696,6 +701,7 @@ static wq_status gemm_int4(const void* A, wq_dtype a_dtype, const uint8_t* w_ker
     fill_common(gp, pl, M, N, K, out, ws, d->status);
     if (pl.decode)
         return finish_launch(z_kernel ? launch_gemm_int4_decode_zp(gp, bf16, pl.grid, (cudaStream_t)stream)
+                             : lut    ? launch_gemm_int4_decode_lut(gp, pl.grid, (cudaStream_t)stream)
                                       : launch_gemm_int4_decode(gp, bf16, pl.grid, (cudaStream_t)stream));
     if (fmt == FMT_LUT4)
         return finish_launch(pl.pair ? launch_gemm_lut4_pair(gp, bf16, pl.grid, (cudaStream_t)stream)

@@ -113,4 +113,42 @@ __device__ __forceinline__ Item decode_item(const GemmParams& p, int item) {
     return it;
 }
 
+// INT4 codebook ("Low Bit Triton Kernels": NF4's 16 non-uniform values are a
+// lookup table held in registers).  The 16 fp16 entries are split into their low
+// bytes (lo[i] byte j = low byte of entry 4i + j) and high bytes, so that byte
+// permutes look up four codes at once: one permute over an 8-byte half of a table
+// per code range 0-7 / 8-15, a select by bit 3 of each code, and two permutes that
+// interleave low and high bytes into fp16 pairs.
+struct Lut16 {
+    uint32_t lo[4], hi[4];
+};
+__device__ __forceinline__ Lut16 lut16_load(const uint16_t* lut) {
+    const uint4 a = __ldg(reinterpret_cast<const uint4*>(lut));       // entries 0-7
+    const uint4 b = __ldg(reinterpret_cast<const uint4*>(lut) + 1);   // entries 8-15
+    const uint32_t e[8] = {a.x, a.y, a.z, a.w, b.x, b.y, b.z, b.w};   // word i: entries 2i, 2i + 1
+    Lut16 t;
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+        t.lo[i] = ptx::prmt(e[2 * i], e[2 * i + 1], 0x6420u);
+        t.hi[i] = ptx::prmt(e[2 * i], e[2 * i + 1], 0x7531u);
+    }
+    return t;
+}
+
+// The four codes of one row in one fragment-order word (bits 0-3 / 16-19 / 8-11 /
+// 24-27 for k, k + 1, k + 8, k + 9 in the lower row half; 4 bits higher in the
+// upper half, hshift = 4) -> the fp16 pairs LUT(k, k + 1) and LUT(k + 8, k + 9).
+__device__ __forceinline__ void lut16_word(uint32_t w, uint32_t hshift, const Lut16& t, uint32_t& p_lo,
+                                           uint32_t& p_hi) {
+    const uint32_t u = w >> hshift;                                     // the row's codes in low nibbles
+    const uint32_t sel = ((u & 0x0F0Fu) | ((u >> 12) & 0xF0F0u)) & 0x7777u;   // k, k+1, k+8, k+9 (3 bits)
+    // 0xFF in the result bytes whose code is >= 8: the sign of word bytes 0, 2, 1, 3
+    // after moving each code's bit 3 to bit 7
+    const uint32_t m = ptx::prmt(u << 4, 0u, 0xB9A8u);
+    const uint32_t lo = ptx::lop3_select(ptx::prmt(t.lo[0], t.lo[1], sel), ptx::prmt(t.lo[2], t.lo[3], sel), m);
+    const uint32_t hi = ptx::lop3_select(ptx::prmt(t.hi[0], t.hi[1], sel), ptx::prmt(t.hi[2], t.hi[3], sel), m);
+    p_lo = ptx::prmt(lo, hi, 0x5140u);
+    p_hi = ptx::prmt(lo, hi, 0x7362u);
+}
+
 }  // namespace wq

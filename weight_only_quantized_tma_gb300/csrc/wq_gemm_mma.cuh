@@ -236,11 +236,17 @@ __device__ __forceinline__ void int4_word_to_frag(uint32_t w, uint32_t off_lo, u
 }
 
 // NT: 8-token MMA column tiles (1 for M <= 8, 2 for M <= 16).  GSTEPS: 16-wide k
-// steps per scale group inside a stage (2, 4, 8 or 16; G >= BK folds once per stage).  One CTA per item (tile, K slice): gridDim.x == n_items, and the slices of
-// a tile form one cluster of p.splits CTAs.
-template <bool BF16, int NT, int GSTEPS, int BK, int STAGES, bool ZP = false>
+// steps per scale group inside a stage (2, 4, 8 or 16; G >= BK folds once per stage).
+// One CTA per item (tile, K slice): gridDim.x == n_items, and the slices of a tile form
+// one cluster of p.splits CTAs.  ZP: per-(group, row) zero points, operands q - z.
+// LUT: the codebook format (fp16 activations), operands LUT[q] looked up with byte
+// permutes from a table in registers (lut16_word gives rows g / g + 8 of a word for
+// shifts 0 / 4, pairs k, k + 1 and k + 8, k + 9: the fragment registers a0 .. a3); the
+// group scale multiplies the fp32 sums, so an output is RN16(s * sum A LUT[q]).
+template <bool BF16, int NT, int GSTEPS, int BK, int STAGES, bool ZP = false, bool LUT = false>
 __global__ void __launch_bounds__(MmaDecodeCfg<BK, STAGES, ZP>::NTHREADS, 2)
     wq_decode_mma_kernel(const __grid_constant__ GemmParams p) {
+    static_assert(!LUT || (!ZP && !BF16), "codebook decode: fp16 activations, no zero points");
     using C = MmaDecodeCfg<BK, STAGES, ZP>;
     constexpr int NZ = C::NZ;
     constexpr int NCW = C::NCW;
@@ -405,6 +411,8 @@ __global__ void __launch_bounds__(MmaDecodeCfg<BK, STAGES, ZP>::NTHREADS, 2)
         // ------------------------------------------------------------ compute warps
         const int g = lane >> 2, c = lane & 3;
         const int slot = int4_slot(lane);
+        Lut16 tab{};
+        if constexpr (LUT) tab = lut16_load(p.lut);   // constant input, like the weights
         const int w_off = warp * RGW * 512 + slot * 16;   // this warp's first 16-row group, this lane's slot
         int sw = 0, sa = 0;
         uint32_t phw = 0, pha = 0;
@@ -468,7 +476,12 @@ __global__ void __launch_bounds__(MmaDecodeCfg<BK, STAGES, ZP>::NTHREADS, 2)
                     const uint4& q4 = wv[t >> 2][j];
                     const uint32_t word = (t & 3) == 0 ? q4.x : (t & 3) == 1 ? q4.y : (t & 3) == 2 ? q4.z : q4.w;
                     uint32_t a[4];
-                    int4_word_to_frag<BF16>(word, off_lo[j], off_hi[j], a);
+                    if constexpr (LUT) {
+                        lut16_word(word, 0u, tab, a[0], a[2]);   // rows g:     k, k + 1 / k + 8, k + 9
+                        lut16_word(word, 4u, tab, a[1], a[3]);   // rows g + 8
+                    } else {
+                        int4_word_to_frag<BF16>(word, off_lo[j], off_hi[j], a);
+                    }
 #pragma unroll
                     for (int nt = 0; nt < NT; ++nt) mma_16816(tmp[j][t % SETS][nt], a, b[nt][0], b[nt][1], BF16);
                 }
@@ -596,10 +609,10 @@ cudaError_t launch_decode_grid(Kernel kernel, const GemmParams& p, int grid, int
     return cudaLaunchKernelEx(&cfg, kernel, p);
 }
 
-template <bool BF16, int NT, int GSTEPS, int BK, int STAGES, bool ZP = false>
+template <bool BF16, int NT, int GSTEPS, int BK, int STAGES, bool ZP = false, bool LUT = false>
 struct MmaDecodeLauncher {
     using C = MmaDecodeCfg<BK, STAGES, ZP>;
-    static constexpr auto kernel = wq_decode_mma_kernel<BF16, NT, GSTEPS, BK, STAGES, ZP>;
+    static constexpr auto kernel = wq_decode_mma_kernel<BF16, NT, GSTEPS, BK, STAGES, ZP, LUT>;
     static cudaError_t prepare() {
         static int attr_set[64] = {0};
         int dev = 0;
@@ -614,7 +627,7 @@ struct MmaDecodeLauncher {
         return e;
     }
     static KernelConfig config(bool query_device) {
-        KernelConfig k{FMT_INT4, BF16 ? 1 : 0, 16, BK, STAGES, 0, C::NTHREADS, C::SMEM_BYTES, 0, 1};
+        KernelConfig k{LUT ? FMT_LUT4 : FMT_INT4, BF16 ? 1 : 0, 16, BK, STAGES, 0, C::NTHREADS, C::SMEM_BYTES, 0, 1};
         if (!query_device || prepare() != cudaSuccess) return k;
         decode_residency(kernel, C::NTHREADS, C::SMEM_BYTES, &k);
         return k;

@@ -165,6 +165,9 @@ cudaError_t launch_gemm_int4_decode(const GemmParams& p, bool bf16, int grid, cu
 // The same decode kernel with per-(group, row) zero points (wq_gemm_zp_decode.cu).
 bool config_int4_decode_zp(bool bf16, bool query, KernelConfig* cfg);
 cudaError_t launch_gemm_int4_decode_zp(const GemmParams& p, bool bf16, int grid, cudaStream_t st);
+// The same decode kernel for the codebook format, fp16 activations (wq_gemm_lut_decode.cu).
+bool config_int4_decode_lut(bool query, KernelConfig* cfg);
+cudaError_t launch_gemm_int4_decode_lut(const GemmParams& p, int grid, cudaStream_t st);
 // FP8 decode kernel (M <= 32, K % 64 == 0): the same register-resident scheme on plain
 // e4m3 weights read through TMA (wq_decode_fp8.cuh); `nt` 8-token column tiles (1, 2
 // or 4) select the instantiation whose configuration is returned.
