@@ -198,9 +198,12 @@ wq_status wq_gemm_w4a16_zp(const void* A, wq_dtype a_dtype, const uint8_t* w_ker
  * for wq_gemm_w4a16 plus lut: 16 fp16 values in device memory, 16-byte aligned (read
  * as two 16-byte vectors); the workspace is sized for WQ_OP_W4A16_LUT.  The operand
  * is RN(LUT[q] * s) in the type of A (the product of two fp16 values is exact in
- * fp32), accumulated in fp32; every M runs on the tile kernels.  lut is read after
- * the kernel waits for the kernel before it on the stream, so it may be written by
- * that kernel. */
+ * fp32), accumulated in fp32, on the tile kernels.  With fp16 A, M <= 16 and
+ * K % 64 == 0 the register decode kernel runs instead (WQ_KERNEL_DECODE): operands
+ * LUT[q] exactly, the group scale on the fp32 sums, out = RN16(sum_g s_g * sum_{k in g}
+ * A LUT[q]).  lut is read after the kernel waits for the kernel before it on the
+ * stream, so it may be written by that kernel; w_kernel and s_kernel follow the rule
+ * of wq_gemm_w4a16. */
 wq_status wq_gemm_w4a16_lut(const void* A, wq_dtype a_dtype, const uint8_t* w_kernel, const void* s_kernel,
                             const void* lut, int64_t M, int64_t N, int64_t K, int32_t G, void* out, void* ws,
                             size_t ws_bytes, wq_stream_t stream);
@@ -319,10 +322,12 @@ typedef struct {
 } wq_plan;
 
 /* Kernels a plan can pick.  TILE: the tcgen05 kernel (weights dequantized into
- * tensor memory, any M).  DECODE: W4A16 with M <= 16 and K % 64 == 0, FP8 with
- * M <= 32 and K % 64 == 0, or FP4 with M <= 16 and K % 256 == 0; MMA operands built in registers (W4A16: from the
- * fragment-order layout, group scale applied in fp32; FP8 / FP4: from the plain codes
- * (and the prepacked block scales), alpha applied in fp32). */
+ * tensor memory, any M).  DECODE: W4A16 (symmetric or zero point) with M <= 16 and
+ * K % 64 == 0, the codebook format with fp16 A, M <= 16 and K % 64 == 0, FP8 with
+ * M <= 32 and K % 64 == 0, or FP4 with M <= 16 and K % 256 == 0; MMA operands built in
+ * registers (W4A16 and codebook: from the fragment-order layout, group scale applied
+ * in fp32; FP8 / FP4: from the plain codes (and the prepacked block scales), alpha
+ * applied in fp32). */
 #define WQ_KERNEL_TILE 0
 #define WQ_KERNEL_DECODE 1
 /* TILE_PAIR: W4A16 with large M.  The tile kernel on two-CTA clusters: 256 weight

@@ -235,6 +235,25 @@ def test_lut_decode_ragged_and_deterministic(M, N, K, G):
         assert torch.equal(p.run(), first)
 
 
+@pytest.mark.parametrize("M", [1, 16, 64])
+def test_lut_table_written_by_the_preceding_kernel(M):
+    # the table may be produced by the kernel right before the GEMM on the stream (the
+    # GEMM may start early, programmatic dependent launch, but reads lut only after
+    # waiting for it): a copy kernel writes the table, then the GEMM runs, back to back,
+    # on the decode kernel (M <= 16) and the tile kernel
+    N, K, G = 1024, 2048, 128
+    lut_new = synth.random_codebook(750 + M)
+    p = LutProblem(M, N, K, G, seed=751 + M, lut=lut_new)
+    src = to_dev_f16bits(lut_new, "f16")
+    for _ in range(3):
+        p.lut_d.zero_()
+        torch.cuda.synchronize()
+        torch.mul(src, 1.0, out=p.lut_d)   # an elementwise kernel, not a copy-engine transfer
+        out = p.run()
+        torch.cuda.synchronize()
+        check_close(out_to_f64(out), p.ref(), what=f"lut written before the GEMM M={M}")
+
+
 def test_lut_bad_arguments():
     N, K, G = 256, 256, 128
     p = LutProblem(4, N, K, G, seed=710)

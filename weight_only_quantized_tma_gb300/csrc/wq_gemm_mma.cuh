@@ -411,8 +411,13 @@ __global__ void __launch_bounds__(MmaDecodeCfg<BK, STAGES, ZP>::NTHREADS, 2)
         // ------------------------------------------------------------ compute warps
         const int g = lane >> 2, c = lane & 3;
         const int slot = int4_slot(lane);
+        // the table may be written by the kernel before this one on the stream: read it
+        // after the dependency wait (the first stage's activations wait for it anyway)
         Lut16 tab{};
-        if constexpr (LUT) tab = lut16_load(p.lut);   // constant input, like the weights
+        if constexpr (LUT) {
+            ptx::grid_dependency_wait();
+            tab = lut16_load(p.lut);
+        }
         const int w_off = warp * RGW * 512 + slot * 16;   // this warp's first 16-row group, this lane's slot
         int sw = 0, sa = 0;
         uint32_t phw = 0, pha = 0;
