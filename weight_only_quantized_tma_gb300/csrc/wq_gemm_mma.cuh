@@ -244,7 +244,7 @@ __device__ __forceinline__ void int4_word_to_frag(uint32_t w, uint32_t off_lo, u
 // shifts 0 / 4, pairs k, k + 1 and k + 8, k + 9: the fragment registers a0 .. a3); the
 // group scale multiplies the fp32 sums, so an output is RN16(s * sum A LUT[q]).
 template <bool BF16, int NT, int GSTEPS, int BK, int STAGES, bool ZP = false, bool LUT = false>
-__global__ void __launch_bounds__(MmaDecodeCfg<BK, STAGES, ZP>::NTHREADS, 2)
+__global__ void __launch_bounds__(MmaDecodeCfg<BK, STAGES, ZP>::NTHREADS, LUT ? 3 : 2)
     wq_decode_mma_kernel(const __grid_constant__ GemmParams p) {
     static_assert(!LUT || (!ZP && !BF16), "codebook decode: fp16 activations, no zero points");
     using C = MmaDecodeCfg<BK, STAGES, ZP>;
@@ -555,21 +555,12 @@ __global__ void __launch_bounds__(MmaDecodeCfg<BK, STAGES, ZP>::NTHREADS, 2)
 // can hold at once (the plan keeps a split-K grid within one such wave).
 template <typename Kernel>
 void decode_residency(Kernel kernel, int threads, int smem_bytes, KernelConfig* k) {
-    int dev = 0, smem_sm = 0, smem_rsv = 0, regs_sm = 0, thr_sm = 0, blk_sm = 0;
-    cudaFuncAttributes fa;
-    if (cudaGetDevice(&dev) != cudaSuccess || cudaFuncGetAttributes(&fa, kernel) != cudaSuccess ||
-        cudaDeviceGetAttribute(&smem_sm, cudaDevAttrMaxSharedMemoryPerMultiprocessor, dev) != cudaSuccess ||
-        cudaDeviceGetAttribute(&smem_rsv, cudaDevAttrReservedSharedMemoryPerBlock, dev) != cudaSuccess ||
-        cudaDeviceGetAttribute(&regs_sm, cudaDevAttrMaxRegistersPerMultiprocessor, dev) != cudaSuccess ||
-        cudaDeviceGetAttribute(&thr_sm, cudaDevAttrMaxThreadsPerMultiProcessor, dev) != cudaSuccess ||
-        cudaDeviceGetAttribute(&blk_sm, cudaDevAttrMaxBlocksPerMultiprocessor, dev) != cudaSuccess)
-        return;
-    const int regs_warp = ((fa.numRegs * 32 + 255) / 256) * 256;
-    int n = regs_sm / (regs_warp * (threads / 32));
-    const int by_smem = smem_sm / (smem_bytes + (int)fa.sharedSizeBytes + smem_rsv);
-    if (by_smem < n) n = by_smem;
-    if (thr_sm / threads < n) n = thr_sm / threads;
-    if (blk_sm < n) n = blk_sm;
+    // the occupancy calculator rather than registers / (registers per CTA): a CTA of
+    // five warps spreads unevenly over the SM's four schedulers, whose register files
+    // are separate (at 133 registers three CTAs fit the SM's total but not the
+    // scheduler that holds four of the fifteen warps)
+    int n = 0;
+    if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, kernel, threads, (size_t)smem_bytes) != cudaSuccess) return;
     if (n >= 1) k->ctas_per_sm = n;
     for (int S = 2; S <= kMaxDecodeCluster; ++S) {
         cudaLaunchConfig_t cfg = {};
