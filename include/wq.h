@@ -243,9 +243,11 @@ wq_status wq_debug_dequant_int2(const uint8_t* w_canon, const void* s_kernel, in
  * 16-byte aligned.  w_canon: uint8 [N][K/4], 16-byte aligned.  s_kernel: output of
  * wq_pack_int2_scales.  out: 16-byte aligned, N % 8 == 0.  ws: workspace sized for
  * WQ_OP_W2A16 (the rules of wq_gemm_w4a16's workspace apply).  The operand is
- * RN((q - 2) * s) in the type of A, accumulated in fp32; every M runs on the tile
- * kernels.  Every input is read after the kernel waits for the kernel before it on
- * the stream. */
+ * RN((q - 2) * s) in the type of A, accumulated in fp32, on the tile kernels.  With
+ * M <= 16, G >= 64 and K % 256 == 0 the register decode kernel runs instead
+ * (WQ_KERNEL_DECODE): operands q - 2 exactly, the group scale on the fp32 sums,
+ * out = RN(sum_g s_g * sum_{k in g} A (q - 2)).  Every input is read after the kernel
+ * waits for the kernel before it on the stream. */
 wq_status wq_gemm_w2a16(const void* A, wq_dtype a_dtype, const uint8_t* w_canon, const void* s_kernel, int64_t M,
                         int64_t N, int64_t K, int32_t G, void* out, void* ws, size_t ws_bytes, wq_stream_t stream);
 
@@ -323,11 +325,12 @@ typedef struct {
 
 /* Kernels a plan can pick.  TILE: the tcgen05 kernel (weights dequantized into
  * tensor memory, any M).  DECODE: W4A16 (symmetric or zero point) with M <= 16 and
- * K % 64 == 0, the codebook format with fp16 A, M <= 16 and K % 64 == 0, FP8 with
+ * K % 64 == 0, the codebook format with fp16 A, M <= 16 and K % 64 == 0, INT2 with
+ * M <= 16, G >= 64 and K % 256 == 0, FP8 with
  * M <= 32 and K % 64 == 0, or FP4 with M <= 16 and K % 256 == 0; MMA operands built in
  * registers (W4A16 and codebook: from the fragment-order layout, group scale applied
- * in fp32; FP8 / FP4: from the plain codes (and the prepacked block scales), alpha
- * applied in fp32). */
+ * in fp32; INT2: from the canonical codes, group scale applied in fp32; FP8 / FP4:
+ * from the plain codes (and the prepacked block scales), alpha applied in fp32). */
 #define WQ_KERNEL_TILE 0
 #define WQ_KERNEL_DECODE 1
 /* TILE_PAIR: W4A16 with large M.  The tile kernel on two-CTA clusters: 256 weight

@@ -119,3 +119,30 @@ def check_close(got, ref, out_dtype="f16", rel_max=REL_MAX, rel_mean=REL_MEAN, w
     assert rmax <= rel_max and rmean_vs <= rel_mean, \
         f"{what} rel_max={rmax:.3e} rel_mean={rmean:.3e} rel_mean_vs_rounded={rmean_vs:.3e}"
     return rmax, rmean
+
+
+class Int2Problem:
+    """Seeded INT2 (W2A16) problem: canonical 2-bit codes on the device and packed scales."""
+
+    def __init__(self, M, N, K, G, a_dtype="f16", seed=0, A_bits=None, codes=None):
+        self.M, self.N, self.K, self.G, self.a_dtype = M, N, K, G, a_dtype
+        self.A = A_bits if A_bits is not None else synth.activations(M, K, a_dtype, seed)
+        self.wts = synth.int2_weights(N, K, G, seed + 1)
+        if codes is not None:
+            self.wts.w = oracle.pack_int2(codes)
+        self.A_d = to_dev_f16bits(self.A, a_dtype)
+        self.w_d = torch.from_numpy(self.wts.w).to(DEV)
+        self.s_d = to_dev_f16bits(self.wts.s, "f16")
+        import weight_only_quantized_tma_gb300 as wq
+        self.sk = wq.wq_pack_int2_scales(self.s_d, N, K, G)
+
+    def run(self):
+        import weight_only_quantized_tma_gb300 as wq
+        return wq.wq_gemm_w2a16(self.A_d, self.w_d, self.sk, self.N, self.K, self.G)
+
+    def ref(self, rows=None):
+        return oracle.gemm_w2a16(self.A, self.a_dtype == "bf16", self.wts.w, self.wts.s, self.M, self.N, self.K,
+                                 self.G, rows=rows)
+
+    def dequant_ref(self):
+        return oracle.dequant_int2(self.wts.w, self.wts.s, self.K, self.G)

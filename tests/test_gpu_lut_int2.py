@@ -8,7 +8,7 @@ import oracle
 import weight_only_quantized_tma_gb300 as wq
 from weight_only_quantized_tma_gb300 import synth
 
-from gpu_helpers import DEV, check_close, out_bits, out_to_f64, to_dev_f16bits
+from gpu_helpers import DEV, Int2Problem, check_close, out_bits, out_to_f64, to_dev_f16bits
 
 pytestmark = pytest.mark.gpu
 
@@ -272,29 +272,6 @@ def test_lut_bad_arguments():
 
 
 # ------------------------------------------------------------------ INT2 (W2A16)
-
-class Int2Problem:
-    def __init__(self, M, N, K, G, a_dtype="f16", seed=0, A_bits=None, codes=None):
-        self.M, self.N, self.K, self.G, self.a_dtype = M, N, K, G, a_dtype
-        self.A = A_bits if A_bits is not None else synth.activations(M, K, a_dtype, seed)
-        self.wts = synth.int2_weights(N, K, G, seed + 1)
-        if codes is not None:
-            self.wts.w = oracle.pack_int2(codes)
-        self.A_d = to_dev_f16bits(self.A, a_dtype)
-        self.w_d = torch.from_numpy(self.wts.w).to(DEV)
-        self.s_d = to_dev_f16bits(self.wts.s, "f16")
-        self.sk = wq.wq_pack_int2_scales(self.s_d, N, K, G)
-
-    def run(self):
-        return wq.wq_gemm_w2a16(self.A_d, self.w_d, self.sk, self.N, self.K, self.G)
-
-    def ref(self, rows=None):
-        return oracle.gemm_w2a16(self.A, self.a_dtype == "bf16", self.wts.w, self.wts.s, self.M, self.N, self.K,
-                                 self.G, rows=rows)
-
-    def dequant_ref(self):
-        return oracle.dequant_int2(self.wts.w, self.wts.s, self.K, self.G)
-
 
 def test_int2_packed_scales_bytes():
     assert wq.wq_int2_packed_scales_bytes(200, 192, 64) == 256 * (256 // 64) * 2

@@ -18,7 +18,7 @@ LIB = os.path.join(HERE, "libwq.so")
 BUILD_DIR = os.path.join(HERE, "_build")
 SOURCES = ["wq_api.cu", "wq_pack.cu", "wq_gemm_int4.cu", "wq_gemm_fp8.cu", "wq_gemm_fp4.cu",
            "wq_noalloc.cu", "wq_quant.cu", "wq_gemm_lut2.cu",
-           "wq_gemm_zp_decode.cu", "wq_gemm_lut_decode.cu", "wq_gemm_fp8_decode.cu", "wq_gemm_fp4_decode.cu"]
+           "wq_gemm_zp_decode.cu", "wq_gemm_lut_decode.cu", "wq_gemm_int2_decode.cu", "wq_gemm_fp8_decode.cu", "wq_gemm_fp4_decode.cu"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 FLAGS = ["-O3", "-lineinfo", "-std=c++17", "-Xcompiler", "-fPIC", "-Xptxas", "-v",
          "-diag-suppress", "177"]

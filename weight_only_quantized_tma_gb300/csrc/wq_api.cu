@@ -117,7 +117,9 @@ constexpr int kCfgDecodeFp4 = 19;
 constexpr int kCfgDecodeFp8N4 = 20;   // FP8 decode with 4 token tiles (M <= 32)
 constexpr int kCfgDecodeFp4N1 = 21;   // FP4 decode with one token tile (M <= 8)
 constexpr int kCfgDecodeLut = 22;     // codebook INT4 decode (fp16 activations)
-constexpr int kNumDecodeCfgs = 7;
+constexpr int kCfgDecodeInt2 = 23;    // INT2 decode with two / one token tiles
+constexpr int kCfgDecodeInt2N1 = 24;
+constexpr int kNumDecodeCfgs = 9;
 constexpr int kCfgPair = 32;           // + format
 
 bool get_config_uncached(int fmt, bool bf16, int bn, bool query, KernelConfig* cfg) {
@@ -128,6 +130,8 @@ bool get_config_uncached(int fmt, bool bf16, int bn, bool query, KernelConfig* c
     if (fmt == kCfgDecodeFp4) return bf16 && config_fp4_decode(2, query, cfg);
     if (fmt == kCfgDecodeFp4N1) return bf16 && config_fp4_decode(1, query, cfg);
     if (fmt == kCfgDecodeLut) return !bf16 && config_int4_decode_lut(query, cfg);
+    if (fmt == kCfgDecodeInt2) return config_int2_decode(bf16, 2, query, cfg);
+    if (fmt == kCfgDecodeInt2N1) return config_int2_decode(bf16, 1, query, cfg);
     if (fmt == kCfgPair + FMT_INT4) return config_int4_pair(bf16, query, cfg);
     if (fmt == kCfgPair + FMT_FP8) return config_fp8_pair(bf16, query, cfg);
     if (fmt == kCfgPair + FMT_FP4) return bf16 && config_fp4_pair(query, cfg);
@@ -207,16 +211,21 @@ wq_status make_plan(int fmt, bool bf16, int64_t M, int64_t N, int64_t K, int sms
     KernelConfig cfg{};
     bool found = false;
     // decode (M <= 16; FP8 M <= 32): the register-resident kernels (W4A16, codebook INT4
-    // with fp16 activations, FP8, FP4);
+    // with fp16 activations, INT2 with G >= 64, FP8, FP4);
     // their activation copy views A as 64-wide boxes, so they need K % 64 == 0 (FP4:
-    // whole 256-code stages, K % 256 == 0, so that no stage reads block scales past K)
+    // whole 256-code stages, K % 256 == 0, so that no stage reads block scales past K;
+    // INT2: whole 256-code stages too, and G >= 64 so that each 64-code chunk lies in
+    // one group)
     // decode_kind (W4A16): 0 symmetric, 1 zero points, -1 no decode kernel
     const bool decode = decode_kind >= 0 &&
-                        (fmt == FMT_INT4 || fmt == FMT_FP8 || fmt == FMT_FP4 || (fmt == FMT_LUT4 && !bf16)) &&
-                        M <= (fmt == FMT_FP8 ? 32 : 16) && K % (fmt == FMT_FP4 ? 256 : 64) == 0 &&
-                        !decode_disabled();
+                        (fmt == FMT_INT4 || fmt == FMT_FP8 || fmt == FMT_FP4 || (fmt == FMT_LUT4 && !bf16) ||
+                         (fmt == FMT_INT2 && G >= 64)) &&
+                        M <= (fmt == FMT_FP8 ? 32 : 16) &&
+                        K % ((fmt == FMT_FP4 || fmt == FMT_INT2) ? 256 : 64) == 0 && !decode_disabled();
     if (decode && fmt == FMT_FP4) {
         found = get_config(M <= 8 ? kCfgDecodeFp4N1 : kCfgDecodeFp4, bf16, 16, sms > 0, &cfg);
+    } else if (decode && fmt == FMT_INT2) {
+        found = get_config(M <= 8 ? kCfgDecodeInt2N1 : kCfgDecodeInt2, bf16, 16, sms > 0, &cfg);
     } else if (decode && fmt == FMT_FP8) {
         found = get_config(M <= 16 ? kCfgDecodeFp8 : kCfgDecodeFp8N4, bf16, 16, sms > 0, &cfg);
     } else if (decode) {
@@ -789,9 +798,11 @@ wq_status wq_gemm_w2a16(const void* A, wq_dtype a_dtype, const uint8_t* w_canon,
     if ((st = check_ws(pl, ws, ws_bytes)) != WQ_OK) return st;
     GemmParams gp;
     std::memset(&gp, 0, sizeof(gp));
-    if (!encode_a(gp, A, bf16, M, K, pl.pair ? pl.cfg.bn / 2 : pl.cfg.bn)) return WQ_ERR_CUDA;
+    if (pl.decode ? !encode_a_boxes(gp, A, bf16, M, K, pl.cfg.bk)
+                  : !encode_a(gp, A, bf16, M, K, pl.pair ? pl.cfg.bn / 2 : pl.cfg.bn))
+        return WQ_ERR_CUDA;
     if (pl.pair && !encode_out(gp, out, bf16, M, N)) return WQ_ERR_CUDA;
-    const int pitch = pl.cfg.bk / 4;   // bytes of one row's codes per k-block
+    const int pitch = pl.cfg.bk / 4;   // bytes of one row's codes per k-block (decode: 64, a 256-code stage)
     if (!encode_2d(&gp.tmap_w, CU_TENSOR_MAP_DATA_TYPE_UINT8, w_canon, (uint64_t)(K / 4), (uint64_t)N,
                    (uint64_t)(K / 4), (uint32_t)pitch, TILE_N, swizzle_for_pitch(pitch)))
         return WQ_ERR_CUDA;
@@ -800,6 +811,7 @@ wq_status wq_gemm_w2a16(const void* A, wq_dtype a_dtype, const uint8_t* w_canon,
     gp.g_shift = G == 32 ? 5 : G == 64 ? 6 : G == 128 ? 7 : 8;
     gp.ngroups_pad = (int)(round_up(K, KPAD_INT4) / G);
     fill_common(gp, pl, M, N, K, out, ws, d->status);
+    if (pl.decode) return finish_launch(launch_gemm_int2_decode(gp, bf16, pl.grid, (cudaStream_t)stream));
     if (pl.pair) return finish_launch(launch_gemm_int2_pair(gp, bf16, pl.grid, (cudaStream_t)stream));
     return finish_launch(launch_gemm_int2(gp, bf16, pl.cfg.bn, pl.grid, (cudaStream_t)stream));
 }

@@ -168,6 +168,10 @@ cudaError_t launch_gemm_int4_decode_zp(const GemmParams& p, bool bf16, int grid,
 // The same decode kernel for the codebook format, fp16 activations (wq_gemm_lut_decode.cu).
 bool config_int4_decode_lut(bool query, KernelConfig* cfg);
 cudaError_t launch_gemm_int4_decode_lut(const GemmParams& p, int grid, cudaStream_t st);
+// INT2 decode kernel (M <= 16, G >= 64, K % 256 == 0): canonical 2-bit codes read through
+// TMA, turned into q - 2 in registers (wq_decode_int2.cuh); `nt` 8-token tiles (1 or 2).
+bool config_int2_decode(bool bf16, int nt, bool query, KernelConfig* cfg);
+cudaError_t launch_gemm_int2_decode(const GemmParams& p, bool bf16, int grid, cudaStream_t st);
 // FP8 decode kernel (M <= 32, K % 64 == 0): the same register-resident scheme on plain
 // e4m3 weights read through TMA (wq_decode_fp8.cuh); `nt` 8-token column tiles (1, 2
 // or 4) select the instantiation whose configuration is returned.
