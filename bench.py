@@ -681,6 +681,13 @@ def run_case(args):
             fn = lambda: wq.wq_gemm_w4a16_lut(A, wk, sk, lut, N, K, Gc)
         else:
             fn = lambda: wq.wq_gemm_w4a16(A, wk, sk, N, K, Gc)
+    elif op == "int2":
+        Gc = int(dims[3]) if len(dims) > 3 else 128
+        A = torch.from_numpy(synth.activations(M, K, "f16", seed).view(np.float16)).to(dev)
+        w = synth.int2_weights(N, K, Gc, seed + 1)
+        w2d = torch.from_numpy(w.w).to(dev)
+        sk2 = wq.wq_pack_int2_scales(torch.from_numpy(w.s.view(np.float16)).to(dev), N, K, Gc)
+        fn = lambda: wq.wq_gemm_w2a16(A, w2d, sk2, N, K, Gc)
     elif op == "fp8":
         A = torch.from_numpy(synth.activations(M, K, "bf16", seed).view(np.int16)).view(torch.bfloat16).to(dev)
         w = synth.fp8_weights(N, K, seed + 1)
@@ -700,8 +707,9 @@ def run_case(args):
         fn()
     torch.cuda.synchronize(dev)
     print(json.dumps({"case": args.case, "reps": args.reps, "plan": wq.get_plan(
-        {"w4a16": wq.WQ_OP_W4A16, "lut": wq.WQ_OP_W4A16_LUT, "fp8": wq.WQ_OP_FP8, "fp4": wq.WQ_OP_FP4}[op],
-        wq.WQ_F16 if op in ("w4a16", "lut") else wq.WQ_BF16, M, N, K, int(dims[3]) if len(dims) > 3 else 128)}))
+        {"w4a16": wq.WQ_OP_W4A16, "lut": wq.WQ_OP_W4A16_LUT, "int2": wq.WQ_OP_W2A16, "fp8": wq.WQ_OP_FP8,
+         "fp4": wq.WQ_OP_FP4}[op],
+        wq.WQ_F16 if op in ("w4a16", "lut", "int2") else wq.WQ_BF16, M, N, K, int(dims[3]) if len(dims) > 3 else 128)}))
 
 
 def main():
@@ -714,7 +722,8 @@ def main():
     ap.add_argument("--skip-cpu", action="store_true")
     ap.add_argument("--cpu-seconds", type=float, default=10.0)
     ap.add_argument("--case", default=None,
-                    help="profiling target: run one GEMM, e.g. w4a16:16:4096:4096:128, lut:M:N:K[:G], fp8:M:N:K, fp4:M:N:K")
+                    help="profiling target: run one GEMM, e.g. w4a16:16:4096:4096:128, lut:M:N:K[:G], int2:M:N:K[:G], "
+                         "fp8:M:N:K, fp4:M:N:K")
     ap.add_argument("--reps", type=int, default=5)
     args = ap.parse_args()
     if args.case:
