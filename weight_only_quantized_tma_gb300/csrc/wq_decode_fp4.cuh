@@ -58,13 +58,6 @@ __device__ __forceinline__ void e2m1x8_scaled_to_bf16(uint32_t q, uint32_t s2, u
     for (int i = 0; i < 4; ++i) o[i] = ptx::f16x2_to_bf16x2_exact(ptx::hmul2_u32(h[i], s2));
 }
 
-__device__ __forceinline__ uint4 ld_shared_v4(uint32_t addr) {
-    uint4 v;
-    asm volatile("ld.shared.v4.b32 {%0, %1, %2, %3}, [%4];" : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w) : "r"(addr)
-                 : "memory");
-    return v;
-}
-
 // NT: 8-token MMA column tiles (1 for M <= 8, 2 for M <= 16).  One CTA per item
 // (tile, K slice): gridDim.x == n_items, the slices of a tile form one cluster.
 template <int NT, int STAGES>

@@ -68,6 +68,13 @@ __device__ __forceinline__ void ld_shared_v2(uint32_t addr, uint32_t& r0, uint32
     asm volatile("ld.shared.v2.b32 {%0, %1}, [%2];" : "=r"(r0), "=r"(r1) : "r"(addr) : "memory");
 }
 
+__device__ __forceinline__ uint4 ld_shared_v4(uint32_t addr) {
+    uint4 v;
+    asm volatile("ld.shared.v4.b32 {%0, %1, %2, %3}, [%4];" : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w) : "r"(addr)
+                 : "memory");
+    return v;
+}
+
 // NT: 8-token MMA column tiles (1 for M <= 8, 2 for M <= 16, 4 for M <= 32).  One CTA per item (tile, K slice): gridDim.x == n_items, the slices of a
 // tile form one cluster.
 template <bool BF16, int NT, int STAGES>

@@ -193,16 +193,18 @@ __global__ void __launch_bounds__(Int2DecodeCfg<STAGES, NT>::NTHREADS, 3)
             for (int hp = 0; hp < CHUNKS / 2; ++hp)
                 w_off[j][hp] = (uint32_t)(row * 64 + (((2 * hp + (lane >> 4)) ^ ((row >> 1) & 3)) << 4));
         }
-        // activation operand of chunk h, step t, MMA column g of tile nt (token 8 nt +
-        // 2 (g % 4) + g / 4, spread over the banks): k = 64h + 16c + 4t .. + 3, i.e. box
-        // h, bytes 32c + 8t of the token's 128-byte row: 16-byte chunk 2c + t / 2 (XOR the
-        // row's swizzle), plus 8 (t % 2)
+        // activation operands of chunk h, steps 2tp and 2tp + 1, MMA column g of tile nt
+        // (token 8 nt + g): k = 64h + 16c + 8tp .. + 7, i.e. box h, bytes 32c + 16tp of the
+        // token's 128-byte row, the 16-byte chunk 2c + tp (XOR the row's swizzle), one
+        // 16-byte load for both steps.  A half-warp reads rows of four consecutive tokens,
+        // two even and two odd: with the swizzle its 16 chunks fall on 8 chunk positions
+        // twice, the two wavefronts 256 bytes need.
         uint32_t a_off[CHUNKS][NT];
 #pragma unroll
         for (int h = 0; h < CHUNKS; ++h)
 #pragma unroll
             for (int nt = 0; nt < NT; ++nt) {
-                const int row = h * p.a_box_rows + nt * 8 + token_of_column<true>(g);
+                const int row = h * p.a_box_rows + nt * 8 + g;
                 a_off[h][nt] = (uint32_t)(row * 128 + (((2 * c) ^ (row & 7)) << 4));
             }
         int s = 0;
@@ -233,13 +235,20 @@ __global__ void __launch_bounds__(Int2DecodeCfg<STAGES, NT>::NTHREADS, 3)
 #pragma unroll
                                     for (int e = 0; e < 4; ++e) tmp[j][x][nt][e] = 0.0f;
                     }
+                    uint4 bv[2][NT];
+#pragma unroll
+                    for (int tp = 0; tp < 2; ++tp)
+#pragma unroll
+                        for (int nt = 0; nt < NT; ++nt) bv[tp][nt] = ld_shared_v4(sa + (a_off[h][nt] ^ (uint32_t)(tp << 4)));
 #pragma unroll
                     for (int t = 0; t < 4; ++t) {
                         uint32_t b[NT][2];
 #pragma unroll
-                        for (int nt = 0; nt < NT; ++nt)
-                            ld_shared_v2(sa + ((a_off[h][nt] ^ (uint32_t)((t >> 1) << 4)) + 8u * (t & 1)), b[nt][0],
-                                         b[nt][1]);
+                        for (int nt = 0; nt < NT; ++nt) {
+                            const uint4& v = bv[t >> 1][nt];
+                            b[nt][0] = (t & 1) ? v.z : v.x;
+                            b[nt][1] = (t & 1) ? v.w : v.y;
+                        }
 #pragma unroll
                         for (int j = 0; j < RGW; ++j) {
                             uint32_t a[4];
@@ -303,7 +312,7 @@ __global__ void __launch_bounds__(Int2DecodeCfg<STAGES, NT>::NTHREADS, 3)
 #pragma unroll
                     for (int e = 0; e < 4; ++e) {
                         const int n = tile * TILE_N + (warp * RGW + j) * 16 + g + 8 * (e >> 1);
-                        const int m = nt * 8 + token_of_column<true>(2 * c + (e & 1));
+                        const int m = nt * 8 + 2 * c + (e & 1);
                         if (n < p.N && m < p.M) store_out<BF16>(p.out, (size_t)m * p.N + n, acc[j][nt][e]);
                     }
         }
@@ -311,7 +320,7 @@ __global__ void __launch_bounds__(Int2DecodeCfg<STAGES, NT>::NTHREADS, 3)
         ptx::cluster_wait();   // every CTA of the cluster has initialised its barriers
         if (warp < NCW) decode_send_partials<NT, RGW>(acc, warp, lane, rank, S, R, sbase + C::INBOX, inbox_bar);
         if (!bounded_wait<true>(inbox_bar, 0u, abort_flag, p.status, DEVICE_TIMEOUT_EPILOGUE, p.timeout_ns)) return;
-        decode_reduce_rows<NT, true>(reinterpret_cast<const float*>(smem + C::INBOX), S, R, rows_own, p.M,
+        decode_reduce_rows<NT, false>(reinterpret_cast<const float*>(smem + C::INBOX), S, R, rows_own, p.M,
                                      [&](int m, int r, float v) {
                                          const int n = tile * TILE_N + row0 + r;
                                          if (n < p.N) store_out<BF16>(p.out, (size_t)m * p.N + n, v);
