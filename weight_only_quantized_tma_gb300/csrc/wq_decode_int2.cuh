@@ -14,9 +14,9 @@
 // 16c + 4t .. 16c + 4t + 3.  The chunk is four 16-wide k steps: in step t the lane's
 // fragment positions 2c, 2c + 1, 2c + 8, 2c + 9 stand for codes 16c + 4t .. 16c + 4t + 3
 // (an MMA sums over k in any order as long as both operands agree), so the lane's
-// activation operand for the step is one 8-byte load of those four values of its
-// token.  A step mixes codes from the whole 64-code chunk, which lies inside one group
-// for G >= 64 (G = 32 stays on the tile kernel).
+// activation operands for steps 2tp and 2tp + 1 are one 16-byte load of those eight
+// values of its token.  A step mixes codes from the whole 64-code chunk, which lies
+// inside one group for G >= 64 (G = 32 stays on the tile kernel).
 //
 // Conversion: byte t copied into both 16-bit halves of a word (one byte permute); an
 // AND-OR with a magic number per half turns the two codes of each half into b + q
