@@ -534,8 +534,8 @@ def run_ours(args, rank, world, local_rank):
                 entry(op, M, N, K, "f16", us, ob, extra, into=zero_point)
                 del wsx
             del Ax, wkz, skz, zkz, outx
-        # codebook INT4 (NF4-style table; the register decode kernel at M <= 16) and INT2
-        # W2A16 (the tile kernels at every M)
+        # codebook INT4 (NF4-style table) and INT2 W2A16: the register decode kernels at
+        # M <= 16 (codebook: fp16 activations; INT2: G >= 64), the tile kernels above
         for (M, N, K, Gc) in [(16, 4096, 4096, 128), (4096, 4096, 4096, 128), (8192, 8192, 8192, 128)]:
             seed = 7000 + M
             Ax = torch.from_numpy(synth.activations(M, K, "f16", seed).view(np.int16)).to(dev).view(torch.float16)
