@@ -401,7 +401,7 @@ def rel_errors(out, ref):
     rel_max  = max|out - ref| / max|ref|
     rel_mean = mean|out - ref| / mean|ref|
     The accuracy check of "Low Bit Triton Kernels" (lecture 34, exercise 4) asks for
-    mean / max relative error near 1e-3 / 5e-3 and to judge the error as a
+    mean / max relative error near 1e-3 / 5e-3 and to read the error as a
     distribution; normalising by the reference's own magnitude keeps near-zero
     outputs from dominating.
     """
